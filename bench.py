@@ -1,0 +1,339 @@
+"""Benchmark of one speculative cycle (Markov-head draft + lossless verify).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C2]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+A step is one full cycle over one batch: spec_markov_draft (gamma sequential
+draft steps) then spec_verify, through the C ABI, on synthetic seeded inputs
+of the named workload.  The metric is verified draft positions per second
+(sum over requests of the verify length L_b per cycle / cycle time); rank 0
+prints ONE JSON line.  Under torchrun every rank runs its own batch on its
+own GPU (independent replicas, weak scaling, no data-path collective).
+
+--impl reference times the float64 CPU oracle on the host cores on a bounded
+sample of the same workload (the pages define no runnable reference system).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft positions/sec and achieved HBM GB/s (% of GB300 peak) at 1 GPU"
+UNIT = "verified draft positions/s"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="C2")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", 6800.0)), float(d.get("bf16_tflops", 1900.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic_bytes(w):
+    """Bytes a cycle must move at least (logits + W2 once per call), after the
+    survey's accounting: draft = B*g*V*s + r*V*s; verify = sum(L+1)*V*s (target
+    rows) + sum(L)*V*s (U rows re-read to rebuild q) + r*V*s."""
+    s = 2 if w.dtype == "bf16" else 4
+    L = w.verify_len.astype(np.int64)
+    draft = w.B * w.gamma * w.V * s + w.r * w.V * s
+    verify = int((L + 1).sum()) * w.V * s + int(L.sum()) * w.V * s + w.r * w.V * s
+    per_stage = {
+        "draft_tile": w.B * w.V * s + w.r * w.V * s / w.gamma,     # per launch (one step)
+        "target_stats": int((L + 1).sum()) * w.V * s,
+        "verify_tile": int(L.sum()) * w.V * s + w.r * w.V * s,
+    }
+    return draft, verify, per_stage
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.f = None
+
+    def __enter__(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.f is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.f.flush()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], parts[5:9]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_timing(name, trial, warmup, steps, seconds):
+    """Time the float64 oracle (as it stands) in a single-threaded subprocess:
+    `warmup` untimed then `steps` timed samples, each a bounded run of whole
+    requests (draft + verify) of the named workload; returns per-step
+    (requests, positions, seconds)."""
+    code = f"""
+import os, sys, time, json
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+from speculative_decoding_draft_04_gb300 import workloads as W
+from oracle import spec_oracle as O
+w = W.make_workload(W.config({name!r}), trial={trial})
+W1, W2 = w.f64("W1"), w.f64("W2")
+b = 0
+def sample(limit):
+    global b
+    t0 = time.perf_counter(); done = 0; pos = 0
+    while True:
+        tb = W.to_f64(w.target[b], w.dtype); ub = W.to_f64(w.U[b], w.dtype)
+        O.cycle_request(tb, ub, W1, W2, w.anchor[b], float(w.temperature[b]),
+                        w.u_draft[b].astype(np.float64), int(w.verify_len[b]),
+                        w.u_accept[b].astype(np.float64), float(w.u_final[b]))
+        done += 1; pos += int(w.verify_len[b]); b = (b + 1) % w.B
+        el = time.perf_counter() - t0
+        if el > limit: return (done, pos, el)
+for _ in range({warmup}): sample({seconds} / 4)
+print(json.dumps([sample({seconds}) for _ in range({steps})]))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                         timeout=(warmup + steps) * seconds * 4 + 900)
+    if out.returncode != 0:
+        raise RuntimeError("oracle timing failed: " + out.stderr[-500:])
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(name, seconds):
+    (req, pos, el), = oracle_timing(name, 0, 0, 1, seconds)
+    return {"value": pos / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{req} whole requests of {name} (draft + verify, float64 numpy, 1 thread) "
+                      f"in {el:.1f} s; host cpus={os.cpu_count()}"}
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    from speculative_decoding_draft_04_gb300 import workloads as W
+    per_step = min(20.0, max(1.0, 150.0 / max(1, args.steps + args.warmup)))
+    samples = oracle_timing(args.config, 0, args.warmup, args.steps, per_step)
+    req = sum(s[0] for s in samples)
+    pos = sum(s[1] for s in samples)
+    el = sum(s[2] for s in samples)
+    v = pos / el
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.config + ": " + W.CONFIG_DESCRIPTIONS[args.config],
+                       "step": f"a bounded sample of about {per_step:.1f} s of whole requests"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{req} whole requests over {args.steps} steps in {el:.1f} s; "
+                                       f"host cpus={os.cpu_count()}"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+
+    from speculative_decoding_draft_04_gb300 import _lib, build, engine
+    from speculative_decoding_draft_04_gb300 import workloads as W
+    build.build()
+    w = W.make_workload(W.config(args.config), trial=rank)
+    d = engine.DeviceWorkload.from_workload(w, dev)
+    bufs = engine.Buffers.for_workload(d, dev)
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def step():
+        engine.cycle(d, bufs, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K cycles, L2 flushed between cycles (outside the events)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    times = [a.elapsed_time(b) for a, b in evs]
+    ms = float(sum(times) / len(times))
+    clocks = clk.summary()
+
+    # ---- second timed pass with per-kernel events (roofline of the top kernel)
+    _lib.spec_profile_enable(True)
+    _lib.spec_profile_read()
+    for i in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    prof = _lib.spec_profile_read()
+    _lib.spec_profile_enable(False)
+
+    # ---- end to end: host inputs -> device, cycle, results -> host
+    pin = {k: getattr(d, k).cpu().pin_memory() for k in
+           ("U", "target", "anchor", "temperature", "verify_len", "u_draft", "u_accept", "u_final")}
+    out_al = torch.empty_like(bufs.accept_len, device="cpu").pin_memory()
+    out_tok = torch.empty_like(bufs.out_tokens, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = out_al.numel() * 4 + out_tok.numel() * 4
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        for k, t in pin.items():
+            getattr(d, k).copy_(t, non_blocking=True)
+        step()
+        out_al.copy_(bufs.accept_len, non_blocking=True)
+        out_tok.copy_(bufs.out_tokens, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = float(sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps)
+
+    positions = int(w.verify_len.sum())
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms, float(positions)], device=dev)
+        mx = t.clone()
+        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
+        tot = t.clone()
+        torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.SUM)
+        ms_all, e2e_all, pos_all = float(mx[0]), float(mx[1]), float(tot[2])
+    else:
+        ms_all, e2e_all, pos_all = ms, e2e_ms, float(positions)
+
+    if rank == 0:
+        hbm_peak, _, peak_src = measured_peaks()
+        draft_b, verify_b, per_stage = algorithmic_bytes(w)
+        cyc_gbs = (draft_b + verify_b) / (ms * 1e-3) / 1e9
+        tot_ms = sum(v[0] for v in prof.values())
+        top = max(per_stage, key=lambda k: prof.get(k, (0.0, 0))[0])
+        t_ms, n_l = prof[top]
+        avg_ms = t_ms / max(n_l, 1)
+        ach = per_stage[top] / (avg_ms * 1e-3) / 1e9
+        launches = sum(v[1] for v in prof.values()) // max(args.steps, 1)
+        line = {
+            "metric": METRIC, "value": pos_all / (ms_all * 1e-3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_all,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": args.config + ": " + W.CONFIG_DESCRIPTIONS[args.config],
+                       "l2": f"flushed between steps ({flush.numel() >> 20} MiB write, outside the events)",
+                       "positions_per_step": positions},
+            "hbm": {"cycle_algorithmic_bytes": draft_b + verify_b, "cycle_gbs": cyc_gbs,
+                    "frac_of_8TBs": cyc_gbs / NOMINAL_HBM_GBS,
+                    "frac_of_measured": cyc_gbs / hbm_peak},
+            "roofline": {"kernel": top, "bound": "hbm", "achieved": ach, "peak": hbm_peak,
+                         "peak_source": peak_src, "unit": "GB/s", "frac": ach / hbm_peak,
+                         "traffic": None, "algorithmic_bytes_per_launch": per_stage[top],
+                         "avg_launch_ms": avg_ms, "share_of_step": t_ms / tot_ms if tot_ms else None},
+            "stages_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]},
+            "e2e": {"value": pos_all / (e2e_all * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_all},
+            "gpu_launches": int(launches * args.steps),
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+/*
+ * spec.h -- C ABI of the GB300 sampling hot path of speculative decoding.
+ *
+ * Two calls make one speculative cycle:
+ *
+ *   spec_markov_draft  DSpark's sequential stage with the Markov head
+ *                      ("[논문리뷰] DSpark: Confidence-Scheduled Speculative
+ *                      Decoding with Semi-Autoregressive Generation", section
+ *                      1.2 "Sequential stage", block factorisation and the
+ *                      "Markov head" equation B(x_{k-1}, .) = W1[x_{k-1}] W2):
+ *                      for k = 1..gamma, q_k = softmax((U_k + W1[x_{k-1}] W2)/T)
+ *                      and x_k is drawn from q_k by inverse CDF.
+ *
+ *   spec_verify        lossless verification ("Speculative Decoding Part 1",
+ *                      VESSL AI blog, section "알고리즘" and section "수락
+ *                      규칙"): ratio tests u_j < p_j(x_{j+1}) / q_j(x_{j+1}) on
+ *                      every position, first reject n, correction token from
+ *                      normalize(max(0, p_n - q_n)) or bonus token from p_L, and
+ *                      alpha_j = sum_v min(p_j(v), q_j(v)); each request stops
+ *                      at its own verify length L_b (DSpark review, section
+ *                      2.2: the scheduler's l_r in {0..gamma}).
+ *
+ * Notation: q = draft distribution, p = target distribution.  Row j of U
+ * (0-based) is the draft logits of token x_{j+1}; row j of the target is the
+ * target logits that test x_{j+1}; target row L_b gives the bonus token.
+ * x_0 is the anchor.  The same temperature T_b divides the draft logits
+ * (U + bias) and the target logits.
+ *
+ * Sampling convention: the token drawn from a distribution pi with a uniform
+ * u is the smallest v (vocabulary order) with sum_{w<=v} pi(w) > u.  A ratio
+ * test accepts iff u < p/q.
+ *
+ * Conventions for every call:
+ *   - Tensor pointers are DEVICE pointers, row-major, 16-byte aligned, owned
+ *     by the caller; the library never allocates device memory.  Scratch
+ *     comes from the caller's workspace (spec_workspace_bytes()).
+ *   - Work is enqueued on `stream` and the call returns at once; outputs are
+ *     valid after the stream reaches that point.  The calls never
+ *     synchronize, so they may be captured in a CUDA graph.
+ *   - Host-detected errors (NULL pointer, unsupported shape or dtype,
+ *     misalignment, workspace too small) return a negative spec_status and
+ *     enqueue nothing.  A failed kernel launch returns SPEC_ECUDA.
+ *   - Data-dependent errors are detected on the device and OR-ed into
+ *     dev_status[0] (SPEC_DEV_* bits); the affected request's outputs are set
+ *     to -1 / NaN.  Read dev_status after synchronizing.
+ *   - Two calls may run concurrently only on distinct workspaces.
+ *   - Supported: 1 <= gamma <= 16, 1 <= B <= 4096, 16 <= V, V % 8 == 0,
+ *     V < 2^24, 1 <= r <= 256 with r % 16 == 0 for bf16 and 1 <= r <= 256 for
+ *     fp32.
+ */
+#ifndef SPEC_GB300_H
+#define SPEC_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Identical to cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* spec_stream_t;
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_EINVAL = -1,        /* NULL pointer or a size out of range           */
+  SPEC_EUNSUPPORTED = -2,  /* dtype / rank / gamma not supported             */
+  SPEC_EALIGN = -3,        /* a pointer is not 16-byte aligned               */
+  SPEC_EWORKSPACE = -4,    /* workspace NULL or smaller than required        */
+  SPEC_ECUDA = -5          /* a CUDA launch or attribute call failed         */
+} spec_status;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+/* Bits of dev_status[0].  dev_status is uint32_t[4]:
+ *   [0] OR of the bits below
+ *   [1] decisions re-decided in extended precision (near a boundary)
+ *   [2] decisions whose token or outcome changed after re-deciding
+ *   [3] requests verified on the extended-precision slow path            */
+enum {
+  SPEC_DEV_BAD_TOKEN = 1,   /* anchor or draft token outside [0, V)          */
+  SPEC_DEV_BAD_LEN = 2,     /* verify_len outside [0, gamma]                 */
+  SPEC_DEV_BAD_TEMP = 4,    /* temperature not finite and > 0                */
+  SPEC_DEV_TIMEOUT = 8,     /* a bounded device wait gave up                 */
+  SPEC_DEV_REFINED = 16,    /* informational: at least one re-decision        */
+  SPEC_DEV_OVERFLOW = 32    /* more near-boundary decisions than list slots   */
+};
+
+/* ---------------------------------------------------------------- draft */
+typedef struct {
+  int32_t B, gamma, V, r;
+  int32_t dtype;              /* spec_dtype of U, W1, W2                        */
+  const void* U;              /* [B][gamma][V] base draft logits U_1..U_gamma   */
+  const void* W1;             /* [V][r]  Markov embedding (row lookup)          */
+  const void* W2;             /* [r][V]  Markov logit projection                */
+  const int32_t* anchor;      /* [B]     x_0                                    */
+  const float* temperature;   /* [B]     T_b > 0                                */
+  const float* u_draft;       /* [B][gamma] uniforms in (0,1); [b][k] draws x_{k+1} */
+  int32_t* draft_tokens;      /* out [B][gamma]  x_1..x_gamma                   */
+  float* q_tok;               /* out [B][gamma]  q_k(x_k)                       */
+  double* lse_q;              /* out [B][gamma]  logsumexp_v((U_k(v)+B(v))/T)   */
+  uint32_t* dev_status;       /* out uint32_t[4], zeroed by the call            */
+  float* diag;                /* optional out [B][gamma][4]: F(x-1), F(x), margin
+                                 bound, first-pass token (before re-deciding)     */
+  void* workspace;
+  size_t workspace_bytes;
+} spec_draft_args;
+
+/* --------------------------------------------------------------- verify */
+typedef struct {
+  int32_t B, gamma, V, r;
+  int32_t dtype;              /* spec_dtype of target, U, W1, W2                */
+  const void* target;         /* [B][gamma+1][V] target logits                  */
+  const void* U;              /* [B][gamma][V]   the draft's base logits        */
+  const void* W1;             /* [V][r]                                         */
+  const void* W2;             /* [r][V]                                         */
+  const int32_t* anchor;      /* [B]                                            */
+  const float* temperature;   /* [B]                                            */
+  const int32_t* draft_tokens;/* [B][gamma] from spec_markov_draft              */
+  const float* q_tok;         /* [B][gamma] from spec_markov_draft              */
+  const double* lse_q;        /* [B][gamma] from spec_markov_draft              */
+  const int32_t* verify_len;  /* [B] L_b in [0, gamma]; 0 = bonus token only    */
+  const float* u_accept;      /* [B][gamma] ratio-test uniforms                 */
+  const float* u_final;       /* [B] one uniform: correction OR bonus token     */
+  int32_t* accept_len;        /* out [B]        n_b (tau = n_b + 1)             */
+  int32_t* out_tokens;        /* out [B][gamma+1] x_1..x_n, correction/bonus, -1 */
+  float* alpha;               /* out [B][gamma] sum_v min(p_j, q_j), j < L_b; NaN beyond */
+  float* p_tok;               /* optional out [B][gamma] p_j(x_{j+1}), j < L_b; NaN beyond */
+  uint32_t* dev_status;       /* out uint32_t[4], zeroed by the call            */
+  float* diag;                /* optional out [B][4]: final draw F(c-1), F(c),
+                                 margin bound, first-pass token                  */
+  void* workspace;
+  size_t workspace_bytes;
+} spec_verify_args;
+
+/* Bytes of workspace either call needs for these sizes (0 if unsupported).
+ * One workspace may serve both calls when they run in stream order.        */
+size_t spec_workspace_bytes(int32_t B, int32_t gamma, int32_t V, int32_t r, int32_t dtype);
+
+/* Draft gamma tokens per request.  Reads U, W1, W2, anchor, temperature,
+ * u_draft; writes draft_tokens, q_tok, lse_q, dev_status (and diag).       */
+int32_t spec_markov_draft(const spec_draft_args* args, spec_stream_t stream);
+
+/* Verify one drafted block per request.  Writes accept_len, out_tokens,
+ * alpha, dev_status (and p_tok, diag when non-NULL).                        */
+int32_t spec_verify(const spec_verify_args* args, spec_stream_t stream);
+
+/* Static text for a spec_status value. */
+const char* spec_status_string(int32_t status);
+
+/* ------------------------------------------------------ tuning / profiling */
+/* Process-wide knobs (not thread-safe against concurrent calls):
+ *   SPEC_OPT_EPS_SCALE   multiplies the near-boundary band (default 1.0)
+ *   SPEC_OPT_FORCE_SIMT  1 = compute the bf16 bias with the SIMT path      */
+enum { SPEC_OPT_EPS_SCALE = 1, SPEC_OPT_FORCE_SIMT = 2 };
+int32_t spec_set_option(int32_t key, double value);
+
+/* Per-stage timing with CUDA events on the calls' streams.  enable(1)
+ * starts recording, read() synchronizes the recorded events and returns, for
+ * each stage id < n, the total milliseconds and launch count since the last
+ * read (then clears them).  Stage names: spec_stage_name(id).              */
+int32_t spec_profile_enable(int32_t on);
+int32_t spec_profile_read(double* ms, int32_t* launches, int32_t n);
+const char* spec_stage_name(int32_t id);
+int32_t spec_num_stages(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_GB300_H */

@@ -1,0 +1,165 @@
+"""ctypes binding of libspec.so: the C ABI of include/spec.h, same names.
+
+Argument marshalling only -- every step of the path runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors (torch is used for device
+memory and streams); pointers, sizes and the stream handle are passed as
+plain integers.  There is no CPU fallback: if the library is missing or a
+call fails, a SpecError is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libspec.so")
+
+SPEC_F32, SPEC_BF16 = 0, 1
+SPEC_OPT_EPS_SCALE, SPEC_OPT_FORCE_SIMT = 1, 2
+DEV_BITS = {1: "BAD_TOKEN", 2: "BAD_LEN", 4: "BAD_TEMP", 8: "TIMEOUT", 16: "REFINED",
+            32: "OVERFLOW"}
+
+EXPORTED = ("spec_workspace_bytes", "spec_markov_draft", "spec_verify", "spec_status_string",
+            "spec_set_option", "spec_profile_enable", "spec_profile_read", "spec_stage_name",
+            "spec_num_stages")
+
+
+class SpecError(RuntimeError):
+    pass
+
+
+_i32, _vp, _sz = ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
+
+
+class DraftArgs(ctypes.Structure):
+    _fields_ = [("B", _i32), ("gamma", _i32), ("V", _i32), ("r", _i32), ("dtype", _i32),
+                ("U", _vp), ("W1", _vp), ("W2", _vp), ("anchor", _vp), ("temperature", _vp),
+                ("u_draft", _vp), ("draft_tokens", _vp), ("q_tok", _vp), ("lse_q", _vp),
+                ("dev_status", _vp), ("diag", _vp), ("workspace", _vp), ("workspace_bytes", _sz)]
+
+
+class VerifyArgs(ctypes.Structure):
+    _fields_ = [("B", _i32), ("gamma", _i32), ("V", _i32), ("r", _i32), ("dtype", _i32),
+                ("target", _vp), ("U", _vp), ("W1", _vp), ("W2", _vp), ("anchor", _vp),
+                ("temperature", _vp), ("draft_tokens", _vp), ("q_tok", _vp), ("lse_q", _vp),
+                ("verify_len", _vp), ("u_accept", _vp), ("u_final", _vp), ("accept_len", _vp),
+                ("out_tokens", _vp), ("alpha", _vp), ("p_tok", _vp), ("dev_status", _vp),
+                ("diag", _vp), ("workspace", _vp), ("workspace_bytes", _sz)]
+
+
+_LIB = None
+
+
+def lib(path: str | None = None) -> ctypes.CDLL:
+    """Load libspec.so (built in-tree by build.build())."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise SpecError(f"{p} is missing: build it with speculative_decoding_draft_04_gb300."
+                        "build.build() (there is no CPU fallback)")
+    L = ctypes.CDLL(p)
+    L.spec_workspace_bytes.restype = _sz
+    L.spec_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
+    L.spec_markov_draft.restype = _i32
+    L.spec_markov_draft.argtypes = [ctypes.POINTER(DraftArgs), _vp]
+    L.spec_verify.restype = _i32
+    L.spec_verify.argtypes = [ctypes.POINTER(VerifyArgs), _vp]
+    L.spec_status_string.restype = ctypes.c_char_p
+    L.spec_status_string.argtypes = [_i32]
+    L.spec_set_option.restype = _i32
+    L.spec_set_option.argtypes = [_i32, ctypes.c_double]
+    L.spec_profile_enable.restype = _i32
+    L.spec_profile_enable.argtypes = [_i32]
+    L.spec_profile_read.restype = _i32
+    L.spec_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i32), _i32]
+    L.spec_stage_name.restype = ctypes.c_char_p
+    L.spec_stage_name.argtypes = [_i32]
+    L.spec_num_stages.restype = _i32
+    L.spec_num_stages.argtypes = []
+    if path is None:
+        _LIB = L
+    return L
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        msg = lib().spec_status_string(rc).decode()
+        raise SpecError(f"{what} failed: {rc} ({msg})")
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise SpecError("tensors must be CUDA tensors")
+    if not t.is_contiguous():
+        raise SpecError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    raise SpecError(f"unsupported logits dtype {t.dtype}")
+
+
+def _stream(stream) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def spec_workspace_bytes(B: int, gamma: int, V: int, r: int, dtype: int) -> int:
+    return int(lib().spec_workspace_bytes(B, gamma, V, r, dtype))
+
+
+def spec_status_string(status: int) -> str:
+    return lib().spec_status_string(status).decode()
+
+
+def spec_set_option(key: int, value: float) -> None:
+    _check(lib().spec_set_option(key, float(value)), "spec_set_option")
+
+
+def spec_markov_draft(U, W1, W2, anchor, temperature, u_draft, draft_tokens, q_tok, lse_q,
+                      dev_status, workspace, diag=None, stream=None) -> None:
+    """Enqueue the Markov-head draft (shapes as in include/spec.h)."""
+    B, gamma, V = U.shape
+    a = DraftArgs(B, gamma, V, W1.shape[1], _dtype_code(U), _ptr(U), _ptr(W1), _ptr(W2),
+                  _ptr(anchor), _ptr(temperature), _ptr(u_draft), _ptr(draft_tokens),
+                  _ptr(q_tok), _ptr(lse_q), _ptr(dev_status), _ptr(diag), _ptr(workspace),
+                  workspace.numel() * workspace.element_size())
+    _check(lib().spec_markov_draft(ctypes.byref(a), _stream(stream)), "spec_markov_draft")
+
+
+def spec_verify(target, U, W1, W2, anchor, temperature, draft_tokens, q_tok, lse_q, verify_len,
+                u_accept, u_final, accept_len, out_tokens, alpha, dev_status, workspace,
+                p_tok=None, diag=None, stream=None) -> None:
+    """Enqueue the verification (shapes as in include/spec.h)."""
+    B, gamma, V = U.shape
+    a = VerifyArgs(B, gamma, V, W1.shape[1], _dtype_code(U), _ptr(target), _ptr(U), _ptr(W1),
+                   _ptr(W2), _ptr(anchor), _ptr(temperature), _ptr(draft_tokens), _ptr(q_tok),
+                   _ptr(lse_q), _ptr(verify_len), _ptr(u_accept), _ptr(u_final),
+                   _ptr(accept_len), _ptr(out_tokens), _ptr(alpha), _ptr(p_tok),
+                   _ptr(dev_status), _ptr(diag), _ptr(workspace),
+                   workspace.numel() * workspace.element_size())
+    _check(lib().spec_verify(ctypes.byref(a), _stream(stream)), "spec_verify")
+
+
+def spec_profile_enable(on: bool) -> None:
+    _check(lib().spec_profile_enable(1 if on else 0), "spec_profile_enable")
+
+
+def spec_profile_read() -> dict[str, tuple[float, int]]:
+    """{stage name: (total ms, launches)} since the previous read."""
+    L = lib()
+    n = L.spec_num_stages()
+    ms = (ctypes.c_double * n)()
+    cnt = (_i32 * n)()
+    _check(L.spec_profile_read(ms, cnt, n), "spec_profile_read")
+    return {L.spec_stage_name(i).decode(): (ms[i], cnt[i]) for i in range(n)}

@@ -1,0 +1,434 @@
+// Host side of the C ABI (include/spec.h): argument validation, workspace
+// layout, launch sequencing on the caller's stream, options and per-stage
+// event timing.  No device memory is ever allocated here.
+#include <mutex>
+#include <vector>
+
+#include "spec_internal.cuh"
+
+namespace spec {
+
+// launchers (spec_draft.cu, spec_verify.cu, spec_refine.cu)
+template <typename DT>
+cudaError_t launch_draft_tile(const Shape&, int, const void*, const void*, const void*, const int*,
+                              const int*, const float*, const Ws&, bool, cudaStream_t);
+template <typename DT>
+cudaError_t launch_draft_sample(const Shape&, int, const void*, const void*, const void*,
+                                const int*, const float*, const float*, int*, float*, double*,
+                                float*, uint32_t*, const Ws&, const Eps&, cudaStream_t);
+cudaError_t launch_verify_prep(const Shape&, const int*, const float*, const int*, const double*,
+                               const int*, const Ws&, uint32_t*, int*, int*, float*, float*,
+                               cudaStream_t);
+template <typename DT>
+cudaError_t launch_target_stats(const Shape&, const void*, const float*, const int*, const Ws&,
+                                cudaStream_t);
+template <typename DT>
+cudaError_t launch_verify_tile(const Shape&, const void*, const void*, const void*, const void*,
+                               const Ws&, bool, cudaStream_t);
+template <typename DT>
+cudaError_t launch_verify_final(const Shape&, const void*, const void*, const void*, const void*,
+                                const int*, const float*, const int*, const float*, const double*,
+                                const int*, const float*, const float*, int*, int*, float*, float*,
+                                float*, uint32_t*, const Ws&, const Eps&, cudaStream_t);
+template <typename DT>
+cudaError_t launch_hp_sums(const Shape&, const HpRows&, const Ws&, int, int, cudaStream_t);
+template <typename DT>
+cudaError_t launch_hp_decide(const Shape&, const HpRows&, const Ws&, int*, float*, double*, int*,
+                             uint32_t*, int, cudaStream_t);
+template <typename DT>
+cudaError_t launch_slow_verify(const Shape&, const HpRows&, const Ws&, const int*, const int*,
+                               const double*, const int*, const float*, const float*, int*, int*,
+                               uint32_t*, int, cudaStream_t);
+
+// ---------------------------------------------------------------- options
+namespace {
+std::mutex g_mu;
+double g_eps_scale = 1.0;
+bool g_force_simt = false;
+
+// Band constants (probability units); see DESIGN.md "Certified decisions".
+constexpr float EPS_ELEM = 2.0e-6f;
+constexpr float EPS_SLICE = 2.0e-6f;
+constexpr float EPS_ABS = 1.0e-9f;
+constexpr float EPS_RATIO = 1.0e-6f;
+constexpr float EPS_NORM = 4.0e-7f;
+
+Eps current_eps() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Eps e;
+  e.elem = EPS_ELEM;
+  e.slice = EPS_SLICE;
+  e.abs_ = EPS_ABS;
+  e.ratio = EPS_RATIO;
+  e.norm = EPS_NORM;
+  e.scale = (float)g_eps_scale;
+  return e;
+}
+
+// ---------------------------------------------------------------- profiling
+enum Stage {
+  ST_DRAFT_TILE, ST_DRAFT_SAMPLE, ST_DRAFT_HP_SUMS, ST_DRAFT_HP_DECIDE, ST_VERIFY_PREP,
+  ST_TARGET_STATS, ST_VERIFY_TILE, ST_VERIFY_FINAL, ST_SLOW_VERIFY, ST_VERIFY_HP_SUMS,
+  ST_VERIFY_HP_RESID, ST_VERIFY_HP_DECIDE, ST_COUNT
+};
+const char* kStageNames[ST_COUNT] = {
+    "draft_tile", "draft_sample", "draft_hp_sums", "draft_hp_decide", "verify_prep",
+    "target_stats", "verify_tile", "verify_final", "slow_verify", "verify_hp_sums",
+    "verify_hp_resid", "verify_hp_decide"};
+bool g_prof = false;
+struct EvPair { cudaEvent_t a, b; int stage; };
+std::vector<EvPair> g_pending;
+std::vector<cudaEvent_t> g_pool;
+
+cudaEvent_t get_event() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Records events around one launch when profiling is on.
+struct ProfScope {
+  cudaStream_t st;
+  int stage;
+  cudaEvent_t a = nullptr;
+  bool on;
+  ProfScope(cudaStream_t s, int sg) : st(s), stage(sg) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    on = g_prof;
+    if (on) {
+      a = get_event();
+      cudaEventRecord(a, st);
+    }
+  }
+  ~ProfScope() {
+    if (!on) return;
+    std::lock_guard<std::mutex> lk(g_mu);
+    cudaEvent_t b = get_event();
+    cudaEventRecord(b, st);
+    g_pending.push_back({a, b, stage});
+  }
+};
+
+int g_num_sms = -1;
+int grid_for_refine() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_num_sms < 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 132;
+    g_num_sms = n;
+  }
+  return 2 * g_num_sms;
+}
+
+// ---------------------------------------------------------------- workspace
+struct Layout {
+  size_t ctrl, items, hpsum, dpart, rowptr, prow, prevtok, vflags, lse_p, bpart, vpart, slow,
+      accbits, rowc, rowp, total;
+  int max_items;
+};
+
+Layout layout(const Shape& sh) {
+  Layout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = (off + bytes + 255) & ~(size_t)255;
+    return o;
+  };
+  const size_t B = sh.B, g = sh.gamma, NS = sh.NS, HB = sh.HB;
+  L.max_items = sh.B;
+  L.ctrl = take(CTRL_WORDS * sizeof(uint32_t));
+  L.items = take((size_t)L.max_items * sizeof(HpItem));
+  L.hpsum = take((size_t)L.max_items * HB * 3 * sizeof(double));
+  L.dpart = take(B * NS * sizeof(float4));
+  L.rowptr = take((B + 1) * sizeof(int));
+  L.prow = take(B * g * sizeof(int2));
+  L.prevtok = take(B * g * sizeof(int));
+  L.vflags = take(B * sizeof(int));
+  L.lse_p = take(B * (g + 1) * sizeof(double));
+  L.bpart = take(B * NS * sizeof(float4));
+  L.vpart = take(B * g * NS * sizeof(float4));
+  L.slow = take(B * sizeof(int));
+  L.accbits = take(B * sizeof(uint32_t));
+  L.rowc = take(B * g * sizeof(float4));
+  L.rowp = take(B * (g + 1) * sizeof(float2));
+  L.total = off;
+  return L;
+}
+
+Ws views(const Layout& L, void* base) {
+  unsigned char* p = static_cast<unsigned char*>(base);
+  Ws w;
+  w.ctrl = reinterpret_cast<uint32_t*>(p + L.ctrl);
+  w.items = reinterpret_cast<HpItem*>(p + L.items);
+  w.max_items = L.max_items;
+  w.hpsum = reinterpret_cast<double*>(p + L.hpsum);
+  w.dpart = reinterpret_cast<float4*>(p + L.dpart);
+  w.rowptr = reinterpret_cast<int*>(p + L.rowptr);
+  w.prow = reinterpret_cast<int2*>(p + L.prow);
+  w.prevtok = reinterpret_cast<int*>(p + L.prevtok);
+  w.vflags = reinterpret_cast<int*>(p + L.vflags);
+  w.lse_p = reinterpret_cast<double*>(p + L.lse_p);
+  w.bpart = reinterpret_cast<float4*>(p + L.bpart);
+  w.vpart = reinterpret_cast<float4*>(p + L.vpart);
+  w.slow = reinterpret_cast<int*>(p + L.slow);
+  w.accbits = reinterpret_cast<uint32_t*>(p + L.accbits);
+  w.rowc = reinterpret_cast<float4*>(p + L.rowc);
+  w.rowp = reinterpret_cast<float2*>(p + L.rowp);
+  return w;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int check_shape(int B, int gamma, int V, int r, int dtype) {
+  if (B < 1 || B > 4096 || gamma < 1 || V < 16 || V >= (1 << 24) || r < 1) return SPEC_EINVAL;
+  if (gamma > MAX_GAMMA) return SPEC_EUNSUPPORTED;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_EUNSUPPORTED;
+  if (V % 8 != 0) return SPEC_EUNSUPPORTED;
+  if (r % 16 != 0) return SPEC_EUNSUPPORTED;
+  if (dtype == SPEC_BF16 && r > 256) return SPEC_EUNSUPPORTED;
+  if (dtype == SPEC_F32 && r > 64) return SPEC_EUNSUPPORTED;
+  return SPEC_OK;
+}
+
+Shape make_shape(int B, int gamma, int V, int r) {
+  Shape s;
+  s.B = B;
+  s.gamma = gamma;
+  s.V = V;
+  s.r = r;
+  s.NS = (V + BN - 1) / BN;
+  s.HB = (V + HPB - 1) / HPB;
+  return s;
+}
+
+#define SPEC_TRY(x)                         \
+  do {                                      \
+    if ((x) != cudaSuccess) return SPEC_ECUDA; \
+  } while (0)
+
+template <typename DT>
+int run_draft(const spec_draft_args* a, cudaStream_t st) {
+  const Shape sh = make_shape(a->B, a->gamma, a->V, a->r);
+  const Layout L = layout(sh);
+  const Ws ws = views(L, a->workspace);
+  const Eps eps = current_eps();
+  bool simt;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    simt = g_force_simt;
+  }
+  const int grid = grid_for_refine();
+  HpRows R{a->U, a->U, a->W1, a->W2, a->temperature};
+  SPEC_TRY(cudaMemsetAsync(a->dev_status, 0, 4 * sizeof(uint32_t), st));
+  for (int k = 0; k < sh.gamma; ++k) {
+    {
+      ProfScope p(st, ST_DRAFT_TILE);
+      SPEC_TRY(launch_draft_tile<DT>(sh, k, a->U, a->W1, a->W2, a->anchor, a->draft_tokens,
+                                     a->temperature, ws, simt, st));
+    }
+    {
+      ProfScope p(st, ST_DRAFT_SAMPLE);
+      SPEC_TRY(launch_draft_sample<DT>(sh, k, a->U, a->W1, a->W2, a->anchor, a->temperature,
+                                       a->u_draft, a->draft_tokens, a->q_tok, a->lse_q, a->diag,
+                                       a->dev_status, ws, eps, st));
+    }
+    {
+      ProfScope p(st, ST_DRAFT_HP_SUMS);
+      SPEC_TRY(launch_hp_sums<DT>(sh, R, ws, 0, grid, st));
+    }
+    {
+      ProfScope p(st, ST_DRAFT_HP_DECIDE);
+      SPEC_TRY(launch_hp_decide<DT>(sh, R, ws, a->draft_tokens, a->q_tok, a->lse_q, nullptr,
+                                    a->dev_status, grid, st));
+    }
+  }
+  return SPEC_OK;
+}
+
+template <typename DT>
+int run_verify(const spec_verify_args* a, cudaStream_t st) {
+  const Shape sh = make_shape(a->B, a->gamma, a->V, a->r);
+  const Layout L = layout(sh);
+  const Ws ws = views(L, a->workspace);
+  const Eps eps = current_eps();
+  bool simt;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    simt = g_force_simt;
+  }
+  const int grid = grid_for_refine();
+  HpRows R{a->target, a->U, a->W1, a->W2, a->temperature};
+  SPEC_TRY(cudaMemsetAsync(a->dev_status, 0, 4 * sizeof(uint32_t), st));
+  {
+    ProfScope p(st, ST_VERIFY_PREP);
+    SPEC_TRY(launch_verify_prep(sh, a->anchor, a->temperature, a->draft_tokens, a->lse_q,
+                                a->verify_len, ws, a->dev_status, a->accept_len, a->out_tokens,
+                                a->alpha, a->p_tok, st));
+  }
+  {
+    ProfScope p(st, ST_TARGET_STATS);
+    SPEC_TRY(launch_target_stats<DT>(sh, a->target, a->temperature, a->verify_len, ws, st));
+  }
+  {
+    ProfScope p(st, ST_VERIFY_TILE);
+    SPEC_TRY(launch_verify_tile<DT>(sh, a->target, a->U, a->W1, a->W2, ws, simt, st));
+  }
+  {
+    ProfScope p(st, ST_VERIFY_FINAL);
+    SPEC_TRY(launch_verify_final<DT>(sh, a->target, a->U, a->W1, a->W2, a->anchor, a->temperature,
+                                     a->draft_tokens, a->q_tok, a->lse_q, a->verify_len,
+                                     a->u_accept, a->u_final, a->accept_len, a->out_tokens,
+                                     a->alpha, a->p_tok, a->diag, a->dev_status, ws, eps, st));
+  }
+  {
+    ProfScope p(st, ST_SLOW_VERIFY);
+    SPEC_TRY(launch_slow_verify<DT>(sh, R, ws, a->anchor, a->draft_tokens, a->lse_q, a->verify_len,
+                                    a->u_accept, a->u_final, a->accept_len, a->out_tokens,
+                                    a->dev_status, grid, st));
+  }
+  {
+    ProfScope p(st, ST_VERIFY_HP_SUMS);
+    SPEC_TRY(launch_hp_sums<DT>(sh, R, ws, 0, grid, st));
+  }
+  {
+    ProfScope p(st, ST_VERIFY_HP_RESID);
+    SPEC_TRY(launch_hp_sums<DT>(sh, R, ws, 1, grid, st));
+  }
+  {
+    ProfScope p(st, ST_VERIFY_HP_DECIDE);
+    SPEC_TRY(launch_hp_decide<DT>(sh, R, ws, nullptr, nullptr, nullptr, a->out_tokens,
+                                  a->dev_status, grid, st));
+  }
+  return SPEC_OK;
+}
+
+}  // namespace
+}  // namespace spec
+
+using namespace spec;
+
+extern "C" {
+
+size_t spec_workspace_bytes(int32_t B, int32_t gamma, int32_t V, int32_t r, int32_t dtype) {
+  if (check_shape(B, gamma, V, r, dtype) != SPEC_OK) return 0;
+  return layout(make_shape(B, gamma, V, r)).total;
+}
+
+int32_t spec_markov_draft(const spec_draft_args* a, spec_stream_t stream) {
+  if (!a) return SPEC_EINVAL;
+  int rc = check_shape(a->B, a->gamma, a->V, a->r, a->dtype);
+  if (rc != SPEC_OK) return rc;
+  if (!a->U || !a->W1 || !a->W2 || !a->anchor || !a->temperature || !a->u_draft ||
+      !a->draft_tokens || !a->q_tok || !a->lse_q || !a->dev_status)
+    return SPEC_EINVAL;
+  if (!aligned(a->U, 16) || !aligned(a->W1, 16) || !aligned(a->W2, 16) || !aligned(a->anchor, 4) ||
+      !aligned(a->temperature, 4) || !aligned(a->u_draft, 4) || !aligned(a->draft_tokens, 4) ||
+      !aligned(a->q_tok, 4) || !aligned(a->lse_q, 8) || !aligned(a->dev_status, 4) ||
+      (a->diag && !aligned(a->diag, 4)))
+    return SPEC_EALIGN;
+  const size_t need = layout(make_shape(a->B, a->gamma, a->V, a->r)).total;
+  if (!a->workspace || a->workspace_bytes < need) return SPEC_EWORKSPACE;
+  if (!aligned(a->workspace, 256)) return SPEC_EALIGN;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return a->dtype == SPEC_BF16 ? run_draft<bf16>(a, st) : run_draft<float>(a, st);
+}
+
+int32_t spec_verify(const spec_verify_args* a, spec_stream_t stream) {
+  if (!a) return SPEC_EINVAL;
+  int rc = check_shape(a->B, a->gamma, a->V, a->r, a->dtype);
+  if (rc != SPEC_OK) return rc;
+  if (!a->target || !a->U || !a->W1 || !a->W2 || !a->anchor || !a->temperature ||
+      !a->draft_tokens || !a->q_tok || !a->lse_q || !a->verify_len || !a->u_accept ||
+      !a->u_final || !a->accept_len || !a->out_tokens || !a->alpha || !a->dev_status)
+    return SPEC_EINVAL;
+  if (!aligned(a->target, 16) || !aligned(a->U, 16) || !aligned(a->W1, 16) || !aligned(a->W2, 16) ||
+      !aligned(a->anchor, 4) || !aligned(a->temperature, 4) || !aligned(a->draft_tokens, 4) ||
+      !aligned(a->q_tok, 4) || !aligned(a->lse_q, 8) || !aligned(a->verify_len, 4) ||
+      !aligned(a->u_accept, 4) || !aligned(a->u_final, 4) || !aligned(a->accept_len, 4) ||
+      !aligned(a->out_tokens, 4) || !aligned(a->alpha, 4) || !aligned(a->dev_status, 4) ||
+      (a->p_tok && !aligned(a->p_tok, 4)) || (a->diag && !aligned(a->diag, 4)))
+    return SPEC_EALIGN;
+  const size_t need = layout(make_shape(a->B, a->gamma, a->V, a->r)).total;
+  if (!a->workspace || a->workspace_bytes < need) return SPEC_EWORKSPACE;
+  if (!aligned(a->workspace, 256)) return SPEC_EALIGN;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return a->dtype == SPEC_BF16 ? run_verify<bf16>(a, st) : run_verify<float>(a, st);
+}
+
+const char* spec_status_string(int32_t s) {
+  switch (s) {
+    case SPEC_OK: return "ok";
+    case SPEC_EINVAL: return "invalid argument (NULL pointer or size out of range)";
+    case SPEC_EUNSUPPORTED: return "unsupported shape or dtype";
+    case SPEC_EALIGN: return "misaligned pointer";
+    case SPEC_EWORKSPACE: return "workspace missing or too small";
+    case SPEC_ECUDA: return "CUDA launch failed";
+    default: return "unknown status";
+  }
+}
+
+int32_t spec_set_option(int32_t key, double value) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  switch (key) {
+    case SPEC_OPT_EPS_SCALE:
+      if (!(value >= 0.0)) return SPEC_EINVAL;
+      g_eps_scale = value;
+      return SPEC_OK;
+    case SPEC_OPT_FORCE_SIMT:
+      g_force_simt = value != 0.0;
+      return SPEC_OK;
+    default:
+      return SPEC_EINVAL;
+  }
+}
+
+int32_t spec_profile_enable(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_prof = on != 0;
+  return SPEC_OK;
+}
+
+int32_t spec_profile_read(double* ms, int32_t* launches, int32_t n) {
+  std::vector<EvPair> pend;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    pend.swap(g_pending);
+  }
+  for (int i = 0; i < n; ++i) {
+    if (ms) ms[i] = 0.0;
+    if (launches) launches[i] = 0;
+  }
+  int rc = SPEC_OK;
+  for (const EvPair& e : pend) {
+    float t = 0.f;
+    if (cudaEventSynchronize(e.b) != cudaSuccess || cudaEventElapsedTime(&t, e.a, e.b) != cudaSuccess)
+      rc = SPEC_ECUDA;
+    if (e.stage < n) {
+      if (ms) ms[e.stage] += t;
+      if (launches) launches[e.stage] += 1;
+    }
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (const EvPair& e : pend) {
+    g_pool.push_back(e.a);
+    g_pool.push_back(e.b);
+  }
+  return rc;
+}
+
+const char* spec_stage_name(int32_t id) {
+  if (id < 0 || id >= ST_COUNT) return "";
+  return kStageNames[id];
+}
+
+int32_t spec_num_stages(void) { return ST_COUNT; }
+
+}  // extern "C"

@@ -1,0 +1,267 @@
+// Internal device/host definitions shared by the kernels of libspec.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <math.h>
+
+#include "../../include/spec.h"
+
+namespace spec {
+
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------- geometry
+constexpr int BN = 128;       // vocabulary columns per slice (one GEMM tile's N)
+constexpr int HPB = 256;      // columns per extended-precision block
+constexpr int NT = 256;       // threads per CTA for every kernel
+constexpr int MAX_GAMMA = 16;
+
+struct Shape {
+  int B, gamma, V, r, NS, HB;   // NS = ceil(V / BN), HB = ceil(V / HPB)
+};
+
+// A decision queued for re-decision in extended precision.
+enum HpKind { HP_DRAFT = 0, HP_BONUS = 1, HP_RESID = 2 };
+struct HpItem {
+  int b, j, kind, prev;   // request, row, kind, previous token (draft rows)
+  float u;                // the decision's uniform
+  int fast_token;         // token chosen by the first pass
+  double shift_q;         // first-pass logsumexp of the draft row
+  double shift_p;         // first-pass logsumexp of the target row
+};
+
+// Control words at the start of the workspace.
+enum { CTRL_ITEMS = 0, CTRL_SLOW = 1, CTRL_NPACKED = 2, CTRL_WORDS = 16 };
+
+// Workspace views (host computes the offsets; see spec_abi.cu).
+struct Ws {
+  uint32_t* ctrl;       // [CTRL_WORDS]
+  HpItem* items;        // [max_items]
+  int max_items;
+  double* hpsum;        // [max_items][HB][3]
+  // draft
+  float4* dpart;        // [B][NS] (c, m, s, q2)
+  // verify
+  int* rowptr;          // [B+1]
+  int2* prow;           // [B*gamma] packed (b, j), j < L_b
+  int* prevtok;         // [B*gamma] x_j of each packed row
+  int* vflags;          // [B] bit0 bad request, bits 8.. ratio flags
+  double* lse_p;        // [B][gamma+1]
+  float4* bpart;        // [B][NS] bonus row (c, s, p2, 0)
+  float4* vpart;        // [B*gamma][NS] (alpha, resid, p2, q2)
+  int* slow;            // [B]
+  uint32_t* accbits;    // [B] first-pass ratio-test outcomes
+  float4* rowc;         // [B*gamma] packed row: 1/T and -lse_q as double-float pairs
+  float2* rowp;         // [B][gamma+1] -lse_p as a double-float pair
+};
+
+// Inputs the extended-precision kernels read.
+struct HpRows {
+  const void* target;
+  const void* U;
+  const void* W1;
+  const void* W2;
+  const float* temp;
+};
+
+// Near-boundary band of a draw from a distribution with first-pass weights
+// (units: probability).  Calibrated constants; see the design doc.
+struct Eps {
+  float elem;    // x sqrt(sum q^2): per-weight rounding of the first pass
+  float slice;   // x sqrt(sum_slice mass^2): per-slice sums and factors
+  float abs_;    // floor
+  float ratio;   // relative band of a ratio test
+  float norm;    // residual draws: error of the two row normalisers
+  float scale;   // user multiplier (SPEC_OPT_EPS_SCALE)
+};
+
+// ---------------------------------------------------------------- loads
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const bf16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float tof(float x) { return x; }
+__device__ __forceinline__ float tof(bf16 x) { return __bfloat162float(x); }
+
+// ---------------------------------------------------------------- first-pass logit
+// x = ((U - c) + bias) * (1/T) with c a reference close to the largest U of
+// the slice: for bf16 data U - c is exact, so the dominant entries carry
+// only the rounding of a small number.  Explicit round-to-nearest intrinsics
+// keep the compiler from fusing differently in different kernels, so a
+// recomputation reproduces the same bits from the same bias.
+__device__ __forceinline__ float fast_x(float Uv, float c, float bias, float invT) {
+  return __fmul_rn(__fadd_rn(__fsub_rn(Uv, c), bias), invT);
+}
+__device__ __forceinline__ float fast_w(float x, float m) { return __expf(__fsub_rn(x, m)); }
+__device__ __forceinline__ float fast_tx(float tv, float c, float invT) {
+  return __fmul_rn(__fsub_rn(tv, c), invT);
+}
+
+// exp(g) for a double g, evaluated in single precision with the low part of g
+// applied as a first-order correction (|g - float(g)| < 2^-24 |g|).
+__device__ __forceinline__ float exp_split(double g) {
+  float gh = (float)g;
+  float gl = (float)(g - (double)gh);
+  return expf(gh) * (1.0f + gl);
+}
+
+// ---------------------------------------------------------------- double-float
+struct df { float hi, lo; };
+
+__device__ __forceinline__ df df_make(float x) { return {x, 0.f}; }
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+__device__ __forceinline__ df df_add(df a, df b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+  float hi = __fadd_rn(s, e);
+  float lo = __fsub_rn(e, __fsub_rn(hi, s));
+  return {hi, lo};
+}
+__device__ __forceinline__ df df_addf(df a, float b) { return df_add(a, df_make(b)); }
+__device__ __forceinline__ df df_neg(df a) { return {-a.hi, -a.lo}; }
+__device__ __forceinline__ double df_d(df a) { return (double)a.hi + (double)a.lo; }
+__device__ __forceinline__ df df_from_d(double x) {
+  float h = (float)x;
+  return {h, (float)(x - (double)h)};
+}
+// a * f for a float f (error ~ 2^-46 relative)
+__device__ __forceinline__ df df_mulf(df a, float f) {
+  float p = __fmul_rn(a.hi, f);
+  float e = fmaf(a.hi, f, -p);
+  e = fmaf(a.lo, f, e);
+  float hi = __fadd_rn(p, e);
+  float lo = __fsub_rn(e, __fsub_rn(hi, p));
+  return {hi, lo};
+}
+__device__ __forceinline__ df shfl_xor_df(df v, int m) {
+  return {__shfl_xor_sync(0xffffffffu, v.hi, m), __shfl_xor_sync(0xffffffffu, v.lo, m)};
+}
+__device__ __forceinline__ df shfl_up_df(df v, int d) {
+  return {__shfl_up_sync(0xffffffffu, v.hi, d), __shfl_up_sync(0xffffffffu, v.lo, d)};
+}
+
+// ---------------------------------------------------------------- block reductions (NT threads)
+__device__ __forceinline__ float warp_max(float v) {
+  for (int m = 16; m; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+  for (int m = 16; m; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+  return v;
+}
+__device__ __forceinline__ df warp_sum_df(df v) {
+  for (int m = 16; m; m >>= 1) v = df_add(v, shfl_xor_df(v, m));
+  return v;
+}
+// Results broadcast to all threads.  `sh` must hold >= 32 floats; calls are
+// separated by __syncthreads inside.
+__device__ __forceinline__ float block_max(float v, float* sh) {
+  v = warp_max(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = (threadIdx.x < (NT >> 5)) ? sh[threadIdx.x] : -INFINITY;
+  if (threadIdx.x < 32) r = warp_max(r);
+  if (threadIdx.x == 0) sh[0] = r;
+  __syncthreads();
+  r = sh[0];
+  __syncthreads();
+  return r;
+}
+__device__ __forceinline__ float block_sum(float v, float* sh) {
+  v = warp_sum(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = (threadIdx.x < (NT >> 5)) ? sh[threadIdx.x] : 0.f;
+  if (threadIdx.x < 32) r = warp_sum(r);
+  if (threadIdx.x == 0) sh[0] = r;
+  __syncthreads();
+  r = sh[0];
+  __syncthreads();
+  return r;
+}
+// Deterministic double-float sum over the block (fixed tree order).
+__device__ __forceinline__ df block_sum_df(df v, float* sh) {
+  v = warp_sum_df(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    sh[2 * (threadIdx.x >> 5)] = v.hi;
+    sh[2 * (threadIdx.x >> 5) + 1] = v.lo;
+  }
+  __syncthreads();
+  df r = {0.f, 0.f};
+  if (threadIdx.x < (NT >> 5)) r = {sh[2 * threadIdx.x], sh[2 * threadIdx.x + 1]};
+  if (threadIdx.x < 32) r = warp_sum_df(r);
+  if (threadIdx.x == 0) { sh[0] = r.hi; sh[1] = r.lo; }
+  __syncthreads();
+  r = {sh[0], sh[1]};
+  __syncthreads();
+  return r;
+}
+// Exclusive prefix (double-float) of one value per thread in thread order;
+// *total receives the block total.  `sh` holds >= 66 floats.
+__device__ __forceinline__ df block_excl_scan_df(df v, df* total, float* sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  df inc = v;
+  for (int d = 1; d < 32; d <<= 1) {
+    df o = shfl_up_df(inc, d);
+    if (lane >= d) inc = df_add(inc, o);
+  }
+  __syncthreads();
+  if (lane == 31) { sh[2 * w] = inc.hi; sh[2 * w + 1] = inc.lo; }
+  __syncthreads();
+  if (w == 0) {
+    df x = (lane < (NT >> 5)) ? df{sh[2 * lane], sh[2 * lane + 1]} : df{0.f, 0.f};
+    df xi = x;
+    for (int d = 1; d < 32; d <<= 1) {
+      df o = shfl_up_df(xi, d);
+      if (lane >= d) xi = df_add(xi, o);
+    }
+    // store exclusive warp offsets and the total
+    df ex = shfl_up_df(xi, 1);
+    if (lane == 0) ex = {0.f, 0.f};
+    if (lane < (NT >> 5)) { sh[2 * lane] = ex.hi; sh[2 * lane + 1] = ex.lo; }
+    if (lane == (NT >> 5) - 1) { sh[64] = xi.hi; sh[65] = xi.lo; }
+  }
+  __syncthreads();
+  df off = {sh[2 * w], sh[2 * w + 1]};
+  *total = {sh[64], sh[65]};
+  df within = shfl_up_df(inc, 1);
+  if (lane == 0) within = {0.f, 0.f};
+  df ex = df_add(off, within);
+  __syncthreads();
+  return ex;
+}
+
+// Double sums over the block (fixed order; few calls per kernel only:
+// GB300 has a low double-precision rate).
+__device__ __forceinline__ double warp_sum_d(double v) {
+  for (int m = 16; m; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+  return v;
+}
+__device__ __forceinline__ double block_sum_d(double v, double* sh) {
+  v = warp_sum_d(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
+  __syncthreads();
+  double r = (threadIdx.x < (NT >> 5)) ? sh[threadIdx.x] : 0.0;
+  if (threadIdx.x < 32) r = warp_sum_d(r);
+  if (threadIdx.x == 0) sh[0] = r;
+  __syncthreads();
+  r = sh[0];
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ void set_status(uint32_t* st, uint32_t bits) {
+  if (st) atomicOr(st, bits);
+}
+__device__ __forceinline__ bool temp_ok(float T) { return isfinite(T) && T > 0.f; }
+
+}  // namespace spec

@@ -1,0 +1,124 @@
+"""Device-side plumbing around the C ABI: moves a seeded workload to the GPU
+(torch allocations), owns the output buffers and the workspace, and
+enqueues one speculative cycle (spec_markov_draft then spec_verify) on a
+stream.  Nothing here computes any part of the method."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+from . import _lib
+from .workloads import Workload
+
+
+def _dev_logits(arr: np.ndarray, dtype: str, device):
+    import torch
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32)).to(device)
+
+
+@dataclasses.dataclass
+class DeviceWorkload:
+    B: int
+    gamma: int
+    V: int
+    r: int
+    dtype: str
+    target: object
+    U: object
+    W1: object
+    W2: object
+    anchor: object
+    temperature: object
+    verify_len: object
+    u_draft: object
+    u_accept: object
+    u_final: object
+
+    @classmethod
+    def from_workload(cls, w: Workload, device="cuda") -> "DeviceWorkload":
+        import torch
+
+        def i32(a):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+        def f32(a):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+
+        return cls(w.B, w.gamma, w.V, w.r, w.dtype, _dev_logits(w.target, w.dtype, device),
+                   _dev_logits(w.U, w.dtype, device), _dev_logits(w.W1, w.dtype, device),
+                   _dev_logits(w.W2, w.dtype, device), i32(w.anchor), f32(w.temperature),
+                   i32(w.verify_len), f32(w.u_draft), f32(w.u_accept), f32(w.u_final))
+
+    @property
+    def dtype_code(self) -> int:
+        return _lib.SPEC_BF16 if self.dtype == "bf16" else _lib.SPEC_F32
+
+
+@dataclasses.dataclass
+class Buffers:
+    draft_tokens: object
+    q_tok: object
+    lse_q: object
+    dstatus: object
+    accept_len: object
+    out_tokens: object
+    alpha: object
+    p_tok: object
+    vstatus: object
+    workspace: object
+    ddiag: object = None
+    vdiag: object = None
+
+    @classmethod
+    def allocate(cls, B, gamma, V, r, dtype_code, device="cuda", diag=False) -> "Buffers":
+        import torch
+        nbytes = _lib.spec_workspace_bytes(B, gamma, V, r, dtype_code)
+        if nbytes == 0:
+            raise _lib.SpecError("unsupported shape for libspec")
+        o = dict(device=device)
+        return cls(
+            draft_tokens=torch.empty((B, gamma), dtype=torch.int32, **o),
+            q_tok=torch.empty((B, gamma), dtype=torch.float32, **o),
+            lse_q=torch.empty((B, gamma), dtype=torch.float64, **o),
+            dstatus=torch.zeros(4, dtype=torch.int32, **o),
+            accept_len=torch.empty(B, dtype=torch.int32, **o),
+            out_tokens=torch.empty((B, gamma + 1), dtype=torch.int32, **o),
+            alpha=torch.empty((B, gamma), dtype=torch.float32, **o),
+            p_tok=torch.empty((B, gamma), dtype=torch.float32, **o),
+            vstatus=torch.zeros(4, dtype=torch.int32, **o),
+            workspace=torch.empty(nbytes, dtype=torch.uint8, **o),
+            ddiag=torch.empty((B, gamma, 4), dtype=torch.float32, **o) if diag else None,
+            vdiag=torch.empty((B, 4), dtype=torch.float32, **o) if diag else None,
+        )
+
+    @classmethod
+    def for_workload(cls, d: DeviceWorkload, device="cuda", diag=False) -> "Buffers":
+        return cls.allocate(d.B, d.gamma, d.V, d.r, d.dtype_code, device, diag)
+
+
+def draft(d: DeviceWorkload, b: Buffers, stream=None) -> None:
+    _lib.spec_markov_draft(d.U, d.W1, d.W2, d.anchor, d.temperature, d.u_draft, b.draft_tokens,
+                           b.q_tok, b.lse_q, b.dstatus, b.workspace, diag=b.ddiag, stream=stream)
+
+
+def verify(d: DeviceWorkload, b: Buffers, stream=None, draft_tokens=None, q_tok=None,
+           lse_q=None) -> None:
+    _lib.spec_verify(d.target, d.U, d.W1, d.W2, d.anchor, d.temperature,
+                     b.draft_tokens if draft_tokens is None else draft_tokens,
+                     b.q_tok if q_tok is None else q_tok,
+                     b.lse_q if lse_q is None else lse_q, d.verify_len, d.u_accept, d.u_final,
+                     b.accept_len, b.out_tokens, b.alpha, b.vstatus, b.workspace, p_tok=b.p_tok,
+                     diag=b.vdiag, stream=stream)
+
+
+def cycle(d: DeviceWorkload, b: Buffers, stream=None) -> None:
+    """One speculative cycle: draft gamma tokens per request, then verify them."""
+    draft(d, b, stream)
+    verify(d, b, stream)
+
+
+def status_words(t) -> list[int]:
+    return [int(x) & 0xFFFFFFFF for x in t.cpu().tolist()]
