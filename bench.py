@@ -236,7 +236,9 @@ def main():
         step()
     torch.cuda.synchronize()
 
-    # ---- timed region: K cycles, L2 flushed between cycles (outside the events)
+    # ---- timed region: K cycles, L2 flushed between cycles (outside the events).
+    # Clocks are sampled every 200 ms over the timed region, repeated untimed
+    # until the sampler has seen at least 5 samples under load.
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     barrier()
@@ -248,6 +250,11 @@ def main():
             step()
             evs[i][1].record(stream)
         torch.cuda.synchronize()
+        t_end = time.time() + 1.2
+        while time.time() < t_end:
+            flush.zero_()
+            step()
+            torch.cuda.synchronize()
     barrier()
     times = [a.elapsed_time(b) for a, b in evs]
     ms = float(sum(times) / len(times))

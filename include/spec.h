@@ -44,9 +44,8 @@
  *     dev_status[0] (SPEC_DEV_* bits); the affected request's outputs are set
  *     to -1 / NaN.  Read dev_status after synchronizing.
  *   - Two calls may run concurrently only on distinct workspaces.
- *   - Supported: 1 <= gamma <= 16, 1 <= B <= 4096, 16 <= V, V % 8 == 0,
- *     V < 2^24, 1 <= r <= 256 with r % 16 == 0 for bf16 and 1 <= r <= 256 for
- *     fp32.
+ *   - Supported: 1 <= gamma <= 16, 1 <= B <= 4096, 16 <= V < 2^24 with
+ *     V % 8 == 0, r % 16 == 0 with r <= 256 (bf16) or r <= 64 (fp32).
  */
 #ifndef SPEC_GB300_H
 #define SPEC_GB300_H
@@ -100,8 +99,9 @@ typedef struct {
   float* q_tok;               /* out [B][gamma]  q_k(x_k)                       */
   double* lse_q;              /* out [B][gamma]  logsumexp_v((U_k(v)+B(v))/T)   */
   uint32_t* dev_status;       /* out uint32_t[4], zeroed by the call            */
-  float* diag;                /* optional out [B][gamma][4]: F(x-1), F(x), margin
-                                 bound, first-pass token (before re-deciding)     */
+  float* diag;                /* optional out [B][gamma][4]: first-pass margins
+                                 u - F(x-1) and F(x) - u, the near-boundary band,
+                                 first-pass token (before any re-decision)        */
   void* workspace;
   size_t workspace_bytes;
 } spec_draft_args;
@@ -127,8 +127,10 @@ typedef struct {
   float* alpha;               /* out [B][gamma] sum_v min(p_j, q_j), j < L_b; NaN beyond */
   float* p_tok;               /* optional out [B][gamma] p_j(x_{j+1}), j < L_b; NaN beyond */
   uint32_t* dev_status;       /* out uint32_t[4], zeroed by the call            */
-  float* diag;                /* optional out [B][4]: final draw F(c-1), F(c),
-                                 margin bound, first-pass token                  */
+  float* diag;                /* optional out [B][4]: final draw's first-pass
+                                 margins u - F(c-1), F(c) - u (in the normalised
+                                 residual or bonus distribution), the band, and
+                                 the first-pass token                            */
   void* workspace;
   size_t workspace_bytes;
 } spec_verify_args;

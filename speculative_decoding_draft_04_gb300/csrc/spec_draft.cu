@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
     const int* __restrict__ anchor, const float* __restrict__ temp,
     const float* __restrict__ u_draft, int* tokens, float* q_tok, double* lse_q, float* diag,
     uint32_t* status, Ws ws, Eps eps) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  DT* slab = reinterpret_cast<DT*>(dsm);      // [r][BN] W2 slab of the crossing slice
   __shared__ float sh_f[72];
   __shared__ float s_a[256];
   __shared__ float s_part[2][BN];
@@ -229,19 +231,15 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
   const float4 PS = P[sl];
   const float fS = slice_factor(PS, cM, mM, invT);
 
-  // ---- recompute the slice's weights (bias by SIMT: two halves of k)
+  // ---- recompute the slice's weights (bias by SIMT: two halves of k, W2 slab in smem)
   for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf(W1 + (size_t)prev * sh.r + i);
-  __syncthreads();
   const int n0 = sl * BN;
+  stage_w2_slab<DT>(slab, W2, sh.V, 0, sh.r, n0, BN);
   {
     const int col = threadIdx.x % BN, half = threadIdx.x / BN;
-    const int v = n0 + col;
+    const int kh = sh.r / 2;
     float acc = 0.f;
-    if (v < sh.V) {
-      const int kh = (sh.r + 1) / 2;
-      const int ib = half * kh, ie = min(sh.r, ib + kh);
-      for (int i = ib; i < ie; ++i) acc = fmaf(s_a[i], ldf(W2 + (size_t)i * sh.V + v), acc);
-    }
+    for (int i = half * kh; i < half * kh + kh; ++i) acc = fmaf(s_a[i], tof(slab[i * BN + col]), acc);
     s_part[half][col] = acc;
   }
   __syncthreads();
@@ -301,9 +299,8 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
     q_tok[ok] = (float)((double)s_w[s_tok] * (double)fS / Z);
     lse_q[ok] = lse;
     if (diag) {
-      double flo = (df_d(pref) + ((double)(tin) - (double)s_lo[0]) * fS) / Z;
-      diag[ok * 4 + 0] = (float)flo;
-      diag[ok * 4 + 1] = (float)(flo + (double)s_w[s_tok] * fS / Z);
+      diag[ok * 4 + 0] = (float)((double)s_lo[0] * fS / Z);
+      diag[ok * 4 + 1] = (float)((double)s_hi[0] * fS / Z);
       diag[ok * 4 + 2] = (float)band;
       diag[ok * 4 + 3] = (float)tok;
     }
@@ -364,7 +361,11 @@ cudaError_t launch_draft_sample(const Shape& sh, int k, const void* U, const voi
                                 const float* u_draft, int* tokens, float* q_tok, double* lse_q,
                                 float* diag, uint32_t* status, const Ws& ws, const Eps& eps,
                                 cudaStream_t st) {
-  draft_sample_kernel<DT><<<sh.B, NT, 0, st>>>(sh, k, (const DT*)U, (const DT*)W1, (const DT*)W2,
+  const size_t smem = (size_t)sh.r * BN * sizeof(DT);
+  cudaError_t e = cudaFuncSetAttribute(draft_sample_kernel<DT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  draft_sample_kernel<DT><<<sh.B, NT, smem, st>>>(sh, k, (const DT*)U, (const DT*)W1, (const DT*)W2,
                                                anchor, temp, u_draft, tokens, q_tok, lse_q, diag,
                                                status, ws, eps);
   return cudaGetLastError();

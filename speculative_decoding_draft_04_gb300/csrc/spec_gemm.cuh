@@ -19,6 +19,24 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::); }
 
+// Stage W2[i0:i0+KC][c0:c0+NC] into shared memory (row stride NC elements);
+// columns >= V are zero.  c0 and NC multiples of 16 bytes' worth of elements.
+template <typename DT>
+__device__ __forceinline__ void stage_w2_slab(DT* dst, const DT* W2, int V, int i0, int KC, int c0,
+                                              int NC) {
+  constexpr int E = 16 / sizeof(DT);
+  const int cpr = NC / E;
+  for (int c = threadIdx.x; c < KC * cpr; c += NT) {
+    const int i = c / cpr, q = c - i * cpr;
+    const int n = c0 + q * E;
+    const bool valid = n < V;
+    cp_async16(dst + (size_t)i * NC + q * E, valid ? W2 + (size_t)(i0 + i) * V + n : W2, valid);
+  }
+  cp_async_commit();
+  cp_async_wait_all();
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------- warp MMA
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"

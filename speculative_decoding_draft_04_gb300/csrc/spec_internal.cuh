@@ -259,6 +259,30 @@ __device__ __forceinline__ double block_sum_d(double v, double* sh) {
   return r;
 }
 
+// sum_{i in [ib, ie)} a[i] * W2[i][v] with fp32 FMAs in i order.  W2 loads
+// are issued 8 rows ahead of their use so the loop is not bound by the
+// latency of one L2 round trip per row.  (ie - ib) % 8 == 0.
+template <typename DT>
+__device__ __forceinline__ float dot_col(const float* a, const DT* __restrict__ W2, int V, int ib,
+                                         int ie, int v) {
+  constexpr int UN = 8;
+  float acc = 0.f;
+  float cur[UN];
+#pragma unroll
+  for (int u = 0; u < UN; ++u) cur[u] = ib + u < ie ? ldf(W2 + (size_t)(ib + u) * V + v) : 0.f;
+  for (int i0 = ib; i0 < ie; i0 += UN) {
+    float nxt[UN];
+    const bool more = i0 + UN < ie;
+#pragma unroll
+    for (int u = 0; u < UN; ++u) nxt[u] = more ? ldf(W2 + (size_t)(i0 + UN + u) * V + v) : 0.f;
+#pragma unroll
+    for (int u = 0; u < UN; ++u) acc = fmaf(a[i0 + u], cur[u], acc);
+#pragma unroll
+    for (int u = 0; u < UN; ++u) cur[u] = nxt[u];
+  }
+  return acc;
+}
+
 __device__ __forceinline__ void set_status(uint32_t* st, uint32_t bits) {
   if (st) atomicOr(st, bits);
 }

@@ -23,7 +23,7 @@
 //   slow_verify_kernel one CTA per request whose ratio test itself was near
 //                     its boundary: re-runs that request's verification with
 //                     extended-precision normalisers (rare).
-#include "spec_internal.cuh"
+#include "spec_gemm.cuh"
 
 namespace spec {
 
@@ -55,17 +55,46 @@ __device__ __forceinline__ double exp_tang(double x, const double* tab) {
 template <typename DT>
 __device__ __forceinline__ double hp_logit_q(const float* a, const DT* __restrict__ W2, int V, int r,
                                              const DT* __restrict__ Urow, int v, double invTd) {
+  constexpr int UN = 16;                      // r % 16 == 0; loads run one batch ahead
+  float s = 0.f, c = 0.f;
+  float cur[UN];
+#pragma unroll
+  for (int u = 0; u < UN; ++u) cur[u] = ldf(W2 + (size_t)u * V + v);
+  for (int i0 = 0; i0 < r; i0 += UN) {
+    float nxt[UN];
+    const bool more = i0 + UN < r;
+#pragma unroll
+    for (int u = 0; u < UN; ++u) nxt[u] = more ? ldf(W2 + (size_t)(i0 + UN + u) * V + v) : 0.f;
+#pragma unroll
+    for (int u = 0; u < UN; ++u) {
+      const float w = cur[u];
+      const float p = __fmul_rn(a[i0 + u], w);
+      const float pe = fmaf(a[i0 + u], w, -p);   // 0 for bf16 operands
+      float t, e;
+      two_sum(s, p, t, e);
+      s = t;
+      c = __fadd_rn(c, __fadd_rn(e, pe));
+    }
+#pragma unroll
+    for (int u = 0; u < UN; ++u) cur[u] = nxt[u];
+  }
+  return ((double)ldf(Urow + v) + ((double)s + (double)c)) * invTd;
+}
+// Same bias, W2 column `col` of a shared-memory slab [r][ld].
+template <typename DT>
+__device__ __forceinline__ double hp_logit_q_smem(const float* a, const DT* slab, int ld, int col,
+                                                  int r, float Uv, double invTd) {
   float s = 0.f, c = 0.f;
   for (int i = 0; i < r; ++i) {
-    const float w = ldf(W2 + (size_t)i * V + v);
+    const float w = tof(slab[(size_t)i * ld + col]);
     const float p = __fmul_rn(a[i], w);
-    const float pe = fmaf(a[i], w, -p);       // 0 for bf16 operands
+    const float pe = fmaf(a[i], w, -p);
     float t, e;
     two_sum(s, p, t, e);
     s = t;
     c = __fadd_rn(c, __fadd_rn(e, pe));
   }
-  return ((double)ldf(Urow + v) + ((double)s + (double)c)) * invTd;
+  return ((double)Uv + ((double)s + (double)c)) * invTd;
 }
 template <typename DT>
 __device__ __forceinline__ double hp_logit_p(const DT* __restrict__ Trow, int v, double invTd) {
@@ -131,6 +160,21 @@ __device__ __forceinline__ void hp_weights(const Shape& sh, const HpRows& R, con
   if (it.kind != HP_DRAFT) ep = exp_tang(hp_logit_p<DT>(c.Trow, v, c.invTd) - it.shift_p, tab);
 }
 
+// Same weights with the W2 columns of block `blk` staged in `slab` ([r][HPB]).
+template <typename DT>
+__device__ __forceinline__ void hp_weights_slab(const Shape& sh, const HpItem& it,
+                                                const ItemCtx<DT>& c, const float* a,
+                                                const DT* slab, const double* tab, int v,
+                                                double& eq, double& ep) {
+  eq = 0.0;
+  ep = 0.0;
+  if (v >= sh.V) return;
+  if (it.kind != HP_BONUS)
+    eq = exp_tang(hp_logit_q_smem<DT>(a, slab, HPB, v % HPB, sh.r, ldf(c.Urow + v), c.invTd) -
+                      it.shift_q, tab);
+  if (it.kind != HP_DRAFT) ep = exp_tang(hp_logit_p<DT>(c.Trow, v, c.invTd) - it.shift_p, tab);
+}
+
 // Totals over the item's block sums, identical in every kernel (fixed order).
 __device__ __forceinline__ double item_total(const double* sums, int HB, int col, double* shd) {
   double s = 0.0;
@@ -140,24 +184,29 @@ __device__ __forceinline__ double item_total(const double* sums, int HB, int col
 
 template <typename DT>
 __global__ void __launch_bounds__(NT) hp_sums_kernel(Shape sh, HpRows R, Ws ws, int phase) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  DT* slab = reinterpret_cast<DT*>(dsm);        // [r][HPB] W2 columns of one block
   __shared__ double tab[32];
   __shared__ double shd[40];
   __shared__ float s_a[256];
+  const int n = min((int)ws.ctrl[CTRL_ITEMS], ws.max_items);
+  if (n == 0) return;
   init_exp_table(tab);
   __syncthreads();
-  const int n = min((int)ws.ctrl[CTRL_ITEMS], ws.max_items);
   for (int w = blockIdx.x; w < n * sh.HB; w += gridDim.x) {
     const int item = w / sh.HB, blk = w - item * sh.HB;
     const HpItem it = ws.items[item];
     if (phase == 1 && it.kind != HP_RESID) continue;
     __syncthreads();
-    if (it.kind != HP_BONUS)
+    if (it.kind != HP_BONUS) {
       for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf((const DT*)R.W1 + (size_t)it.prev * sh.r + i);
+      stage_w2_slab<DT>(slab, (const DT*)R.W2, sh.V, 0, sh.r, blk * HPB, HPB);
+    }
     __syncthreads();
     const ItemCtx<DT> c = item_ctx<DT>(sh, R, it);
     const int v = blk * HPB + threadIdx.x;
     double eq, ep;
-    hp_weights<DT>(sh, R, it, c, s_a, tab, v, eq, ep);
+    hp_weights_slab<DT>(sh, it, c, s_a, slab, tab, v, eq, ep);
     double* sums = ws.hpsum + (size_t)item * sh.HB * 3;
     if (phase == 0) {
       double A = block_sum_d(it.kind == HP_DRAFT ? eq : ep, shd);
@@ -180,14 +229,17 @@ template <typename DT>
 __global__ void __launch_bounds__(NT) hp_decide_kernel(Shape sh, HpRows R, Ws ws, int* tokens,
                                                        float* q_tok, double* lse_q,
                                                        int* out_tokens, uint32_t* status) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  DT* slab = reinterpret_cast<DT*>(dsm);        // [r][HPB] W2 columns of the crossing block
   __shared__ double tab[32];
   __shared__ double shd[40];
   __shared__ float s_a[256];
   __shared__ int s_blk, s_tok;
   __shared__ double s_pref, s_val;
+  const int n = min((int)ws.ctrl[CTRL_ITEMS], ws.max_items);
+  if (n == 0) return;
   init_exp_table(tab);
   __syncthreads();
-  const int n = min((int)ws.ctrl[CTRL_ITEMS], ws.max_items);
   for (int item = blockIdx.x; item < n; item += gridDim.x) {
     const HpItem it = ws.items[item];
     const double* sums = ws.hpsum + (size_t)item * sh.HB * 3;
@@ -237,13 +289,15 @@ __global__ void __launch_bounds__(NT) hp_decide_kernel(Shape sh, HpRows R, Ws ws
     }
     const int blk = s_blk;
     // recompute the block
-    if (it.kind != HP_BONUS)
+    if (it.kind != HP_BONUS) {
       for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf((const DT*)R.W1 + (size_t)it.prev * sh.r + i);
+      stage_w2_slab<DT>(slab, (const DT*)R.W2, sh.V, 0, sh.r, blk * HPB, HPB);
+    }
     __syncthreads();
     const ItemCtx<DT> c = item_ctx<DT>(sh, R, it);
     const int v = blk * HPB + threadIdx.x;
     double eq, ep;
-    hp_weights<DT>(sh, R, it, c, s_a, tab, v, eq, ep);
+    hp_weights_slab<DT>(sh, it, c, s_a, slab, tab, v, eq, ep);
     double val;
     if (it.kind == HP_DRAFT) val = eq;
     else if (resid && !empty) val = (v < sh.V) ? fmax(0.0, ep / Zp - eq / Zq) : 0.0;
@@ -314,9 +368,10 @@ __global__ void __launch_bounds__(NT) slow_verify_kernel(
   __shared__ double shd[40];
   __shared__ float s_a[256];
   __shared__ int s_tok;
+  const int nslow = min((int)ws.ctrl[CTRL_SLOW], sh.B);
+  if (nslow == 0) return;
   init_exp_table(tab);
   __syncthreads();
-  const int nslow = min((int)ws.ctrl[CTRL_SLOW], sh.B);
   for (int q = blockIdx.x; q < nslow; q += gridDim.x) {
     const int b = ws.slow[q];
     const int L = vlen[b];
@@ -426,14 +481,22 @@ __global__ void __launch_bounds__(NT) slow_verify_kernel(
 template <typename DT>
 cudaError_t launch_hp_sums(const Shape& sh, const HpRows& R, const Ws& ws, int phase, int grid,
                            cudaStream_t st) {
-  hp_sums_kernel<DT><<<grid, NT, 0, st>>>(sh, R, ws, phase);
+  const size_t smem = (size_t)sh.r * HPB * sizeof(DT);
+  cudaError_t e = cudaFuncSetAttribute(hp_sums_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  hp_sums_kernel<DT><<<grid, NT, smem, st>>>(sh, R, ws, phase);
   return cudaGetLastError();
 }
 template <typename DT>
 cudaError_t launch_hp_decide(const Shape& sh, const HpRows& R, const Ws& ws, int* tokens,
                              float* q_tok, double* lse_q, int* out_tokens, uint32_t* status,
                              int grid, cudaStream_t st) {
-  hp_decide_kernel<DT><<<grid, NT, 0, st>>>(sh, R, ws, tokens, q_tok, lse_q, out_tokens, status);
+  const size_t smem = (size_t)sh.r * HPB * sizeof(DT);
+  cudaError_t e = cudaFuncSetAttribute(hp_decide_kernel<DT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  hp_decide_kernel<DT><<<grid, NT, smem, st>>>(sh, R, ws, tokens, q_tok, lse_q, out_tokens, status);
   return cudaGetLastError();
 }
 template <typename DT>

@@ -306,6 +306,8 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
     const int* __restrict__ vlen, const float* __restrict__ u_acc, const float* __restrict__ u_fin,
     int* accept_len, int* out_tokens, float* alpha, float* p_tok, float* diag, uint32_t* status,
     Ws ws, Eps eps) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  DT* slab = reinterpret_cast<DT*>(dsm);      // [r][BN] W2 slab of the crossing slice
   __shared__ float sh_f[72];
   __shared__ float s_a[256];
   __shared__ float s_part[2][BN];
@@ -454,15 +456,11 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
   float w = 0.f, fslice = 1.f;
   if (resid) {
     for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf(W1 + (size_t)prev * sh.r + i);
-    __syncthreads();
+    stage_w2_slab<DT>(slab, W2, sh.V, 0, sh.r, n0, BN);
     const int col = threadIdx.x % BN, half = threadIdx.x / BN;
-    const int v = n0 + col;
+    const int kh = sh.r / 2;
     float acc = 0.f;
-    if (v < sh.V) {
-      const int kh = (sh.r + 1) / 2;
-      const int ib = half * kh, ie = min(sh.r, ib + kh);
-      for (int i = ib; i < ie; ++i) acc = fmaf(s_a[i], ldf(W2 + (size_t)i * sh.V + v), acc);
-    }
+    for (int i = half * kh; i < half * kh + kh; ++i) acc = fmaf(s_a[i], tof(slab[i * BN + col]), acc);
     s_part[half][col] = acc;
     __syncthreads();
     float uv = -INFINITY, tv = -INFINITY, bias = 0.f;
@@ -531,9 +529,8 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
         (((double)eps.elem * sqrt((double)e2) + (double)eps.slice * sqrt((double)m2) +
           (resid ? (double)eps.norm : 0.0)) / Zs + (double)eps.abs_);
     if (diag) {
-      double flo = (df_d(pref) + (tin - (double)s_lo) * fslice) / Zs;
-      diag[(size_t)b * 4 + 0] = (float)flo;
-      diag[(size_t)b * 4 + 1] = (float)(flo + (double)s_w[s_tok] * fslice / Zs);
+      diag[(size_t)b * 4 + 0] = (float)((double)s_lo * fslice / Zs);
+      diag[(size_t)b * 4 + 1] = (float)((double)s_hi * fslice / Zs);
       diag[(size_t)b * 4 + 2] = (float)band;
       diag[(size_t)b * 4 + 3] = (float)tok;
     }
@@ -613,7 +610,11 @@ cudaError_t launch_verify_final(const Shape& sh, const void* target, const void*
                                 int* accept_len, int* out_tokens, float* alpha, float* p_tok,
                                 float* diag, uint32_t* status, const Ws& ws, const Eps& eps,
                                 cudaStream_t st) {
-  verify_final_kernel<DT><<<sh.B, NT, 0, st>>>(
+  const size_t smem = (size_t)sh.r * BN * sizeof(DT);
+  cudaError_t e = cudaFuncSetAttribute(verify_final_kernel<DT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  verify_final_kernel<DT><<<sh.B, NT, smem, st>>>(
       sh, (const DT*)target, (const DT*)U, (const DT*)W1, (const DT*)W2, anchor, temp, dtok, q_tok,
       lse_q, vlen, u_acc, u_fin, accept_len, out_tokens, alpha, p_tok, diag, status, ws, eps);
   return cudaGetLastError();

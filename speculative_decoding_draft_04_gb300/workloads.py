@@ -79,11 +79,12 @@ CONFIG_DESCRIPTIONS = {
 }
 
 
-def config(name: str, **overrides: Any) -> dict[str, Any]:
-    """A copy of a named workload spec with fields overridden."""
-    spec = dict(CONFIGS[name])
+def config(cfg: str, **overrides: Any) -> dict[str, Any]:
+    """A copy of a named workload spec with fields overridden (including its
+    display ``name``)."""
+    spec = dict(CONFIGS[cfg])
+    spec["name"] = cfg
     spec.update(overrides)
-    spec.setdefault("name", name)
     return spec
 
 
