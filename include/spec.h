@@ -153,8 +153,11 @@ const char* spec_status_string(int32_t status);
 /* ------------------------------------------------------ tuning / profiling */
 /* Process-wide knobs (not thread-safe against concurrent calls):
  *   SPEC_OPT_EPS_SCALE   multiplies the near-boundary band (default 1.0)
- *   SPEC_OPT_FORCE_SIMT  1 = compute the bf16 bias with the SIMT path      */
-enum { SPEC_OPT_EPS_SCALE = 1, SPEC_OPT_FORCE_SIMT = 2 };
+ *   SPEC_OPT_FORCE_SIMT  1 = compute the bias with plain fp32 FMAs
+ *   SPEC_OPT_BIAS_PATH   tensor path of the bf16 bias tiles: 1 = warp MMA,
+ *                        2 = tcgen05 with the accumulator in tensor memory
+ *                        (default; used when r % 64 == 0)                   */
+enum { SPEC_OPT_EPS_SCALE = 1, SPEC_OPT_FORCE_SIMT = 2, SPEC_OPT_BIAS_PATH = 3 };
 int32_t spec_set_option(int32_t key, double value);
 
 /* Per-stage timing with CUDA events on the calls' streams.  enable(1)

@@ -11,7 +11,7 @@ namespace spec {
 // launchers (spec_draft.cu, spec_verify.cu, spec_refine.cu)
 template <typename DT>
 cudaError_t launch_draft_tile(const Shape&, int, const void*, const void*, const void*, const int*,
-                              const int*, const float*, const Ws&, bool, cudaStream_t);
+                              const int*, const float*, const Ws&, int, uint32_t*, cudaStream_t);
 template <typename DT>
 cudaError_t launch_draft_sample(const Shape&, int, const void*, const void*, const void*,
                                 const int*, const float*, const float*, int*, float*, double*,
@@ -24,7 +24,7 @@ cudaError_t launch_target_stats(const Shape&, const void*, const float*, const i
                                 cudaStream_t);
 template <typename DT>
 cudaError_t launch_verify_tile(const Shape&, const void*, const void*, const void*, const void*,
-                               const Ws&, bool, cudaStream_t);
+                               const Ws&, int, uint32_t*, cudaStream_t);
 template <typename DT>
 cudaError_t launch_verify_final(const Shape&, const void*, const void*, const void*, const void*,
                                 const int*, const float*, const int*, const float*, const double*,
@@ -45,6 +45,7 @@ namespace {
 std::mutex g_mu;
 double g_eps_scale = 1.0;
 bool g_force_simt = false;
+int g_bias_path = 2;          // 1 warp MMA, 2 tcgen05 (see SPEC_OPT_BIAS_PATH)
 
 // Band constants (probability units); see DESIGN.md "Certified decisions".
 // Largest first-pass margin error seen against the float64 oracle over C0-C4
@@ -223,10 +224,10 @@ int run_draft(const spec_draft_args* a, cudaStream_t st) {
   const Layout L = layout(sh);
   const Ws ws = views(L, a->workspace);
   const Eps eps = current_eps();
-  bool simt;
+  int path;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    simt = g_force_simt;
+    path = g_force_simt ? 0 : g_bias_path;
   }
   const int grid = grid_for_refine();
   HpRows R{a->U, a->U, a->W1, a->W2, a->temperature};
@@ -235,7 +236,7 @@ int run_draft(const spec_draft_args* a, cudaStream_t st) {
     {
       ProfScope p(st, ST_DRAFT_TILE);
       SPEC_TRY(launch_draft_tile<DT>(sh, k, a->U, a->W1, a->W2, a->anchor, a->draft_tokens,
-                                     a->temperature, ws, simt, st));
+                                     a->temperature, ws, path, a->dev_status, st));
     }
     {
       ProfScope p(st, ST_DRAFT_SAMPLE);
@@ -262,10 +263,10 @@ int run_verify(const spec_verify_args* a, cudaStream_t st) {
   const Layout L = layout(sh);
   const Ws ws = views(L, a->workspace);
   const Eps eps = current_eps();
-  bool simt;
+  int path;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    simt = g_force_simt;
+    path = g_force_simt ? 0 : g_bias_path;
   }
   const int grid = grid_for_refine();
   HpRows R{a->target, a->U, a->W1, a->W2, a->temperature};
@@ -282,7 +283,7 @@ int run_verify(const spec_verify_args* a, cudaStream_t st) {
   }
   {
     ProfScope p(st, ST_VERIFY_TILE);
-    SPEC_TRY(launch_verify_tile<DT>(sh, a->target, a->U, a->W1, a->W2, ws, simt, st));
+    SPEC_TRY(launch_verify_tile<DT>(sh, a->target, a->U, a->W1, a->W2, ws, path, a->dev_status, st));
   }
   {
     ProfScope p(st, ST_VERIFY_FINAL);
@@ -387,6 +388,10 @@ int32_t spec_set_option(int32_t key, double value) {
       return SPEC_OK;
     case SPEC_OPT_FORCE_SIMT:
       g_force_simt = value != 0.0;
+      return SPEC_OK;
+    case SPEC_OPT_BIAS_PATH:
+      if (value != 1.0 && value != 2.0) return SPEC_EINVAL;
+      g_bias_path = (int)value;
       return SPEC_OK;
     default:
       return SPEC_EINVAL;

@@ -14,26 +14,22 @@
 //                        the token (smallest v with F(v) > u).  Decisions within the
 //                        first pass's error band of a CDF breakpoint are queued for
 //                        re-decision in extended precision (spec_refine.cu).
-#include "spec_gemm.cuh"
+#include "spec_tc.cuh"
 
 namespace spec {
 
-template <typename DT, int BM, bool SIMT>
+// PATH: 0 = SIMT fp32 FMAs, 1 = warp MMA (mma.sync), 2 = tcgen05 / TMEM (BM = 128).
+template <typename DT, int BM, int PATH>
 __global__ void __launch_bounds__(NT) draft_tile_kernel(Shape sh, int k, const DT* __restrict__ U,
                                                         const DT* __restrict__ W1,
                                                         const DT* __restrict__ W2,
                                                         const int* __restrict__ anchor,
                                                         const int* __restrict__ tokens,
-                                                        const float* __restrict__ temp, Ws ws) {
-  extern __shared__ __align__(16) unsigned char smem[];
+                                                        const float* __restrict__ temp, Ws ws,
+                                                        uint32_t* status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int s_tok[BM];
   __shared__ size_t s_off[BM];
-  const TileLayout<DT> lay(BM, sh.r, false);
-  DT* As = reinterpret_cast<DT*>(smem + lay.offA);
-  DT* Wsm = reinterpret_cast<DT*>(smem + lay.offW);
-  DT* Us = reinterpret_cast<DT*>(smem + lay.offU);
-  float* stage = reinterpret_cast<float*>(smem + lay.offStage);
-
   const int slice = blockIdx.x, m0 = blockIdx.y * BM, n0 = slice * BN;
   const int nrows = min(BM, sh.B - m0);
   if (slice == 0 && blockIdx.y == 0 && threadIdx.x == 0) ws.ctrl[CTRL_ITEMS] = 0;
@@ -49,16 +45,58 @@ __global__ void __launch_bounds__(NT) draft_tile_kernel(Shape sh, int k, const D
     }
     s_tok[m] = t;
   }
-  __syncthreads();
-  load_A_rows<DT>(As, lay.sa, W1, s_tok, nrows, BM, sh.r);
-  load_W2_tile<DT>(Wsm, lay.sw, W2, sh.V, n0, sh.r);
-  load_X_rows<DT>(Us, lay.su, U, s_off, nrows, BM, sh.V, n0);
-  cp_async_commit();
-  cp_async_wait_all();
-  __syncthreads();
-
-  bias_tile<DT, BM, SIMT>(As, lay.sa, Wsm, lay.sw, sh.r, stage);
-  __syncthreads();
+  DT* Us;
+  float* stage;
+  int su;
+  if constexpr (PATH == 2) {
+    static_assert(BM == TC_M, "tensor-memory path uses 128-row tiles");
+    unsigned char* smem = align1k(smem_raw);
+    const TcLayout lay(sh.r, false);
+    bf16* As = reinterpret_cast<bf16*>(smem + lay.offA);
+    bf16* Wsm = reinterpret_cast<bf16*>(smem + lay.offW);
+    Us = reinterpret_cast<DT*>(smem + lay.offU);
+    stage = reinterpret_cast<float*>(smem + lay.offStage);
+    su = BN + 8;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + lay.offBar);
+    uint32_t* holder = reinterpret_cast<uint32_t*>(smem + lay.offBar + 8);
+    if (threadIdx.x == 0) mbar_init(bar, 1);
+    if (threadIdx.x < 32) tc_alloc(holder, TC_TMEM_COLS);
+    __syncthreads();
+    tc_load_A(As, reinterpret_cast<const bf16*>(W1), s_tok, nrows, sh.r);
+    tc_load_W2(Wsm, reinterpret_cast<const bf16*>(W2), sh.V, n0, sh.r);
+    load_X_rows<DT>(Us, su, U, s_off, nrows, BM, sh.V, n0);
+    cp_async_commit();
+    cp_async_wait_all();
+    fence_async_shared();
+    tc_fence_before();
+    __syncthreads();
+    const uint32_t taddr = *holder;
+    const bool ok = bias_tile_tc(As, Wsm, sh.r, taddr, bar, stage);
+    if (!ok) {
+      if (threadIdx.x == 0) set_status(status, SPEC_DEV_TIMEOUT);
+      mbar_wait(bar, 0, 1u << 22);     // let an in-flight MMA drain before freeing TMEM
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) tc_dealloc(taddr, TC_TMEM_COLS);
+    if (!ok) return;
+    __syncthreads();
+  } else {
+    const TileLayout<DT> lay(BM, sh.r, false);
+    DT* As = reinterpret_cast<DT*>(smem_raw + lay.offA);
+    DT* Wsm = reinterpret_cast<DT*>(smem_raw + lay.offW);
+    Us = reinterpret_cast<DT*>(smem_raw + lay.offU);
+    stage = reinterpret_cast<float*>(smem_raw + lay.offStage);
+    su = lay.su;
+    __syncthreads();
+    load_A_rows<DT>(As, lay.sa, W1, s_tok, nrows, BM, sh.r);
+    load_W2_tile<DT>(Wsm, lay.sw, W2, sh.V, n0, sh.r);
+    load_X_rows<DT>(Us, lay.su, U, s_off, nrows, BM, sh.V, n0);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    bias_tile<DT, BM, PATH == 0>(As, lay.sa, Wsm, lay.sw, sh.r, stage);
+    __syncthreads();
+  }
 
   // ---- epilogue: TPR threads per row, each COLS consecutive columns
   constexpr int TPR = NT / BM, COLS = BN / TPR;
@@ -69,7 +107,7 @@ __global__ void __launch_bounds__(NT) draft_tile_kernel(Shape sh, int k, const D
   const float invT = rowok ? 1.0f / temp[b] : 1.0f;
   const int cbeg = part * COLS;
   const int cend = min(cbeg + COLS, sh.V - n0);   // valid columns of this thread
-  const DT* urow = Us + (size_t)m * lay.su;
+  const DT* urow = Us + (size_t)m * su;
   const float* brow = stage + m * SS;
 
   float c = -INFINITY;
@@ -319,39 +357,40 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
 }
 
 // ---------------------------------------------------------------- launchers
-template <typename DT>
-static size_t tile_smem(int BM, int r) { return TileLayout<DT>(BM, r, false).total; }
-
-template <typename DT, int BM, bool SIMT>
+template <typename DT, int BM, int PATH>
 static cudaError_t launch_tile(const Shape& sh, int k, const DT* U, const DT* W1, const DT* W2,
                                const int* anchor, const int* tokens, const float* temp, const Ws& ws,
-                               cudaStream_t st) {
-  size_t smem = tile_smem<DT>(BM, sh.r);
-  auto kern = draft_tile_kernel<DT, BM, SIMT>;
+                               uint32_t* status, cudaStream_t st) {
+  const size_t smem = PATH == 2 ? TcLayout(sh.r, false).total : TileLayout<DT>(BM, sh.r, false).total;
+  auto kern = draft_tile_kernel<DT, BM, PATH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(sh.NS, (sh.B + BM - 1) / BM);
-  kern<<<grid, NT, smem, st>>>(sh, k, U, W1, W2, anchor, tokens, temp, ws);
+  kern<<<grid, NT, smem, st>>>(sh, k, U, W1, W2, anchor, tokens, temp, ws, status);
   return cudaGetLastError();
 }
 
+// path: 0 SIMT, 1 warp MMA, 2 tcgen05 (bf16 with r % 64 == 0 only; else warp MMA)
 template <typename DT>
 cudaError_t launch_draft_tile(const Shape& sh, int k, const void* U, const void* W1, const void* W2,
                               const int* anchor, const int* tokens, const float* temp, const Ws& ws,
-                              bool simt, cudaStream_t st) {
+                              int path, uint32_t* status, cudaStream_t st) {
   const DT* u = (const DT*)U;
   const DT* w1 = (const DT*)W1;
   const DT* w2 = (const DT*)W2;
   const int BM = sh.B <= 32 ? 32 : (sh.B <= 64 ? 64 : 128);
-#define SPEC_TILE(BMV, S) launch_tile<DT, BMV, S>(sh, k, u, w1, w2, anchor, tokens, temp, ws, st)
-  if (simt || sizeof(DT) == 4) {
-    if (BM == 32) return SPEC_TILE(32, true);
-    if (BM == 64) return SPEC_TILE(64, true);
-    return SPEC_TILE(128, true);
+#define SPEC_TILE(BMV, P) launch_tile<DT, BMV, P>(sh, k, u, w1, w2, anchor, tokens, temp, ws, status, st)
+  if (path == 0 || sizeof(DT) == 4) {
+    if (BM == 32) return SPEC_TILE(32, 0);
+    if (BM == 64) return SPEC_TILE(64, 0);
+    return SPEC_TILE(128, 0);
   }
-  if (BM == 32) return SPEC_TILE(32, false);
-  if (BM == 64) return SPEC_TILE(64, false);
-  return SPEC_TILE(128, false);
+  if constexpr (sizeof(DT) == 2) {
+    if (path == 2 && sh.r % 64 == 0) return SPEC_TILE(128, 2);
+  }
+  if (BM == 32) return SPEC_TILE(32, 1);
+  if (BM == 64) return SPEC_TILE(64, 1);
+  return SPEC_TILE(128, 1);
 #undef SPEC_TILE
 }
 
@@ -373,10 +412,10 @@ cudaError_t launch_draft_sample(const Shape& sh, int k, const void* U, const voi
 
 template cudaError_t launch_draft_tile<float>(const Shape&, int, const void*, const void*,
                                               const void*, const int*, const int*, const float*,
-                                              const Ws&, bool, cudaStream_t);
+                                              const Ws&, int, uint32_t*, cudaStream_t);
 template cudaError_t launch_draft_tile<bf16>(const Shape&, int, const void*, const void*,
                                              const void*, const int*, const int*, const float*,
-                                             const Ws&, bool, cudaStream_t);
+                                             const Ws&, int, uint32_t*, cudaStream_t);
 template cudaError_t launch_draft_sample<float>(const Shape&, int, const void*, const void*,
                                                 const void*, const int*, const float*, const float*,
                                                 int*, float*, double*, float*, uint32_t*, const Ws&,

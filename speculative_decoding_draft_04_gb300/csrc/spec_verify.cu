@@ -19,7 +19,7 @@
 //                        draw (crossing slice from the slice sums, that slice
 //                        recomputed and scanned).  Near-boundary draws are queued
 //                        for extended-precision re-decision (spec_refine.cu).
-#include "spec_gemm.cuh"
+#include "spec_tc.cuh"
 
 namespace spec {
 
@@ -211,24 +211,19 @@ __global__ void __launch_bounds__(NT) target_stats_kernel(Shape sh, const DT* __
 }
 
 // ---------------------------------------------------------------- alpha / residual tiles
-template <typename DT, int BM, bool SIMT>
+template <typename DT, int BM, int PATH>
 __global__ void __launch_bounds__(NT) verify_tile_kernel(Shape sh, const DT* __restrict__ target,
                                                          const DT* __restrict__ U,
                                                          const DT* __restrict__ W1,
-                                                         const DT* __restrict__ W2, Ws ws) {
-  extern __shared__ __align__(16) unsigned char smem[];
+                                                         const DT* __restrict__ W2, Ws ws,
+                                                         uint32_t* status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int s_tok[BM];
   __shared__ size_t s_offu[BM], s_offt[BM];
   const int P = (int)ws.ctrl[CTRL_NPACKED];
   const int slice = blockIdx.x, m0 = blockIdx.y * BM, n0 = slice * BN;
   if (m0 >= P) return;
   const int nrows = min(BM, P - m0);
-  const TileLayout<DT> lay(BM, sh.r, true);
-  DT* As = reinterpret_cast<DT*>(smem + lay.offA);
-  DT* Wsm = reinterpret_cast<DT*>(smem + lay.offW);
-  DT* Us = reinterpret_cast<DT*>(smem + lay.offU);
-  DT* Ts = reinterpret_cast<DT*>(smem + lay.offT);
-  float* stage = reinterpret_cast<float*>(smem + lay.offStage);
   for (int m = threadIdx.x; m < BM; m += NT) {
     if (m < nrows) {
       const int2 bj = ws.prow[m0 + m];
@@ -241,17 +236,62 @@ __global__ void __launch_bounds__(NT) verify_tile_kernel(Shape sh, const DT* __r
       s_offt[m] = 0;
     }
   }
-  __syncthreads();
-  load_A_rows<DT>(As, lay.sa, W1, s_tok, nrows, BM, sh.r);
-  load_W2_tile<DT>(Wsm, lay.sw, W2, sh.V, n0, sh.r);
-  load_X_rows<DT>(Us, lay.su, U, s_offu, nrows, BM, sh.V, n0);
-  load_X_rows<DT>(Ts, lay.su, target, s_offt, nrows, BM, sh.V, n0);
-  cp_async_commit();
-  cp_async_wait_all();
-  __syncthreads();
-
-  bias_tile<DT, BM, SIMT>(As, lay.sa, Wsm, lay.sw, sh.r, stage);
-  __syncthreads();
+  DT *Us, *Ts;
+  float* stage;
+  int su;
+  if constexpr (PATH == 2) {
+    static_assert(BM == TC_M, "tensor-memory path uses 128-row tiles");
+    unsigned char* smem = align1k(smem_raw);
+    const TcLayout lay(sh.r, true);
+    bf16* As = reinterpret_cast<bf16*>(smem + lay.offA);
+    bf16* Wsm = reinterpret_cast<bf16*>(smem + lay.offW);
+    Us = reinterpret_cast<DT*>(smem + lay.offU);
+    Ts = reinterpret_cast<DT*>(smem + lay.offT);
+    stage = reinterpret_cast<float*>(smem + lay.offStage);
+    su = BN + 8;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + lay.offBar);
+    uint32_t* holder = reinterpret_cast<uint32_t*>(smem + lay.offBar + 8);
+    if (threadIdx.x == 0) mbar_init(bar, 1);
+    if (threadIdx.x < 32) tc_alloc(holder, TC_TMEM_COLS);
+    __syncthreads();
+    tc_load_A(As, reinterpret_cast<const bf16*>(W1), s_tok, nrows, sh.r);
+    tc_load_W2(Wsm, reinterpret_cast<const bf16*>(W2), sh.V, n0, sh.r);
+    load_X_rows<DT>(Us, su, U, s_offu, nrows, BM, sh.V, n0);
+    load_X_rows<DT>(Ts, su, target, s_offt, nrows, BM, sh.V, n0);
+    cp_async_commit();
+    cp_async_wait_all();
+    fence_async_shared();
+    tc_fence_before();
+    __syncthreads();
+    const uint32_t taddr = *holder;
+    const bool ok = bias_tile_tc(As, Wsm, sh.r, taddr, bar, stage);
+    if (!ok) {
+      if (threadIdx.x == 0) set_status(status, SPEC_DEV_TIMEOUT);
+      mbar_wait(bar, 0, 1u << 22);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) tc_dealloc(taddr, TC_TMEM_COLS);
+    if (!ok) return;
+    __syncthreads();
+  } else {
+    const TileLayout<DT> lay(BM, sh.r, true);
+    DT* As = reinterpret_cast<DT*>(smem_raw + lay.offA);
+    DT* Wsm = reinterpret_cast<DT*>(smem_raw + lay.offW);
+    Us = reinterpret_cast<DT*>(smem_raw + lay.offU);
+    Ts = reinterpret_cast<DT*>(smem_raw + lay.offT);
+    stage = reinterpret_cast<float*>(smem_raw + lay.offStage);
+    su = lay.su;
+    __syncthreads();
+    load_A_rows<DT>(As, lay.sa, W1, s_tok, nrows, BM, sh.r);
+    load_W2_tile<DT>(Wsm, lay.sw, W2, sh.V, n0, sh.r);
+    load_X_rows<DT>(Us, lay.su, U, s_offu, nrows, BM, sh.V, n0);
+    load_X_rows<DT>(Ts, lay.su, target, s_offt, nrows, BM, sh.V, n0);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    bias_tile<DT, BM, PATH == 0>(As, lay.sa, Wsm, lay.sw, sh.r, stage);
+    __syncthreads();
+  }
 
   constexpr int TPR = NT / BM, COLS = BN / TPR;
   constexpr int SS = TileLayout<DT>::SS;
@@ -268,8 +308,8 @@ __global__ void __launch_bounds__(NT) verify_tile_kernel(Shape sh, const DT* __r
   const float invT = rc.x;
   const int cbeg = part * COLS;
   const int cend = min(cbeg + COLS, sh.V - n0);
-  const DT* urow = Us + (size_t)m * lay.su;
-  const DT* trow = Ts + (size_t)m * lay.su;
+  const DT* urow = Us + (size_t)m * su;
+  const DT* trow = Ts + (size_t)m * su;
   const float* brow = stage + m * SS;
   float cU = -INFINITY, cT = -INFINITY;
   for (int i = cbeg; i < cend; ++i) {
@@ -568,37 +608,41 @@ cudaError_t launch_target_stats(const Shape& sh, const void* target, const float
   return cudaGetLastError();
 }
 
-template <typename DT, int BM, bool SIMT>
+template <typename DT, int BM, int PATH>
 static cudaError_t launch_vtile(const Shape& sh, const DT* target, const DT* U, const DT* W1,
-                                const DT* W2, const Ws& ws, cudaStream_t st) {
-  const size_t smem = TileLayout<DT>(BM, sh.r, true).total;
-  auto kern = verify_tile_kernel<DT, BM, SIMT>;
+                                const DT* W2, const Ws& ws, uint32_t* status, cudaStream_t st) {
+  const size_t smem = PATH == 2 ? TcLayout(sh.r, true).total : TileLayout<DT>(BM, sh.r, true).total;
+  auto kern = verify_tile_kernel<DT, BM, PATH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int pmax = sh.B * sh.gamma;
   dim3 grid(sh.NS, (pmax + BM - 1) / BM);
-  kern<<<grid, NT, smem, st>>>(sh, target, U, W1, W2, ws);
+  kern<<<grid, NT, smem, st>>>(sh, target, U, W1, W2, ws, status);
   return cudaGetLastError();
 }
 
 template <typename DT>
 cudaError_t launch_verify_tile(const Shape& sh, const void* target, const void* U, const void* W1,
-                               const void* W2, const Ws& ws, bool simt, cudaStream_t st) {
+                               const void* W2, const Ws& ws, int path, uint32_t* status,
+                               cudaStream_t st) {
   const DT* t = (const DT*)target;
   const DT* u = (const DT*)U;
   const DT* w1 = (const DT*)W1;
   const DT* w2 = (const DT*)W2;
   const int pmax = sh.B * sh.gamma;
   const int BM = pmax <= 32 ? 32 : (pmax <= 64 ? 64 : 128);
-#define SPEC_VT(BMV, S) launch_vtile<DT, BMV, S>(sh, t, u, w1, w2, ws, st)
-  if (simt || sizeof(DT) == 4) {
-    if (BM == 32) return SPEC_VT(32, true);
-    if (BM == 64) return SPEC_VT(64, true);
-    return SPEC_VT(128, true);
+#define SPEC_VT(BMV, P) launch_vtile<DT, BMV, P>(sh, t, u, w1, w2, ws, status, st)
+  if (path == 0 || sizeof(DT) == 4) {
+    if (BM == 32) return SPEC_VT(32, 0);
+    if (BM == 64) return SPEC_VT(64, 0);
+    return SPEC_VT(128, 0);
   }
-  if (BM == 32) return SPEC_VT(32, false);
-  if (BM == 64) return SPEC_VT(64, false);
-  return SPEC_VT(128, false);
+  if constexpr (sizeof(DT) == 2) {
+    if (path == 2 && sh.r % 64 == 0) return SPEC_VT(128, 2);
+  }
+  if (BM == 32) return SPEC_VT(32, 1);
+  if (BM == 64) return SPEC_VT(64, 1);
+  return SPEC_VT(128, 1);
 #undef SPEC_VT
 }
 
@@ -624,7 +668,7 @@ cudaError_t launch_verify_final(const Shape& sh, const void* target, const void*
   template cudaError_t launch_target_stats<DT>(const Shape&, const void*, const float*, const int*, \
                                                const Ws&, cudaStream_t);                          \
   template cudaError_t launch_verify_tile<DT>(const Shape&, const void*, const void*, const void*, \
-                                              const void*, const Ws&, bool, cudaStream_t);        \
+                                              const void*, const Ws&, int, uint32_t*, cudaStream_t); \
   template cudaError_t launch_verify_final<DT>(                                                   \
       const Shape&, const void*, const void*, const void*, const void*, const int*, const float*, \
       const int*, const float*, const double*, const int*, const float*, const float*, int*, int*, \

@@ -221,3 +221,52 @@ def test_profile_api_counts_launches():
     assert prof["draft_tile"][1] == w.gamma
     assert prof["verify_tile"][1] == 1
     assert all(ms >= 0 for ms, _ in prof.values())
+
+
+# ----------------------------------------------------------------------------- tcgen05 path
+
+@pytest.fixture()
+def tc_path():
+    _lib.spec_set_option(_lib.SPEC_OPT_BIAS_PATH, 2)
+    yield
+    _lib.spec_set_option(_lib.SPEC_OPT_BIAS_PATH, 2)
+
+
+@pytest.fixture()
+def warp_mma_path():
+    _lib.spec_set_option(_lib.SPEC_OPT_BIAS_PATH, 1)
+    yield
+    _lib.spec_set_option(_lib.SPEC_OPT_BIAS_PATH, 2)
+
+
+@pytest.mark.parametrize("trial", range(2))
+def test_warp_mma_bias_path_parity(warp_mma_path, trial):
+    """The legacy warp-MMA bias path stays selectable and exact."""
+    w = W.make_workload(dict(SMALL, r=256, name="wmma"), trial=trial)
+    g, res, rep = run_and_compare(w)
+    assert_parity(rep)
+
+
+@pytest.mark.parametrize("B_,V,r,gamma", [(8, 1024, 64, 3), (130, 4104, 128, 4), (40, 4104, 256, 5),
+                                         (3, 264, 256, 2)])
+def test_tcgen05_bias_path_parity(tc_path, B_, V, r, gamma):
+    """Tensor-memory bias tiles (one or two 128-row tiles, ragged tails)."""
+    spec = dict(SMALL, B=B_, V=V, r=r, gamma=gamma, L=("uniform", 0, gamma), name="tc")
+    w = W.make_workload(spec, trial=4)
+    g, res, rep = run_and_compare(w)
+    assert g.dstatus[0] & 8 == 0 and g.vstatus[0] & 8 == 0, "bounded wait expired"
+    assert_parity(rep)
+    w2 = W.make_workload(W.stress(spec), trial=4)
+    g2, res2, rep2 = run_and_compare(w2)
+    assert_parity(rep2)
+
+
+@pytest.mark.parametrize("name,sample", [("C2", 24), ("C4", 5)])
+def test_tcgen05_full_size(tc_path, name, sample):
+    w = W.make_workload(W.config(name), trial=1)
+    rng = np.random.default_rng(7)
+    rows = sorted(rng.choice(w.B, size=sample, replace=False).tolist())
+    g, res, rep = run_and_compare(w, rows=rows)
+    print(name, "tcgen05", rep.summary(), g.dstatus, g.vstatus)
+    assert g.dstatus[0] & 8 == 0 and g.vstatus[0] & 8 == 0
+    assert_parity(rep)
