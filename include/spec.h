@@ -147,6 +147,36 @@ int32_t spec_markov_draft(const spec_draft_args* args, spec_stream_t stream);
  * alpha, dev_status (and p_tok, diag when non-NULL).                        */
 int32_t spec_verify(const spec_verify_args* args, spec_stream_t stream);
 
+/* ------------------------------------------- draft without caller scratch */
+/* No counterpart on the pages: this is a deployment convenience.
+ *
+ * Some callers cannot allocate device memory when they draft: code that runs
+ * while another component is capturing the stream into a CUDA graph (an
+ * allocation there would break or serialise the capture), services that
+ * reserve their whole device-memory budget at start-up and forbid later
+ * allocations, and plug-ins that receive only a stream from a host framework
+ * that owns the allocator.  spec_markov_draft_static does the same work as
+ * spec_markov_draft but ignores args->workspace / workspace_bytes and uses a
+ * scratch area of SPEC_STATIC_SCRATCH_BYTES compiled into the library as
+ * device memory; every GPU that loads the library holds that area until the
+ * process exits.  It never calls cudaMalloc, cudaFree or any allocating
+ * library routine.
+ *
+ *   - Size limit: the draft scratch is 64 + B*40 + B*ceil(V/256)*24 +
+ *     B*ceil(V/128)*16 bytes (each term rounded up to 256); larger problems
+ *     are rejected with SPEC_EWORKSPACE before anything is enqueued.  All five
+ *     named workloads fit (C4, the largest, needs about 7 MiB).
+ *   - The first call on a device looks up the area's device address with
+ *     cudaGetSymbolAddress (with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls in the process share the one area, and it keeps the previous
+ *     call's contents (the call clears the words that must start at zero).
+ *     Calls whose GPU work overlaps -- on different streams, or from
+ *     different threads without ordering -- race on it: serialise them.
+ */
+#define SPEC_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+int32_t spec_markov_draft_static(const spec_draft_args* args, spec_stream_t stream);
+
 /* Static text for a spec_status value. */
 const char* spec_status_string(int32_t status);
 

@@ -19,7 +19,8 @@ SPEC_OPT_EPS_SCALE, SPEC_OPT_FORCE_SIMT, SPEC_OPT_BIAS_PATH = 1, 2, 3
 DEV_BITS = {1: "BAD_TOKEN", 2: "BAD_LEN", 4: "BAD_TEMP", 8: "TIMEOUT", 16: "REFINED",
             32: "OVERFLOW"}
 
-EXPORTED = ("spec_workspace_bytes", "spec_markov_draft", "spec_verify", "spec_status_string",
+EXPORTED = ("spec_workspace_bytes", "spec_markov_draft", "spec_markov_draft_static",
+            "spec_verify", "spec_status_string",
             "spec_set_option", "spec_profile_enable", "spec_profile_read", "spec_stage_name",
             "spec_num_stages")
 
@@ -64,6 +65,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.spec_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
     L.spec_markov_draft.restype = _i32
     L.spec_markov_draft.argtypes = [ctypes.POINTER(DraftArgs), _vp]
+    L.spec_markov_draft_static.restype = _i32
+    L.spec_markov_draft_static.argtypes = [ctypes.POINTER(DraftArgs), _vp]
     L.spec_verify.restype = _i32
     L.spec_verify.argtypes = [ctypes.POINTER(VerifyArgs), _vp]
     L.spec_status_string.restype = ctypes.c_char_p
@@ -135,6 +138,18 @@ def spec_markov_draft(U, W1, W2, anchor, temperature, u_draft, draft_tokens, q_t
                   _ptr(q_tok), _ptr(lse_q), _ptr(dev_status), _ptr(diag), _ptr(workspace),
                   workspace.numel() * workspace.element_size())
     _check(lib().spec_markov_draft(ctypes.byref(a), _stream(stream)), "spec_markov_draft")
+
+
+def spec_markov_draft_static(U, W1, W2, anchor, temperature, u_draft, draft_tokens, q_tok,
+                             lse_q, dev_status, diag=None, stream=None) -> None:
+    """The draft with the library's built-in scratch area instead of a caller
+    workspace, for callers that cannot allocate device memory (see spec.h)."""
+    B, gamma, V = U.shape
+    a = DraftArgs(B, gamma, V, W1.shape[1], _dtype_code(U), _ptr(U), _ptr(W1), _ptr(W2),
+                  _ptr(anchor), _ptr(temperature), _ptr(u_draft), _ptr(draft_tokens),
+                  _ptr(q_tok), _ptr(lse_q), _ptr(dev_status), _ptr(diag), None, 0)
+    _check(lib().spec_markov_draft_static(ctypes.byref(a), _stream(stream)),
+           "spec_markov_draft_static")
 
 
 def spec_verify(target, U, W1, W2, anchor, temperature, draft_tokens, q_tok, lse_q, verify_len,

@@ -314,6 +314,91 @@ int run_verify(const spec_verify_args* a, cudaStream_t st) {
   return SPEC_OK;
 }
 
+// ---------------------------------------------------------------- static scratch
+// Scratch of spec_markov_draft_static: only the regions the draft touches.
+Layout draft_only_layout(const Shape& sh) {
+  Layout L = {};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = (off + bytes + 255) & ~(size_t)255;
+    return o;
+  };
+  L.max_items = sh.B;
+  L.ctrl = take(CTRL_WORDS * sizeof(uint32_t));
+  L.items = take((size_t)L.max_items * sizeof(HpItem));
+  L.hpsum = take((size_t)L.max_items * sh.HB * 3 * sizeof(double));
+  L.dpart = take((size_t)sh.B * sh.NS * sizeof(float4));
+  L.total = off;
+  return L;
+}
+
+Ws draft_only_views(const Layout& L, void* base) {
+  unsigned char* p = static_cast<unsigned char*>(base);
+  Ws w = {};
+  w.ctrl = reinterpret_cast<uint32_t*>(p + L.ctrl);
+  w.items = reinterpret_cast<HpItem*>(p + L.items);
+  w.max_items = L.max_items;
+  w.hpsum = reinterpret_cast<double*>(p + L.hpsum);
+  w.dpart = reinterpret_cast<float4*>(p + L.dpart);
+  return w;
+}
+
+template <typename DT>
+int run_draft_static(const spec_draft_args* a, void* scratch, cudaStream_t st) {
+  const Shape sh = make_shape(a->B, a->gamma, a->V, a->r);
+  const Layout L = draft_only_layout(sh);
+  const Ws ws = draft_only_views(L, scratch);
+  const Eps eps = current_eps();
+  int path;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    path = g_force_simt ? 0 : g_bias_path;
+  }
+  const int grid = grid_for_refine();
+  HpRows R{a->U, a->U, a->W1, a->W2, a->temperature};
+  SPEC_TRY(cudaMemsetAsync(a->dev_status, 0, 4 * sizeof(uint32_t), st));
+  SPEC_TRY(cudaMemsetAsync(ws.ctrl, 0, CTRL_WORDS * sizeof(uint32_t), st));
+  for (int k = 0; k < sh.gamma; ++k) {
+    SPEC_TRY(launch_draft_tile<DT>(sh, k, a->U, a->W1, a->W2, a->anchor, a->draft_tokens,
+                                   a->temperature, ws, path, a->dev_status, st));
+    SPEC_TRY(launch_draft_sample<DT>(sh, k, a->U, a->W1, a->W2, a->anchor, a->temperature,
+                                     a->u_draft, a->draft_tokens, a->q_tok, a->lse_q, a->diag,
+                                     a->dev_status, ws, eps, st));
+    SPEC_TRY(launch_hp_sums<DT>(sh, R, ws, 0, grid, st));
+    SPEC_TRY(launch_hp_decide<DT>(sh, R, ws, a->draft_tokens, a->q_tok, a->lse_q, nullptr,
+                                  a->dev_status, grid, st));
+  }
+  return SPEC_OK;
+}
+
+}  // namespace
+}  // namespace spec
+
+// The scratch area itself.  Host code must not use this symbol as a pointer:
+// on the host it names a stand-in object, so its device address is obtained
+// with cudaGetSymbolAddress once per device and passed to the kernels.
+static __device__ __align__(256) unsigned char g_spec_static_scratch[SPEC_STATIC_SCRATCH_BYTES];
+
+namespace spec {
+namespace {
+std::mutex g_static_mu;
+constexpr int kMaxDevices = 64;
+void* g_static_addr[kMaxDevices] = {};
+
+// Device address of the scratch area on the current device (cached).
+int static_scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ECUDA;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_spec_static_scratch) != cudaSuccess || !p) return SPEC_ECUDA;
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return SPEC_OK;
+}
 }  // namespace
 }  // namespace spec
 
@@ -365,6 +450,28 @@ int32_t spec_verify(const spec_verify_args* a, spec_stream_t stream) {
   if (!aligned(a->workspace, 256)) return SPEC_EALIGN;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return a->dtype == SPEC_BF16 ? run_verify<bf16>(a, st) : run_verify<float>(a, st);
+}
+
+int32_t spec_markov_draft_static(const spec_draft_args* a, spec_stream_t stream) {
+  if (!a) return SPEC_EINVAL;
+  int rc = check_shape(a->B, a->gamma, a->V, a->r, a->dtype);
+  if (rc != SPEC_OK) return rc;
+  if (!a->U || !a->W1 || !a->W2 || !a->anchor || !a->temperature || !a->u_draft ||
+      !a->draft_tokens || !a->q_tok || !a->lse_q || !a->dev_status)
+    return SPEC_EINVAL;
+  if (!aligned(a->U, 16) || !aligned(a->W1, 16) || !aligned(a->W2, 16) || !aligned(a->anchor, 4) ||
+      !aligned(a->temperature, 4) || !aligned(a->u_draft, 4) || !aligned(a->draft_tokens, 4) ||
+      !aligned(a->q_tok, 4) || !aligned(a->lse_q, 8) || !aligned(a->dev_status, 4) ||
+      (a->diag && !aligned(a->diag, 4)))
+    return SPEC_EALIGN;
+  if (draft_only_layout(make_shape(a->B, a->gamma, a->V, a->r)).total > SPEC_STATIC_SCRATCH_BYTES)
+    return SPEC_EWORKSPACE;
+  void* scratch = nullptr;
+  rc = static_scratch_address(&scratch);
+  if (rc != SPEC_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return a->dtype == SPEC_BF16 ? run_draft_static<bf16>(a, scratch, st)
+                               : run_draft_static<float>(a, scratch, st);
 }
 
 const char* spec_status_string(int32_t s) {
