@@ -186,8 +186,14 @@ const char* spec_status_string(int32_t status);
  *   SPEC_OPT_FORCE_SIMT  1 = compute the bias with plain fp32 FMAs
  *   SPEC_OPT_BIAS_PATH   tensor path of the bf16 bias tiles: 1 = warp MMA,
  *                        2 = tcgen05 with the accumulator in tensor memory
- *                        (default; used when r % 64 == 0)                   */
-enum { SPEC_OPT_EPS_SCALE = 1, SPEC_OPT_FORCE_SIMT = 2, SPEC_OPT_BIAS_PATH = 3 };
+ *                        (default; used when r % 64 == 0)
+ *   SPEC_OPT_DRAFT_MODE  0 = spec_markov_draft launches its kernels step by
+ *                        step; 1 (default) = the whole draft runs as one
+ *                        cooperative launch (all CTAs co-resident, bounded
+ *                        grid barriers; spec_markov_draft_static always uses
+ *                        the step-by-step kernels)                          */
+enum { SPEC_OPT_EPS_SCALE = 1, SPEC_OPT_FORCE_SIMT = 2, SPEC_OPT_BIAS_PATH = 3,
+       SPEC_OPT_DRAFT_MODE = 4 };
 int32_t spec_set_option(int32_t key, double value);
 
 /* Per-stage timing with CUDA events on the calls' streams.  enable(1)

@@ -16,6 +16,10 @@ template <typename DT>
 cudaError_t launch_draft_sample(const Shape&, int, const void*, const void*, const void*,
                                 const int*, const float*, const float*, int*, float*, double*,
                                 float*, uint32_t*, const Ws&, const Eps&, cudaStream_t);
+template <typename DT>
+cudaError_t launch_draft_persistent(const Shape&, const void*, const void*, const void*, const int*,
+                                    const float*, const float*, int*, float*, double*, float*,
+                                    uint32_t*, const Ws&, const Eps&, int, int, cudaStream_t);
 cudaError_t launch_verify_prep(const Shape&, const int*, const float*, const int*, const double*,
                                const int*, const Ws&, uint32_t*, int*, int*, float*, float*,
                                cudaStream_t);
@@ -46,6 +50,7 @@ std::mutex g_mu;
 double g_eps_scale = 1.0;
 bool g_force_simt = false;
 int g_bias_path = 2;          // 1 warp MMA, 2 tcgen05 (see SPEC_OPT_BIAS_PATH)
+int g_draft_mode = 1;         // 0 one launch per step, 1 persistent (SPEC_OPT_DRAFT_MODE)
 
 // Band constants (probability units); see DESIGN.md "Certified decisions".
 // Largest first-pass margin error seen against the float64 oracle over C0-C4
@@ -71,12 +76,12 @@ Eps current_eps() {
 
 // ---------------------------------------------------------------- profiling
 enum Stage {
-  ST_DRAFT_TILE, ST_DRAFT_SAMPLE, ST_DRAFT_HP_SUMS, ST_DRAFT_HP_DECIDE, ST_VERIFY_PREP,
+  ST_DRAFT_PERSISTENT, ST_DRAFT_TILE, ST_DRAFT_SAMPLE, ST_DRAFT_HP_SUMS, ST_DRAFT_HP_DECIDE, ST_VERIFY_PREP,
   ST_TARGET_STATS, ST_VERIFY_TILE, ST_VERIFY_FINAL, ST_SLOW_VERIFY, ST_VERIFY_HP_SUMS,
   ST_VERIFY_HP_RESID, ST_VERIFY_HP_DECIDE, ST_COUNT
 };
 const char* kStageNames[ST_COUNT] = {
-    "draft_tile", "draft_sample", "draft_hp_sums", "draft_hp_decide", "verify_prep",
+    "draft_persistent", "draft_tile", "draft_sample", "draft_hp_sums", "draft_hp_decide", "verify_prep",
     "target_stats", "verify_tile", "verify_final", "slow_verify", "verify_hp_sums",
     "verify_hp_resid", "verify_hp_decide"};
 bool g_prof = false;
@@ -119,7 +124,9 @@ struct ProfScope {
 };
 
 int g_num_sms = -1;
-int grid_for_refine() {
+int num_sms();
+int grid_for_refine() { return 2 * num_sms(); }
+int num_sms() {
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_num_sms < 0) {
     int dev = 0, n = 0;
@@ -128,7 +135,7 @@ int grid_for_refine() {
       n = 132;
     g_num_sms = n;
   }
-  return 2 * g_num_sms;
+  return g_num_sms;
 }
 
 // ---------------------------------------------------------------- workspace
@@ -231,7 +238,20 @@ int run_draft(const spec_draft_args* a, cudaStream_t st) {
   }
   const int grid = grid_for_refine();
   HpRows R{a->U, a->U, a->W1, a->W2, a->temperature};
+  int mode;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    mode = g_draft_mode;
+  }
   SPEC_TRY(cudaMemsetAsync(a->dev_status, 0, 4 * sizeof(uint32_t), st));
+  if (mode == 1) {
+    SPEC_TRY(cudaMemsetAsync(ws.ctrl, 0, CTRL_WORDS * sizeof(uint32_t), st));
+    ProfScope p(st, ST_DRAFT_PERSISTENT);
+    SPEC_TRY(launch_draft_persistent<DT>(sh, a->U, a->W1, a->W2, a->anchor, a->temperature,
+                                         a->u_draft, a->draft_tokens, a->q_tok, a->lse_q, a->diag,
+                                         a->dev_status, ws, eps, path, num_sms(), st));
+    return SPEC_OK;
+  }
   for (int k = 0; k < sh.gamma; ++k) {
     {
       ProfScope p(st, ST_DRAFT_TILE);
@@ -499,6 +519,10 @@ int32_t spec_set_option(int32_t key, double value) {
     case SPEC_OPT_BIAS_PATH:
       if (value != 1.0 && value != 2.0) return SPEC_EINVAL;
       g_bias_path = (int)value;
+      return SPEC_OK;
+    case SPEC_OPT_DRAFT_MODE:
+      if (value != 0.0 && value != 1.0) return SPEC_EINVAL;
+      g_draft_mode = (int)value;
       return SPEC_OK;
     default:
       return SPEC_EINVAL;

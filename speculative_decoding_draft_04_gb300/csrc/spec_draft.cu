@@ -15,29 +15,38 @@
 //                        first pass's error band of a CDF breakpoint are queued for
 //                        re-decision in extended precision (spec_refine.cu).
 #include "spec_tc.cuh"
+#include "spec_hp.cuh"
 
 namespace spec {
 
-// PATH: 0 = SIMT fp32 FMAs, 1 = warp MMA (mma.sync), 2 = tcgen05 / TMEM (BM = 128).
+// Tensor-memory context of a CTA: accumulator columns, MMA-completion
+// mbarrier and the parity of its next phase.
+struct TcCtx {
+  uint32_t taddr;
+  uint64_t* bar;
+  uint32_t phase;
+};
+
+// One (request tile, slice) of draft step k.  PATH: 0 = SIMT fp32 FMAs,
+// 1 = warp MMA (mma.sync), 2 = tcgen05 / TMEM (BM = 128; `tc` set up by the
+// caller).  Returns false if the MMA did not complete within the bound.
+// Tokens written by other CTAs of the same launch are read through L2.
 template <typename DT, int BM, int PATH>
-__global__ void __launch_bounds__(NT) draft_tile_kernel(Shape sh, int k, const DT* __restrict__ U,
-                                                        const DT* __restrict__ W1,
-                                                        const DT* __restrict__ W2,
-                                                        const int* __restrict__ anchor,
-                                                        const int* __restrict__ tokens,
-                                                        const float* __restrict__ temp, Ws ws,
-                                                        uint32_t* status) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+__device__ bool draft_tile_body(const Shape& sh, int k, int slice, int mtile, const DT* __restrict__ U,
+                                const DT* __restrict__ W1, const DT* __restrict__ W2,
+                                const int* __restrict__ anchor, const int* tokens,
+                                const float* __restrict__ temp, const Ws& ws, uint32_t* status,
+                                unsigned char* smem_raw, TcCtx* tc) {
   __shared__ int s_tok[BM];
   __shared__ size_t s_off[BM];
-  const int slice = blockIdx.x, m0 = blockIdx.y * BM, n0 = slice * BN;
+  const int m0 = mtile * BM, n0 = slice * BN;
   const int nrows = min(BM, sh.B - m0);
-  if (slice == 0 && blockIdx.y == 0 && threadIdx.x == 0) ws.ctrl[CTRL_ITEMS] = 0;
+  __syncthreads();      // previous use of the shared buffers is finished
   for (int m = threadIdx.x; m < BM; m += NT) {
     int t = 0;
     if (m < nrows) {
       int b = m0 + m;
-      t = (k == 0) ? anchor[b] : tokens[(size_t)b * sh.gamma + k - 1];
+      t = (k == 0) ? anchor[b] : __ldcg(tokens + (size_t)b * sh.gamma + k - 1);
       t = min(max(t, 0), sh.V - 1);          // bad tokens are reported by the sampler
       s_off[m] = ((size_t)b * sh.gamma + k) * sh.V;
     } else {
@@ -57,10 +66,6 @@ __global__ void __launch_bounds__(NT) draft_tile_kernel(Shape sh, int k, const D
     Us = reinterpret_cast<DT*>(smem + lay.offU);
     stage = reinterpret_cast<float*>(smem + lay.offStage);
     su = BN + 8;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + lay.offBar);
-    uint32_t* holder = reinterpret_cast<uint32_t*>(smem + lay.offBar + 8);
-    if (threadIdx.x == 0) mbar_init(bar, 1);
-    if (threadIdx.x < 32) tc_alloc(holder, TC_TMEM_COLS);
     __syncthreads();
     tc_load_A(As, reinterpret_cast<const bf16*>(W1), s_tok, nrows, sh.r);
     tc_load_W2(Wsm, reinterpret_cast<const bf16*>(W2), sh.V, n0, sh.r);
@@ -70,15 +75,14 @@ __global__ void __launch_bounds__(NT) draft_tile_kernel(Shape sh, int k, const D
     fence_async_shared();
     tc_fence_before();
     __syncthreads();
-    const uint32_t taddr = *holder;
-    const bool ok = bias_tile_tc(As, Wsm, sh.r, taddr, bar, stage);
+    const bool ok = bias_tile_tc(As, Wsm, sh.r, tc->taddr, tc->bar, tc->phase, stage);
     if (!ok) {
       if (threadIdx.x == 0) set_status(status, SPEC_DEV_TIMEOUT);
-      mbar_wait(bar, 0, 1u << 22);     // let an in-flight MMA drain before freeing TMEM
+      mbar_wait(tc->bar, tc->phase, 1u << 22);   // let an in-flight MMA drain
+      tc->phase ^= 1u;
+      return false;
     }
-    __syncthreads();
-    if (threadIdx.x < 32) tc_dealloc(taddr, TC_TMEM_COLS);
-    if (!ok) return;
+    tc->phase ^= 1u;
     __syncthreads();
   } else {
     const TileLayout<DT> lay(BM, sh.r, false);
@@ -127,6 +131,7 @@ __global__ void __launch_bounds__(NT) draft_tile_kernel(Shape sh, int k, const D
   q2 = group_sum<TPR>(q2);
   if (rowok && part == 0)
     ws.dpart[(size_t)b * sh.NS + slice] = make_float4(c, xm, df_d(s) /*rounded*/, q2);
+  return true;
 }
 
 // Weighted slice mass relative to the row's largest slice reference, in units
@@ -136,13 +141,17 @@ __device__ __forceinline__ float slice_factor(float4 p, float cM, float mM, floa
   return expf(a);
 }
 
+// Draw token x_{k+1} of request b from its slice partials (one CTA).  Queues
+// the draw on `counter` / ws.items when it lies inside the error band.
+// `dsm` holds an r x BN slab.  Partials and tokens written by other CTAs of
+// the same launch are read through L2.
 template <typename DT>
-__global__ void __launch_bounds__(NT) draft_sample_kernel(
-    Shape sh, int k, const DT* __restrict__ U, const DT* __restrict__ W1, const DT* __restrict__ W2,
-    const int* __restrict__ anchor, const float* __restrict__ temp,
-    const float* __restrict__ u_draft, int* tokens, float* q_tok, double* lse_q, float* diag,
-    uint32_t* status, Ws ws, Eps eps) {
-  extern __shared__ __align__(16) unsigned char dsm[];
+__device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __restrict__ U,
+                                  const DT* __restrict__ W1, const DT* __restrict__ W2,
+                                  const int* __restrict__ anchor, const float* __restrict__ temp,
+                                  const float* __restrict__ u_draft, int* tokens, float* q_tok,
+                                  double* lse_q, float* diag, uint32_t* status, const Ws& ws,
+                                  const Eps& eps, uint32_t* counter, unsigned char* dsm) {
   DT* slab = reinterpret_cast<DT*>(dsm);      // [r][BN] W2 slab of the crossing slice
   __shared__ float sh_f[72];
   __shared__ float s_a[256];
@@ -151,9 +160,9 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
   __shared__ float s_pref[2];
   __shared__ float s_w[BN];
 
-  const int b = blockIdx.x;
+  __syncthreads();      // previous use of the shared buffers is finished
   const size_t ok = (size_t)b * sh.gamma + k;
-  const int prev = (k == 0) ? anchor[b] : tokens[ok - 1];
+  const int prev = (k == 0) ? anchor[b] : __ldcg(tokens + ok - 1);
   const float T = temp[b];
   if (prev < 0 || prev >= sh.V || !temp_ok(T)) {
     if (threadIdx.x == 0) {
@@ -167,6 +176,7 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
   }
   const float invT = 1.0f / T;
   const float4* P = ws.dpart + (size_t)b * sh.NS;
+  auto part = [&](int s) { return __ldcg(P + s); };
 
   // ---- reference slice: largest c/T + m (ties: any; only a shift)
   const int per = (sh.NS + NT - 1) / NT;
@@ -174,7 +184,7 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
   float best = -INFINITY;
   int bidx = 0;
   for (int s = s0; s < s1; ++s) {
-    float4 p = P[s];
+    float4 p = part(s);
     float key = fmaf(p.x, invT, p.y);
     if (key > best) { best = key; bidx = s; }
   }
@@ -191,7 +201,7 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
     s_slice = c2;
   }
   __syncthreads();
-  const float4 PM = P[s_slice];
+  const float4 PM = part(s_slice);
   const float cM = PM.x, mM = PM.y;
   __syncthreads();
 
@@ -199,7 +209,7 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
   df loc = {0.f, 0.f};
   float q2 = 0.f, m2 = 0.f;
   for (int s = s0; s < s1; ++s) {
-    float4 p = P[s];
+    float4 p = part(s);
     float f = slice_factor(p, cM, mM, invT);
     float w = p.z * f;
     loc = df_addf(loc, w);
@@ -224,7 +234,7 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
     df tneg = df_neg(target);
     if (df_d(df_add(excl, tneg)) <= 0.0 && df_d(df_add(df_add(excl, loc), tneg)) > 0.0) {
       for (int s = s0; s < s1; ++s) {
-        float4 p = P[s];
+        float4 p = part(s);
         df nxt = df_addf(run, p.z * slice_factor(p, cM, mM, invT));
         if (df_d(df_add(nxt, tneg)) > 0.0) {
           my_slice = s;
@@ -248,7 +258,7 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
     fallback = true;
     if (threadIdx.x == 0) {
       int sl = sh.NS - 1;
-      while (sl > 0 && !(P[sl].z > 0.f)) --sl;
+      while (sl > 0 && !(part(sl).z > 0.f)) --sl;
       s_slice = sl;
     }
     __syncthreads();
@@ -256,7 +266,7 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
     df run = {0.f, 0.f};
     if (threadIdx.x == 0) {
       for (int s = 0; s < s_slice; ++s) {
-        float4 p = P[s];
+        float4 p = part(s);
         run = df_addf(run, p.z * slice_factor(p, cM, mM, invT));
       }
       s_pref[0] = run.hi;
@@ -266,7 +276,7 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
   }
   const int sl = s_slice;
   const df pref = {s_pref[0], s_pref[1]};
-  const float4 PS = P[sl];
+  const float4 PS = part(sl);
   const float fS = slice_factor(PS, cM, mM, invT);
 
   // ---- recompute the slice's weights (bias by SIMT: two halves of k, W2 slab in smem)
@@ -343,7 +353,7 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
       diag[ok * 4 + 3] = (float)tok;
     }
     if (fallback || dmargin <= band) {
-      uint32_t it = atomicAdd(&ws.ctrl[CTRL_ITEMS], 1u);
+      uint32_t it = atomicAdd(counter, 1u);
       if ((int)it < ws.max_items) {
         HpItem h;
         h.b = b; h.j = k; h.kind = HP_DRAFT; h.prev = prev; h.u = u; h.fast_token = tok;
@@ -353,6 +363,127 @@ __global__ void __launch_bounds__(NT) draft_sample_kernel(
         set_status(status, SPEC_DEV_OVERFLOW);
       }
     }
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- kernels
+// One launch per step: tiles (grid = slices x request tiles).
+template <typename DT, int BM, int PATH>
+__global__ void __launch_bounds__(NT) draft_tile_kernel(Shape sh, int k, const DT* __restrict__ U,
+                                                        const DT* __restrict__ W1,
+                                                        const DT* __restrict__ W2,
+                                                        const int* __restrict__ anchor,
+                                                        const int* __restrict__ tokens,
+                                                        const float* __restrict__ temp, Ws ws,
+                                                        uint32_t* status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ uint64_t s_bar;
+  __shared__ uint32_t s_holder;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) ws.ctrl[CTRL_ITEMS] = 0;
+  TcCtx tc{0u, &s_bar, 0u};
+  if constexpr (PATH == 2) {
+    if (threadIdx.x == 0) mbar_init(&s_bar, 1);
+    if (threadIdx.x < 32) tc_alloc(&s_holder, TC_TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    tc.taddr = s_holder;
+  }
+  draft_tile_body<DT, BM, PATH>(sh, k, blockIdx.x, blockIdx.y, U, W1, W2, anchor, tokens, temp, ws,
+                                status, smem_raw, &tc);
+  if constexpr (PATH == 2) {
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) tc_dealloc(tc.taddr, TC_TMEM_COLS);
+  }
+}
+
+// One launch per step: one CTA per request.
+template <typename DT>
+__global__ void __launch_bounds__(NT) draft_sample_kernel(
+    Shape sh, int k, const DT* __restrict__ U, const DT* __restrict__ W1, const DT* __restrict__ W2,
+    const int* __restrict__ anchor, const float* __restrict__ temp,
+    const float* __restrict__ u_draft, int* tokens, float* q_tok, double* lse_q, float* diag,
+    uint32_t* status, Ws ws, Eps eps) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  draft_sample_body<DT>(sh, k, blockIdx.x, U, W1, W2, anchor, temp, u_draft, tokens, q_tok, lse_q,
+                        diag, status, ws, eps, ws.ctrl + CTRL_ITEMS, dsm);
+}
+
+struct DraftParams {
+  Shape sh;
+  const void* U;
+  const void* W1;
+  const void* W2;
+  const int* anchor;
+  const float* temp;
+  const float* u_draft;
+  int* tokens;
+  float* q_tok;
+  double* lse_q;
+  float* diag;
+  uint32_t* status;
+  Ws ws;
+  Eps eps;
+};
+
+// The whole draft in one cooperative launch: for each step k, the tile phase
+// (tiles strided over the CTAs), a grid barrier, the sampling phase (requests
+// strided over the CTAs), a grid barrier, and -- only when that step queued
+// near-boundary draws -- the two extended-precision phases, each followed by
+// a grid barrier.  Tensor memory is allocated once per CTA.
+template <typename DT, int BM, int PATH>
+__global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(DraftParams P) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ uint64_t s_bar;
+  __shared__ uint32_t s_holder;
+  const Shape& sh = P.sh;
+  const DT* U = (const DT*)P.U;
+  const DT* W1 = (const DT*)P.W1;
+  const DT* W2 = (const DT*)P.W2;
+  uint32_t* ctrl = P.ws.ctrl;
+  TcCtx tc{0u, &s_bar, 0u};
+  if constexpr (PATH == 2) {
+    if (threadIdx.x == 0) mbar_init(&s_bar, 1);
+    if (threadIdx.x < 32) tc_alloc(&s_holder, TC_TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    tc.taddr = s_holder;
+  }
+  uint32_t gen = threadIdx.x == 0 ? ld_acquire_gpu(ctrl + CTRL_BAR_GEN) : 0u;
+  const HpRows R{P.U, P.U, P.W1, P.W2, P.temp};
+  const int n_mt = (sh.B + BM - 1) / BM;
+  const int n_tiles = sh.NS * n_mt;
+  const uint32_t G = gridDim.x;
+  for (int k = 0; k < sh.gamma; ++k) {
+    bool ok = true;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += G)
+      ok = draft_tile_body<DT, BM, PATH>(sh, k, t % sh.NS, t / sh.NS, U, W1, W2, P.anchor, P.tokens,
+                                         P.temp, P.ws, P.status, smem_raw, &tc);
+    if (!ok) {
+      if (threadIdx.x == 0) atomicExch(ctrl + CTRL_ABORT, 1u);
+      break;
+    }
+    if (!grid_sync(ctrl, G, gen, P.status)) break;
+    for (int b = blockIdx.x; b < sh.B; b += G)
+      draft_sample_body<DT>(sh, k, b, U, W1, W2, P.anchor, P.temp, P.u_draft, P.tokens, P.q_tok,
+                            P.lse_q, P.diag, P.status, P.ws, P.eps, ctrl + CTRL_STEP0 + k,
+                            smem_raw);
+    if (!grid_sync(ctrl, G, gen, P.status)) break;
+    const int n = min((int)__ldcg(ctrl + CTRL_STEP0 + k), P.ws.max_items);
+    if (n > 0) {
+      hp_sums_body<DT>(sh, R, P.ws, 0, n, smem_raw);
+      if (!grid_sync(ctrl, G, gen, P.status)) break;
+      hp_decide_body<DT>(sh, R, P.ws, n, P.tokens, P.q_tok, P.lse_q, nullptr, P.status, smem_raw);
+      if (!grid_sync(ctrl, G, gen, P.status)) break;
+    }
+  }
+  if constexpr (PATH == 2) {
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) tc_dealloc(tc.taddr, TC_TMEM_COLS);
   }
 }
 
@@ -410,6 +541,67 @@ cudaError_t launch_draft_sample(const Shape& sh, int k, const void* U, const voi
   return cudaGetLastError();
 }
 
+template <typename DT, int BM, int PATH>
+static cudaError_t launch_persist(const DraftParams& P, int nsm, cudaStream_t st) {
+  size_t smem = PATH == 2 ? TcLayout(P.sh.r, false).total : TileLayout<DT>(BM, P.sh.r, false).total;
+  smem = smem > (size_t)P.sh.r * HPB * sizeof(DT) ? smem : (size_t)P.sh.r * HPB * sizeof(DT);
+  auto kern = draft_persistent_kernel<DT, BM, PATH>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int n_tiles = P.sh.NS * ((P.sh.B + BM - 1) / BM);
+  int G = nsm;                             // one CTA per SM (all must be co-resident)
+  G = G < n_tiles ? G : n_tiles;
+  G = G > P.sh.B ? G : (P.sh.B < nsm ? P.sh.B : nsm);
+  G = G < 1 ? 1 : G;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+// Whole draft in one cooperative launch (the control words must be zeroed).
+template <typename DT>
+cudaError_t launch_draft_persistent(const Shape& sh, const void* U, const void* W1, const void* W2,
+                                    const int* anchor, const float* temp, const float* u_draft,
+                                    int* tokens, float* q_tok, double* lse_q, float* diag,
+                                    uint32_t* status, const Ws& ws, const Eps& eps, int path,
+                                    int nsm, cudaStream_t st) {
+  DraftParams P{sh, U, W1, W2, anchor, temp, u_draft, tokens, q_tok, lse_q, diag, status, ws, eps};
+  const int BM = sh.B <= 32 ? 32 : (sh.B <= 64 ? 64 : 128);
+  if (path == 0 || sizeof(DT) == 4) {
+    if (BM == 32) return launch_persist<DT, 32, 0>(P, nsm, st);
+    if (BM == 64) return launch_persist<DT, 64, 0>(P, nsm, st);
+    return launch_persist<DT, 128, 0>(P, nsm, st);
+  }
+  if constexpr (sizeof(DT) == 2) {
+    if (path == 2 && sh.r % 64 == 0) return launch_persist<DT, 128, 2>(P, nsm, st);
+  }
+  if (BM == 32) return launch_persist<DT, 32, 1>(P, nsm, st);
+  if (BM == 64) return launch_persist<DT, 64, 1>(P, nsm, st);
+  return launch_persist<DT, 128, 1>(P, nsm, st);
+}
+
+template cudaError_t launch_draft_persistent<float>(const Shape&, const void*, const void*,
+                                                    const void*, const int*, const float*,
+                                                    const float*, int*, float*, double*, float*,
+                                                    uint32_t*, const Ws&, const Eps&, int, int,
+                                                    cudaStream_t);
+template cudaError_t launch_draft_persistent<bf16>(const Shape&, const void*, const void*,
+                                                   const void*, const int*, const float*,
+                                                   const float*, int*, float*, double*, float*,
+                                                   uint32_t*, const Ws&, const Eps&, int, int,
+                                                   cudaStream_t);
 template cudaError_t launch_draft_tile<float>(const Shape&, int, const void*, const void*,
                                               const void*, const int*, const int*, const float*,
                                               const Ws&, int, uint32_t*, cudaStream_t);

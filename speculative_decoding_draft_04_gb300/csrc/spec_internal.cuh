@@ -33,7 +33,12 @@ struct HpItem {
 };
 
 // Control words at the start of the workspace.
-enum { CTRL_ITEMS = 0, CTRL_SLOW = 1, CTRL_NPACKED = 2, CTRL_WORDS = 16 };
+//   CTRL_BAR_COUNT / CTRL_BAR_GEN / CTRL_ABORT: grid barrier of the persistent
+//   draft kernel; CTRL_STEP0 + k: queued re-decisions of draft step k.
+enum {
+  CTRL_ITEMS = 0, CTRL_SLOW = 1, CTRL_NPACKED = 2, CTRL_BAR_COUNT = 3, CTRL_BAR_GEN = 4,
+  CTRL_ABORT = 5, CTRL_STEP0 = 8, CTRL_WORDS = 32
+};
 
 // Workspace views (host computes the offsets; see spec_abi.cu).
 struct Ws {
@@ -287,5 +292,51 @@ __device__ __forceinline__ void set_status(uint32_t* st, uint32_t bits) {
   if (st) atomicOr(st, bits);
 }
 __device__ __forceinline__ bool temp_ok(float T) { return isfinite(T) && T > 0.f; }
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Barrier across all CTAs of a cooperative launch (all co-resident).  Thread 0
+// of each CTA arrives on a counter; the last arrival resets it and advances
+// the generation word the others wait on.  Every wait is bounded: on timeout,
+// or when another CTA has aborted, it sets SPEC_DEV_TIMEOUT / the abort word
+// and returns false, and the caller leaves the kernel.  `gen` is thread 0's
+// copy of the generation (read once at kernel start).
+__device__ __forceinline__ bool grid_sync(uint32_t* ctrl, uint32_t nblocks, uint32_t& gen,
+                                          uint32_t* status) {
+  __shared__ int s_gs_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const uint32_t g = gen;
+    __threadfence();
+    const uint32_t arrived = atomicAdd(ctrl + CTRL_BAR_COUNT, 1u);
+    if (arrived == nblocks - 1) {
+      atomicExch(ctrl + CTRL_BAR_COUNT, 0u);
+      __threadfence();
+      atomicAdd(ctrl + CTRL_BAR_GEN, 1u);
+    } else {
+      uint32_t it = 0;
+      while (ld_acquire_gpu(ctrl + CTRL_BAR_GEN) == g) {
+        if (ld_acquire_gpu(ctrl + CTRL_ABORT) != 0u) { ok = 0; break; }
+        if (++it > (1u << 24)) {
+          ok = 0;
+          atomicExch(ctrl + CTRL_ABORT, 1u);
+          set_status(status, SPEC_DEV_TIMEOUT);
+          break;
+        }
+        if (it > 32) __nanosleep(40);
+      }
+    }
+    __threadfence();
+    gen = g + 1;
+    s_gs_ok = ok;
+  }
+  __syncthreads();
+  return s_gs_ok != 0;
+}
 
 }  // namespace spec

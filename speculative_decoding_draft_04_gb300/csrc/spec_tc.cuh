@@ -161,12 +161,13 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
 
 // ---------------------------------------------------------------- the tile
 // Preconditions: A and W2 staged (cp.async complete, fence.proxy.async issued,
-// CTA synchronised), TMEM allocated at `taddr`, `bar` initialised.
+// CTA synchronised), TMEM allocated at `taddr`, `bar` initialised and
+// `parity` the phase this commit will complete.
 // Writes the 128 x 128 fp32 tile to `stage` (row stride SS floats), which may
 // alias A and W2.  Returns false (and leaves `stage` unspecified) if the MMA
 // did not complete within the bound.
 __device__ __forceinline__ bool bias_tile_tc(const bf16* As, const bf16* Ws, int r, uint32_t taddr,
-                                             uint64_t* bar, float* stage) {
+                                             uint64_t* bar, uint32_t parity, float* stage) {
   constexpr int SS = TileLayout<bf16>::SS;
   if (threadIdx.x == 0) {
     tc_fence_after();
@@ -180,7 +181,7 @@ __device__ __forceinline__ bool bias_tile_tc(const bf16* As, const bf16* Ws, int
     tc_commit(bar);
   }
   __syncwarp();
-  const bool ok = mbar_wait(bar, 0, 1u << 22);
+  const bool ok = mbar_wait(bar, parity, 1u << 22);
   tc_fence_after();
   // all threads must agree before the operands are overwritten
   const bool all_ok = __syncthreads_and(ok ? 1 : 0);

@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(NT) verify_tile_kernel(Shape sh, const DT* __r
     tc_fence_before();
     __syncthreads();
     const uint32_t taddr = *holder;
-    const bool ok = bias_tile_tc(As, Wsm, sh.r, taddr, bar, stage);
+    const bool ok = bias_tile_tc(As, Wsm, sh.r, taddr, bar, 0, stage);
     if (!ok) {
       if (threadIdx.x == 0) set_status(status, SPEC_DEV_TIMEOUT);
       mbar_wait(bar, 0, 1u << 22);

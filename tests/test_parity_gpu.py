@@ -270,3 +270,69 @@ def test_tcgen05_full_size(tc_path, name, sample):
     print(name, "tcgen05", rep.summary(), g.dstatus, g.vstatus)
     assert g.dstatus[0] & 8 == 0 and g.vstatus[0] & 8 == 0
     assert_parity(rep)
+
+
+# ----------------------------------------------------------------------------- persistent draft
+
+@pytest.fixture()
+def persistent():
+    _lib.spec_set_option(_lib.SPEC_OPT_DRAFT_MODE, 1)
+    yield
+    _lib.spec_set_option(_lib.SPEC_OPT_DRAFT_MODE, 1)
+
+
+@pytest.fixture()
+def per_step():
+    _lib.spec_set_option(_lib.SPEC_OPT_DRAFT_MODE, 0)
+    yield
+    _lib.spec_set_option(_lib.SPEC_OPT_DRAFT_MODE, 1)
+
+
+@pytest.mark.parametrize("spec_name", ["C0", "small", "adversarial"])
+def test_per_step_draft_parity(per_step, spec_name):
+    """The step-by-step draft launches stay selectable and exact."""
+    spec = {"C0": W.config("C0"), "small": SMALL, "adversarial": dict(SMALL, B=24)}[spec_name]
+    w = W.make_workload(spec, trial=6)
+    if spec_name == "adversarial":
+        res = oracle_cycle(w)
+        for b in range(w.B):
+            w.u_draft[b, 1] = _near(res.draft[b].F_hi[1])
+    g, res, rep = run_and_compare(w)
+    assert_parity(rep)
+
+
+@pytest.mark.parametrize("spec_name", ["C0", "small", "stress", "tc-two-tiles"])
+def test_persistent_draft_parity(persistent, spec_name):
+    """The whole draft as one cooperative launch (grid barriers between the
+    tile, sampling and re-decision phases of every step)."""
+    spec = {"C0": W.config("C0"), "small": SMALL, "stress": W.stress(SMALL),
+            "tc-two-tiles": dict(SMALL, B=130, r=256, gamma=4, L=("uniform", 0, 4))}[spec_name]
+    for trial in range(3):
+        w = W.make_workload(spec, trial=trial)
+        g, res, rep = run_and_compare(w)
+        assert g.dstatus[0] & 8 == 0, "grid barrier or MMA wait timed out"
+        assert_parity(rep)
+
+
+def test_persistent_adversarial(persistent):
+    w = W.make_workload(dict(SMALL, B=24, name="adv-p"), trial=5)
+    res = oracle_cycle(w)
+    for b in range(w.B):
+        for k in range(w.gamma):
+            if (b + k) % 3 == 0:
+                w.u_draft[b, k] = _near(res.draft[b].F_hi[k] if b % 2 else res.draft[b].F_lo[k])
+    g, res2, rep = run_and_compare(w)
+    assert_parity(rep)
+    assert g.dstatus[1] > 0 and g.dstatus[0] & 8 == 0
+
+
+@pytest.mark.parametrize("name,sample", [("C1", None), ("C2", 24), ("C3", 3), ("C4", 5)])
+def test_persistent_full_size(persistent, name, sample):
+    w = W.make_workload(W.config(name), trial=2)
+    rows = None
+    if sample is not None:
+        rows = sorted(np.random.default_rng(9).choice(w.B, size=sample, replace=False).tolist())
+    g, res, rep = run_and_compare(w, rows=rows)
+    print(name, "persistent", rep.summary(), g.dstatus)
+    assert g.dstatus[0] & 8 == 0
+    assert_parity(rep)
