@@ -43,8 +43,6 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--draft-mode", type=int, default=1, choices=[0, 1],
-                    help="0: one launch per draft step; 1: one persistent cooperative launch")
     return ap.parse_args()
 
 
@@ -74,7 +72,6 @@ def algorithmic_bytes(w):
     verify = int((L + 1).sum()) * w.V * s + int(L.sum()) * w.V * s + w.r * w.V * s
     per_stage = {
         "draft_persistent": draft,                                  # per launch (whole draft)
-        "draft_tile": w.B * w.V * s + w.r * w.V * s / w.gamma,     # per launch (one step)
         "target_stats": int((L + 1).sum()) * w.V * s,
         "verify_tile": int(L.sum()) * w.V * s + w.r * w.V * s,
     }
@@ -220,7 +217,6 @@ def main():
     from speculative_decoding_draft_04_gb300 import _lib, build, engine
     from speculative_decoding_draft_04_gb300 import workloads as W
     build.build()
-    _lib.spec_set_option(_lib.SPEC_OPT_DRAFT_MODE, args.draft_mode)
     w = W.make_workload(W.config(args.config), trial=rank)
     d = engine.DeviceWorkload.from_workload(w, dev)
     bufs = engine.Buffers.for_workload(d, dev)
@@ -324,7 +320,6 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": args.config + ": " + W.CONFIG_DESCRIPTIONS[args.config],
-                       "draft_mode": ["per-step launches", "persistent"][args.draft_mode],
                        "l2": f"flushed between steps ({flush.numel() >> 20} MiB write, outside the events)",
                        "positions_per_step": positions},
             "hbm": {"cycle_algorithmic_bytes": draft_b + verify_b, "cycle_gbs": cyc_gbs,

@@ -140,7 +140,12 @@ typedef struct {
 size_t spec_workspace_bytes(int32_t B, int32_t gamma, int32_t V, int32_t r, int32_t dtype);
 
 /* Draft gamma tokens per request.  Reads U, W1, W2, anchor, temperature,
- * u_draft; writes draft_tokens, q_tok, lse_q, dev_status (and diag).       */
+ * u_draft; writes draft_tokens, q_tok, lse_q, dev_status (and diag).
+ * The work is two cudaMemsetAsync (dev_status, the workspace's control
+ * words) and ONE cooperative kernel launch on `stream` with one CTA per SM
+ * (fewer when there are fewer tiles); it returns SPEC_ECUDA when the device
+ * cannot make the CTAs co-resident.  Its grid barriers are bounded waits: a
+ * barrier that gives up sets SPEC_DEV_TIMEOUT and every CTA returns.       */
 int32_t spec_markov_draft(const spec_draft_args* args, spec_stream_t stream);
 
 /* Verify one drafted block per request.  Writes accept_len, out_tokens,
@@ -162,10 +167,10 @@ int32_t spec_verify(const spec_verify_args* args, spec_stream_t stream);
  * process exits.  It never calls cudaMalloc, cudaFree or any allocating
  * library routine.
  *
- *   - Size limit: the draft scratch is 64 + B*40 + B*ceil(V/256)*24 +
- *     B*ceil(V/128)*16 bytes (each term rounded up to 256); larger problems
+ *   - Size limit: the draft scratch is 128 + B*40 + B*ceil(V/256)*24 +
+ *     B*ceil(V/32)*16 bytes (each term rounded up to 256); larger problems
  *     are rejected with SPEC_EWORKSPACE before anything is enqueued.  All five
- *     named workloads fit (C4, the largest, needs about 7 MiB).
+ *     named workloads fit (C4, the largest, needs about 19 MiB).
  *   - The first call on a device looks up the area's device address with
  *     cudaGetSymbolAddress (with that device current) and caches it; make
  *     that first call before any stream capture.
@@ -174,7 +179,7 @@ int32_t spec_verify(const spec_verify_args* args, spec_stream_t stream);
  *     Calls whose GPU work overlaps -- on different streams, or from
  *     different threads without ordering -- race on it: serialise them.
  */
-#define SPEC_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+#define SPEC_STATIC_SCRATCH_BYTES ((size_t)24 << 20)
 int32_t spec_markov_draft_static(const spec_draft_args* args, spec_stream_t stream);
 
 /* Static text for a spec_status value. */
@@ -187,13 +192,10 @@ const char* spec_status_string(int32_t status);
  *   SPEC_OPT_BIAS_PATH   tensor path of the bf16 bias tiles: 1 = warp MMA,
  *                        2 = tcgen05 with the accumulator in tensor memory
  *                        (default; used when r % 64 == 0)
- *   SPEC_OPT_DRAFT_MODE  0 = spec_markov_draft launches its kernels step by
- *                        step; 1 (default) = the whole draft runs as one
- *                        cooperative launch (all CTAs co-resident, bounded
- *                        grid barriers; spec_markov_draft_static always uses
- *                        the step-by-step kernels)                          */
+ *   SPEC_OPT_TRACE       1 = the persistent draft records globaltimer stamps
+ *                        of its phase boundaries in the workspace (profiling) */
 enum { SPEC_OPT_EPS_SCALE = 1, SPEC_OPT_FORCE_SIMT = 2, SPEC_OPT_BIAS_PATH = 3,
-       SPEC_OPT_DRAFT_MODE = 4 };
+       SPEC_OPT_TRACE = 5 };   /* 4 is unused */
 int32_t spec_set_option(int32_t key, double value);
 
 /* Per-stage timing with CUDA events on the calls' streams.  enable(1)

@@ -10,13 +10,6 @@ namespace spec {
 
 // launchers (spec_draft.cu, spec_verify.cu, spec_refine.cu)
 template <typename DT>
-cudaError_t launch_draft_tile(const Shape&, int, const void*, const void*, const void*, const int*,
-                              const int*, const float*, const Ws&, int, uint32_t*, cudaStream_t);
-template <typename DT>
-cudaError_t launch_draft_sample(const Shape&, int, const void*, const void*, const void*,
-                                const int*, const float*, const float*, int*, float*, double*,
-                                float*, uint32_t*, const Ws&, const Eps&, cudaStream_t);
-template <typename DT>
 cudaError_t launch_draft_persistent(const Shape&, const void*, const void*, const void*, const int*,
                                     const float*, const float*, int*, float*, double*, float*,
                                     uint32_t*, const Ws&, const Eps&, int, int, cudaStream_t);
@@ -50,9 +43,9 @@ std::mutex g_mu;
 double g_eps_scale = 1.0;
 bool g_force_simt = false;
 int g_bias_path = 2;          // 1 warp MMA, 2 tcgen05 (see SPEC_OPT_BIAS_PATH)
-int g_draft_mode = 1;         // 0 one launch per step, 1 persistent (SPEC_OPT_DRAFT_MODE)
+bool g_trace = false;         // SPEC_OPT_TRACE
 
-// Band constants (probability units); see DESIGN.md "Certified decisions".
+// Band constants (probability units) of the certified first-pass decisions.
 // Largest first-pass margin error seen against the float64 oracle over C0-C4
 // (about 4.3k draws): 2.6e-8 absolute, at most 1.4e-7 x sqrt(sum q^2) and
 // 1.1e-7 x sqrt(sum slice mass^2).  The constants keep a factor >= 5 on each.
@@ -76,12 +69,12 @@ Eps current_eps() {
 
 // ---------------------------------------------------------------- profiling
 enum Stage {
-  ST_DRAFT_PERSISTENT, ST_DRAFT_TILE, ST_DRAFT_SAMPLE, ST_DRAFT_HP_SUMS, ST_DRAFT_HP_DECIDE, ST_VERIFY_PREP,
+  ST_DRAFT_PERSISTENT, ST_VERIFY_PREP,
   ST_TARGET_STATS, ST_VERIFY_TILE, ST_VERIFY_FINAL, ST_SLOW_VERIFY, ST_VERIFY_HP_SUMS,
   ST_VERIFY_HP_RESID, ST_VERIFY_HP_DECIDE, ST_COUNT
 };
 const char* kStageNames[ST_COUNT] = {
-    "draft_persistent", "draft_tile", "draft_sample", "draft_hp_sums", "draft_hp_decide", "verify_prep",
+    "draft_persistent", "verify_prep",
     "target_stats", "verify_tile", "verify_final", "slow_verify", "verify_hp_sums",
     "verify_hp_resid", "verify_hp_decide"};
 bool g_prof = false;
@@ -140,7 +133,7 @@ int num_sms() {
 
 // ---------------------------------------------------------------- workspace
 struct Layout {
-  size_t ctrl, items, hpsum, dpart, rowptr, prow, prevtok, vflags, lse_p, bpart, vpart, slow,
+  size_t ctrl, trace, items, hpsum, dpart, rowptr, prow, prevtok, vflags, lse_p, bpart, vpart, slow,
       accbits, rowc, rowp, total;
   int max_items;
 };
@@ -156,9 +149,10 @@ Layout layout(const Shape& sh) {
   const size_t B = sh.B, g = sh.gamma, NS = sh.NS, HB = sh.HB;
   L.max_items = sh.B;
   L.ctrl = take(CTRL_WORDS * sizeof(uint32_t));
+  L.trace = take(MAX_GAMMA * TRACE_SLOTS * sizeof(unsigned long long));
   L.items = take((size_t)L.max_items * sizeof(HpItem));
   L.hpsum = take((size_t)L.max_items * HB * 3 * sizeof(double));
-  L.dpart = take(B * NS * sizeof(float4));
+  L.dpart = take(B * sh.NC * sizeof(float4));
   L.rowptr = take((B + 1) * sizeof(int));
   L.prow = take(B * g * sizeof(int2));
   L.prevtok = take(B * g * sizeof(int));
@@ -178,6 +172,7 @@ Ws views(const Layout& L, void* base) {
   unsigned char* p = static_cast<unsigned char*>(base);
   Ws w;
   w.ctrl = reinterpret_cast<uint32_t*>(p + L.ctrl);
+  w.trace = nullptr;
   w.items = reinterpret_cast<HpItem*>(p + L.items);
   w.max_items = L.max_items;
   w.hpsum = reinterpret_cast<double*>(p + L.hpsum);
@@ -216,6 +211,7 @@ Shape make_shape(int B, int gamma, int V, int r) {
   s.V = V;
   s.r = r;
   s.NS = (V + BN - 1) / BN;
+  s.NC = (V + CW - 1) / CW;
   s.HB = (V + HPB - 1) / HPB;
   return s;
 }
@@ -225,56 +221,35 @@ Shape make_shape(int B, int gamma, int V, int r) {
     if ((x) != cudaSuccess) return SPEC_ECUDA; \
   } while (0)
 
+// The whole draft: one cooperative launch (the control words are zeroed first
+// on the same stream; the grid barrier counts on it).
 template <typename DT>
-int run_draft(const spec_draft_args* a, cudaStream_t st) {
-  const Shape sh = make_shape(a->B, a->gamma, a->V, a->r);
-  const Layout L = layout(sh);
-  const Ws ws = views(L, a->workspace);
-  const Eps eps = current_eps();
+int launch_draft(const spec_draft_args* a, const Shape& sh, const Ws& ws, cudaStream_t st) {
   int path;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     path = g_force_simt ? 0 : g_bias_path;
   }
-  const int grid = grid_for_refine();
-  HpRows R{a->U, a->U, a->W1, a->W2, a->temperature};
-  int mode;
+  SPEC_TRY(cudaMemsetAsync(a->dev_status, 0, 4 * sizeof(uint32_t), st));
+  SPEC_TRY(cudaMemsetAsync(ws.ctrl, 0, CTRL_WORDS * sizeof(uint32_t), st));
+  ProfScope p(st, ST_DRAFT_PERSISTENT);
+  SPEC_TRY(launch_draft_persistent<DT>(sh, a->U, a->W1, a->W2, a->anchor, a->temperature, a->u_draft,
+                                       a->draft_tokens, a->q_tok, a->lse_q, a->diag, a->dev_status,
+                                       ws, current_eps(), path, num_sms(), st));
+  return SPEC_OK;
+}
+
+template <typename DT>
+int run_draft(const spec_draft_args* a, cudaStream_t st) {
+  const Shape sh = make_shape(a->B, a->gamma, a->V, a->r);
+  const Layout L = layout(sh);
+  Ws ws = views(L, a->workspace);
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    mode = g_draft_mode;
+    if (g_trace)
+      ws.trace = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(a->workspace) + L.trace);
   }
-  SPEC_TRY(cudaMemsetAsync(a->dev_status, 0, 4 * sizeof(uint32_t), st));
-  if (mode == 1) {
-    SPEC_TRY(cudaMemsetAsync(ws.ctrl, 0, CTRL_WORDS * sizeof(uint32_t), st));
-    ProfScope p(st, ST_DRAFT_PERSISTENT);
-    SPEC_TRY(launch_draft_persistent<DT>(sh, a->U, a->W1, a->W2, a->anchor, a->temperature,
-                                         a->u_draft, a->draft_tokens, a->q_tok, a->lse_q, a->diag,
-                                         a->dev_status, ws, eps, path, num_sms(), st));
-    return SPEC_OK;
-  }
-  for (int k = 0; k < sh.gamma; ++k) {
-    {
-      ProfScope p(st, ST_DRAFT_TILE);
-      SPEC_TRY(launch_draft_tile<DT>(sh, k, a->U, a->W1, a->W2, a->anchor, a->draft_tokens,
-                                     a->temperature, ws, path, a->dev_status, st));
-    }
-    {
-      ProfScope p(st, ST_DRAFT_SAMPLE);
-      SPEC_TRY(launch_draft_sample<DT>(sh, k, a->U, a->W1, a->W2, a->anchor, a->temperature,
-                                       a->u_draft, a->draft_tokens, a->q_tok, a->lse_q, a->diag,
-                                       a->dev_status, ws, eps, st));
-    }
-    {
-      ProfScope p(st, ST_DRAFT_HP_SUMS);
-      SPEC_TRY(launch_hp_sums<DT>(sh, R, ws, 0, grid, st));
-    }
-    {
-      ProfScope p(st, ST_DRAFT_HP_DECIDE);
-      SPEC_TRY(launch_hp_decide<DT>(sh, R, ws, a->draft_tokens, a->q_tok, a->lse_q, nullptr,
-                                    a->dev_status, grid, st));
-    }
-  }
-  return SPEC_OK;
+  return launch_draft<DT>(a, sh, ws, st);
 }
 
 template <typename DT>
@@ -348,7 +323,7 @@ Layout draft_only_layout(const Shape& sh) {
   L.ctrl = take(CTRL_WORDS * sizeof(uint32_t));
   L.items = take((size_t)L.max_items * sizeof(HpItem));
   L.hpsum = take((size_t)L.max_items * sh.HB * 3 * sizeof(double));
-  L.dpart = take((size_t)sh.B * sh.NS * sizeof(float4));
+  L.dpart = take((size_t)sh.B * sh.NC * sizeof(float4));
   L.total = off;
   return L;
 }
@@ -367,29 +342,7 @@ Ws draft_only_views(const Layout& L, void* base) {
 template <typename DT>
 int run_draft_static(const spec_draft_args* a, void* scratch, cudaStream_t st) {
   const Shape sh = make_shape(a->B, a->gamma, a->V, a->r);
-  const Layout L = draft_only_layout(sh);
-  const Ws ws = draft_only_views(L, scratch);
-  const Eps eps = current_eps();
-  int path;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    path = g_force_simt ? 0 : g_bias_path;
-  }
-  const int grid = grid_for_refine();
-  HpRows R{a->U, a->U, a->W1, a->W2, a->temperature};
-  SPEC_TRY(cudaMemsetAsync(a->dev_status, 0, 4 * sizeof(uint32_t), st));
-  SPEC_TRY(cudaMemsetAsync(ws.ctrl, 0, CTRL_WORDS * sizeof(uint32_t), st));
-  for (int k = 0; k < sh.gamma; ++k) {
-    SPEC_TRY(launch_draft_tile<DT>(sh, k, a->U, a->W1, a->W2, a->anchor, a->draft_tokens,
-                                   a->temperature, ws, path, a->dev_status, st));
-    SPEC_TRY(launch_draft_sample<DT>(sh, k, a->U, a->W1, a->W2, a->anchor, a->temperature,
-                                     a->u_draft, a->draft_tokens, a->q_tok, a->lse_q, a->diag,
-                                     a->dev_status, ws, eps, st));
-    SPEC_TRY(launch_hp_sums<DT>(sh, R, ws, 0, grid, st));
-    SPEC_TRY(launch_hp_decide<DT>(sh, R, ws, a->draft_tokens, a->q_tok, a->lse_q, nullptr,
-                                  a->dev_status, grid, st));
-  }
-  return SPEC_OK;
+  return launch_draft<DT>(a, sh, draft_only_views(draft_only_layout(sh), scratch), st);
 }
 
 }  // namespace
@@ -520,9 +473,8 @@ int32_t spec_set_option(int32_t key, double value) {
       if (value != 1.0 && value != 2.0) return SPEC_EINVAL;
       g_bias_path = (int)value;
       return SPEC_OK;
-    case SPEC_OPT_DRAFT_MODE:
-      if (value != 0.0 && value != 1.0) return SPEC_EINVAL;
-      g_draft_mode = (int)value;
+    case SPEC_OPT_TRACE:
+      g_trace = value != 0.0;
       return SPEC_OK;
     default:
       return SPEC_EINVAL;

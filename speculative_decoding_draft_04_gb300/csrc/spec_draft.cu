@@ -1,42 +1,42 @@
-// Draft side: one step k of DSpark's sequential stage with the Markov head
-// ("[논문리뷰] DSpark ...", section 1.2: p_k(v | x_0, x_<k) = softmax(U_k + B_k),
+// Draft side: DSpark's sequential stage with the Markov head ("[논문리뷰]
+// DSpark ...", section 1.2: p_k(v | x_0, x_<k) = softmax(U_k + B_k),
 // B(x_{k-1}, .) = W1[x_{k-1}] W2; sampled left to right), tempered by T_b.
+// The whole draft is one cooperative launch that walks the gamma steps; each
+// step has three phases separated by grid barriers:
 //
-//   draft_tile_kernel    grid (slices of BN columns) x (row tiles of BM requests).
-//                        Gathers W1[x_{k-1}] rows, computes the bias tile, adds U_k,
-//                        scales by 1/T and writes per (request, slice) the softmax
-//                        partial (c, m, s, q2): c = max U over the slice, m = max of
-//                        x = ((U-c)+bias)/T, s = sum exp(x-m), q2 = sum exp(x-m)^2.
-//                        The full-vocabulary logits never leave the SM.
-//   draft_sample_kernel  one CTA per request: merges the slice partials into the
-//                        normaliser, finds the slice where the running mass crosses
-//                        u * Z, recomputes that slice's BN weights and scans them for
-//                        the token (smallest v with F(v) > u).  Decisions within the
-//                        first pass's error band of a CDF breakpoint are queued for
-//                        re-decision in extended precision (spec_refine.cu).
-#include "spec_tc.cuh"
+//   tiles     (request tile, slice of BN columns) pairs strided over the CTAs.
+//             Gathers W1[x_{k-1}] rows, computes the bias tile, adds U_k,
+//             scales by 1/T and writes per (request, slice) the softmax partial
+//             (c, m, s, q2): c = max U over the slice, m = max of
+//             x = ((U-c)+bias)/T, s = sum exp(x-m), q2 = sum exp(x-m)^2, plus
+//             the masses of the slice's four 32-column chunks.  The
+//             full-vocabulary logits never leave the SM.
+//   sampling  one CTA per request: merges the slice partials into the
+//             normaliser, finds the slice and then the 32-column chunk where
+//             the running mass crosses u * Z, recomputes that chunk's weights
+//             and scans them for the token (smallest v with F(v) > u).
+//             Decisions within the first pass's error band of a CDF breakpoint
+//             are queued for re-decision in extended precision.
+//   re-decision  (only when the step queued draws) the two extended-precision
+//             phases of spec_hp.cuh.
+#include <cstring>
+
+#include "spec_tile_tc.cuh"
 #include "spec_hp.cuh"
 
 namespace spec {
 
-// Tensor-memory context of a CTA: accumulator columns, MMA-completion
-// mbarrier and the parity of its next phase.
-struct TcCtx {
-  uint32_t taddr;
-  uint64_t* bar;
-  uint32_t phase;
-};
-
-// One (request tile, slice) of draft step k.  PATH: 0 = SIMT fp32 FMAs,
-// 1 = warp MMA (mma.sync), 2 = tcgen05 / TMEM (BM = 128; `tc` set up by the
-// caller).  Returns false if the MMA did not complete within the bound.
-// Tokens written by other CTAs of the same launch are read through L2.
+// One (request tile, slice) of draft step k on the SIMT (PATH 0, fp32 FMAs)
+// or warp-MMA (PATH 1, mma.sync) bias tile; the tensor-memory path is the
+// pipelined engine below.  Tokens written by other CTAs of the same launch are
+// read through L2.
 template <typename DT, int BM, int PATH>
-__device__ bool draft_tile_body(const Shape& sh, int k, int slice, int mtile, const DT* __restrict__ U,
+__device__ void draft_tile_body(const Shape& sh, int k, int slice, int mtile, const DT* __restrict__ U,
                                 const DT* __restrict__ W1, const DT* __restrict__ W2,
                                 const int* __restrict__ anchor, const int* tokens,
-                                const float* __restrict__ temp, const Ws& ws, uint32_t* status,
-                                unsigned char* smem_raw, TcCtx* tc) {
+                                const float* __restrict__ temp, const Ws& ws,
+                                unsigned char* smem_raw) {
+  static_assert(PATH == 0 || PATH == 1, "tensor-memory tiles use the pipelined engine");
   __shared__ int s_tok[BM];
   __shared__ size_t s_off[BM];
   const int m0 = mtile * BM, n0 = slice * BN;
@@ -57,34 +57,7 @@ __device__ bool draft_tile_body(const Shape& sh, int k, int slice, int mtile, co
   DT* Us;
   float* stage;
   int su;
-  if constexpr (PATH == 2) {
-    static_assert(BM == TC_M, "tensor-memory path uses 128-row tiles");
-    unsigned char* smem = align1k(smem_raw);
-    const TcLayout lay(sh.r, false);
-    bf16* As = reinterpret_cast<bf16*>(smem + lay.offA);
-    bf16* Wsm = reinterpret_cast<bf16*>(smem + lay.offW);
-    Us = reinterpret_cast<DT*>(smem + lay.offU);
-    stage = reinterpret_cast<float*>(smem + lay.offStage);
-    su = BN + 8;
-    __syncthreads();
-    tc_load_A(As, reinterpret_cast<const bf16*>(W1), s_tok, nrows, sh.r);
-    tc_load_W2(Wsm, reinterpret_cast<const bf16*>(W2), sh.V, n0, sh.r);
-    load_X_rows<DT>(Us, su, U, s_off, nrows, BM, sh.V, n0);
-    cp_async_commit();
-    cp_async_wait_all();
-    fence_async_shared();
-    tc_fence_before();
-    __syncthreads();
-    const bool ok = bias_tile_tc(As, Wsm, sh.r, tc->taddr, tc->bar, tc->phase, stage);
-    if (!ok) {
-      if (threadIdx.x == 0) set_status(status, SPEC_DEV_TIMEOUT);
-      mbar_wait(tc->bar, tc->phase, 1u << 22);   // let an in-flight MMA drain
-      tc->phase ^= 1u;
-      return false;
-    }
-    tc->phase ^= 1u;
-    __syncthreads();
-  } else {
+  {
     const TileLayout<DT> lay(BM, sh.r, false);
     DT* As = reinterpret_cast<DT*>(smem_raw + lay.offA);
     DT* Wsm = reinterpret_cast<DT*>(smem_raw + lay.offW);
@@ -102,49 +75,156 @@ __device__ bool draft_tile_body(const Shape& sh, int k, int slice, int mtile, co
     __syncthreads();
   }
 
-  // ---- epilogue: TPR threads per row, each COLS consecutive columns
+  // ---- epilogue: TPR threads per row, each COLS consecutive columns; one
+  // partial per CW-column chunk (two threads share a chunk when COLS < CW)
   constexpr int TPR = NT / BM, COLS = BN / TPR;
   constexpr int SS = TileLayout<DT>::SS;
+  constexpr int SPAN = COLS < CW ? COLS : CW;        // columns of one chunk in this thread
+  constexpr int CPT = COLS / SPAN;                   // chunk pieces per thread
   const int m = threadIdx.x / TPR, part = threadIdx.x % TPR;
   const bool rowok = m < nrows;
   const int b = m0 + m;
   const float invT = rowok ? 1.0f / temp[b] : 1.0f;
-  const int cbeg = part * COLS;
-  const int cend = min(cbeg + COLS, sh.V - n0);   // valid columns of this thread
   const DT* urow = Us + (size_t)m * su;
   const float* brow = stage + m * SS;
-
-  float c = -INFINITY;
-  for (int i = cbeg; i < cend; ++i) c = fmaxf(c, tof(urow[i]));
-  c = group_max<TPR>(c);
-  float xm = -INFINITY;
-  for (int i = cbeg; i < cend; ++i) xm = fmaxf(xm, fast_x(tof(urow[i]), c, brow[i], invT));
-  xm = group_max<TPR>(xm);
-  Kahan ks;
-  float q2 = 0.f;
-  for (int i = cbeg; i < cend; ++i) {
-    float w = fast_w(fast_x(tof(urow[i]), c, brow[i], invT), xm);
-    ks.add(w);
-    q2 = fmaf(w, w, q2);
+#pragma unroll
+  for (int q = 0; q < CPT; ++q) {
+    const int cb = part * COLS + q * SPAN;
+    const int ce = min(cb + SPAN, sh.V - n0);        // valid columns of this piece
+    float c = -INFINITY;
+    for (int i = cb; i < ce; ++i) c = fmaxf(c, tof(urow[i]));
+    if constexpr (SPAN < CW) c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, 1));
+    float xm = -INFINITY;
+    for (int i = cb; i < ce; ++i) xm = fmaxf(xm, fast_x(tof(urow[i]), c, brow[i], invT));
+    if constexpr (SPAN < CW) xm = fmaxf(xm, __shfl_xor_sync(0xffffffffu, xm, 1));
+    Kahan ks;
+    float q2 = 0.f;
+    for (int i = cb; i < ce; ++i) {
+      const float w = fast_w(fast_x(tof(urow[i]), c, brow[i], invT), xm);
+      ks.add(w);
+      q2 = fmaf(w, w, q2);
+    }
+    df sdf = ks.value();
+    if constexpr (SPAN < CW) {
+      sdf = df_add(sdf, df{__shfl_xor_sync(0xffffffffu, sdf.hi, 1), __shfl_xor_sync(0xffffffffu, sdf.lo, 1)});
+      q2 += __shfl_xor_sync(0xffffffffu, q2, 1);
+    }
+    const int chunk = (n0 + cb) / CW;
+    const bool owner = SPAN == CW || (part & 1) == 0;
+    if (rowok && owner && chunk < sh.NC)
+      ws.dpart[(size_t)b * sh.NC + chunk] = make_float4(c, xm, (float)df_d(sdf), q2);
   }
-  df s = group_sum_df<TPR>(ks.value());
-  q2 = group_sum<TPR>(q2);
-  if (rowok && part == 0)
-    ws.dpart[(size_t)b * sh.NS + slice] = make_float4(c, xm, df_d(s) /*rounded*/, q2);
-  return true;
 }
 
-// Weighted slice mass relative to the row's largest slice reference, in units
+// ---------------------------------------------------------------- tensor-memory tiles
+// Partial (c, m, s, q2) of one CW-column chunk of a row from its packed bf16
+// logits `u` (16 words) and its bias row `x` (overwritten with the tempered
+// logits); `nv` valid columns.  Four interleaved max / Kahan / square-sum
+// chains keep the dependent-latency per column low.
+template <bool FULL>
+__device__ __forceinline__ float4 chunk_partial(const uint4 (&u)[4], float (&x)[32], int nv, float invT) {
+  auto uval = [&](int i) {
+    const uint4 q = u[i >> 3];
+    const uint32_t w = ((i >> 1) & 3) == 0 ? q.x : ((i >> 1) & 3) == 1 ? q.y : ((i >> 1) & 3) == 2 ? q.z : q.w;
+    return (i & 1) ? bf_hi(w) : bf_lo(w);
+  };
+  float c4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (FULL || i < nv) c4[i & 3] = fmaxf(c4[i & 3], uval(i));
+  const float c = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    x[i] = fast_x(uval(i), c, x[i], invT);
+    if (FULL || i < nv) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+  }
+  const float xm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+  Kahan k4[4];
+  float q4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    if (FULL || i < nv) {
+      const float w = fast_w(x[i], xm);
+      k4[i & 3].add(w);
+      q4[i & 3] = fmaf(w, w, q4[i & 3]);
+    }
+  }
+  const df s = df_add(df_add(k4[0].value(), k4[1].value()), df_add(k4[2].value(), k4[3].value()));
+  return make_float4(c, xm, (float)df_d(s), (q4[0] + q4[1]) + (q4[2] + q4[3]));
+}
+
+// Draft step k on the warp-specialised engine of spec_tile_tc.cuh: the W1 row
+// of each request's previous token, and the epilogue of one tile row.
+struct DraftEpi {
+  const Shape& sh;
+  int k;
+  const int* anchor;
+  const int* tokens;
+  const float* temp;
+  float4* dpart;
+
+  __device__ int step() const { return k; }
+  // W1 row of row m of request tile mt (-1: no such request; its A row is zero)
+  __device__ int token(int mt, int m) const {
+    const int b = mt * TC_M + m;
+    if (b >= sh.B) return -1;
+    const int t = (k == 0) ? anchor[b] : __ldcg(tokens + (size_t)b * sh.gamma + k - 1);
+    return min(max(t, 0), sh.V - 1);          // bad tokens are reported by the sampler
+  }
+  // Row m of tile (mt, sl): the partials of the slice's four chunks, from the
+  // U row in `ub` (swizzled) and the accumulator row at TMEM address `trow`;
+  // two chunks per TMEM wait.
+  __device__ void epilogue(int mt, int sl, int m, const unsigned char* ub, uint32_t trow) const {
+    const int b = mt * TC_M + m;
+    const bool rowok = b < sh.B;
+    const int n0 = sl * BN;
+    const float invT = rowok ? 1.0f / temp[b] : 1.0f;
+#pragma unroll 1
+    for (int pr = 0; pr < 2; ++pr) {
+      float x0[32], x1[32];
+      tc_ld32_issue(trow + (uint32_t)(64 * pr), x0);
+      tc_ld32_issue(trow + (uint32_t)(64 * pr + 32), x1);
+      uint4 u0[4], u1[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        u0[j] = lds128(tp_uchunk(ub, m, 8 * pr + j));
+        u1[j] = lds128(tp_uchunk(ub, m, 8 * pr + 4 + j));
+      }
+      tc_wait_ld();
+      const int cb = n0 + 64 * pr;
+      const int nv0 = min(CW, sh.V - cb), nv1 = min(CW, sh.V - cb - CW);
+      float4 p0 = make_float4(0.f, 0.f, 0.f, 0.f), p1 = p0;
+      if (nv1 >= CW) {
+        p0 = chunk_partial<true>(u0, x0, CW, invT);
+        p1 = chunk_partial<true>(u1, x1, CW, invT);
+      } else {
+        if (nv0 > 0) p0 = chunk_partial<false>(u0, x0, nv0, invT);
+        if (nv1 > 0) p1 = chunk_partial<false>(u1, x1, nv1, invT);
+      }
+      if (rowok) {
+        float4* o = dpart + (size_t)b * sh.NC + cb / CW;
+        if (nv0 > 0) o[0] = p0;
+        if (nv1 > 0) o[1] = p1;
+      }
+    }
+  }
+};
+
+// Weighted chunk mass relative to the row's largest chunk reference, in units
 // of exp(reference logit):  f = exp((c - cM)/T + (m - mM)).
-__device__ __forceinline__ float slice_factor(float4 p, float cM, float mM, float invT) {
+__device__ __forceinline__ float chunk_factor(float4 p, float cM, float mM, float invT) {
   float a = __fadd_rn(__fmul_rn(__fsub_rn(p.x, cM), invT), __fsub_rn(p.y, mM));
   return expf(a);
 }
 
-// Draw token x_{k+1} of request b from its slice partials (one CTA).  Queues
-// the draw on `counter` / ws.items when it lies inside the error band.
-// `dsm` holds an r x BN slab.  Partials and tokens written by other CTAs of
-// the same launch are read through L2.
+// Draw token x_{k+1} of request b from its chunk partials (one CTA): merge
+// the chunk masses (double-float), find the chunk where the running mass
+// crosses u*Z, recompute that chunk's CW weights and scan them.  Queues the
+// draw on `counter` / ws.items when it lies inside the error band.  `dsm`
+// holds an r x CW W2 slab.  Partials and tokens written by other CTAs of the
+// same launch are read through L2.
+
 template <typename DT>
 __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __restrict__ U,
                                   const DT* __restrict__ W1, const DT* __restrict__ W2,
@@ -152,13 +232,13 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
                                   const float* __restrict__ u_draft, int* tokens, float* q_tok,
                                   double* lse_q, float* diag, uint32_t* status, const Ws& ws,
                                   const Eps& eps, uint32_t* counter, unsigned char* dsm) {
-  DT* slab = reinterpret_cast<DT*>(dsm);      // [r][BN] W2 slab of the crossing slice
+  DT* slab = reinterpret_cast<DT*>(dsm);      // [r][CW] W2 columns of the crossing chunk
   __shared__ float sh_f[72];
   __shared__ float s_a[256];
-  __shared__ float s_part[2][BN];
-  __shared__ int s_slice;
-  __shared__ float s_pref[2];
-  __shared__ float s_w[BN];
+  __shared__ float s_part[NT / CW][CW];
+  __shared__ int s_slice, s_tok;
+  __shared__ float s_pref[2], s_lo, s_hi, s_wtok;
+  __shared__ double s_tin;
 
   __syncthreads();      // previous use of the shared buffers is finished
   const size_t ok = (size_t)b * sh.gamma + k;
@@ -174,68 +254,70 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
     }
     return;
   }
+  for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf(W1 + (size_t)prev * sh.r + i);
   const float invT = 1.0f / T;
-  const float4* P = ws.dpart + (size_t)b * sh.NS;
-  auto part = [&](int s) { return __ldcg(P + s); };
+  const float4* P = ws.dpart + (size_t)b * sh.NC;
 
-  // ---- reference slice: largest c/T + m (ties: any; only a shift)
-  const int per = (sh.NS + NT - 1) / NT;
-  const int s0 = threadIdx.x * per, s1 = min(s0 + per, sh.NS);
+  // ---- this thread's contiguous range of chunks (the first 8 kept in registers)
+  const int per = (sh.NC + NT - 1) / NT;
+  const int s0 = threadIdx.x * per, s1 = min(s0 + per, sh.NC);
+  float4 pv[8];
   float best = -INFINITY;
   int bidx = 0;
-  for (int s = s0; s < s1; ++s) {
-    float4 p = part(s);
-    float key = fmaf(p.x, invT, p.y);
+  for (int s = s0, q = 0; s < s1; ++s, ++q) {
+    const float4 p = __ldcg(P + s);
+    if (q < 8) pv[q] = p;
+    const float key = fmaf(p.x, invT, p.y);
     if (key > best) { best = key; bidx = s; }
   }
-  float bmax = block_max(best, sh_f);
-  // lowest index attaining the max
-  int cand = (best == bmax) ? bidx : 0x7fffffff;
-  for (int m = 16; m; m >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, m));
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) reinterpret_cast<int*>(sh_f)[threadIdx.x >> 5] = cand;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int c2 = 0x7fffffff;
-    for (int w = 0; w < NT / 32; ++w) c2 = min(c2, reinterpret_cast<int*>(sh_f)[w]);
-    s_slice = c2;
+  // reference chunk: lowest index attaining the largest c/T + m
+  {
+    const float bmax = block_max(best, sh_f);
+    int cand = (best == bmax) ? bidx : 0x7fffffff;
+    for (int m = 16; m; m >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, m));
+    if ((threadIdx.x & 31) == 0) reinterpret_cast<int*>(sh_f)[32 + (threadIdx.x >> 5)] = cand;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int c2 = 0x7fffffff;
+      for (int w = 0; w < NT / 32; ++w) c2 = min(c2, reinterpret_cast<int*>(sh_f)[32 + w]);
+      s_slice = c2;
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  const float4 PM = part(s_slice);
+  const float4 PM = __ldcg(P + s_slice);
   const float cM = PM.x, mM = PM.y;
-  __syncthreads();
 
-  // ---- per-thread slice masses (double-float) and error-estimate sums
+  // ---- chunk masses (double-float), normaliser and error-estimate sums
   df loc = {0.f, 0.f};
   float q2 = 0.f, m2 = 0.f;
-  for (int s = s0; s < s1; ++s) {
-    float4 p = part(s);
-    float f = slice_factor(p, cM, mM, invT);
-    float w = p.z * f;
+  for (int s = s0, q = 0; s < s1; ++s, ++q) {
+    const float4 p = (q < 8) ? pv[q] : __ldcg(P + s);
+    const float f = chunk_factor(p, cM, mM, invT);
+    const float w = p.z * f;
     loc = df_addf(loc, w);
     q2 = fmaf(p.w * f, f, q2);
     m2 = fmaf(w, w, m2);
   }
   df Zdf;
-  df excl = block_excl_scan_df(loc, &Zdf, sh_f);
+  const df excl = block_excl_scan_df(loc, &Zdf, sh_f);
   q2 = block_sum(q2, sh_f);
   m2 = block_sum(m2, sh_f);
   const double Z = df_d(Zdf);
   const float u = u_draft[ok];
   const df target = df_from_d((double)u * Z);
 
-  // ---- crossing slice: first s with prefix_incl(s) > target
+  // ---- crossing chunk: first s with prefix_incl(s) > target
   if (threadIdx.x == 0) s_slice = 0x7fffffff;
   __syncthreads();
   int my_slice = -1;
   df my_pref = {0.f, 0.f};
   {
-    df run = excl;
-    df tneg = df_neg(target);
+    const df tneg = df_neg(target);
     if (df_d(df_add(excl, tneg)) <= 0.0 && df_d(df_add(df_add(excl, loc), tneg)) > 0.0) {
-      for (int s = s0; s < s1; ++s) {
-        float4 p = part(s);
-        df nxt = df_addf(run, p.z * slice_factor(p, cM, mM, invT));
+      df run = excl;
+      for (int s = s0, q = 0; s < s1; ++s, ++q) {
+        const float4 p = (q < 8) ? pv[q] : __ldcg(P + s);
+        const df nxt = df_addf(run, p.z * chunk_factor(p, cM, mM, invT));
         if (df_d(df_add(nxt, tneg)) > 0.0) {
           my_slice = s;
           my_pref = run;
@@ -247,28 +329,21 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
     }
   }
   __syncthreads();
-  if (my_slice >= 0 && my_slice == s_slice) {
-    s_pref[0] = my_pref.hi;
-    s_pref[1] = my_pref.lo;
-  }
+  if (my_slice >= 0 && my_slice == s_slice) { s_pref[0] = my_pref.hi; s_pref[1] = my_pref.lo; }
   __syncthreads();
   bool fallback = false;
   if (s_slice == 0x7fffffff) {
-    // rounding left the total at or below u*Z: last slice with mass
+    // rounding left the total at or below u*Z: last chunk with mass
     fallback = true;
     if (threadIdx.x == 0) {
-      int sl = sh.NS - 1;
-      while (sl > 0 && !(part(sl).z > 0.f)) --sl;
-      s_slice = sl;
-    }
-    __syncthreads();
-    // prefix of everything before that slice
-    df run = {0.f, 0.f};
-    if (threadIdx.x == 0) {
-      for (int s = 0; s < s_slice; ++s) {
-        float4 p = part(s);
-        run = df_addf(run, p.z * slice_factor(p, cM, mM, invT));
+      int sl = sh.NC - 1;
+      while (sl > 0 && !(__ldcg(P + sl).z > 0.f)) --sl;
+      df run = {0.f, 0.f};
+      for (int s = 0; s < sl; ++s) {
+        const float4 p = __ldcg(P + s);
+        run = df_addf(run, p.z * chunk_factor(p, cM, mM, invT));
       }
+      s_slice = sl;
       s_pref[0] = run.hi;
       s_pref[1] = run.lo;
     }
@@ -276,79 +351,77 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   }
   const int sl = s_slice;
   const df pref = {s_pref[0], s_pref[1]};
-  const float4 PS = part(sl);
-  const float fS = slice_factor(PS, cM, mM, invT);
+  const float4 PS = __ldcg(P + sl);
+  const float fS = chunk_factor(PS, cM, mM, invT);
+  if (threadIdx.x == 0) s_tin = (df_d(target) - df_d(pref)) / (double)fS;   // chunk units
+  __syncthreads();
+  const int n0 = sl * CW;
 
-  // ---- recompute the slice's weights (bias by SIMT: two halves of k, W2 slab in smem)
-  for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf(W1 + (size_t)prev * sh.r + i);
-  const int n0 = sl * BN;
-  stage_w2_slab<DT>(slab, W2, sh.V, 0, sh.r, n0, BN);
+  // ---- recompute the chunk's CW weights: 8 k-groups x CW columns
+  stage_w2_slab<DT>(slab, W2, sh.V, 0, sh.r, n0, CW);
   {
-    const int col = threadIdx.x % BN, half = threadIdx.x / BN;
-    const int kh = sh.r / 2;
+    const int col = threadIdx.x % CW, grp = threadIdx.x / CW;
+    const int kg = sh.r / (NT / CW);           // r % 16 == 0, so r / 8 is whole
     float acc = 0.f;
-    for (int i = half * kh; i < half * kh + kh; ++i) acc = fmaf(s_a[i], tof(slab[i * BN + col]), acc);
-    s_part[half][col] = acc;
+    for (int i = grp * kg; i < grp * kg + kg; ++i) acc = fmaf(s_a[i], tof(slab[i * CW + col]), acc);
+    s_part[grp][col] = acc;
   }
   __syncthreads();
-  float w = 0.f;
-  if (threadIdx.x < BN) {
-    const int v = n0 + threadIdx.x;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int v = n0 + lane;
+    float w = 0.f;
     if (v < sh.V) {
-      float bias = __fadd_rn(s_part[0][threadIdx.x], s_part[1][threadIdx.x]);
+      float bias = s_part[0][lane];
+#pragma unroll
+      for (int g = 1; g < NT / CW; ++g) bias = __fadd_rn(bias, s_part[g][lane]);
       w = fast_w(fast_x(ldf(U + ok * sh.V + v), PS.x, bias, invT), PS.y);
     }
-    s_w[threadIdx.x] = w;
-  }
-  __syncthreads();
-  // in-slice target in slice units
-  const double tin = (df_d(target) - df_d(pref)) / (double)fS;
-  df wtot;
-  df wex = block_excl_scan_df(df_make(threadIdx.x < BN ? w : 0.f), &wtot, sh_f);
-  __shared__ int s_tok;
-  __shared__ float s_lo[2], s_hi[2];
-  if (threadIdx.x == 0) s_tok = 0x7fffffff;
-  __syncthreads();
-  double my_lo = 0.0, my_hi = 0.0;
-  bool claim = false;
-  if (threadIdx.x < BN && w > 0.f) {
-    my_lo = df_d(wex);
-    my_hi = df_d(df_addf(wex, w));
-    if (my_lo <= tin && my_hi > tin) {
-      claim = true;
-      atomicMin(&s_tok, (int)threadIdx.x);
+    // inclusive double-float scan across the warp
+    df inc = df_make(w);
+    for (int d = 1; d < 32; d <<= 1) {
+      const df o = shfl_up_df(inc, d);
+      if (lane >= d) inc = df_add(inc, o);
     }
-  }
-  __syncthreads();
-  if (claim && (int)threadIdx.x == s_tok) {
-    s_lo[0] = (float)(tin - my_lo);
-    s_hi[0] = (float)(my_hi - tin);
-  }
-  __syncthreads();
-  if (s_tok == 0x7fffffff) {
-    fallback = true;
-    if (threadIdx.x == 0) {
-      int t = BN - 1;
-      while (t > 0 && !(s_w[t] > 0.f)) --t;
+    df ex = shfl_up_df(inc, 1);
+    if (lane == 0) ex = {0.f, 0.f};
+    const double lo = df_d(ex), hi = df_d(inc), tin = s_tin;
+    const bool claim = w > 0.f && lo <= tin && hi > tin;
+    const uint32_t cl = __ballot_sync(0xffffffffu, claim);
+    const uint32_t pos = __ballot_sync(0xffffffffu, w > 0.f);
+    int t;
+    float dlo = 0.f, dhi = 0.f;
+    if (cl) {
+      t = __ffs(cl) - 1;
+      dlo = __shfl_sync(0xffffffffu, (float)(tin - lo), t);
+      dhi = __shfl_sync(0xffffffffu, (float)(hi - tin), t);
+    } else {
+      fallback = true;
+      t = pos ? 31 - __clz(pos) : 0;           // last entry with mass
+    }
+    const float wt = __shfl_sync(0xffffffffu, w, t);
+    if (lane == 0) {
       s_tok = t;
-      s_lo[0] = 0.f;
-      s_hi[0] = 0.f;
+      s_lo = dlo;
+      s_hi = dhi;
+      s_wtok = wt;
     }
-    __syncthreads();
   }
+  __syncthreads();
+  if (s_lo == 0.f && s_hi == 0.f) fallback = true;
   if (threadIdx.x == 0) {
     const int tok = n0 + s_tok;
-    const double dmargin = fmin((double)s_lo[0], (double)s_hi[0]) * (double)fS / Z;
+    const double dmargin = fmin((double)s_lo, (double)s_hi) * (double)fS / Z;
     const double qrow = sqrt((double)q2) / Z, mrow = sqrt((double)m2) / Z;
     const double band = (double)eps.scale * ((double)eps.elem * qrow + (double)eps.slice * mrow +
                                              (double)eps.abs_);
     const double lse = ((double)cM * (1.0 / (double)T) + (double)mM) + log(Z);
     tokens[ok] = tok;
-    q_tok[ok] = (float)((double)s_w[s_tok] * (double)fS / Z);
+    q_tok[ok] = (float)((double)s_wtok * (double)fS / Z);
     lse_q[ok] = lse;
     if (diag) {
-      diag[ok * 4 + 0] = (float)((double)s_lo[0] * fS / Z);
-      diag[ok * 4 + 1] = (float)((double)s_hi[0] * fS / Z);
+      diag[ok * 4 + 0] = (float)((double)s_lo * fS / Z);
+      diag[ok * 4 + 1] = (float)((double)s_hi * fS / Z);
       diag[ok * 4 + 2] = (float)band;
       diag[ok * 4 + 3] = (float)tok;
     }
@@ -367,51 +440,9 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   __syncthreads();
 }
 
-// ---------------------------------------------------------------- kernels
-// One launch per step: tiles (grid = slices x request tiles).
-template <typename DT, int BM, int PATH>
-__global__ void __launch_bounds__(NT) draft_tile_kernel(Shape sh, int k, const DT* __restrict__ U,
-                                                        const DT* __restrict__ W1,
-                                                        const DT* __restrict__ W2,
-                                                        const int* __restrict__ anchor,
-                                                        const int* __restrict__ tokens,
-                                                        const float* __restrict__ temp, Ws ws,
-                                                        uint32_t* status) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  __shared__ uint64_t s_bar;
-  __shared__ uint32_t s_holder;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) ws.ctrl[CTRL_ITEMS] = 0;
-  TcCtx tc{0u, &s_bar, 0u};
-  if constexpr (PATH == 2) {
-    if (threadIdx.x == 0) mbar_init(&s_bar, 1);
-    if (threadIdx.x < 32) tc_alloc(&s_holder, TC_TMEM_COLS);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    tc.taddr = s_holder;
-  }
-  draft_tile_body<DT, BM, PATH>(sh, k, blockIdx.x, blockIdx.y, U, W1, W2, anchor, tokens, temp, ws,
-                                status, smem_raw, &tc);
-  if constexpr (PATH == 2) {
-    tc_fence_before();
-    __syncthreads();
-    if (threadIdx.x < 32) tc_dealloc(tc.taddr, TC_TMEM_COLS);
-  }
-}
-
-// One launch per step: one CTA per request.
-template <typename DT>
-__global__ void __launch_bounds__(NT) draft_sample_kernel(
-    Shape sh, int k, const DT* __restrict__ U, const DT* __restrict__ W1, const DT* __restrict__ W2,
-    const int* __restrict__ anchor, const float* __restrict__ temp,
-    const float* __restrict__ u_draft, int* tokens, float* q_tok, double* lse_q, float* diag,
-    uint32_t* status, Ws ws, Eps eps) {
-  extern __shared__ __align__(16) unsigned char dsm[];
-  draft_sample_body<DT>(sh, k, blockIdx.x, U, W1, W2, anchor, temp, u_draft, tokens, q_tok, lse_q,
-                        diag, status, ws, eps, ws.ctrl + CTRL_ITEMS, dsm);
-}
-
-struct DraftParams {
+// ---------------------------------------------------------------- kernel
+struct alignas(64) DraftParams {
+  TpMaps maps;       // tensor-memory path only
   Shape sh;
   const void* U;
   const void* W1;
@@ -434,116 +465,137 @@ struct DraftParams {
 // near-boundary draws -- the two extended-precision phases, each followed by
 // a grid barrier.  Tensor memory is allocated once per CTA.
 template <typename DT, int BM, int PATH>
-__global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(DraftParams P) {
+__global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_constant__ DraftParams P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  __shared__ uint64_t s_bar;
+  __shared__ uint64_t s_bar[TB_COUNT];
   __shared__ uint32_t s_holder;
+  __shared__ int s_tok[TC_M];
+  __shared__ int s_fail;
   const Shape& sh = P.sh;
   const DT* U = (const DT*)P.U;
   const DT* W1 = (const DT*)P.W1;
   const DT* W2 = (const DT*)P.W2;
   uint32_t* ctrl = P.ws.ctrl;
-  TcCtx tc{0u, &s_bar, 0u};
+  TpState st{0u, s_bar, &s_fail, 0u, 0u};
   if constexpr (PATH == 2) {
-    if (threadIdx.x == 0) mbar_init(&s_bar, 1);
-    if (threadIdx.x < 32) tc_alloc(&s_holder, TC_TMEM_COLS);
+    if (threadIdx.x == 0) {
+      tp_init(s_bar);
+      s_fail = 0;
+    }
+    if (threadIdx.x < 32) tc_alloc(&s_holder, TP_TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    tc.taddr = s_holder;
+    st.tmem = s_holder;
   }
   uint32_t gen = threadIdx.x == 0 ? ld_acquire_gpu(ctrl + CTRL_BAR_GEN) : 0u;
   const HpRows R{P.U, P.U, P.W1, P.W2, P.temp};
   const int n_mt = (sh.B + BM - 1) / BM;
   const int n_tiles = sh.NS * n_mt;
   const uint32_t G = gridDim.x;
+  unsigned long long* tr = (P.ws.trace && blockIdx.x == 0 && threadIdx.x == 0) ? P.ws.trace : nullptr;
   for (int k = 0; k < sh.gamma; ++k) {
     bool ok = true;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += G)
-      ok = draft_tile_body<DT, BM, PATH>(sh, k, t % sh.NS, t / sh.NS, U, W1, W2, P.anchor, P.tokens,
-                                         P.temp, P.ws, P.status, smem_raw, &tc);
+    if (tr) tr[k * TRACE_SLOTS + 0] = globaltimer_ns();
+    if constexpr (PATH == 2) {
+      const DraftEpi e{sh, k, P.anchor, P.tokens, P.temp, P.ws.dpart};
+      const int n = (int)blockIdx.x < n_tiles ? (n_tiles - (int)blockIdx.x + (int)G - 1) / (int)G : 0;
+      ok = tp_run(e, sh, P.maps, reinterpret_cast<const bf16*>(W1), (int)blockIdx.x, (int)G, n,
+                  smem_raw, st, s_tok);
+      if (!ok && threadIdx.x == 0) set_status(P.status, SPEC_DEV_TIMEOUT);
+    } else {
+      for (int t = blockIdx.x; t < n_tiles; t += G)
+        draft_tile_body<DT, BM, PATH>(sh, k, t % sh.NS, t / sh.NS, U, W1, W2, P.anchor, P.tokens,
+                                      P.temp, P.ws, smem_raw);
+    }
     if (!ok) {
       if (threadIdx.x == 0) atomicExch(ctrl + CTRL_ABORT, 1u);
       break;
     }
+    if (tr) tr[k * TRACE_SLOTS + 1] = globaltimer_ns();
     if (!grid_sync(ctrl, G, gen, P.status)) break;
+    if (tr) tr[k * TRACE_SLOTS + 2] = globaltimer_ns();
     for (int b = blockIdx.x; b < sh.B; b += G)
       draft_sample_body<DT>(sh, k, b, U, W1, W2, P.anchor, P.temp, P.u_draft, P.tokens, P.q_tok,
                             P.lse_q, P.diag, P.status, P.ws, P.eps, ctrl + CTRL_STEP0 + k,
                             smem_raw);
+    if (tr) tr[k * TRACE_SLOTS + 3] = globaltimer_ns();
     if (!grid_sync(ctrl, G, gen, P.status)) break;
+    if (tr) tr[k * TRACE_SLOTS + 4] = globaltimer_ns();
     const int n = min((int)__ldcg(ctrl + CTRL_STEP0 + k), P.ws.max_items);
     if (n > 0) {
       hp_sums_body<DT>(sh, R, P.ws, 0, n, smem_raw);
       if (!grid_sync(ctrl, G, gen, P.status)) break;
+      if (tr) tr[k * TRACE_SLOTS + 5] = globaltimer_ns();
       hp_decide_body<DT>(sh, R, P.ws, n, P.tokens, P.q_tok, P.lse_q, nullptr, P.status, smem_raw);
       if (!grid_sync(ctrl, G, gen, P.status)) break;
+    }
+    if (tr) {
+      tr[k * TRACE_SLOTS + 6] = globaltimer_ns();
+      tr[k * TRACE_SLOTS + 7] = (unsigned long long)n;
     }
   }
   if constexpr (PATH == 2) {
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x < 32) tc_dealloc(tc.taddr, TC_TMEM_COLS);
+    if (threadIdx.x < 32) tc_dealloc(st.tmem, TP_TMEM_COLS);
   }
 }
 
-// ---------------------------------------------------------------- launchers
-template <typename DT, int BM, int PATH>
-static cudaError_t launch_tile(const Shape& sh, int k, const DT* U, const DT* W1, const DT* W2,
-                               const int* anchor, const int* tokens, const float* temp, const Ws& ws,
-                               uint32_t* status, cudaStream_t st) {
-  const size_t smem = PATH == 2 ? TcLayout(sh.r, false).total : TileLayout<DT>(BM, sh.r, false).total;
-  auto kern = draft_tile_kernel<DT, BM, PATH>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid(sh.NS, (sh.B + BM - 1) / BM);
-  kern<<<grid, NT, smem, st>>>(sh, k, U, W1, W2, anchor, tokens, temp, ws, status);
-  return cudaGetLastError();
+// ---------------------------------------------------------------- launcher
+// cuTensorMapEncodeTiled through the runtime's driver entry point (the library
+// links no driver library of its own).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
 }
 
-// path: 0 SIMT, 1 warp MMA, 2 tcgen05 (bf16 with r % 64 == 0 only; else warp MMA)
-template <typename DT>
-cudaError_t launch_draft_tile(const Shape& sh, int k, const void* U, const void* W1, const void* W2,
-                              const int* anchor, const int* tokens, const float* temp, const Ws& ws,
-                              int path, uint32_t* status, cudaStream_t st) {
-  const DT* u = (const DT*)U;
-  const DT* w1 = (const DT*)W1;
-  const DT* w2 = (const DT*)W2;
-  const int BM = sh.B <= 32 ? 32 : (sh.B <= 64 ? 64 : 128);
-#define SPEC_TILE(BMV, P) launch_tile<DT, BMV, P>(sh, k, u, w1, w2, anchor, tokens, temp, ws, status, st)
-  if (path == 0 || sizeof(DT) == 4) {
-    if (BM == 32) return SPEC_TILE(32, 0);
-    if (BM == 64) return SPEC_TILE(64, 0);
-    return SPEC_TILE(128, 0);
+// Tensor maps of the draft's tensor-memory path: U as [B][gamma][V] with
+// 64 x 1 x 128 boxes, W2 as [r][V] with 64 x r boxes, both bf16 with the
+// 128-byte swizzle; reads outside the tensors return zeros.
+static cudaError_t encode_draft_maps(const Shape& sh, const void* U, const void* W2, TpMaps* maps) {
+  const EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t V = (cuuint64_t)sh.V;
+  {
+    const cuuint64_t dims[3] = {V, (cuuint64_t)sh.gamma, (cuuint64_t)sh.B};
+    const cuuint64_t strides[2] = {V * 2, V * 2 * (cuuint64_t)sh.gamma};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)TC_M};
+    const cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&maps->u, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(U), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
   }
-  if constexpr (sizeof(DT) == 2) {
-    if (path == 2 && sh.r % 64 == 0) return SPEC_TILE(128, 2);
+  {
+    const cuuint64_t dims[2] = {V, (cuuint64_t)sh.r};
+    const cuuint64_t strides[1] = {V * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)sh.r};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&maps->w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
   }
-  if (BM == 32) return SPEC_TILE(32, 1);
-  if (BM == 64) return SPEC_TILE(64, 1);
-  return SPEC_TILE(128, 1);
-#undef SPEC_TILE
-}
-
-template <typename DT>
-cudaError_t launch_draft_sample(const Shape& sh, int k, const void* U, const void* W1,
-                                const void* W2, const int* anchor, const float* temp,
-                                const float* u_draft, int* tokens, float* q_tok, double* lse_q,
-                                float* diag, uint32_t* status, const Ws& ws, const Eps& eps,
-                                cudaStream_t st) {
-  const size_t smem = (size_t)sh.r * BN * sizeof(DT);
-  cudaError_t e = cudaFuncSetAttribute(draft_sample_kernel<DT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  draft_sample_kernel<DT><<<sh.B, NT, smem, st>>>(sh, k, (const DT*)U, (const DT*)W1, (const DT*)W2,
-                                               anchor, temp, u_draft, tokens, q_tok, lse_q, diag,
-                                               status, ws, eps);
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 template <typename DT, int BM, int PATH>
 static cudaError_t launch_persist(const DraftParams& P, int nsm, cudaStream_t st) {
-  size_t smem = PATH == 2 ? TcLayout(P.sh.r, false).total : TileLayout<DT>(BM, P.sh.r, false).total;
+  size_t smem = PATH == 2 ? TpLayout(P.sh.r).total : TileLayout<DT>(BM, P.sh.r, false).total;
   smem = smem > (size_t)P.sh.r * HPB * sizeof(DT) ? smem : (size_t)P.sh.r * HPB * sizeof(DT);
   auto kern = draft_persistent_kernel<DT, BM, PATH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -577,7 +629,22 @@ cudaError_t launch_draft_persistent(const Shape& sh, const void* U, const void* 
                                     int* tokens, float* q_tok, double* lse_q, float* diag,
                                     uint32_t* status, const Ws& ws, const Eps& eps, int path,
                                     int nsm, cudaStream_t st) {
-  DraftParams P{sh, U, W1, W2, anchor, temp, u_draft, tokens, q_tok, lse_q, diag, status, ws, eps};
+  DraftParams P;
+  memset(&P.maps, 0, sizeof(P.maps));
+  P.sh = sh;
+  P.U = U;
+  P.W1 = W1;
+  P.W2 = W2;
+  P.anchor = anchor;
+  P.temp = temp;
+  P.u_draft = u_draft;
+  P.tokens = tokens;
+  P.q_tok = q_tok;
+  P.lse_q = lse_q;
+  P.diag = diag;
+  P.status = status;
+  P.ws = ws;
+  P.eps = eps;
   const int BM = sh.B <= 32 ? 32 : (sh.B <= 64 ? 64 : 128);
   if (path == 0 || sizeof(DT) == 4) {
     if (BM == 32) return launch_persist<DT, 32, 0>(P, nsm, st);
@@ -585,7 +652,11 @@ cudaError_t launch_draft_persistent(const Shape& sh, const void* U, const void* 
     return launch_persist<DT, 128, 0>(P, nsm, st);
   }
   if constexpr (sizeof(DT) == 2) {
-    if (path == 2 && sh.r % 64 == 0) return launch_persist<DT, 128, 2>(P, nsm, st);
+    if (path == 2 && sh.r % 64 == 0) {
+      const cudaError_t e = encode_draft_maps(sh, U, W2, &P.maps);
+      if (e != cudaSuccess) return e;
+      return launch_persist<DT, 128, 2>(P, nsm, st);
+    }
   }
   if (BM == 32) return launch_persist<DT, 32, 1>(P, nsm, st);
   if (BM == 64) return launch_persist<DT, 64, 1>(P, nsm, st);
@@ -602,19 +673,5 @@ template cudaError_t launch_draft_persistent<bf16>(const Shape&, const void*, co
                                                    const float*, int*, float*, double*, float*,
                                                    uint32_t*, const Ws&, const Eps&, int, int,
                                                    cudaStream_t);
-template cudaError_t launch_draft_tile<float>(const Shape&, int, const void*, const void*,
-                                              const void*, const int*, const int*, const float*,
-                                              const Ws&, int, uint32_t*, cudaStream_t);
-template cudaError_t launch_draft_tile<bf16>(const Shape&, int, const void*, const void*,
-                                             const void*, const int*, const int*, const float*,
-                                             const Ws&, int, uint32_t*, cudaStream_t);
-template cudaError_t launch_draft_sample<float>(const Shape&, int, const void*, const void*,
-                                                const void*, const int*, const float*, const float*,
-                                                int*, float*, double*, float*, uint32_t*, const Ws&,
-                                                const Eps&, cudaStream_t);
-template cudaError_t launch_draft_sample<bf16>(const Shape&, int, const void*, const void*,
-                                               const void*, const int*, const float*, const float*,
-                                               int*, float*, double*, float*, uint32_t*, const Ws&,
-                                               const Eps&, cudaStream_t);
 
 }  // namespace spec

@@ -14,12 +14,13 @@ typedef __nv_bfloat16 bf16;
 
 // ---------------------------------------------------------------- geometry
 constexpr int BN = 128;       // vocabulary columns per slice (one GEMM tile's N)
+constexpr int CW = 32;        // vocabulary columns per draft partial (chunk)
 constexpr int HPB = 256;      // columns per extended-precision block
 constexpr int NT = 256;       // threads per CTA for every kernel
 constexpr int MAX_GAMMA = 16;
 
 struct Shape {
-  int B, gamma, V, r, NS, HB;   // NS = ceil(V / BN), HB = ceil(V / HPB)
+  int B, gamma, V, r, NS, NC, HB;   // NS = ceil(V / BN), NC = ceil(V / CW), HB = ceil(V / HPB)
 };
 
 // A decision queued for re-decision in extended precision.
@@ -41,13 +42,15 @@ enum {
 };
 
 // Workspace views (host computes the offsets; see spec_abi.cu).
+constexpr int TRACE_SLOTS = 8;   // timestamps per draft step (persistent kernel trace)
 struct Ws {
   uint32_t* ctrl;       // [CTRL_WORDS]
+  unsigned long long* trace;  // [MAX_GAMMA][TRACE_SLOTS] globaltimer ns, CTA 0
   HpItem* items;        // [max_items]
   int max_items;
   double* hpsum;        // [max_items][HB][3]
   // draft
-  float4* dpart;        // [B][NS] (c, m, s, q2)
+  float4* dpart;        // [B][NC] draft partials per CW-column chunk: (c, m, s, q2)
   // verify
   int* rowptr;          // [B+1]
   int2* prow;           // [B*gamma] packed (b, j), j < L_b
@@ -292,6 +295,12 @@ __device__ __forceinline__ void set_status(uint32_t* st, uint32_t bits) {
   if (st) atomicOr(st, bits);
 }
 __device__ __forceinline__ bool temp_ok(float T) { return isfinite(T) && T > 0.f; }
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;

@@ -1,0 +1,309 @@
+// Warp-specialised tensor-memory tile engine for the draft step's rank-r bias
+// tiles (bf16, r % 64 == 0).  A CTA walks its share of (request tile, slice of
+// BN vocabulary columns) tiles; the roles run concurrently and hand buffers to
+// each other through shared-memory mbarriers:
+//
+//   warp 4, one lane   TMA producer: the W2 slice (r x BN, read in place as the
+//                      MN-major B operand, 128-byte swizzle) and the U_k tile
+//                      (128 rows x BN logits, 128-byte swizzle) of each tile.
+//   warps 6-7          gather the W1[x_{k-1}] rows of a request tile (the A
+//                      operand, K-major, 128-byte swizzle) with cp.async, once
+//                      per request tile, after the last MMA that read the old
+//                      rows has completed (a barrier of its own, committed once
+//                      per request tile: every waiter waits for each phase of
+//                      the barriers it polls in turn, so a parity test is never
+//                      two phases behind).
+//   warp 5, one lane   issues the r/16 MMAs of a tile (M = 128, N = 128, K = 16)
+//                      into one of two 128-column TMEM accumulators and commits
+//                      them to the accumulator's "full" barrier and to the W2
+//                      stage's "empty" barrier.
+//   warps 0-3          epilogue, thread = tile row = TMEM lane: reads its row of
+//                      the accumulator (tcgen05.ld) and of the U tile (shared
+//                      memory) and reduces it to the slice partial without
+//                      exchanging anything with other threads.
+//
+// Barrier phases are counted with running per-CTA counters (tiles, request
+// tiles) that every thread advances identically, so the state carries over
+// from one draft step to the next without re-initialising the barriers.
+// Every wait is bounded; a wait that gives up raises a CTA-wide failure flag
+// that makes every other wait return at once.
+#pragma once
+
+#include <cuda.h>
+
+#include "spec_tc.cuh"
+
+namespace spec {
+
+constexpr uint32_t TP_TMEM_COLS = 256;         // two 128-column fp32 accumulators
+constexpr int TP_UBYTES = TC_M * BN * 2;       // one U tile (bf16)
+
+// Barrier slots.
+enum : int {
+  TB_W2_FULL = 0,    // + stage (2)
+  TB_W2_EMPTY = 2,   // + stage (2)
+  TB_U_FULL = 4,     // + buffer (2)
+  TB_U_EMPTY = 6,    // + buffer (2)
+  TB_T_FULL = 8,     // + accumulator (2)
+  TB_T_EMPTY = 10,   // + accumulator (2)
+  TB_A_FULL = 12,
+  TB_A_EMPTY = 13,   // committed after the last MMA of each request tile
+  TB_COUNT = 14
+};
+
+// Shared-memory plan (offsets from a 1024-byte aligned base).
+struct TpLayout {
+  int nw;                                      // W2 stages (2 when they fit)
+  size_t offA, offW, offU, total;
+  __host__ __device__ TpLayout(int r) {
+    const size_t a = (size_t)(r / 64) * 16384, w = (size_t)2 * r * 128;
+    nw = (a + 2 * w + 2 * TP_UBYTES <= (size_t)208 * 1024) ? 2 : 1;
+    offA = 0;
+    offW = a;
+    offU = offW + (size_t)nw * w;
+    total = offU + 2 * (size_t)TP_UBYTES + 1024;   // + slack for 1 KB alignment
+  }
+};
+
+// Tensor maps of one draft call (encoded on the host, passed as a
+// __grid_constant__ kernel parameter).
+struct alignas(64) TpMaps {
+  CUtensorMap u;     // U viewed as [B][gamma][V], box 64 x 1 x 128, 128-byte swizzle
+  CUtensorMap w2;    // W2 viewed as [r][V],       box 64 x r,       128-byte swizzle
+};
+
+// Pipeline state of a CTA, identical in every thread.
+struct TpState {
+  uint32_t tmem;     // base of the 256 TMEM columns
+  uint64_t* bar;     // TB_COUNT mbarriers
+  int* fail;         // CTA-wide failure flag (shared)
+  uint32_t gi;       // tiles processed so far by this CTA
+  uint32_t ga;       // request tiles gathered so far
+};
+
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void tp_init(uint64_t* bar) {
+  for (int s = 0; s < 2; ++s) {
+    mbar_init(bar + TB_W2_FULL + s, 1);
+    mbar_init(bar + TB_W2_EMPTY + s, 1);
+    mbar_init(bar + TB_U_FULL + s, 1);
+    mbar_init(bar + TB_U_EMPTY + s, TC_M);
+    mbar_init(bar + TB_T_FULL + s, 1);
+    mbar_init(bar + TB_T_EMPTY + s, TC_M);
+  }
+  mbar_init(bar + TB_A_FULL, 64);
+  mbar_init(bar + TB_A_EMPTY, 1);
+}
+
+// ---------------------------------------------------------------- primitives
+// Bounded wait for the completion of the phase with parity `parity`; gives up
+// after about 2^22 polls, or at once when another thread raised *fail.
+__device__ __forceinline__ bool tp_wait(uint64_t* bar, uint32_t parity, volatile int* fail) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t it = 0; it < (1u << 22); ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity));
+    if (done) return true;
+    if ((it & 63) == 63) {
+      if (*fail) return false;
+      __nanosleep(64);
+    }
+  }
+  *fail = 1;
+  return false;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// TMA tile loads into shared memory, completing on `bar` (bytes counted).
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4}], [%5];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(const unsigned char* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p)));
+  return v;
+}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// 16-byte chunk j (0..15) of row m of a 128-byte-swizzled [128][BN] bf16 tile
+// stored as two 64-column boxes.
+__device__ __forceinline__ const unsigned char* tp_uchunk(const unsigned char* ub, int m, int j) {
+  return ub + (j >> 3) * (TC_M * 128) + m * 128 + (((j & 7) ^ (m & 7)) << 4);
+}
+
+// ---------------------------------------------------------------- the engine
+// Tile list of this CTA: tiles t0 + i * G, i < n; tile t is (request tile
+// t / NS, slice t % NS).  E supplies:
+//   int  step()                              draft step k (U_k, tokens x_{k-1})
+//   int  token(int mtile, int m)             W1 row of row m, -1 for none
+//   void epilogue(int mtile, int slice, int m, const unsigned char* ub,
+//                 uint32_t tmem_row)         one row of one tile
+// `s_tok` is a 128-entry shared array for the gatherers.  Returns false if a
+// wait gave up (after draining what it started).
+template <class E>
+__device__ __forceinline__ bool tp_run(const E& e, const Shape& sh, const TpMaps& maps,
+                                       const bf16* W1, int t0, int G, int n,
+                                       unsigned char* smem_raw, TpState& st, int* s_tok) {
+  if (n <= 0) return true;
+  unsigned char* smem = align1k(smem_raw);
+  const TpLayout lay(sh.r);
+  unsigned char* As = smem + lay.offA;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = sh.r, k = e.step();
+  const uint32_t wbytes = (uint32_t)(2 * r * 128);
+  uint64_t* bar = st.bar;
+  volatile int* fail = st.fail;
+  auto mt_of = [&](int i) { return (t0 + i * G) / sh.NS; };
+  auto sl_of = [&](int i) { return (t0 + i * G) % sh.NS; };
+
+  // Earlier generic-proxy use of these buffers (sampling, re-decision phases)
+  // is ordered before this phase's TMA and MMA accesses.
+  fence_async_shared();
+  __syncthreads();
+
+  if (warp == 4) {
+    if (lane == 0) {
+      tma_prefetch_map(&maps.u);
+      tma_prefetch_map(&maps.w2);
+      for (int i = 0; i < n && !*fail; ++i) {
+        const uint32_t g = st.gi + i;
+        const int s = (int)(g % (uint32_t)lay.nw);
+        const uint32_t f = g / (uint32_t)lay.nw;
+        if (f >= 1 && !tp_wait(bar + TB_W2_EMPTY + s, (f - 1) & 1u, fail)) break;
+        unsigned char* wb = smem + lay.offW + (size_t)s * wbytes;
+        const int n0 = sl_of(i) * BN;
+        mbar_expect_tx(bar + TB_W2_FULL + s, wbytes);
+        tma_load_2d(wb, &maps.w2, n0, 0, bar + TB_W2_FULL + s);
+        tma_load_2d(wb + r * 128, &maps.w2, n0 + 64, 0, bar + TB_W2_FULL + s);
+        const int b = (int)(g & 1u);
+        const uint32_t fu = g >> 1;
+        if (fu >= 1 && !tp_wait(bar + TB_U_EMPTY + b, (fu - 1) & 1u, fail)) break;
+        unsigned char* ub = smem + lay.offU + (size_t)b * TP_UBYTES;
+        const int m0 = mt_of(i) * TC_M;
+        mbar_expect_tx(bar + TB_U_FULL + b, (uint32_t)TP_UBYTES);
+        tma_load_3d(ub, &maps.u, n0, k, m0, bar + TB_U_FULL + b);
+        tma_load_3d(ub + TC_M * 128, &maps.u, n0 + 64, k, m0, bar + TB_U_FULL + b);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      const uint32_t idesc = tc_idesc();
+      const uint32_t a0 = smem_u32(As);
+      uint32_t ga = st.ga;
+      for (int i = 0; i < n; ++i) {
+        const uint32_t g = st.gi + i;
+        if (i == 0 || mt_of(i) != mt_of(i - 1)) {
+          if (!tp_wait(bar + TB_A_FULL, ga & 1u, fail)) break;
+          ++ga;
+        }
+        const int s = (int)(g % (uint32_t)lay.nw);
+        if (!tp_wait(bar + TB_W2_FULL + s, (g / (uint32_t)lay.nw) & 1u, fail)) break;
+        const int b = (int)(g & 1u);
+        if (g >= 2 && !tp_wait(bar + TB_T_EMPTY + b, ((g >> 1) - 1) & 1u, fail)) break;
+        tc_fence_after();
+        const uint32_t w0 = smem_u32(smem + lay.offW + (size_t)s * wbytes);
+        const uint32_t d = st.tmem + (uint32_t)(b * 128);
+        for (int kk = 0; kk < r; kk += 16) {
+          const uint64_t ad = tc_sdesc(a0 + (uint32_t)((kk >> 6) * 16384 + (kk & 63) * 2), 16, 1024);
+          const uint64_t bd = tc_sdesc(w0 + (uint32_t)(kk * 128), (uint32_t)(r * 128), 1024);
+          tc_mma(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar + TB_T_FULL + b);
+        tc_commit(bar + TB_W2_EMPTY + s);
+        if (i == n - 1 || mt_of(i + 1) != mt_of(i)) tc_commit(bar + TB_A_EMPTY);
+      }
+    }
+  } else if (warp >= 6) {
+    // 64 gatherers; thread q copies 16-byte chunks q, q + 64, ... of the A tile
+    const int q0 = threadIdx.x - 192;
+    const int cpr = r / 8;
+    uint32_t ga = st.ga;
+    for (int i = 0; i < n && !*fail; ++i) {
+      if (i > 0 && mt_of(i) == mt_of(i - 1)) continue;
+      // the last MMA that read the previous request tile's rows
+      if (ga >= 1 && !tp_wait(bar + TB_A_EMPTY, (ga - 1) & 1u, fail)) break;
+      ++ga;
+      const int mt = mt_of(i);
+      for (int m = q0; m < TC_M; m += 64) s_tok[m] = e.token(mt, m);
+      named_bar(1, 64);
+      for (int c = q0; c < TC_M * cpr; c += 64) {
+        const int m = c / cpr, j = c - m * cpr;
+        const int tok = s_tok[m];
+        const bool valid = tok >= 0;
+        const bf16* src = valid ? W1 + (size_t)tok * r + j * 8 : W1;
+        unsigned char* dst = As + (size_t)(j >> 3) * 16384 + m * 128 + (((j & 7) ^ (m & 7)) << 4);
+        cp_async16(dst, src, valid);
+      }
+      cp_async_commit();
+      cp_async_wait_all();
+      fence_async_shared();
+      mbar_arrive(bar + TB_A_FULL);
+      named_bar(1, 64);          // s_tok is free for the next request tile
+    }
+  } else {
+    // epilogue: thread = row
+    const int m = threadIdx.x;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    for (int i = 0; i < n; ++i) {
+      const uint32_t g = st.gi + i;
+      const int b = (int)(g & 1u);
+      if (!tp_wait(bar + TB_U_FULL + b, (g >> 1) & 1u, fail)) break;
+      if (!tp_wait(bar + TB_T_FULL + b, (g >> 1) & 1u, fail)) break;
+      tc_fence_after();
+      e.epilogue(mt_of(i), sl_of(i), m, smem + lay.offU + (size_t)b * TP_UBYTES,
+                 st.tmem + lane_base + (uint32_t)(b * 128));
+      tc_fence_before();
+      mbar_arrive(bar + TB_T_EMPTY + b);
+      mbar_arrive(bar + TB_U_EMPTY + b);
+    }
+  }
+  // advance the running counters identically in every thread
+  uint32_t segs = 0;
+  for (int i = 0; i < n; ++i) segs += (i == 0 || mt_of(i) != mt_of(i - 1)) ? 1u : 0u;
+  st.gi += (uint32_t)n;
+  st.ga += segs;
+  __syncwarp();
+  __syncthreads();
+  if (*fail) {
+    // drain: the last accumulator's commit covers every MMA issued before it
+    const uint32_t g = st.gi - 1;
+    if (threadIdx.x == 0) mbar_wait(bar + TB_T_FULL + (g & 1u), (g >> 1) & 1u, 1u << 20);
+    __syncthreads();
+    return false;
+  }
+  return true;
+}
+
+}  // namespace spec

@@ -100,7 +100,8 @@ def test_status_strings_and_options(L):
     assert L.spec_set_option(_lib.SPEC_OPT_EPS_SCALE, 1.0) == 0
     n = L.spec_num_stages()
     names = [L.spec_stage_name(i).decode() for i in range(n)]
-    assert "draft_tile" in names and "verify_tile" in names and len(set(names)) == n
+    assert "draft_persistent" in names and "verify_tile" in names and len(set(names)) == n
+    assert L.spec_set_option(4, 1.0) == -1          # unused key
 
 
 def test_missing_library_fails_loudly(tmp_path):

@@ -218,7 +218,7 @@ def test_profile_api_counts_launches():
         prof = _lib.spec_profile_read()
     finally:
         _lib.spec_profile_enable(False)
-    assert prof["draft_tile"][1] == w.gamma
+    assert prof["draft_persistent"][1] == 1           # the whole draft: one cooperative launch
     assert prof["verify_tile"][1] == 1
     assert all(ms >= 0 for ms, _ in prof.values())
 
@@ -274,35 +274,23 @@ def test_tcgen05_full_size(tc_path, name, sample):
 
 # ----------------------------------------------------------------------------- persistent draft
 
-@pytest.fixture()
-def persistent():
-    _lib.spec_set_option(_lib.SPEC_OPT_DRAFT_MODE, 1)
-    yield
-    _lib.spec_set_option(_lib.SPEC_OPT_DRAFT_MODE, 1)
-
-
-@pytest.fixture()
-def per_step():
-    _lib.spec_set_option(_lib.SPEC_OPT_DRAFT_MODE, 0)
-    yield
-    _lib.spec_set_option(_lib.SPEC_OPT_DRAFT_MODE, 1)
-
-
-@pytest.mark.parametrize("spec_name", ["C0", "small", "adversarial"])
-def test_per_step_draft_parity(per_step, spec_name):
-    """The step-by-step draft launches stay selectable and exact."""
-    spec = {"C0": W.config("C0"), "small": SMALL, "adversarial": dict(SMALL, B=24)}[spec_name]
+@pytest.mark.parametrize("spec_name", ["C0", "small"])
+def test_draft_near_boundary_at_step_one(spec_name):
+    """Every request's second draw sits just past a CDF breakpoint (the draw
+    after the first token, so the step reads tokens written by the previous
+    step of the same launch)."""
+    spec = {"C0": W.config("C0"), "small": dict(SMALL, B=24)}[spec_name]
     w = W.make_workload(spec, trial=6)
-    if spec_name == "adversarial":
-        res = oracle_cycle(w)
-        for b in range(w.B):
-            w.u_draft[b, 1] = _near(res.draft[b].F_hi[1])
+    res = oracle_cycle(w)
+    for b in range(w.B):
+        w.u_draft[b, 1] = _near(res.draft[b].F_hi[1])
     g, res, rep = run_and_compare(w)
+    assert g.dstatus[0] & 8 == 0
     assert_parity(rep)
 
 
 @pytest.mark.parametrize("spec_name", ["C0", "small", "stress", "tc-two-tiles"])
-def test_persistent_draft_parity(persistent, spec_name):
+def test_persistent_draft_parity(spec_name):
     """The whole draft as one cooperative launch (grid barriers between the
     tile, sampling and re-decision phases of every step)."""
     spec = {"C0": W.config("C0"), "small": SMALL, "stress": W.stress(SMALL),
@@ -314,7 +302,7 @@ def test_persistent_draft_parity(persistent, spec_name):
         assert_parity(rep)
 
 
-def test_persistent_adversarial(persistent):
+def test_persistent_adversarial():
     w = W.make_workload(dict(SMALL, B=24, name="adv-p"), trial=5)
     res = oracle_cycle(w)
     for b in range(w.B):
@@ -327,7 +315,7 @@ def test_persistent_adversarial(persistent):
 
 
 @pytest.mark.parametrize("name,sample", [("C1", None), ("C2", 24), ("C3", 3), ("C4", 5)])
-def test_persistent_full_size(persistent, name, sample):
+def test_persistent_full_size(name, sample):
     w = W.make_workload(W.config(name), trial=2)
     rows = None
     if sample is not None:
