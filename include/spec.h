@@ -141,8 +141,8 @@ size_t spec_workspace_bytes(int32_t B, int32_t gamma, int32_t V, int32_t r, int3
 
 /* Draft gamma tokens per request.  Reads U, W1, W2, anchor, temperature,
  * u_draft; writes draft_tokens, q_tok, lse_q, dev_status (and diag).
- * The work is two cudaMemsetAsync (dev_status, the workspace's control
- * words) and ONE cooperative kernel launch on `stream` with one CTA per SM
+ * The work is three cudaMemsetAsync (dev_status, the workspace's control
+ * words and counters) and ONE cooperative kernel launch on `stream` with one CTA per SM
  * (fewer when there are fewer tiles); it returns SPEC_ECUDA when the device
  * cannot make the CTAs co-resident.  Its grid barriers are bounded waits: a
  * barrier that gives up sets SPEC_DEV_TIMEOUT and every CTA returns.       */
@@ -167,10 +167,10 @@ int32_t spec_verify(const spec_verify_args* args, spec_stream_t stream);
  * process exits.  It never calls cudaMalloc, cudaFree or any allocating
  * library routine.
  *
- *   - Size limit: the draft scratch is 128 + B*40 + B*ceil(V/256)*24 +
+ *   - Size limit: the draft scratch is 128 + B*40 + B*ceil(V/32)*8 + B*4 +
  *     B*ceil(V/32)*16 bytes (each term rounded up to 256); larger problems
  *     are rejected with SPEC_EWORKSPACE before anything is enqueued.  All five
- *     named workloads fit (C4, the largest, needs about 19 MiB).
+ *     named workloads fit (C4, the largest, needs about 24 MiB).
  *   - The first call on a device looks up the area's device address with
  *     cudaGetSymbolAddress (with that device current) and caches it; make
  *     that first call before any stream capture.
@@ -179,7 +179,7 @@ int32_t spec_verify(const spec_verify_args* args, spec_stream_t stream);
  *     Calls whose GPU work overlaps -- on different streams, or from
  *     different threads without ordering -- race on it: serialise them.
  */
-#define SPEC_STATIC_SCRATCH_BYTES ((size_t)24 << 20)
+#define SPEC_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 int32_t spec_markov_draft_static(const spec_draft_args* args, spec_stream_t stream);
 
 /* Static text for a spec_status value. */

@@ -133,7 +133,7 @@ int num_sms() {
 
 // ---------------------------------------------------------------- workspace
 struct Layout {
-  size_t ctrl, trace, items, hpsum, dpart, rowptr, prow, prevtok, vflags, lse_p, bpart, vpart, slow,
+  size_t ctrl, trace, items, hpsum, hpcnt, dpart, rowptr, prow, prevtok, vflags, lse_p, bpart, vpart, slow,
       accbits, rowc, rowp, total;
   int max_items;
 };
@@ -146,12 +146,13 @@ Layout layout(const Shape& sh) {
     off = (off + bytes + 255) & ~(size_t)255;
     return o;
   };
-  const size_t B = sh.B, g = sh.gamma, NS = sh.NS, HB = sh.HB;
+  const size_t B = sh.B, g = sh.gamma, NS = sh.NS;
   L.max_items = sh.B;
   L.ctrl = take(CTRL_WORDS * sizeof(uint32_t));
   L.trace = take(MAX_GAMMA * TRACE_SLOTS * sizeof(unsigned long long));
   L.items = take((size_t)L.max_items * sizeof(HpItem));
-  L.hpsum = take((size_t)L.max_items * HB * 3 * sizeof(double));
+  L.hpsum = take((size_t)L.max_items * 3 * sh.NC * sizeof(float2));
+  L.hpcnt = take((size_t)L.max_items * sizeof(uint32_t));
   L.dpart = take(B * sh.NC * sizeof(float4));
   L.rowptr = take((B + 1) * sizeof(int));
   L.prow = take(B * g * sizeof(int2));
@@ -175,7 +176,9 @@ Ws views(const Layout& L, void* base) {
   w.trace = nullptr;
   w.items = reinterpret_cast<HpItem*>(p + L.items);
   w.max_items = L.max_items;
-  w.hpsum = reinterpret_cast<double*>(p + L.hpsum);
+  w.hpsum = reinterpret_cast<float2*>(p + L.hpsum);
+  w.hp_cols = 3;
+  w.hpcnt = reinterpret_cast<uint32_t*>(p + L.hpcnt);
   w.dpart = reinterpret_cast<float4*>(p + L.dpart);
   w.rowptr = reinterpret_cast<int*>(p + L.rowptr);
   w.prow = reinterpret_cast<int2*>(p + L.prow);
@@ -232,6 +235,7 @@ int launch_draft(const spec_draft_args* a, const Shape& sh, const Ws& ws, cudaSt
   }
   SPEC_TRY(cudaMemsetAsync(a->dev_status, 0, 4 * sizeof(uint32_t), st));
   SPEC_TRY(cudaMemsetAsync(ws.ctrl, 0, CTRL_WORDS * sizeof(uint32_t), st));
+  SPEC_TRY(cudaMemsetAsync(ws.hpcnt, 0, (size_t)ws.max_items * sizeof(uint32_t), st));
   ProfScope p(st, ST_DRAFT_PERSISTENT);
   SPEC_TRY(launch_draft_persistent<DT>(sh, a->U, a->W1, a->W2, a->anchor, a->temperature, a->u_draft,
                                        a->draft_tokens, a->q_tok, a->lse_q, a->diag, a->dev_status,
@@ -322,7 +326,8 @@ Layout draft_only_layout(const Shape& sh) {
   L.max_items = sh.B;
   L.ctrl = take(CTRL_WORDS * sizeof(uint32_t));
   L.items = take((size_t)L.max_items * sizeof(HpItem));
-  L.hpsum = take((size_t)L.max_items * sh.HB * 3 * sizeof(double));
+  L.hpsum = take((size_t)L.max_items * sh.NC * sizeof(float2));
+  L.hpcnt = take((size_t)L.max_items * sizeof(uint32_t));
   L.dpart = take((size_t)sh.B * sh.NC * sizeof(float4));
   L.total = off;
   return L;
@@ -334,7 +339,9 @@ Ws draft_only_views(const Layout& L, void* base) {
   w.ctrl = reinterpret_cast<uint32_t*>(p + L.ctrl);
   w.items = reinterpret_cast<HpItem*>(p + L.items);
   w.max_items = L.max_items;
-  w.hpsum = reinterpret_cast<double*>(p + L.hpsum);
+  w.hpsum = reinterpret_cast<float2*>(p + L.hpsum);
+  w.hp_cols = 1;
+  w.hpcnt = reinterpret_cast<uint32_t*>(p + L.hpcnt);
   w.dpart = reinterpret_cast<float4*>(p + L.dpart);
   return w;
 }

@@ -238,9 +238,10 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   __shared__ float s_part[NT / CW][CW];
   __shared__ int s_slice, s_tok;
   __shared__ float s_pref[2], s_lo, s_hi, s_wtok;
-  __shared__ double s_tin;
+  __shared__ df s_tab[DD_EXP_TAB];
 
   __syncthreads();      // previous use of the shared buffers is finished
+  if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(s_tab, threadIdx.x);
   const size_t ok = (size_t)b * sh.gamma + k;
   const int prev = (k == 0) ? anchor[b] : __ldcg(tokens + ok - 1);
   const float T = temp[b];
@@ -302,30 +303,27 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   const df excl = block_excl_scan_df(loc, &Zdf, sh_f);
   q2 = block_sum(q2, sh_f);
   m2 = block_sum(m2, sh_f);
-  const double Z = df_d(Zdf);
+  // (fp32 and double-float only below: GB300's fp64 rate is low)
   const float u = u_draft[ok];
-  const df target = df_from_d((double)u * Z);
+  const df target = dd_mul_f(Zdf, u);
 
   // ---- crossing chunk: first s with prefix_incl(s) > target
   if (threadIdx.x == 0) s_slice = 0x7fffffff;
   __syncthreads();
   int my_slice = -1;
   df my_pref = {0.f, 0.f};
-  {
-    const df tneg = df_neg(target);
-    if (df_d(df_add(excl, tneg)) <= 0.0 && df_d(df_add(df_add(excl, loc), tneg)) > 0.0) {
-      df run = excl;
-      for (int s = s0, q = 0; s < s1; ++s, ++q) {
-        const float4 p = (q < 8) ? pv[q] : __ldcg(P + s);
-        const df nxt = df_addf(run, p.z * chunk_factor(p, cM, mM, invT));
-        if (df_d(df_add(nxt, tneg)) > 0.0) {
-          my_slice = s;
-          my_pref = run;
-          atomicMin(&s_slice, s);
-          break;
-        }
-        run = nxt;
+  if (s0 < s1 && dd_le(excl, target) && !dd_le(df_add(excl, loc), target)) {
+    df run = excl;
+    for (int s = s0, q = 0; s < s1; ++s, ++q) {
+      const float4 p = (q < 8) ? pv[q] : __ldcg(P + s);
+      const df nxt = df_addf(run, p.z * chunk_factor(p, cM, mM, invT));
+      if (!dd_le(nxt, target)) {
+        my_slice = s;
+        my_pref = run;
+        atomicMin(&s_slice, s);
+        break;
       }
+      run = nxt;
     }
   }
   __syncthreads();
@@ -353,8 +351,6 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   const df pref = {s_pref[0], s_pref[1]};
   const float4 PS = __ldcg(P + sl);
   const float fS = chunk_factor(PS, cM, mM, invT);
-  if (threadIdx.x == 0) s_tin = (df_d(target) - df_d(pref)) / (double)fS;   // chunk units
-  __syncthreads();
   const int n0 = sl * CW;
 
   // ---- recompute the chunk's CW weights: 8 k-groups x CW columns
@@ -377,6 +373,8 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
       for (int g = 1; g < NT / CW; ++g) bias = __fadd_rn(bias, s_part[g][lane]);
       w = fast_w(fast_x(ldf(U + ok * sh.V + v), PS.x, bias, invT), PS.y);
     }
+    // target inside the chunk, in the chunk's units: (u Z - prefix) / fS
+    const df tin = dd_mul(dd_add(target, dd_neg(pref)), dd_recip(fS));
     // inclusive double-float scan across the warp
     df inc = df_make(w);
     for (int d = 1; d < 32; d <<= 1) {
@@ -385,16 +383,15 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
     }
     df ex = shfl_up_df(inc, 1);
     if (lane == 0) ex = {0.f, 0.f};
-    const double lo = df_d(ex), hi = df_d(inc), tin = s_tin;
-    const bool claim = w > 0.f && lo <= tin && hi > tin;
+    const bool claim = w > 0.f && dd_le(ex, tin) && !dd_le(inc, tin);
     const uint32_t cl = __ballot_sync(0xffffffffu, claim);
     const uint32_t pos = __ballot_sync(0xffffffffu, w > 0.f);
     int t;
     float dlo = 0.f, dhi = 0.f;
     if (cl) {
       t = __ffs(cl) - 1;
-      dlo = __shfl_sync(0xffffffffu, (float)(tin - lo), t);
-      dhi = __shfl_sync(0xffffffffu, (float)(hi - tin), t);
+      dlo = __shfl_sync(0xffffffffu, dd_add(tin, dd_neg(ex)).hi, t);
+      dhi = __shfl_sync(0xffffffffu, dd_add(inc, dd_neg(tin)).hi, t);
     } else {
       fallback = true;
       t = pos ? 31 - __clz(pos) : 0;           // last entry with mass
@@ -411,18 +408,21 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   if (s_lo == 0.f && s_hi == 0.f) fallback = true;
   if (threadIdx.x == 0) {
     const int tok = n0 + s_tok;
-    const double dmargin = fmin((double)s_lo, (double)s_hi) * (double)fS / Z;
-    const double qrow = sqrt((double)q2) / Z, mrow = sqrt((double)m2) / Z;
-    const double band = (double)eps.scale * ((double)eps.elem * qrow + (double)eps.slice * mrow +
-                                             (double)eps.abs_);
-    const double lse = ((double)cM * (1.0 / (double)T) + (double)mM) + log(Z);
+    const float Zf = Zdf.hi;
+    const float scale = __fdiv_rn(fS, Zf);                 // chunk units -> probability
+    const float dmargin = fminf(s_lo, s_hi) * scale;
+    const float band = eps.scale * (eps.elem * __fdiv_rn(sqrtf(q2), Zf) +
+                                    eps.slice * __fdiv_rn(sqrtf(m2), Zf) + eps.abs_);
+    // lse = cM / T + mM + log Z
+    const df ref = dd_add_f(dd_mul_f(dd_recip(T), cM), mM);
+    const double lse = dd_to_double(ref) + dd_log(Zdf, s_tab);
     tokens[ok] = tok;
-    q_tok[ok] = (float)((double)s_wtok * (double)fS / Z);
+    q_tok[ok] = s_wtok * scale;
     lse_q[ok] = lse;
     if (diag) {
-      diag[ok * 4 + 0] = (float)((double)s_lo * fS / Z);
-      diag[ok * 4 + 1] = (float)((double)s_hi * fS / Z);
-      diag[ok * 4 + 2] = (float)band;
+      diag[ok * 4 + 0] = s_lo * scale;
+      diag[ok * 4 + 1] = s_hi * scale;
+      diag[ok * 4 + 2] = band;
       diag[ok * 4 + 3] = (float)tok;
     }
     if (fallback || dmargin <= band) {
@@ -441,7 +441,7 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
 }
 
 // ---------------------------------------------------------------- kernel
-struct alignas(64) DraftParams {
+struct DraftParams {
   TpMaps maps;       // tensor-memory path only
   Shape sh;
   const void* U;
@@ -524,10 +524,9 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
     if (tr) tr[k * TRACE_SLOTS + 4] = globaltimer_ns();
     const int n = min((int)__ldcg(ctrl + CTRL_STEP0 + k), P.ws.max_items);
     if (n > 0) {
-      hp_sums_body<DT>(sh, R, P.ws, 0, n, smem_raw);
-      if (!grid_sync(ctrl, G, gen, P.status)) break;
+      // block sums; the CTA that completes an item's last block re-decides it
+      hp_sums_body<DT>(sh, R, P.ws, 0, n, smem_raw, true, P.tokens, P.q_tok, P.lse_q, P.status);
       if (tr) tr[k * TRACE_SLOTS + 5] = globaltimer_ns();
-      hp_decide_body<DT>(sh, R, P.ws, n, P.tokens, P.q_tok, P.lse_q, nullptr, P.status, smem_raw);
       if (!grid_sync(ctrl, G, gen, P.status)) break;
     }
     if (tr) {
@@ -596,7 +595,8 @@ static cudaError_t encode_draft_maps(const Shape& sh, const void* U, const void*
 template <typename DT, int BM, int PATH>
 static cudaError_t launch_persist(const DraftParams& P, int nsm, cudaStream_t st) {
   size_t smem = PATH == 2 ? TpLayout(P.sh.r).total : TileLayout<DT>(BM, P.sh.r, false).total;
-  smem = smem > (size_t)P.sh.r * HPB * sizeof(DT) ? smem : (size_t)P.sh.r * HPB * sizeof(DT);
+  const size_t slab = (size_t)P.sh.r * HPB * sizeof(DT);    // re-decision W2 slab (> sampler's)
+  smem = smem > slab ? smem : slab;
   auto kern = draft_persistent_kernel<DT, BM, PATH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -1,7 +1,10 @@
-// Extended-precision re-decision: shared device code (see spec_refine.cu for
-// the method and its sources).  Data written by other CTAs of the same launch
-// (queued items, block sums) is read through L2 (ld.global.cg) so the bodies
-// also serve the persistent draft kernel.
+// Extended-precision re-decision: shared device code (spec_refine.cu describes
+// the method).  Every weight, sum and scan here is a double-float (spec_df.cuh)
+// -- accurate to about 1e-13 relative, far below the first pass's error band
+// -- so the path runs at the fp32 rate; fp64 appears only in a few per-item
+// scalars.  Data written by other CTAs of the same launch (queued items, block
+// sums) is read through L2 (ld.global.cg), so the bodies also serve the
+// persistent draft kernel.
 #pragma once
 
 #include "spec_gemm.cuh"
@@ -23,36 +26,49 @@ __device__ __forceinline__ HpItem ldcg_item(const HpItem* p) {
   return h;
 }
 
-__device__ __forceinline__ void init_exp_table(double* tab) {
-  if (threadIdx.x < 32) tab[threadIdx.x] = exp2((double)threadIdx.x / 32.0);
-}
-
-// e^x, |relative error| ~ 1e-15 for -745 < x < 700.
-__device__ __forceinline__ double exp_tang(double x, const double* tab) {
-  if (!(x > -745.0)) return 0.0;
-  const double LN2 = 0.6931471805599453094172321;
-  const double kd = rint(x * (32.0 / LN2));
-  const double r = fma(-kd, LN2 / 32.0, x);
-  const int k = (int)kd;
-  const int j = k & 31;
-  const int n = (k - j) >> 5;
-  double p = 1.0 / 720.0;
-  p = fma(p, r, 1.0 / 120.0);
-  p = fma(p, r, 1.0 / 24.0);
-  p = fma(p, r, 1.0 / 6.0);
-  p = fma(p, r, 0.5);
-  p = fma(p, r, 1.0);
-  p = fma(p, r, 1.0);
-  return ldexp(tab[j] * p, n);
-}
-
-// Tempered draft logit (U[v] + W1[x] W2[:, v]) / T with the bias as an
-// error-free double-float sum.  `a` holds W1[x] widened to float.
+// Per-item constants, identical in every thread.
 template <typename DT>
-__device__ __forceinline__ double hp_logit_q(const float* a, const DT* __restrict__ W2, int V, int r,
-                                             const DT* __restrict__ Urow, int v, double invTd) {
-  constexpr int UN = 16;                      // r % 16 == 0; loads run one batch ahead
-  float s = 0.f, c = 0.f;
+struct ItemCtx {
+  const DT* Urow;
+  const DT* Trow;
+  df invT;     // 1 / T_b
+  df nsq;      // -shift_q (logsumexp of the draft row when known, else 0)
+  df nsp;      // -shift_p (logsumexp of the target row)
+};
+
+template <typename DT>
+__device__ __forceinline__ ItemCtx<DT> item_ctx(const Shape& sh, const HpRows& R, const HpItem& it) {
+  ItemCtx<DT> c;
+  c.Urow = (const DT*)R.U + ((size_t)it.b * sh.gamma + (it.kind == HP_BONUS ? 0 : it.j)) * sh.V;
+  c.Trow = (const DT*)R.target + ((size_t)it.b * (sh.gamma + 1) + it.j) * sh.V;
+  c.invT = dd_recip(R.temp[it.b]);
+  c.nsq = dd_from_double(-it.shift_q);
+  c.nsp = dd_from_double(-it.shift_p);
+  return c;
+}
+
+// The same constants computed by thread 0 and shared (a CTA-wide call; the
+// fp64 -> double-float conversions then cost one thread, not all).
+template <typename DT>
+__device__ __forceinline__ ItemCtx<DT> item_ctx_shared(const Shape& sh, const HpRows& R, const HpItem& it,
+                                                       ItemCtx<DT>* slot) {
+  if (threadIdx.x == 0) *slot = item_ctx<DT>(sh, R, it);
+  __syncthreads();
+  const ItemCtx<DT> c = *slot;
+  __syncthreads();
+  return c;
+}
+
+// Transition bias W1[x] . W2[:, v] as a double-float: four interleaved compensated
+// chains over r (the products of bf16 operands are exact in fp32; fp32
+// operands add each product's FMA remainder to a separate sum).  `a` holds
+// W1[x] widened to float.  W2 is read straight from global memory, one column
+// per thread (coalesced), one batch of 16 rows ahead.
+template <typename DT>
+__device__ __forceinline__ df hp_bias(const float* a, const DT* __restrict__ W2, int V, int r, int v) {
+  constexpr int UN = 16;                        // r % 16 == 0
+  DdSum k0, k1, k2, k3;
+  float perr = 0.f;
   float cur[UN];
 #pragma unroll
   for (int u = 0; u < UN; ++u) cur[u] = ldf(W2 + (size_t)u * V + v);
@@ -62,267 +78,303 @@ __device__ __forceinline__ double hp_logit_q(const float* a, const DT* __restric
 #pragma unroll
     for (int u = 0; u < UN; ++u) nxt[u] = more ? ldf(W2 + (size_t)(i0 + UN + u) * V + v) : 0.f;
 #pragma unroll
-    for (int u = 0; u < UN; ++u) {
-      const float w = cur[u];
-      const float p = __fmul_rn(a[i0 + u], w);
-      const float pe = fmaf(a[i0 + u], w, -p);   // 0 for bf16 operands
-      float t, e;
-      two_sum(s, p, t, e);
-      s = t;
-      c = __fadd_rn(c, __fadd_rn(e, pe));
+    for (int u = 0; u < UN; u += 4) {
+      const float p0 = __fmul_rn(a[i0 + u], cur[u]), p1 = __fmul_rn(a[i0 + u + 1], cur[u + 1]);
+      const float p2 = __fmul_rn(a[i0 + u + 2], cur[u + 2]), p3 = __fmul_rn(a[i0 + u + 3], cur[u + 3]);
+      if constexpr (sizeof(DT) == 4) {
+        perr += fmaf(a[i0 + u], cur[u], -p0) + fmaf(a[i0 + u + 1], cur[u + 1], -p1) +
+                fmaf(a[i0 + u + 2], cur[u + 2], -p2) + fmaf(a[i0 + u + 3], cur[u + 3], -p3);
+      }
+      k0.add(p0);
+      k1.add(p1);
+      k2.add(p2);
+      k3.add(p3);
     }
 #pragma unroll
     for (int u = 0; u < UN; ++u) cur[u] = nxt[u];
   }
-  return ((double)ldf(Urow + v) + ((double)s + (double)c)) * invTd;
+  df s = dd_add(dd_add(k0.value(), k1.value()), dd_add(k2.value(), k3.value()));
+  if constexpr (sizeof(DT) == 4) s = dd_add_f(s, perr);
+  return s;
 }
-// Same bias, W2 column `col` of a shared-memory slab [r][ld].
+// The same bias with the r x HPB slab of W2 columns staged in shared memory
+// (`col` = v's column in the slab); 16 slab rows are loaded per batch.
 template <typename DT>
-__device__ __forceinline__ double hp_logit_q_smem(const float* a, const DT* slab, int ld, int col,
-                                                  int r, float Uv, double invTd) {
-  float s = 0.f, c = 0.f;
-  for (int i = 0; i < r; ++i) {
-    const float w = tof(slab[(size_t)i * ld + col]);
-    const float p = __fmul_rn(a[i], w);
-    const float pe = fmaf(a[i], w, -p);
-    float t, e;
-    two_sum(s, p, t, e);
-    s = t;
-    c = __fadd_rn(c, __fadd_rn(e, pe));
-  }
-  return ((double)Uv + ((double)s + (double)c)) * invTd;
-}
-template <typename DT>
-__device__ __forceinline__ double hp_logit_p(const DT* __restrict__ Trow, int v, double invTd) {
-  return (double)ldf(Trow + v) * invTd;
-}
-
-// Exclusive prefix (double) of one value per thread, thread order.
-__device__ __forceinline__ double block_excl_scan_d(double v, double* total, double* sh) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  double inc = v;
-  for (int d = 1; d < 32; d <<= 1) {
-    double o = __shfl_up_sync(0xffffffffu, inc, d);
-    if (lane >= d) inc += o;
-  }
-  __syncthreads();
-  if (lane == 31) sh[w] = inc;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double run = 0.0;
-    for (int q = 0; q < NT / 32; ++q) {
-      double t = sh[q];
-      sh[q] = run;
-      run += t;
+__device__ __forceinline__ df hp_bias_slab(const float* a, const DT* slab, int r, int col) {
+  constexpr int UN = 16;
+  DdSum k0, k1, k2, k3;
+  float perr = 0.f;
+  for (int i0 = 0; i0 < r; i0 += UN) {
+    float w[UN];
+#pragma unroll
+    for (int u = 0; u < UN; ++u) w[u] = tof(slab[(size_t)(i0 + u) * HPB + col]);
+#pragma unroll
+    for (int u = 0; u < UN; u += 4) {
+      const float p0 = __fmul_rn(a[i0 + u], w[u]), p1 = __fmul_rn(a[i0 + u + 1], w[u + 1]);
+      const float p2 = __fmul_rn(a[i0 + u + 2], w[u + 2]), p3 = __fmul_rn(a[i0 + u + 3], w[u + 3]);
+      if constexpr (sizeof(DT) == 4) {
+        perr += fmaf(a[i0 + u], w[u], -p0) + fmaf(a[i0 + u + 1], w[u + 1], -p1) +
+                fmaf(a[i0 + u + 2], w[u + 2], -p2) + fmaf(a[i0 + u + 3], w[u + 3], -p3);
+      }
+      k0.add(p0);
+      k1.add(p1);
+      k2.add(p2);
+      k3.add(p3);
     }
-    sh[NT / 32] = run;
   }
-  __syncthreads();
-  double within = __shfl_up_sync(0xffffffffu, inc, 1);
-  if (lane == 0) within = 0.0;
-  double ex = sh[w] + within;
-  *total = sh[NT / 32];
-  __syncthreads();
-  return ex;
+  df s = dd_add(dd_add(k0.value(), k1.value()), dd_add(k2.value(), k3.value()));
+  if constexpr (sizeof(DT) == 4) s = dd_add_f(s, perr);
+  return s;
 }
-
-
+// Draft weight exp((U[v] + bias) / T - shift_q) and target weight
+// exp(t[v] / T - shift_p), unnormalised unless the shifts are the row's
+// logsumexp.
 template <typename DT>
-struct ItemCtx {
-  const DT* Urow;
-  const DT* Trow;
-  double invTd;
-};
-
-template <typename DT>
-__device__ __forceinline__ ItemCtx<DT> item_ctx(const Shape& sh, const HpRows& R, const HpItem& it) {
-  ItemCtx<DT> c;
-  c.Urow = (const DT*)R.U + ((size_t)it.b * sh.gamma + (it.kind == HP_BONUS ? 0 : it.j)) * sh.V;
-  c.Trow = (const DT*)R.target + ((size_t)it.b * (sh.gamma + 1) + it.j) * sh.V;
-  c.invTd = 1.0 / (double)R.temp[it.b];
-  return c;
+__device__ __forceinline__ df hp_wq(const ItemCtx<DT>& c, df bias, int v, const df* tab) {
+  const df l = dd_add(dd_mul(dd_add_f(bias, ldf(c.Urow + v)), c.invT), c.nsq);
+  return dd_exp(l, tab);
 }
-
-// unnormalised extended-precision weights of entry v for an item
+template <typename DT>
+__device__ __forceinline__ df hp_wp(const ItemCtx<DT>& c, int v, const df* tab) {
+  const df l = dd_add(dd_mul_f(c.invT, ldf(c.Trow + v)), c.nsp);
+  return dd_exp(l, tab);
+}
+// Both weights of entry v for an item (zero beyond V; eq is zero for a bonus
+// item, ep for a draft item).
 template <typename DT>
 __device__ __forceinline__ void hp_weights(const Shape& sh, const HpRows& R, const HpItem& it,
-                                           const ItemCtx<DT>& c, const float* a, const double* tab,
-                                           int v, double& eq, double& ep) {
-  eq = 0.0;
-  ep = 0.0;
+                                           const ItemCtx<DT>& c, const float* a, const df* tab,
+                                           int v, df& eq, df& ep) {
+  eq = {0.f, 0.f};
+  ep = {0.f, 0.f};
   if (v >= sh.V) return;
-  if (it.kind != HP_BONUS)
-    eq = exp_tang(hp_logit_q<DT>(a, (const DT*)R.W2, sh.V, sh.r, c.Urow, v, c.invTd) - it.shift_q, tab);
-  if (it.kind != HP_DRAFT) ep = exp_tang(hp_logit_p<DT>(c.Trow, v, c.invTd) - it.shift_p, tab);
+  if (it.kind != HP_BONUS) eq = hp_wq<DT>(c, hp_bias<DT>(a, (const DT*)R.W2, sh.V, sh.r, v), v, tab);
+  if (it.kind != HP_DRAFT) ep = hp_wp<DT>(c, v, tab);
 }
-
-// Same weights with the W2 columns of block `blk` staged in `slab` ([r][HPB]).
+// Weights of entry v = blk * HPB + threadIdx.x of a block whose W2 columns
+// are staged in `slab` (r x HPB).
 template <typename DT>
 __device__ __forceinline__ void hp_weights_slab(const Shape& sh, const HpItem& it,
                                                 const ItemCtx<DT>& c, const float* a,
-                                                const DT* slab, const double* tab, int v,
-                                                double& eq, double& ep) {
-  eq = 0.0;
-  ep = 0.0;
+                                                const DT* slab, const df* tab, int v, df& eq,
+                                                df& ep) {
+  eq = {0.f, 0.f};
+  ep = {0.f, 0.f};
   if (v >= sh.V) return;
-  if (it.kind != HP_BONUS)
-    eq = exp_tang(hp_logit_q_smem<DT>(a, slab, HPB, v % HPB, sh.r, ldf(c.Urow + v), c.invTd) -
-                      it.shift_q, tab);
-  if (it.kind != HP_DRAFT) ep = exp_tang(hp_logit_p<DT>(c.Trow, v, c.invTd) - it.shift_p, tab);
+  if (it.kind != HP_BONUS) eq = hp_wq<DT>(c, hp_bias_slab<DT>(a, slab, sh.r, v % HPB), v, tab);
+  if (it.kind != HP_DRAFT) ep = hp_wp<DT>(c, v, tab);
 }
 
-// Totals over the item's block sums, identical in every kernel (fixed order).
-__device__ __forceinline__ double item_total(const double* sums, int HB, int col, double* shd) {
-  double s = 0.0;
-  for (int q = threadIdx.x; q < HB; q += NT) s += __ldcg(sums + (size_t)q * 3 + col);
-  return block_sum_d(s, shd);
+// max(0, ep / Zp - eq / Zq) given the reciprocals
+__device__ __forceinline__ df hp_resid(df ep, df eq, df izp, df izq) {
+  const df d = dd_add(dd_mul(ep, izp), dd_neg(dd_mul(eq, izq)));
+  return d.hi > 0.f ? d : df{0.f, 0.f};
 }
 
-// Block sums of the n queued items' weights (phase 0) or residuals (phase 1),
-// grid-stride over (item, block of HPB columns).  `dsm` holds r*HPB elements.
-template <typename DT>
-__device__ void hp_sums_body(const Shape& sh, const HpRows& R, const Ws& ws, int phase, int n,
-                             unsigned char* dsm) {
-  DT* slab = reinterpret_cast<DT*>(dsm);        // [r][HPB] W2 columns of one block
-  __shared__ double tab[32];
-  __shared__ double shd[40];
-  __shared__ float s_a[256];
-  init_exp_table(tab);
+__device__ __forceinline__ void hp_table(df* tab) {
+  if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(tab, threadIdx.x);
+}
+
+// Chunk sums of one item: column col (0: the item's own weights -- p for a
+// verify item, q for a draft item; 1: q of a verify item; 2: the residual),
+// NC double-floats of CW columns each.
+__device__ __forceinline__ float2* item_sums(const Ws& ws, const Shape& sh, int item, int col) {
+  return ws.hpsum + ((size_t)item * ws.hp_cols + col) * sh.NC;
+}
+__device__ __forceinline__ df ld_sum(const float2* p) {
+  const float2 v = __ldcg(p);
+  return {v.x, v.y};
+}
+// Sum over an item's chunk sums (fixed order).
+__device__ __forceinline__ df item_total(const float2* sums, int NC, float* shf) {
+  df s = {0.f, 0.f};
+  for (int q = threadIdx.x; q < NC; q += NT) s = dd_add(s, ld_sum(sums + q));
+  return block_sum_df(s, shf);
+}
+// Reciprocal of a positive double-float, computed once (thread 0) and shared.
+__device__ __forceinline__ df shared_recip(df z, df* slot) {
+  if (threadIdx.x == 0) {
+    // one Newton step on the fp32 reciprocal: 1/z ~ h (2 - z h)
+    const float h = __frcp_rn(z.hi);
+    const df e = dd_add_f(dd_neg(dd_mul_f(z, h)), 1.0f);      // 1 - z h
+    *slot = dd_add_f(dd_mul_f(e, h), h);
+  }
   __syncthreads();
-  for (int w = blockIdx.x; w < n * sh.HB; w += gridDim.x) {
-    const int item = w / sh.HB, blk = w - item * sh.HB;
-    const HpItem it = ldcg_item(ws.items + item);
-    if (phase == 1 && it.kind != HP_RESID) continue;
-    __syncthreads();
-    if (it.kind != HP_BONUS) {
-      for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf((const DT*)R.W1 + (size_t)it.prev * sh.r + i);
-      stage_w2_slab<DT>(slab, (const DT*)R.W2, sh.V, 0, sh.r, blk * HPB, HPB);
+  const df r = *slot;
+  __syncthreads();
+  return r;
+}
+
+// Shared state of the re-decision bodies.
+struct HpShared {
+  df tab[DD_EXP_TAB];
+  float shf[72];
+  float a[256];
+  df part[NT / 32][CW];
+  df rc[2];
+  df pref;
+  int sel;
+  int last;
+  ItemCtx<float> cf;
+  ItemCtx<bf16> cb;
+  template <typename DT>
+  __device__ ItemCtx<DT>* ctx() {
+    if constexpr (sizeof(DT) == 4) return &cf; else return &cb;
+  }
+};
+
+// One block (HPB columns) of an item: the weights of its columns and, per
+// warp, the sum over the warp's CW columns -- phase 0: columns 0 and 1 (1 only
+// for verify items), phase 1: the residual (column 2) given the normalisers.
+template <typename DT>
+__device__ void hp_block(const Shape& sh, const HpRows& R, const Ws& ws, int phase, int item,
+                         int blk, const HpItem& it, HpShared& S, DT* slab) {
+  __syncthreads();
+  if (it.kind != HP_BONUS) {
+    for (int i = threadIdx.x; i < sh.r; i += NT) S.a[i] = ldf((const DT*)R.W1 + (size_t)it.prev * sh.r + i);
+    stage_w2_slab<DT>(slab, (const DT*)R.W2, sh.V, 0, sh.r, blk * HPB, HPB);
+  }
+  __syncthreads();
+  df izp = {0.f, 0.f}, izq = {0.f, 0.f};
+  if (phase == 1) {
+    izp = shared_recip(item_total(item_sums(ws, sh, item, 0), sh.NC, S.shf), &S.rc[0]);
+    izq = shared_recip(item_total(item_sums(ws, sh, item, 1), sh.NC, S.shf), &S.rc[1]);
+  }
+  const ItemCtx<DT> c = item_ctx_shared<DT>(sh, R, it, S.template ctx<DT>());
+  const int v = blk * HPB + threadIdx.x;
+  df eq, ep;
+  hp_weights_slab<DT>(sh, it, c, S.a, slab, S.tab, v, eq, ep);
+  const int chunk = v / CW;                      // = blk * (HPB / CW) + warp
+  const bool store = (threadIdx.x & 31) == 0 && chunk < sh.NC;
+  if (phase == 0) {
+    const df A = warp_sum_df(it.kind == HP_DRAFT ? eq : ep);
+    if (store) item_sums(ws, sh, item, 0)[chunk] = make_float2(A.hi, A.lo);
+    if (it.kind != HP_DRAFT) {
+      const df Bq = warp_sum_df(eq);
+      if (store) item_sums(ws, sh, item, 1)[chunk] = make_float2(Bq.hi, Bq.lo);
     }
-    __syncthreads();
-    const ItemCtx<DT> c = item_ctx<DT>(sh, R, it);
-    const int v = blk * HPB + threadIdx.x;
-    double eq, ep;
-    hp_weights_slab<DT>(sh, it, c, s_a, slab, tab, v, eq, ep);
-    double* sums = ws.hpsum + (size_t)item * sh.HB * 3;
-    if (phase == 0) {
-      double A = block_sum_d(it.kind == HP_DRAFT ? eq : ep, shd);
-      double Bq = block_sum_d(eq, shd);
-      if (threadIdx.x == 0) {
-        sums[(size_t)blk * 3 + 0] = A;
-        sums[(size_t)blk * 3 + 1] = Bq;
-      }
-    } else {
-      const double Zp = item_total(sums, sh.HB, 0, shd);
-      const double Zq = item_total(sums, sh.HB, 1, shd);
-      double rr = (v < sh.V) ? fmax(0.0, ep / Zp - eq / Zq) : 0.0;
-      double C = block_sum_d(rr, shd);
-      if (threadIdx.x == 0) sums[(size_t)blk * 3 + 2] = C;
-    }
+  } else {
+    const df rr = (v < sh.V) ? hp_resid(ep, eq, izp, izq) : df{0.f, 0.f};
+    const df C = warp_sum_df(rr);
+    if (store) item_sums(ws, sh, item, 2)[chunk] = make_float2(C.hi, C.lo);
   }
 }
 
-// Re-decide the n queued items: one CTA per item (grid-stride).
+// Re-decide one item from its chunk sums: find the chunk where the running
+// mass crosses u * Z, recompute that chunk's CW weights (the r products of each
+// column split over the NT/32 warps) and scan them; write the token (and for
+// a draft item q(x) and the row's logsumexp).
 template <typename DT>
-__device__ void hp_decide_body(const Shape& sh, const HpRows& R, const Ws& ws, int n, int* tokens,
+__device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, int item, int* tokens,
                                float* q_tok, double* lse_q, int* out_tokens, uint32_t* status,
-                               unsigned char* dsm) {
-  DT* slab = reinterpret_cast<DT*>(dsm);        // [r][HPB] W2 columns of the crossing block
-  __shared__ double tab[32];
-  __shared__ double shd[40];
-  __shared__ float s_a[256];
-  __shared__ int s_blk, s_tok;
-  __shared__ double s_pref, s_val;
-  init_exp_table(tab);
+                               HpShared& S, DT* slab) {
+  const HpItem it = ldcg_item(ws.items + item);
+  const bool resid = it.kind == HP_RESID;
+  const df Zp = item_total(item_sums(ws, sh, item, 0), sh.NC, S.shf);
+  const df Zq = resid ? item_total(item_sums(ws, sh, item, 1), sh.NC, S.shf) : df{1.f, 0.f};
+  const df Zc = resid ? item_total(item_sums(ws, sh, item, 2), sh.NC, S.shf) : df{0.f, 0.f};
+  // residual with no mass: draw from p (a probability-zero event)
+  const bool use_r = resid && Zc.hi > 0.f;
+  const float2* sums = item_sums(ws, sh, item, use_r ? 2 : 0);
+  const df Z = use_r ? Zc : Zp;
+  const df target = dd_mul_f(Z, it.u);
+  // crossing chunk: per-thread contiguous range of chunks, double-float scan
+  const int per = (sh.NC + NT - 1) / NT;
+  const int q0 = threadIdx.x * per, q1 = min(q0 + per, sh.NC);
+  df loc = {0.f, 0.f};
+  for (int q = q0; q < q1; ++q) loc = dd_add(loc, ld_sum(sums + q));
+  df tot;
+  const df ex = block_excl_scan_df(loc, &tot, S.shf);
+  if (threadIdx.x == 0) S.sel = 0x7fffffff;
   __syncthreads();
-  for (int item = blockIdx.x; item < n; item += gridDim.x) {
-    const HpItem it = ldcg_item(ws.items + item);
-    const double* sums = ws.hpsum + (size_t)item * sh.HB * 3;
-    const bool resid = it.kind == HP_RESID;
-    double Zp = item_total(sums, sh.HB, 0, shd);
-    double Zq = resid ? item_total(sums, sh.HB, 1, shd) : 0.0;
-    double Zc = resid ? item_total(sums, sh.HB, 2, shd) : 0.0;
-    // residual with no mass: draw from p (a probability-zero event)
-    const bool empty = resid && !(Zc > 0.0);
-    const int col = (resid && !empty) ? 2 : 0;
-    const double Z = (resid && !empty) ? Zc : Zp;
-    const double target = (double)it.u * Z;
-    // crossing block
-    const int per = (sh.HB + NT - 1) / NT;
-    const int q0 = threadIdx.x * per, q1 = min(q0 + per, sh.HB);
-    double loc = 0.0;
-    for (int q = q0; q < q1; ++q) loc += __ldcg(sums + (size_t)q * 3 + col);
-    double tot;
-    double ex = block_excl_scan_d(loc, &tot, shd);
-    if (threadIdx.x == 0) { s_blk = 0x7fffffff; s_tok = 0x7fffffff; }
-    __syncthreads();
-    int myb = -1;
-    double mypref = 0.0;
-    if (ex <= target && ex + loc > target) {
-      double run = ex;
-      for (int q = q0; q < q1; ++q) {
-        double nx = run + __ldcg(sums + (size_t)q * 3 + col);
-        if (nx > target) { myb = q; mypref = run; atomicMin(&s_blk, q); break; }
-        run = nx;
+  int mine = -1;
+  df mypref = {0.f, 0.f};
+  if (q0 < q1 && dd_le(ex, target) && !dd_le(dd_add(ex, loc), target)) {
+    df run = ex;
+    for (int q = q0; q < q1; ++q) {
+      const df nx = dd_add(run, ld_sum(sums + q));
+      if (!dd_le(nx, target)) {
+        mine = q;
+        mypref = run;
+        atomicMin(&S.sel, q);
+        break;
       }
+      run = nx;
     }
-    __syncthreads();
-    if (myb >= 0 && myb == s_blk) s_pref = mypref;
-    __syncthreads();
-    bool fallback = false;
-    if (s_blk == 0x7fffffff) {
-      fallback = true;
-      if (threadIdx.x == 0) {
-        int q = sh.HB - 1;
-        while (q > 0 && !(__ldcg(sums + (size_t)q * 3 + col) > 0.0)) --q;
-        double run = 0.0;
-        for (int t = 0; t < q; ++t) run += __ldcg(sums + (size_t)t * 3 + col);
-        s_blk = q;
-        s_pref = run;
-      }
-      __syncthreads();
-    }
-    const int blk = s_blk;
-    // recompute the block
-    if (it.kind != HP_BONUS) {
-      for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf((const DT*)R.W1 + (size_t)it.prev * sh.r + i);
-      stage_w2_slab<DT>(slab, (const DT*)R.W2, sh.V, 0, sh.r, blk * HPB, HPB);
-    }
-    __syncthreads();
-    const ItemCtx<DT> c = item_ctx<DT>(sh, R, it);
-    const int v = blk * HPB + threadIdx.x;
-    double eq, ep;
-    hp_weights_slab<DT>(sh, it, c, s_a, slab, tab, v, eq, ep);
-    double val;
-    if (it.kind == HP_DRAFT) val = eq;
-    else if (resid && !empty) val = (v < sh.V) ? fmax(0.0, ep / Zp - eq / Zq) : 0.0;
-    else val = ep;
-    double btot;
-    double bex = block_excl_scan_d(val, &btot, shd);
-    const double tin = target - s_pref;
-    if (val > 0.0 && bex <= tin && bex + val > tin) atomicMin(&s_tok, (int)threadIdx.x);
-    __syncthreads();
-    if (s_tok == 0x7fffffff) {
-      // rounding left no crossing inside the block: last positive entry
-      fallback = true;
-      __syncthreads();
-      if (threadIdx.x == 0) s_tok = -1;
-      __syncthreads();
-      if (val > 0.0) atomicMax(&s_tok, (int)threadIdx.x);
-      __syncthreads();
-      if (s_tok < 0) {
-        if (threadIdx.x == 0) s_tok = 0;
-        __syncthreads();
-      }
-    }
-    if ((int)threadIdx.x == s_tok) s_val = val;
-    __syncthreads();
+  }
+  __syncthreads();
+  if (mine >= 0 && mine == S.sel) S.pref = mypref;
+  __syncthreads();
+  if (S.sel == 0x7fffffff) {
+    // rounding left the total at or below u*Z: last chunk with mass
     if (threadIdx.x == 0) {
-      const int tok = blk * HPB + s_tok;
+      int q = sh.NC - 1;
+      while (q > 0 && !(ld_sum(sums + q).hi > 0.f)) --q;
+      df run = {0.f, 0.f};
+      for (int t = 0; t < q; ++t) run = dd_add(run, ld_sum(sums + t));
+      S.sel = q;
+      S.pref = run;
+    }
+    __syncthreads();
+  }
+  const int n0 = S.sel * CW;
+  const df izp = use_r ? shared_recip(Zp, &S.rc[0]) : df{0.f, 0.f};
+  const df izq = use_r ? shared_recip(Zq, &S.rc[1]) : df{0.f, 0.f};
+  // ---- the chunk's biases: warp w sums rows [w r/8, (w+1) r/8) of column lane
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (it.kind != HP_BONUS) {
+    for (int i = threadIdx.x; i < sh.r; i += NT) S.a[i] = ldf((const DT*)R.W1 + (size_t)it.prev * sh.r + i);
+    stage_w2_slab<DT>(slab, (const DT*)R.W2, sh.V, 0, sh.r, n0, CW);
+    const int kw = sh.r / (NT / 32);             // r % 16 == 0
+    DdSum acc;
+    float perr = 0.f;
+    for (int i = w * kw; i < (w + 1) * kw; ++i) {
+      const float wv = tof(slab[(size_t)i * CW + lane]);
+      const float p = __fmul_rn(S.a[i], wv);
+      if constexpr (sizeof(DT) == 4) perr += fmaf(S.a[i], wv, -p);
+      acc.add(p);
+    }
+    df part = acc.value();
+    if constexpr (sizeof(DT) == 4) part = dd_add_f(part, perr);
+    S.part[w][lane] = part;
+  }
+  __syncthreads();
+  const ItemCtx<DT> c = item_ctx_shared<DT>(sh, R, it, S.template ctx<DT>());
+  if (w == 0) {
+    const int v = n0 + lane;
+    df eq = {0.f, 0.f}, ep = {0.f, 0.f};
+    if (v < sh.V) {
+      if (it.kind != HP_BONUS) {
+        df bias = S.part[0][lane];
+        for (int g = 1; g < NT / 32; ++g) bias = dd_add(bias, S.part[g][lane]);
+        eq = hp_wq<DT>(c, bias, v, S.tab);
+      }
+      if (it.kind != HP_DRAFT) ep = hp_wp<DT>(c, v, S.tab);
+    }
+    df val;
+    if (it.kind == HP_DRAFT) val = eq;
+    else if (use_r) val = (v < sh.V) ? hp_resid(ep, eq, izp, izq) : df{0.f, 0.f};
+    else val = ep;
+    // inclusive double-float scan across the warp
+    df inc = val;
+    for (int d = 1; d < 32; d <<= 1) {
+      const df o = shfl_up_df(inc, d);
+      if (lane >= d) inc = dd_add(inc, o);
+    }
+    const df hi = dd_add(S.pref, inc), lo = dd_add(hi, dd_neg(val));
+    const bool positive = val.hi > 0.f;
+    const uint32_t cl = __ballot_sync(0xffffffffu, positive && dd_le(lo, target) && !dd_le(hi, target));
+    const uint32_t pos = __ballot_sync(0xffffffffu, positive);
+    // no crossing: rounding left the total at u*Z -> last positive entry
+    const int t = cl ? __ffs(cl) - 1 : (pos ? 31 - __clz(pos) : 0);
+    const float vt = __shfl_sync(0xffffffffu, val.hi, t);
+    if (lane == 0) {
+      const int tok = n0 + t;
       if (it.kind == HP_DRAFT) {
         const size_t o = (size_t)it.b * sh.gamma + it.j;
         tokens[o] = tok;
-        q_tok[o] = (float)(s_val / Z);
-        lse_q[o] = it.shift_q + log(Z);
+        q_tok[o] = __fdiv_rn(vt, Z.hi);
+        lse_q[o] = it.shift_q + dd_log(Z, S.tab);
       } else {
         out_tokens[(size_t)it.b * (sh.gamma + 1) + it.j] = tok;
       }
@@ -332,9 +384,54 @@ __device__ void hp_decide_body(const Shape& sh, const HpRows& R, const Ws& ws, i
         atomicOr(status, (uint32_t)SPEC_DEV_REFINED);
       }
     }
-    (void)fallback;
-    __syncthreads();
   }
+  __syncthreads();
+}
+
+// Block sums of the n queued items (phase 0: weights, phase 1: residuals of
+// residual items), grid-stride over (item, block of HPB columns).  With
+// `fused` (draft items only), the CTA that completes an item's last block
+// re-decides the item at once; the per-item counters start at zero and are
+// left at zero.
+template <typename DT>
+__device__ void hp_sums_body(const Shape& sh, const HpRows& R, const Ws& ws, int phase, int n,
+                             unsigned char* dsm, bool fused = false, int* tokens = nullptr,
+                             float* q_tok = nullptr, double* lse_q = nullptr,
+                             uint32_t* status = nullptr) {
+  DT* slab = reinterpret_cast<DT*>(dsm);        // [r][HPB] W2 columns of one block
+  __shared__ HpShared S;
+  hp_table(S.tab);
+  __syncthreads();
+  for (int w = blockIdx.x; w < n * sh.HB; w += gridDim.x) {
+    const int item = w / sh.HB, blk = w - item * sh.HB;
+    const HpItem it = ldcg_item(ws.items + item);
+    if (phase == 1 && it.kind != HP_RESID) continue;
+    hp_block<DT>(sh, R, ws, phase, item, blk, it, S, slab);
+    if (fused) {
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) S.last = atomicAdd(ws.hpcnt + item, 1u) == (uint32_t)sh.HB - 1u;
+      __syncthreads();
+      if (S.last) {
+        __threadfence();
+        hp_decide_item<DT>(sh, R, ws, item, tokens, q_tok, lse_q, nullptr, status, S, slab);
+        if (threadIdx.x == 0) ws.hpcnt[item] = 0u;
+      }
+    }
+  }
+}
+
+// Re-decide the n queued items: one CTA per item (grid-stride).
+template <typename DT>
+__device__ void hp_decide_body(const Shape& sh, const HpRows& R, const Ws& ws, int n, int* tokens,
+                               float* q_tok, double* lse_q, int* out_tokens, uint32_t* status,
+                               unsigned char* dsm) {
+  DT* slab = reinterpret_cast<DT*>(dsm);
+  __shared__ HpShared S;
+  hp_table(S.tab);
+  __syncthreads();
+  for (int item = blockIdx.x; item < n; item += gridDim.x)
+    hp_decide_item<DT>(sh, R, ws, item, tokens, q_tok, lse_q, out_tokens, status, S, slab);
 }
 
 }  // namespace spec

@@ -7,6 +7,7 @@
 #include <math.h>
 
 #include "../../include/spec.h"
+#include "spec_df.cuh"
 
 namespace spec {
 
@@ -48,7 +49,9 @@ struct Ws {
   unsigned long long* trace;  // [MAX_GAMMA][TRACE_SLOTS] globaltimer ns, CTA 0
   HpItem* items;        // [max_items]
   int max_items;
-  double* hpsum;        // [max_items][HB][3]
+  float2* hpsum;        // [max_items][hp_cols][NC] chunk sums of the re-decided rows (hi, lo)
+  int hp_cols;          // 3 (draft and verify) or 1 (draft only)
+  uint32_t* hpcnt;      // [max_items] blocks summed so far (zeroed before the draft)
   // draft
   float4* dpart;        // [B][NC] draft partials per CW-column chunk: (c, m, s, q2)
   // verify
@@ -114,7 +117,7 @@ __device__ __forceinline__ float exp_split(double g) {
 }
 
 // ---------------------------------------------------------------- double-float
-struct df { float hi, lo; };
+// (struct df and the host-portable operations are in spec_df.cuh)
 
 __device__ __forceinline__ df df_make(float x) { return {x, 0.f}; }
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
@@ -247,25 +250,6 @@ __device__ __forceinline__ df block_excl_scan_df(df v, df* total, float* sh) {
   return ex;
 }
 
-// Double sums over the block (fixed order; few calls per kernel only:
-// GB300 has a low double-precision rate).
-__device__ __forceinline__ double warp_sum_d(double v) {
-  for (int m = 16; m; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
-  return v;
-}
-__device__ __forceinline__ double block_sum_d(double v, double* sh) {
-  v = warp_sum_d(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
-  __syncthreads();
-  double r = (threadIdx.x < (NT >> 5)) ? sh[threadIdx.x] : 0.0;
-  if (threadIdx.x < 32) r = warp_sum_d(r);
-  if (threadIdx.x == 0) sh[0] = r;
-  __syncthreads();
-  r = sh[0];
-  __syncthreads();
-  return r;
-}
 
 // sum_{i in [ib, ie)} a[i] * W2[i][v] with fp32 FMAs in i order.  W2 loads
 // are issued 8 rows ahead of their use so the loop is not bound by the

@@ -3,16 +3,16 @@
 // The first pass (spec_draft.cu, spec_verify.cu) decides every draw in single
 // precision and measures how far the uniform lies from the nearest CDF
 // breakpoint.  Draws closer than the first pass's error band are re-decided
-// here with per-vocabulary-entry weights accurate to ~1e-15:
-//   - transition bias W1[x] W2 as an exact double-float sum (bf16 x bf16
-//     products are exact in fp32; fp32 products are split with an FMA;
-//     partial sums are carried error-free with TwoSum),
-//   - logits and exponentials in double precision; the exponential uses
-//     the table-driven method of P. T. P. Tang, "Table-driven implementation
-//     of the exponential function in IEEE floating-point arithmetic", ACM
-//     TOMS 15(2), 1989 (32-entry table of 2^(j/32), degree-6 polynomial on
-//     |r| <= ln2/64), which needs far fewer double operations than a general
-//     libm-style exp -- GB300's double rate is low.
+// here with per-vocabulary-entry weights accurate to ~1e-13, all in
+// double-float arithmetic (spec_df.cuh) because GB300's fp64 rate is low:
+//   - transition bias W1[x] W2 as a compensated (Kahan) sum of the products
+//     (bf16 x bf16 products are exact in fp32; fp32 products carry their FMA
+//     remainder),
+//   - logits in double-float, exponentials by a double-float version of the
+//     table-driven method of P. T. P. Tang, "Table-driven implementation of
+//     the exponential function in IEEE floating-point arithmetic", ACM TOMS
+//     15(2), 1989 (64-entry table of 2^(j/64), |r| <= ln2/128),
+//   - block sums and scans in double-float, in a fixed order.
 //
 //   hp_sums_kernel    grid-stride over (item, block of HPB columns): block sums
 //                     of the item's unnormalised weights (phase 0), or of the
@@ -48,16 +48,15 @@ __global__ void __launch_bounds__(NT) hp_decide_kernel(Shape sh, HpRows R, Ws ws
 // ---------------------------------------------------------------- slow path
 // One CTA re-verifies one request whose ratio test sat inside its error band.
 template <typename DT>
-__device__ double row_total(const Shape& sh, const HpRows& R, const HpItem& it, const float* a,
-                            const double* tab, double* shd) {
-  const ItemCtx<DT> c = item_ctx<DT>(sh, R, it);
-  double s = 0.0;
+__device__ df row_total(const Shape& sh, const HpRows& R, const HpItem& it, const ItemCtx<DT>& c,
+                        const float* a, const df* tab, float* shf) {
+  df s = {0.f, 0.f};
   for (int v = threadIdx.x; v < sh.V; v += NT) {
-    double eq, ep;
+    df eq, ep;
     hp_weights<DT>(sh, R, it, c, a, tab, v, eq, ep);
-    s += (it.kind == HP_DRAFT) ? eq : ep;
+    s = dd_add(s, (it.kind == HP_DRAFT) ? eq : ep);
   }
-  return block_sum_d(s, shd);
+  return block_sum_df(s, shf);
 }
 
 template <typename DT>
@@ -66,20 +65,20 @@ __global__ void __launch_bounds__(NT) slow_verify_kernel(
     const double* __restrict__ lse_q, const int* __restrict__ vlen,
     const float* __restrict__ u_acc, const float* __restrict__ u_fin, int* accept_len,
     int* out_tokens, uint32_t* status) {
-  __shared__ double tab[32];
-  __shared__ double shd[40];
+  __shared__ df tab[DD_EXP_TAB];
+  __shared__ float shf[72];
   __shared__ float s_a[256];
-  __shared__ int s_tok;
+  __shared__ df s_rc;
+  __shared__ int s_tok, s_last;
   const int nslow = min((int)ws.ctrl[CTRL_SLOW], sh.B);
   if (nslow == 0) return;
-  init_exp_table(tab);
+  hp_table(tab);
   __syncthreads();
   for (int q = blockIdx.x; q < nslow; q += gridDim.x) {
     const int b = ws.slow[q];
     const int L = vlen[b];
     const uint32_t flags = (uint32_t)ws.vflags[b] >> 8;
     const uint32_t acc = ws.accbits[b];
-    const double invTd = 1.0 / (double)R.temp[b];
     int n = L;
     int nhp = 0;
     for (int j = 0; j < L; ++j) {
@@ -95,12 +94,15 @@ __global__ void __launch_bounds__(NT) slow_verify_kernel(
         __syncthreads();
         for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf((const DT*)R.W1 + (size_t)prev * sh.r + i);
         __syncthreads();
-        const double Zp = row_total<DT>(sh, R, ip, s_a, tab, shd);
-        const double Zq = row_total<DT>(sh, R, iq, s_a, tab, shd);
         const ItemCtx<DT> c = item_ctx<DT>(sh, R, iq);
-        const double lp = hp_logit_p<DT>(c.Trow, x, invTd) - ip.shift_p - log(Zp);
-        const double lq = hp_logit_q<DT>(s_a, (const DT*)R.W2, sh.V, sh.r, c.Urow, x, invTd) -
-                          iq.shift_q - log(Zq);
+        const double Zp = dd_to_double(row_total<DT>(sh, R, ip, c, s_a, tab, shf));
+        const double Zq = dd_to_double(row_total<DT>(sh, R, iq, c, s_a, tab, shf));
+        const df lpx = dd_add(dd_mul_f(c.invT, ldf(c.Trow + x)), c.nsp);
+        const df lqx = dd_add(
+            dd_mul(dd_add_f(hp_bias<DT>(s_a, (const DT*)R.W2, sh.V, sh.r, x), ldf(c.Urow + x)), c.invT),
+            c.nsq);
+        const double lp = dd_to_double(lpx) - log(Zp);
+        const double lq = dd_to_double(lqx) - log(Zq);
         const double ratio = exp(lp - lq);
         const bool nacc = (double)u_acc[(size_t)b * sh.gamma + j] < ratio;
         if (nacc != accept && threadIdx.x == 0 && status) atomicAdd(status + 2, 1u);
@@ -116,27 +118,29 @@ __global__ void __launch_bounds__(NT) slow_verify_kernel(
     ip.shift_p = ws.lse_p[(size_t)b * (sh.gamma + 1) + row];
     ip.shift_q = resid ? lse_q[(size_t)b * sh.gamma + row] : 0.0;
     HpItem iq = ip; iq.kind = HP_DRAFT;
+    HpItem ir = ip; ir.kind = resid ? HP_RESID : HP_BONUS;
     __syncthreads();
     if (resid)
       for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf((const DT*)R.W1 + (size_t)ip.prev * sh.r + i);
     __syncthreads();
-    const double Zp = row_total<DT>(sh, R, ip, s_a, tab, shd);
-    const double Zq = resid ? row_total<DT>(sh, R, iq, s_a, tab, shd) : 1.0;
-    const ItemCtx<DT> c = item_ctx<DT>(sh, R, iq);
+    const ItemCtx<DT> c = item_ctx<DT>(sh, R, ir);
+    const df Zp = row_total<DT>(sh, R, ip, c, s_a, tab, shf);
+    const df Zq = resid ? row_total<DT>(sh, R, iq, c, s_a, tab, shf) : df{1.f, 0.f};
+    const df izp = shared_recip(Zp, &s_rc);
+    const df izq = shared_recip(Zq, &s_rc);
     // total residual mass
     double Zr = 0.0;
     if (resid) {
-      double s = 0.0;
+      df s = {0.f, 0.f};
       for (int v = threadIdx.x; v < sh.V; v += NT) {
-        double eq, ep;
-        HpItem ir = ip; ir.kind = HP_RESID; ir.shift_q = iq.shift_q;
+        df eq, ep;
         hp_weights<DT>(sh, R, ir, c, s_a, tab, v, eq, ep);
-        s += fmax(0.0, ep / Zp - eq / Zq);
+        s = dd_add(s, hp_resid(ep, eq, izp, izq));
       }
-      Zr = block_sum_d(s, shd);
+      Zr = dd_to_double(block_sum_df(s, shf));
     }
     const bool use_r = resid && Zr > 0.0;
-    const double Z = use_r ? Zr : Zp;
+    const double Z = use_r ? Zr : dd_to_double(Zp);
     const double target = (double)ip.u * Z;
     double run = 0.0;
     if (threadIdx.x == 0) s_tok = 0x7fffffff;
@@ -144,20 +148,19 @@ __global__ void __launch_bounds__(NT) slow_verify_kernel(
     int last_pos = -1;
     for (int v0 = 0; v0 < sh.V; v0 += NT) {
       const int v = v0 + threadIdx.x;
-      double eq = 0.0, ep = 0.0;
-      HpItem ir = ip; ir.kind = resid ? HP_RESID : HP_BONUS; ir.shift_q = iq.shift_q;
+      df eq = {0.f, 0.f}, ep = {0.f, 0.f};
       hp_weights<DT>(sh, R, ir, c, s_a, tab, v, eq, ep);
-      double val = use_r ? ((v < sh.V) ? fmax(0.0, ep / Zp - eq / Zq) : 0.0) : ep;
-      double tot;
-      double ex = block_excl_scan_d(val, &tot, shd);
-      if (val > 0.0 && run + ex <= target && run + ex + val > target) atomicMin(&s_tok, v);
-      if (val > 0.0) last_pos = v;
+      const df val = use_r ? ((v < sh.V) ? hp_resid(ep, eq, izp, izq) : df{0.f, 0.f}) : ep;
+      df tot;
+      const double ex = dd_to_double(block_excl_scan_df(val, &tot, shf));
+      const double vd = dd_to_double(val);
+      if (vd > 0.0 && run + ex <= target && run + ex + vd > target) atomicMin(&s_tok, v);
+      if (vd > 0.0) last_pos = v;
       __syncthreads();
       if (s_tok != 0x7fffffff) break;
-      run += tot;
+      run += dd_to_double(tot);
     }
     // no crossing found means rounding left the total at u*Z: last positive entry
-    __shared__ int s_last;
     if (threadIdx.x == 0) s_last = -1;
     __syncthreads();
     atomicMax(&s_last, last_pos);

@@ -40,13 +40,11 @@ struct TcLayout {
   }
 };
 
+// Advance a shared-memory pointer to the next 1024-byte boundary of the
+// shared window.
 __device__ __forceinline__ unsigned char* align1k(unsigned char* p) {
-  uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  // shared window addresses: align the shared-space offset
-  uint32_t s = smem_u32(p);
-  uint32_t pad = (1024u - (s & 1023u)) & 1023u;
-  (void)a;
-  return p + pad;
+  const uint32_t s = smem_u32(p);
+  return p + ((1024u - (s & 1023u)) & 1023u);
 }
 
 // ---------------------------------------------------------------- operand loads

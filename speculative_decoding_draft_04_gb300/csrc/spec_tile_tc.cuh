@@ -67,7 +67,7 @@ struct TpLayout {
 
 // Tensor maps of one draft call (encoded on the host, passed as a
 // __grid_constant__ kernel parameter).
-struct alignas(64) TpMaps {
+struct TpMaps {
   CUtensorMap u;     // U viewed as [B][gamma][V], box 64 x 1 x 128, 128-byte swizzle
   CUtensorMap w2;    // W2 viewed as [r][V],       box 64 x r,       128-byte swizzle
 };

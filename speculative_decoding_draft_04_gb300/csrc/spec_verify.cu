@@ -119,8 +119,7 @@ __global__ void __launch_bounds__(NT) verify_prep_kernel(
     ws.rowptr[b] = run;
     if (ws.vflags[b] & 1) continue;
     const int L = vlen[b];
-    const double invTd = 1.0 / (double)temp[b];
-    const df it = d2df(invTd);
+    const df it = dd_recip(temp[b]);
     for (int j = 0; j < L; ++j) {
       ws.prow[run + j] = make_int2(b, j);
       ws.prevtok[run + j] = j == 0 ? anchor[b] : dtok[(size_t)b * sh.gamma + j - 1];
@@ -143,10 +142,12 @@ __global__ void __launch_bounds__(NT) target_stats_kernel(Shape sh, const DT* __
                                                           const float* __restrict__ temp,
                                                           const int* __restrict__ vlen, Ws ws) {
   __shared__ float s_c[NT / 16], s_hi[NT / 16], s_lo[NT / 16];
+  __shared__ df s_tab[DD_EXP_TAB];
   const int j = blockIdx.x, b = blockIdx.y;
   if (ws.vflags[b] & 1) return;
   const int L = vlen[b];
   if (j > L) return;
+  if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(s_tab, threadIdx.x);
   const float T = temp[b];
   const float invT = 1.0f / T;
   const DT* row = target + ((size_t)b * (sh.gamma + 1) + j) * sh.V;
@@ -203,7 +204,8 @@ __global__ void __launch_bounds__(NT) target_stats_kernel(Shape sh, const DT* __
     df Z = {0.f, 0.f};
     for (int h = 0; h < NT / 16; ++h)
       if (s_c[h] != -INFINITY) Z = df_add(Z, df_mulf({s_hi[h], s_lo[h]}, expf(fast_tx(s_c[h], M, invT))));
-    const double lse = (double)M * (1.0 / (double)T) + log(df_d(Z));
+    // lse = M / T + log Z (double-float steps; fp64 only to assemble the result)
+    const double lse = dd_to_double(dd_mul_f(dd_recip(T), M)) + dd_log(Z, s_tab);
     ws.lse_p[(size_t)b * (sh.gamma + 1) + j] = lse;
     const df nlp = d2df(-lse);
     ws.rowp[(size_t)b * (sh.gamma + 1) + j] = make_float2(nlp.hi, nlp.lo);
@@ -354,14 +356,18 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
   __shared__ float s_w[BN];
   __shared__ int s_n, s_slice, s_tok, s_slow;
   __shared__ float s_pref[2], s_lo, s_hi;
+  __shared__ df s_tab[DD_EXP_TAB];
 
   const int b = blockIdx.x;
   if (ws.vflags[b] & 1) return;
+  if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(s_tab, threadIdx.x);
+  __syncthreads();
   const int L = vlen[b];
   const int rp = ws.rowptr[b];
   const float T = temp[b];
   const float invT = 1.0f / T;
-  const double invTd = 1.0 / (double)T;
+  const df invTdf = dd_recip(T);
+  // (fp32 and double-float only below: GB300's fp64 rate is low)
 
   // ---- alpha_j = sum over slices (double-float, fixed order)
   for (int j = 0; j < sh.gamma; ++j) {
@@ -379,12 +385,13 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
     if (j < L) {
       const int x = dtok[(size_t)b * sh.gamma + j];
       const float tx = ldf(target + ((size_t)b * (sh.gamma + 1) + j) * sh.V + x);
-      const double pt = exp((double)tx * invTd - ws.lse_p[(size_t)b * (sh.gamma + 1) + j]);
-      const double ratio = pt / (double)q_tok[(size_t)b * sh.gamma + j];
-      const double u = (double)u_acc[(size_t)b * sh.gamma + j];
+      const float2 nlp = ws.rowp[(size_t)b * (sh.gamma + 1) + j];       // -lse_p
+      const float pt = dd_exp(dd_add(dd_mul_f(invTdf, tx), df{nlp.x, nlp.y}), s_tab).hi;
+      const float ratio = __fdiv_rn(pt, q_tok[(size_t)b * sh.gamma + j]);
+      const float u = u_acc[(size_t)b * sh.gamma + j];
       acc = u < ratio;
-      near = fabs(u - ratio) <= (double)eps.scale * (double)eps.ratio * ratio;
-      if (p_tok) p_tok[(size_t)b * sh.gamma + j] = (float)pt;
+      near = fabsf(u - ratio) <= eps.scale * eps.ratio * ratio;
+      if (p_tok) p_tok[(size_t)b * sh.gamma + j] = pt;
     } else if (j < sh.gamma && p_tok) {
       p_tok[(size_t)b * sh.gamma + j] = NAN;
     }
@@ -441,31 +448,26 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
   const df excl = block_excl_scan_df(loc, &Zdf, sh_f);
   e2 = block_sum(e2, sh_f);
   m2 = block_sum(m2, sh_f);
-  const double Z = df_d(Zdf);
   const float u = u_fin[b];
-  const double target_d = (double)u * Z;
-  const df tgt = d2df(target_d);
-  bool fallback = !(Z > 0.0);
+  const df tgt = dd_mul_f(Zdf, u);
+  bool fallback = !(Zdf.hi > 0.f);
 
   if (threadIdx.x == 0) s_slice = 0x7fffffff;
   __syncthreads();
   int my_slice = -1;
   df my_pref = {0.f, 0.f};
-  if (!fallback) {
-    const df tneg = df_neg(tgt);
-    if (df_d(df_add(excl, tneg)) <= 0.0 && df_d(df_add(df_add(excl, loc), tneg)) > 0.0) {
-      df run = excl;
-      for (int s = s0; s < s1; ++s) {
-        float wsl = resid ? VP[s].y : __fmul_rn(BP[s].y, expf(fast_tx(BP[s].x, cM, invT)));
-        df nxt = df_addf(run, wsl);
-        if (df_d(df_add(nxt, tneg)) > 0.0) {
-          my_slice = s;
-          my_pref = run;
-          atomicMin(&s_slice, s);
-          break;
-        }
-        run = nxt;
+  if (!fallback && s0 < s1 && dd_le(excl, tgt) && !dd_le(df_add(excl, loc), tgt)) {
+    df run = excl;
+    for (int s = s0; s < s1; ++s) {
+      float wsl = resid ? VP[s].y : __fmul_rn(BP[s].y, expf(fast_tx(BP[s].x, cM, invT)));
+      df nxt = df_addf(run, wsl);
+      if (!dd_le(nxt, tgt)) {
+        my_slice = s;
+        my_pref = run;
+        atomicMin(&s_slice, s);
+        break;
       }
+      run = nxt;
     }
   }
   __syncthreads();
@@ -529,20 +531,23 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
   if (threadIdx.x < BN) s_w[threadIdx.x] = w;
   __syncthreads();
   // in-slice target in slice units
-  const double tin = (target_d - df_d(pref)) / (double)fslice;
+  const df tin = dd_mul(dd_add(tgt, dd_neg(pref)), dd_recip(fslice));
   df wtot;
   const df wex = block_excl_scan_df(df_make(threadIdx.x < BN ? w : 0.f), &wtot, sh_f);
   if (threadIdx.x == 0) s_tok = 0x7fffffff;
   __syncthreads();
-  double my_lo = 0.0, my_hi = 0.0;
+  df my_lo = {0.f, 0.f}, my_hi = {0.f, 0.f};
   bool claim = false;
   if (!fallback && threadIdx.x < BN && w > 0.f) {
-    my_lo = df_d(wex);
-    my_hi = df_d(df_addf(wex, w));
-    if (my_lo <= tin && my_hi > tin) { claim = true; atomicMin(&s_tok, (int)threadIdx.x); }
+    my_lo = wex;
+    my_hi = df_addf(wex, w);
+    if (dd_le(my_lo, tin) && !dd_le(my_hi, tin)) { claim = true; atomicMin(&s_tok, (int)threadIdx.x); }
   }
   __syncthreads();
-  if (claim && (int)threadIdx.x == s_tok) { s_lo = (float)(tin - my_lo); s_hi = (float)(my_hi - tin); }
+  if (claim && (int)threadIdx.x == s_tok) {
+    s_lo = dd_add(tin, dd_neg(my_lo)).hi;
+    s_hi = dd_add(my_hi, dd_neg(tin)).hi;
+  }
   __syncthreads();
   if (s_tok == 0x7fffffff) {
     fallback = true;
@@ -562,16 +567,17 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
     out[n] = tok;
     for (int j = n + 1; j <= sh.gamma; ++j) out[j] = -1;
     accept_len[b] = n;
-    const double Zs = Z > 0.0 ? Z : 1.0;
-    const double dmargin = fmin((double)s_lo, (double)s_hi) * (double)fslice / Zs;
-    const double band =
-        (double)eps.scale *
-        (((double)eps.elem * sqrt((double)e2) + (double)eps.slice * sqrt((double)m2) +
-          (resid ? (double)eps.norm : 0.0)) / Zs + (double)eps.abs_);
+    const float Zs = Zdf.hi > 0.f ? Zdf.hi : 1.0f;
+    const float scale = __fdiv_rn(fslice, Zs);                 // slice units -> probability
+    const float dmargin = fminf(s_lo, s_hi) * scale;
+    const float band = eps.scale * (__fdiv_rn(eps.elem * sqrtf(e2) + eps.slice * sqrtf(m2) +
+                                                  (resid ? eps.norm : 0.f),
+                                              Zs) +
+                                    eps.abs_);
     if (diag) {
-      diag[(size_t)b * 4 + 0] = (float)((double)s_lo * fslice / Zs);
-      diag[(size_t)b * 4 + 1] = (float)((double)s_hi * fslice / Zs);
-      diag[(size_t)b * 4 + 2] = (float)band;
+      diag[(size_t)b * 4 + 0] = s_lo * scale;
+      diag[(size_t)b * 4 + 1] = s_hi * scale;
+      diag[(size_t)b * 4 + 2] = band;
       diag[(size_t)b * 4 + 3] = (float)tok;
     }
     if (fallback || dmargin <= band) {
