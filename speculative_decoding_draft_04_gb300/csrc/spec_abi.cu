@@ -146,7 +146,7 @@ Layout layout(const Shape& sh) {
     off = (off + bytes + 255) & ~(size_t)255;
     return o;
   };
-  const size_t B = sh.B, g = sh.gamma, NS = sh.NS;
+  const size_t B = sh.B, g = sh.gamma;
   L.max_items = sh.B;
   L.ctrl = take(CTRL_WORDS * sizeof(uint32_t));
   L.trace = take(MAX_GAMMA * TRACE_SLOTS * sizeof(unsigned long long));
@@ -159,8 +159,8 @@ Layout layout(const Shape& sh) {
   L.prevtok = take(B * g * sizeof(int));
   L.vflags = take(B * sizeof(int));
   L.lse_p = take(B * (g + 1) * sizeof(double));
-  L.bpart = take(B * NS * sizeof(float4));
-  L.vpart = take(B * g * NS * sizeof(float4));
+  L.bpart = take(B * sh.NSV * sizeof(float4));
+  L.vpart = take(B * g * sh.NSV * sizeof(float4));
   L.slow = take(B * sizeof(int));
   L.accbits = take(B * sizeof(uint32_t));
   L.rowc = take(B * g * sizeof(float4));
@@ -215,6 +215,7 @@ Shape make_shape(int B, int gamma, int V, int r) {
   s.r = r;
   s.NS = (V + BN - 1) / BN;
   s.NC = (V + CW - 1) / CW;
+  s.NSV = (V + VB - 1) / VB;
   s.HB = (V + HPB - 1) / HPB;
   return s;
 }

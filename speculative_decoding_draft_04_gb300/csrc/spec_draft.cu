@@ -23,6 +23,7 @@
 
 #include "spec_tile_tc.cuh"
 #include "spec_hp.cuh"
+#include "spec_tmap.cuh"
 
 namespace spec {
 
@@ -163,8 +164,16 @@ struct DraftEpi {
   const int* tokens;
   const float* temp;
   float4* dpart;
+  const CUtensorMap* umap;   // U as [B][gamma][V] (a __grid_constant__ parameter)
 
-  __device__ int step() const { return k; }
+  // the U_k tile of (mt, sl): two 64-column TMA boxes of 128 rows
+  __device__ void load_x(int mt, int sl, unsigned char* xb, uint64_t* full, int lane, int, int) const {
+    if (lane != 0) return;
+    const int n0 = sl * BN, m0 = mt * TC_M;
+    mbar_expect_tx(full, (uint32_t)(TC_M * BN * 2));
+    tma_load_3d(xb, umap, n0, k, m0, full);
+    tma_load_3d(xb + TC_M * 128, umap, n0 + 64, k, m0, full);
+  }
   // W1 row of row m of request tile mt (-1: no such request; its A row is zero)
   __device__ int token(int mt, int m) const {
     const int b = mt * TC_M + m;
@@ -175,7 +184,7 @@ struct DraftEpi {
   // Row m of tile (mt, sl): the partials of the slice's four chunks, from the
   // U row in `ub` (swizzled) and the accumulator row at TMEM address `trow`;
   // two chunks per TMEM wait.
-  __device__ void epilogue(int mt, int sl, int m, const unsigned char* ub, uint32_t trow) const {
+  __device__ void epilogue(int mt, int sl, int m, const unsigned char* ub, uint32_t trow, int) const {
     const int b = mt * TC_M + m;
     const bool rowok = b < sh.B;
     const int n0 = sl * BN;
@@ -479,8 +488,9 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
   TpState st{0u, s_bar, &s_fail, 0u, 0u};
   if constexpr (PATH == 2) {
     if (threadIdx.x == 0) {
-      tp_init(s_bar);
+      tp_init(s_bar, 1);
       s_fail = 0;
+      tma_prefetch_map(&P.maps.u);
     }
     if (threadIdx.x < 32) tc_alloc(&s_holder, TP_TMEM_COLS);
     tc_fence_before();
@@ -498,10 +508,10 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
     bool ok = true;
     if (tr) tr[k * TRACE_SLOTS + 0] = globaltimer_ns();
     if constexpr (PATH == 2) {
-      const DraftEpi e{sh, k, P.anchor, P.tokens, P.temp, P.ws.dpart};
+      const DraftEpi e{sh, k, P.anchor, P.tokens, P.temp, P.ws.dpart, &P.maps.u};
       const int n = (int)blockIdx.x < n_tiles ? (n_tiles - (int)blockIdx.x + (int)G - 1) / (int)G : 0;
-      ok = tp_run(e, sh, P.maps, reinterpret_cast<const bf16*>(W1), (int)blockIdx.x, (int)G, n,
-                  smem_raw, st, s_tok);
+      ok = tp_run<BN>(e, sh, P.maps, reinterpret_cast<const bf16*>(W1), sh.NS, (int)blockIdx.x,
+                      (int)G, n, smem_raw, st, s_tok);
       if (!ok && threadIdx.x == 0) set_status(P.status, SPEC_DEV_TIMEOUT);
     } else {
       for (int t = blockIdx.x; t < n_tiles; t += G)
@@ -542,59 +552,9 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
 }
 
 // ---------------------------------------------------------------- launcher
-// cuTensorMapEncodeTiled through the runtime's driver entry point (the library
-// links no driver library of its own).
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<EncodeTiledFn>(p);
-  }();
-  return fn;
-}
-
-// Tensor maps of the draft's tensor-memory path: U as [B][gamma][V] with
-// 64 x 1 x 128 boxes, W2 as [r][V] with 64 x r boxes, both bf16 with the
-// 128-byte swizzle; reads outside the tensors return zeros.
-static cudaError_t encode_draft_maps(const Shape& sh, const void* U, const void* W2, TpMaps* maps) {
-  const EncodeTiledFn enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t V = (cuuint64_t)sh.V;
-  {
-    const cuuint64_t dims[3] = {V, (cuuint64_t)sh.gamma, (cuuint64_t)sh.B};
-    const cuuint64_t strides[2] = {V * 2, V * 2 * (cuuint64_t)sh.gamma};
-    const cuuint32_t box[3] = {64, 1, (cuuint32_t)TC_M};
-    const cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&maps->u, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(U), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    const cuuint64_t dims[2] = {V, (cuuint64_t)sh.r};
-    const cuuint64_t strides[1] = {V * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)sh.r};
-    const cuuint32_t es[2] = {1, 1};
-    if (enc(&maps->w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  return cudaSuccess;
-}
-
 template <typename DT, int BM, int PATH>
 static cudaError_t launch_persist(const DraftParams& P, int nsm, cudaStream_t st) {
-  size_t smem = PATH == 2 ? TpLayout(P.sh.r).total : TileLayout<DT>(BM, P.sh.r, false).total;
+  size_t smem = PATH == 2 ? TpLayout(P.sh.r, BN).total : TileLayout<DT>(BM, P.sh.r, false).total;
   const size_t slab = (size_t)P.sh.r * HPB * sizeof(DT);    // re-decision W2 slab (> sampler's)
   smem = smem > slab ? smem : slab;
   auto kern = draft_persistent_kernel<DT, BM, PATH>;
@@ -653,7 +613,8 @@ cudaError_t launch_draft_persistent(const Shape& sh, const void* U, const void* 
   }
   if constexpr (sizeof(DT) == 2) {
     if (path == 2 && sh.r % 64 == 0) {
-      const cudaError_t e = encode_draft_maps(sh, U, W2, &P.maps);
+      cudaError_t e = encode_u_map(sh, U, &P.maps.u);
+      if (e == cudaSuccess) e = encode_w2_map(sh, W2, &P.maps.w2);
       if (e != cudaSuccess) return e;
       return launch_persist<DT, 128, 2>(P, nsm, st);
     }

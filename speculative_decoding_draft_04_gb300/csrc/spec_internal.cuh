@@ -16,12 +16,15 @@ typedef __nv_bfloat16 bf16;
 // ---------------------------------------------------------------- geometry
 constexpr int BN = 128;       // vocabulary columns per slice (one GEMM tile's N)
 constexpr int CW = 32;        // vocabulary columns per draft partial (chunk)
+constexpr int VB = 32;        // vocabulary columns per verification slice
+constexpr int VT = 64;        // vocabulary columns per verification tensor-memory tile
 constexpr int HPB = 256;      // columns per extended-precision block
 constexpr int NT = 256;       // threads per CTA for every kernel
 constexpr int MAX_GAMMA = 16;
 
 struct Shape {
-  int B, gamma, V, r, NS, NC, HB;   // NS = ceil(V / BN), NC = ceil(V / CW), HB = ceil(V / HPB)
+  int B, gamma, V, r, NS, NC, NSV, HB;   // NS = ceil(V / BN), NC = ceil(V / CW),
+                                          // NSV = ceil(V / VB), HB = ceil(V / HPB)
 };
 
 // A decision queued for re-decision in extended precision.
@@ -60,8 +63,8 @@ struct Ws {
   int* prevtok;         // [B*gamma] x_j of each packed row
   int* vflags;          // [B] bit0 bad request, bits 8.. ratio flags
   double* lse_p;        // [B][gamma+1]
-  float4* bpart;        // [B][NS] bonus row (c, s, p2, 0)
-  float4* vpart;        // [B*gamma][NS] (alpha, resid, p2, q2)
+  float4* bpart;        // [B][NSV] bonus row (c, s, p2, 0)
+  float4* vpart;        // [B*gamma][NSV] (alpha, resid, p2, q2)
   int* slow;            // [B]
   uint32_t* accbits;    // [B] first-pass ratio-test outcomes
   float4* rowc;         // [B*gamma] packed row: 1/T and -lse_q as double-float pairs
@@ -312,16 +315,22 @@ __device__ __forceinline__ bool grid_sync(uint32_t* ctrl, uint32_t nblocks, uint
       __threadfence();
       atomicAdd(ctrl + CTRL_BAR_GEN, 1u);
     } else {
+      // bounded by wall-clock time (1 s; a phase takes microseconds)
       uint32_t it = 0;
+      unsigned long long t0 = 0;
       while (ld_acquire_gpu(ctrl + CTRL_BAR_GEN) == g) {
         if (ld_acquire_gpu(ctrl + CTRL_ABORT) != 0u) { ok = 0; break; }
-        if (++it > (1u << 24)) {
-          ok = 0;
-          atomicExch(ctrl + CTRL_ABORT, 1u);
-          set_status(status, SPEC_DEV_TIMEOUT);
-          break;
+        ++it;
+        if (it == 32) t0 = globaltimer_ns();
+        if (it > 32) {
+          if ((it & 63) == 0 && globaltimer_ns() - t0 > 1000ull * 1000 * 1000) {
+            ok = 0;
+            atomicExch(ctrl + CTRL_ABORT, 1u);
+            set_status(status, SPEC_DEV_TIMEOUT);
+            break;
+          }
+          __nanosleep(40);
         }
-        if (it > 32) __nanosleep(40);
       }
     }
     __threadfence();

@@ -86,11 +86,12 @@ __device__ __forceinline__ uint64_t tc_sdesc(uint32_t saddr, uint32_t lbo, uint3
   return d;
 }
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, A K-major,
-// B MN-major, N = 128, M = 128.
-__device__ __forceinline__ uint32_t tc_idesc() {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) | ((uint32_t)(TC_N >> 3) << 17) |
+// B MN-major, M = 128, N = n (a multiple of 16 up to 256).
+__device__ __forceinline__ uint32_t tc_idesc_n(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(TC_M >> 4) << 24);
 }
+__device__ __forceinline__ uint32_t tc_idesc() { return tc_idesc_n(TC_N); }
 
 // ---------------------------------------------------------------- primitives
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -153,6 +154,14 @@ __device__ __forceinline__ void tc_ld32_issue(uint32_t taddr, float (&v)[32]) {
         "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
         "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
+}
+// 8 consecutive fp32 columns of this thread's lane, without waiting.
+__device__ __forceinline__ void tc_ld8_issue(uint32_t taddr, float (&v)[8]) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr));
 }
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 // 32 consecutive fp32 columns of this thread's lane

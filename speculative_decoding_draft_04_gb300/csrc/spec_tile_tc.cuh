@@ -1,11 +1,14 @@
-// Warp-specialised tensor-memory tile engine for the draft step's rank-r bias
-// tiles (bf16, r % 64 == 0).  A CTA walks its share of (request tile, slice of
-// BN vocabulary columns) tiles; the roles run concurrently and hand buffers to
+// Warp-specialised tensor-memory tile engine for the rank-r bias tiles
+// (bf16, r % 64 == 0) of the draft step (N = 128 columns per tile) and of the
+// verification (N = 64).  A CTA walks its share of (row tile, slice of N
+// vocabulary columns) tiles; the roles run concurrently and hand buffers to
 // each other through shared-memory mbarriers:
 //
-//   warp 4, one lane   TMA producer: the W2 slice (r x BN, read in place as the
-//                      MN-major B operand, 128-byte swizzle) and the U_k tile
-//                      (128 rows x BN logits, 128-byte swizzle) of each tile.
+//   warp 4             producer: one lane loads the W2 slice (r x N, read in
+//                      place as the MN-major B operand, 128-byte swizzle) by
+//                      TMA; the epilogue object loads the tile's logit rows
+//                      (TMA for the draft's U_k, a cp.async row gather for the
+//                      verification's packed U and target rows).
 //   warps 6-7          gather the W1[x_{k-1}] rows of a request tile (the A
 //                      operand, K-major, 128-byte swizzle) with cp.async, once
 //                      per request tile, after the last MMA that read the old
@@ -18,9 +21,12 @@
 //                      them to the accumulator's "full" barrier and to the W2
 //                      stage's "empty" barrier.
 //   warps 0-3          epilogue, thread = tile row = TMEM lane: reads its row of
-//                      the accumulator (tcgen05.ld) and of the U tile (shared
-//                      memory) and reduces it to the slice partial without
-//                      exchanging anything with other threads.
+//   (and 8-11)         the accumulator (tcgen05.ld) and of the logit tile (shared
+//                      memory) and reduces it to its partials without
+//                      exchanging anything with other threads.  With EG = 2
+//                      epilogue groups (a 384-thread CTA) the second group,
+//                      warps 8-11 (same TMEM lanes: warp % 4), takes the other
+//                      half of each tile's columns.
 //
 // Barrier phases are counted with running per-CTA counters (tiles, request
 // tiles) that every thread advances identically, so the state carries over
@@ -35,14 +41,15 @@
 
 namespace spec {
 
-constexpr uint32_t TP_TMEM_COLS = 256;         // two 128-column fp32 accumulators
-constexpr int TP_UBYTES = TC_M * BN * 2;       // one U tile (bf16)
+constexpr uint32_t TP_TMEM_COLS = 256;         // two accumulators of up to 128 fp32 columns
+constexpr int TP_XBYTES = 32768;               // logit rows of one tile: 128 x 128 bf16, or
+                                               // 128 x 64 U rows + 128 x 64 target rows
 
 // Barrier slots.
 enum : int {
   TB_W2_FULL = 0,    // + stage (2)
   TB_W2_EMPTY = 2,   // + stage (2)
-  TB_U_FULL = 4,     // + buffer (2)
+  TB_U_FULL = 4,     // + buffer (2): the tile's logit rows
   TB_U_EMPTY = 6,    // + buffer (2)
   TB_T_FULL = 8,     // + accumulator (2)
   TB_T_EMPTY = 10,   // + accumulator (2)
@@ -51,22 +58,24 @@ enum : int {
   TB_COUNT = 14
 };
 
-// Shared-memory plan (offsets from a 1024-byte aligned base).
+// Shared-memory plan (offsets from a 1024-byte aligned base) for N-column
+// tiles.
 struct TpLayout {
   int nw;                                      // W2 stages (2 when they fit)
-  size_t offA, offW, offU, total;
-  __host__ __device__ TpLayout(int r) {
-    const size_t a = (size_t)(r / 64) * 16384, w = (size_t)2 * r * 128;
-    nw = (a + 2 * w + 2 * TP_UBYTES <= (size_t)208 * 1024) ? 2 : 1;
+  size_t offA, offW, wbytes, offU, total;
+  __host__ __device__ TpLayout(int r, int N) {
+    const size_t a = (size_t)(r / 64) * 16384;
+    wbytes = (size_t)(N / 64) * r * 128;
+    nw = (a + 2 * wbytes + 2 * TP_XBYTES <= (size_t)208 * 1024) ? 2 : 1;
     offA = 0;
     offW = a;
-    offU = offW + (size_t)nw * w;
-    total = offU + 2 * (size_t)TP_UBYTES + 1024;   // + slack for 1 KB alignment
+    offU = offW + (size_t)nw * wbytes;
+    total = offU + 2 * (size_t)TP_XBYTES + 1024;   // + slack for 1 KB alignment
   }
 };
 
-// Tensor maps of one draft call (encoded on the host, passed as a
-// __grid_constant__ kernel parameter).
+// Tensor maps of one call (encoded on the host, passed as a __grid_constant__
+// kernel parameter).
 struct TpMaps {
   CUtensorMap u;     // U viewed as [B][gamma][V], box 64 x 1 x 128, 128-byte swizzle
   CUtensorMap w2;    // W2 viewed as [r][V],       box 64 x r,       128-byte swizzle
@@ -85,42 +94,61 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-__device__ __forceinline__ void tp_init(uint64_t* bar) {
+// xfull_count: arrivals that complete a logit-row fill (1 for a TMA fill
+// with its byte count, 32 for a cp.async gather by the producer warp);
+// eg: epilogue groups of 128 threads.
+__device__ __forceinline__ void tp_init(uint64_t* bar, uint32_t xfull_count, uint32_t eg = 1) {
   for (int s = 0; s < 2; ++s) {
     mbar_init(bar + TB_W2_FULL + s, 1);
     mbar_init(bar + TB_W2_EMPTY + s, 1);
-    mbar_init(bar + TB_U_FULL + s, 1);
-    mbar_init(bar + TB_U_EMPTY + s, TC_M);
+    mbar_init(bar + TB_U_FULL + s, xfull_count);
+    mbar_init(bar + TB_U_EMPTY + s, TC_M * eg);
     mbar_init(bar + TB_T_FULL + s, 1);
-    mbar_init(bar + TB_T_EMPTY + s, TC_M);
+    mbar_init(bar + TB_T_EMPTY + s, TC_M * eg);
   }
   mbar_init(bar + TB_A_FULL, 64);
   mbar_init(bar + TB_A_EMPTY, 1);
 }
 
 // ---------------------------------------------------------------- primitives
-// Bounded wait for the completion of the phase with parity `parity`; gives up
-// after about 2^22 polls, or at once when another thread raised *fail.
+// Bounded wait for the completion of the phase with parity `parity`: polls
+// without blocking (mbarrier.test_wait), backs off, and gives up after
+// TP_WAIT_NS of wall-clock time (the pipeline's stages take microseconds), or
+// at once when another thread raised *fail.
+constexpr unsigned long long TP_WAIT_NS = 100ull * 1000 * 1000;
+__device__ __forceinline__ bool tp_test(uint32_t a, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return done != 0;
+}
 __device__ __forceinline__ bool tp_wait(uint64_t* bar, uint32_t parity, volatile int* fail) {
   const uint32_t a = smem_u32(bar);
-  for (uint32_t it = 0; it < (1u << 22); ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(a), "r"(parity));
-    if (done) return true;
-    if ((it & 63) == 63) {
+  for (int it = 0; it < 64; ++it)
+    if (tp_test(a, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (tp_test(a, parity)) return true;
+    if ((it & 15) == 15) {
       if (*fail) return false;
-      __nanosleep(64);
+      if (globaltimer_ns() - t0 > TP_WAIT_NS) break;
     }
+    __nanosleep(64);
   }
   *fail = 1;
   return false;
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+// Arrive on `bar` once all of this thread's earlier cp.async copies are done
+// (the arrival is one of the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
@@ -164,29 +192,36 @@ __device__ __forceinline__ const unsigned char* tp_uchunk(const unsigned char* u
 }
 
 // ---------------------------------------------------------------- the engine
-// Tile list of this CTA: tiles t0 + i * G, i < n; tile t is (request tile
-// t / NS, slice t % NS).  E supplies:
-//   int  step()                              draft step k (U_k, tokens x_{k-1})
+// Tile list of this CTA: tiles t0 + i * stride, i < n; tile t is (row tile
+// t / nsl, slice t % nsl) of N columns.  E supplies (all threads may call):
 //   int  token(int mtile, int m)             W1 row of row m, -1 for none
-//   void epilogue(int mtile, int slice, int m, const unsigned char* ub,
-//                 uint32_t tmem_row)         one row of one tile
+//   void load_x(int mtile, int slice, unsigned char* xb, uint64_t* full, int lane,
+//               int next_mtile, int next_slice)
+//                                            fill the tile's logit rows (called by
+//                                            the 32 lanes of the producer warp; the
+//                                            next tile, -1 if none, may be prefetched)
+//   void epilogue(int mtile, int slice, int m, const unsigned char* xb,
+//                 uint32_t tmem_row, int grp) one row of one tile (grp: the
+//                                            epilogue group, 0 when EG == 1)
 // `s_tok` is a 128-entry shared array for the gatherers.  Returns false if a
 // wait gave up (after draining what it started).
-template <class E>
+template <int N, class E, int EG = 1>
 __device__ __forceinline__ bool tp_run(const E& e, const Shape& sh, const TpMaps& maps,
-                                       const bf16* W1, int t0, int G, int n,
+                                       const bf16* W1, int nsl, int t0, int stride, int n,
                                        unsigned char* smem_raw, TpState& st, int* s_tok) {
+  static_assert(N == 64 || N == 128, "tile width");
+  static_assert(EG == 1 || EG == 2, "epilogue groups");
   if (n <= 0) return true;
   unsigned char* smem = align1k(smem_raw);
-  const TpLayout lay(sh.r);
+  const TpLayout lay(sh.r, N);
   unsigned char* As = smem + lay.offA;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = sh.r, k = e.step();
-  const uint32_t wbytes = (uint32_t)(2 * r * 128);
+  const int r = sh.r;
+  const uint32_t wbytes = (uint32_t)lay.wbytes;
   uint64_t* bar = st.bar;
   volatile int* fail = st.fail;
-  auto mt_of = [&](int i) { return (t0 + i * G) / sh.NS; };
-  auto sl_of = [&](int i) { return (t0 + i * G) % sh.NS; };
+  auto mt_of = [&](int i) { return (t0 + i * stride) / nsl; };
+  auto sl_of = [&](int i) { return (t0 + i * stride) % nsl; };
 
   // Earlier generic-proxy use of these buffers (sampling, re-decision phases)
   // is ordered before this phase's TMA and MMA accesses.
@@ -194,32 +229,31 @@ __device__ __forceinline__ bool tp_run(const E& e, const Shape& sh, const TpMaps
   __syncthreads();
 
   if (warp == 4) {
-    if (lane == 0) {
-      tma_prefetch_map(&maps.u);
-      tma_prefetch_map(&maps.w2);
-      for (int i = 0; i < n && !*fail; ++i) {
-        const uint32_t g = st.gi + i;
+    if (lane == 0) tma_prefetch_map(&maps.w2);
+    for (int i = 0; i < n && !*fail; ++i) {
+      const uint32_t g = st.gi + i;
+      const int n0 = sl_of(i) * N;
+      if (lane == 0) {
         const int s = (int)(g % (uint32_t)lay.nw);
         const uint32_t f = g / (uint32_t)lay.nw;
-        if (f >= 1 && !tp_wait(bar + TB_W2_EMPTY + s, (f - 1) & 1u, fail)) break;
-        unsigned char* wb = smem + lay.offW + (size_t)s * wbytes;
-        const int n0 = sl_of(i) * BN;
-        mbar_expect_tx(bar + TB_W2_FULL + s, wbytes);
-        tma_load_2d(wb, &maps.w2, n0, 0, bar + TB_W2_FULL + s);
-        tma_load_2d(wb + r * 128, &maps.w2, n0 + 64, 0, bar + TB_W2_FULL + s);
-        const int b = (int)(g & 1u);
-        const uint32_t fu = g >> 1;
-        if (fu >= 1 && !tp_wait(bar + TB_U_EMPTY + b, (fu - 1) & 1u, fail)) break;
-        unsigned char* ub = smem + lay.offU + (size_t)b * TP_UBYTES;
-        const int m0 = mt_of(i) * TC_M;
-        mbar_expect_tx(bar + TB_U_FULL + b, (uint32_t)TP_UBYTES);
-        tma_load_3d(ub, &maps.u, n0, k, m0, bar + TB_U_FULL + b);
-        tma_load_3d(ub + TC_M * 128, &maps.u, n0 + 64, k, m0, bar + TB_U_FULL + b);
+        if (f == 0 || tp_wait(bar + TB_W2_EMPTY + s, (f - 1) & 1u, fail)) {
+          unsigned char* wb = smem + lay.offW + (size_t)s * wbytes;
+          mbar_expect_tx(bar + TB_W2_FULL + s, wbytes);
+          for (int h = 0; h < N / 64; ++h)
+            tma_load_2d(wb + h * r * 128, &maps.w2, n0 + 64 * h, 0, bar + TB_W2_FULL + s);
+        }
       }
+      __syncwarp();
+      if (*fail) break;
+      const int b = (int)(g & 1u);
+      const uint32_t fu = g >> 1;
+      if (fu >= 1 && !tp_wait(bar + TB_U_EMPTY + b, (fu - 1) & 1u, fail)) break;
+      e.load_x(mt_of(i), sl_of(i), smem + lay.offU + (size_t)b * TP_XBYTES, bar + TB_U_FULL + b, lane,
+               i + 1 < n ? mt_of(i + 1) : -1, i + 1 < n ? sl_of(i + 1) : -1);
     }
   } else if (warp == 5) {
     if (lane == 0) {
-      const uint32_t idesc = tc_idesc();
+      const uint32_t idesc = tc_idesc_n(N);
       const uint32_t a0 = smem_u32(As);
       uint32_t ga = st.ga;
       for (int i = 0; i < n; ++i) {
@@ -234,7 +268,7 @@ __device__ __forceinline__ bool tp_run(const E& e, const Shape& sh, const TpMaps
         if (g >= 2 && !tp_wait(bar + TB_T_EMPTY + b, ((g >> 1) - 1) & 1u, fail)) break;
         tc_fence_after();
         const uint32_t w0 = smem_u32(smem + lay.offW + (size_t)s * wbytes);
-        const uint32_t d = st.tmem + (uint32_t)(b * 128);
+        const uint32_t d = st.tmem + (uint32_t)(b * N);
         for (int kk = 0; kk < r; kk += 16) {
           const uint64_t ad = tc_sdesc(a0 + (uint32_t)((kk >> 6) * 16384 + (kk & 63) * 2), 16, 1024);
           const uint64_t bd = tc_sdesc(w0 + (uint32_t)(kk * 128), (uint32_t)(r * 128), 1024);
@@ -245,7 +279,7 @@ __device__ __forceinline__ bool tp_run(const E& e, const Shape& sh, const TpMaps
         if (i == n - 1 || mt_of(i + 1) != mt_of(i)) tc_commit(bar + TB_A_EMPTY);
       }
     }
-  } else if (warp >= 6) {
+  } else if (warp == 6 || warp == 7) {
     // 64 gatherers; thread q copies 16-byte chunks q, q + 64, ... of the A tile
     const int q0 = threadIdx.x - 192;
     const int cpr = r / 8;
@@ -274,16 +308,17 @@ __device__ __forceinline__ bool tp_run(const E& e, const Shape& sh, const TpMaps
     }
   } else {
     // epilogue: thread = row
-    const int m = threadIdx.x;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const int m = threadIdx.x & (TC_M - 1);
+    const int grp = warp >= 8 ? 1 : 0;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     for (int i = 0; i < n; ++i) {
       const uint32_t g = st.gi + i;
       const int b = (int)(g & 1u);
       if (!tp_wait(bar + TB_U_FULL + b, (g >> 1) & 1u, fail)) break;
       if (!tp_wait(bar + TB_T_FULL + b, (g >> 1) & 1u, fail)) break;
       tc_fence_after();
-      e.epilogue(mt_of(i), sl_of(i), m, smem + lay.offU + (size_t)b * TP_UBYTES,
-                 st.tmem + lane_base + (uint32_t)(b * 128));
+      e.epilogue(mt_of(i), sl_of(i), m, smem + lay.offU + (size_t)b * TP_XBYTES,
+                 st.tmem + lane_base + (uint32_t)(b * N), grp);
       tc_fence_before();
       mbar_arrive(bar + TB_T_EMPTY + b);
       mbar_arrive(bar + TB_U_EMPTY + b);

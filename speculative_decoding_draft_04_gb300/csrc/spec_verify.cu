@@ -19,7 +19,10 @@
 //                        draw (crossing slice from the slice sums, that slice
 //                        recomputed and scanned).  Near-boundary draws are queued
 //                        for extended-precision re-decision (spec_refine.cu).
-#include "spec_tc.cuh"
+#include <cstring>
+
+#include "spec_tile_tc.cuh"
+#include "spec_tmap.cuh"
 
 namespace spec {
 
@@ -44,6 +47,23 @@ __device__ __forceinline__ float norm_factor(float c, df invT, df nlse) {
 __device__ __forceinline__ df d2df(double x) {
   float h = (float)x;
   return {h, (float)(x - (double)h)};
+}
+
+// Unnormalised verification weights relative to a slice reference c, with
+// s2 = log2(e) / T folded in: q = 2^(((U - c) + bias) s2), p = 2^((t - c) s2)
+// (one hardware exp2 each).  The tile epilogue and the final draw's slice
+// recompute use these same two expressions.
+constexpr float LOG2E_F = 1.44269504f;
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float vq(float u, float c, float bias, float s2) {
+  return ex2_approx(__fmul_rn(__fadd_rn(__fsub_rn(u, c), bias), s2));
+}
+__device__ __forceinline__ float vp(float t, float c, float s2) {
+  return ex2_approx(__fmul_rn(__fsub_rn(t, c), s2));
 }
 
 // 8 consecutive values (16-byte aligned)
@@ -137,11 +157,49 @@ __global__ void __launch_bounds__(NT) verify_prep_kernel(
 }
 
 // ---------------------------------------------------------------- target statistics
+// Merge of per-thread log-sum-exp partials (reference m, sum acc of
+// exp((x - m)/T)) over the block; returns (M, Z) to every thread.
+__device__ __forceinline__ void lse_merge(float& m, df& acc, float invT, float* sh) {
+  auto comb = [&](float m2, df a2) {
+    const float mn = fmaxf(m, m2);
+    if (mn == -INFINITY) return;
+    const df x = m == -INFINITY ? df{0.f, 0.f} : df_mulf(acc, expf(fast_tx(m, mn, invT)));
+    const df y = m2 == -INFINITY ? df{0.f, 0.f} : df_mulf(a2, expf(fast_tx(m2, mn, invT)));
+    acc = df_add(x, y);
+    m = mn;
+  };
+  for (int o = 16; o; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const df a2 = shfl_xor_df(acc, o);
+    comb(m2, a2);
+  }
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) { sh[3 * w] = m; sh[3 * w + 1] = acc.hi; sh[3 * w + 2] = acc.lo; }
+  __syncthreads();
+  if (w == 0) {
+    m = lane < NT / 32 ? sh[3 * lane] : -INFINITY;
+    acc = lane < NT / 32 ? df{sh[3 * lane + 1], sh[3 * lane + 2]} : df{0.f, 0.f};
+    for (int o = 16; o; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const df a2 = shfl_xor_df(acc, o);
+      comb(m2, a2);
+    }
+    if (lane == 0) { sh[0] = m; sh[1] = acc.hi; sh[2] = acc.lo; }
+  }
+  __syncthreads();
+  m = sh[0];
+  acc = {sh[1], sh[2]};
+  __syncthreads();
+}
+
+// One CTA per target row j <= L_b of request b: its logsumexp; the bonus row
+// (j = L_b) also writes the per-VB-slice partials (c, s, p2) its draw needs.
 template <typename DT>
 __global__ void __launch_bounds__(NT) target_stats_kernel(Shape sh, const DT* __restrict__ target,
                                                           const float* __restrict__ temp,
                                                           const int* __restrict__ vlen, Ws ws) {
-  __shared__ float s_c[NT / 16], s_hi[NT / 16], s_lo[NT / 16];
+  __shared__ float s_m[3 * (NT / 32)];
   __shared__ df s_tab[DD_EXP_TAB];
   const int j = blockIdx.x, b = blockIdx.y;
   if (ws.vflags[b] & 1) return;
@@ -151,61 +209,92 @@ __global__ void __launch_bounds__(NT) target_stats_kernel(Shape sh, const DT* __
   const float T = temp[b];
   const float invT = 1.0f / T;
   const DT* row = target + ((size_t)b * (sh.gamma + 1) + j) * sh.V;
-  const bool bonus = j == L;
-  const int hw = threadIdx.x >> 4, hl = threadIdx.x & 15;
-  float cref = -INFINITY;
+  float mref = -INFINITY;
   df acc = {0.f, 0.f};
-  // every lane runs the same trip count (full-warp shuffles below)
-  for (int base = 0; base < sh.NS; base += NT / 16) {
-    const int s = base + hw;
-    const bool sv = s < sh.NS;
-    const int n = s * BN + hl * 8;
-    const bool valid = sv && n < sh.V;
-    float vals[8];
-    if (valid) load8(row + n, vals);
-    float c = -INFINITY;
-    if (valid)
+  if (j == L) {
+    // bonus row: GS threads (8 columns each) per VB-column slice; every lane
+    // runs the same trip count (full-warp shuffles); UNR slices' loads issued
+    // before any is reduced
+    constexpr int GS = VB / 8, NG = NT / GS, UNR = 4;
+    const int hw = threadIdx.x / GS, hl = threadIdx.x % GS;
+    for (int base = 0; base < sh.NSV; base += NG * UNR) {
+      float vals[UNR][8];
+      bool ok[UNR];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) c = fmaxf(c, vals[e]);
-#pragma unroll
-    for (int m = 8; m; m >>= 1) c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, m));
-    float ssum = 0.f, p2 = 0.f;
-    if (valid)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float wv = __expf(fast_tx(vals[e], c, invT));
-        ssum = __fadd_rn(ssum, wv);
-        p2 = fmaf(wv, wv, p2);
+      for (int u = 0; u < UNR; ++u) {
+        const int s = base + hw + NG * u;
+        const int n = s * VB + hl * 8;
+        ok[u] = s < sh.NSV && n < sh.V;
+        if (ok[u]) load8(row + n, vals[u]);
       }
 #pragma unroll
-    for (int m = 8; m; m >>= 1) {
-      ssum += __shfl_xor_sync(0xffffffffu, ssum, m);
-      p2 += __shfl_xor_sync(0xffffffffu, p2, m);
+      for (int u = 0; u < UNR; ++u) {
+        const int s = base + hw + NG * u;
+        float c = -INFINITY;
+        if (ok[u])
+#pragma unroll
+          for (int e = 0; e < 8; ++e) c = fmaxf(c, vals[u][e]);
+#pragma unroll
+        for (int m = GS / 2; m; m >>= 1) c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, m));
+        float ssum = 0.f, p2 = 0.f;
+        if (ok[u])
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float wv = __expf(fast_tx(vals[u][e], c, invT));
+            ssum = __fadd_rn(ssum, wv);
+            p2 = fmaf(wv, wv, p2);
+          }
+#pragma unroll
+        for (int m = GS / 2; m; m >>= 1) {
+          ssum += __shfl_xor_sync(0xffffffffu, ssum, m);
+          p2 += __shfl_xor_sync(0xffffffffu, p2, m);
+        }
+        if (s >= sh.NSV || hl != 0) continue;        // one lane per group accumulates
+        ws.bpart[(size_t)b * sh.NSV + s] = make_float4(c, ssum, p2, 0.f);
+        if (c > mref) {
+          if (mref != -INFINITY) acc = df_mulf(acc, expf(fast_tx(mref, c, invT)));
+          mref = c;
+          acc = df_addf(acc, ssum);
+        } else {
+          acc = df_addf(acc, __fmul_rn(ssum, expf(fast_tx(c, mref, invT))));
+        }
+      }
     }
-    if (!sv) continue;
-    if (bonus && hl == 0) ws.bpart[(size_t)b * sh.NS + s] = make_float4(c, ssum, p2, 0.f);
-    if (c > cref) {
-      if (cref != -INFINITY) acc = df_mulf(acc, expf(fast_tx(cref, c, invT)));
-      cref = c;
-      acc = df_addf(acc, ssum);
-    } else {
-      acc = df_addf(acc, __fmul_rn(ssum, expf(fast_tx(c, cref, invT))));
+  } else {
+    // other rows: per-thread online max and compensated sum over 16-byte
+    // chunks strided by the block (coalesced), UNR chunks' loads in flight
+    constexpr int UNR = 4;
+    const int nch = sh.V / 8;
+    for (int c0 = threadIdx.x; c0 < nch; c0 += NT * UNR) {
+      float vals[UNR][8];
+      bool ok[UNR];
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int c = c0 + NT * u;
+        ok[u] = c < nch;
+        if (ok[u]) load8(row + (size_t)c * 8, vals[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        if (!ok[u]) continue;
+        float c = vals[u][0];
+#pragma unroll
+        for (int e = 1; e < 8; ++e) c = fmaxf(c, vals[u][e]);
+        if (c > mref) {
+          if (mref != -INFINITY) acc = df_mulf(acc, expf(fast_tx(mref, c, invT)));
+          mref = c;
+        }
+        float ssum = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ssum = __fadd_rn(ssum, __expf(fast_tx(vals[u][e], mref, invT)));
+        acc = df_addf(acc, ssum);
+      }
     }
   }
-  if (hl == 0) {
-    s_c[hw] = cref;
-    s_hi[hw] = acc.hi;
-    s_lo[hw] = acc.lo;
-  }
-  __syncthreads();
+  lse_merge(mref, acc, invT, s_m);
   if (threadIdx.x == 0) {
-    float M = -INFINITY;
-    for (int h = 0; h < NT / 16; ++h) M = fmaxf(M, s_c[h]);
-    df Z = {0.f, 0.f};
-    for (int h = 0; h < NT / 16; ++h)
-      if (s_c[h] != -INFINITY) Z = df_add(Z, df_mulf({s_hi[h], s_lo[h]}, expf(fast_tx(s_c[h], M, invT))));
     // lse = M / T + log Z (double-float steps; fp64 only to assemble the result)
-    const double lse = dd_to_double(dd_mul_f(dd_recip(T), M)) + dd_log(Z, s_tab);
+    const double lse = dd_to_double(dd_mul_f(dd_recip(T), mref)) + dd_log(acc, s_tab);
     ws.lse_p[(size_t)b * (sh.gamma + 1) + j] = lse;
     const df nlp = d2df(-lse);
     ws.rowp[(size_t)b * (sh.gamma + 1) + j] = make_float2(nlp.hi, nlp.lo);
@@ -238,44 +327,12 @@ __global__ void __launch_bounds__(NT) verify_tile_kernel(Shape sh, const DT* __r
       s_offt[m] = 0;
     }
   }
+  static_assert(PATH == 0 || PATH == 1, "the tensor-memory path is verify_tiles_tc_kernel");
+  (void)status;
   DT *Us, *Ts;
   float* stage;
   int su;
-  if constexpr (PATH == 2) {
-    static_assert(BM == TC_M, "tensor-memory path uses 128-row tiles");
-    unsigned char* smem = align1k(smem_raw);
-    const TcLayout lay(sh.r, true);
-    bf16* As = reinterpret_cast<bf16*>(smem + lay.offA);
-    bf16* Wsm = reinterpret_cast<bf16*>(smem + lay.offW);
-    Us = reinterpret_cast<DT*>(smem + lay.offU);
-    Ts = reinterpret_cast<DT*>(smem + lay.offT);
-    stage = reinterpret_cast<float*>(smem + lay.offStage);
-    su = BN + 8;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + lay.offBar);
-    uint32_t* holder = reinterpret_cast<uint32_t*>(smem + lay.offBar + 8);
-    if (threadIdx.x == 0) mbar_init(bar, 1);
-    if (threadIdx.x < 32) tc_alloc(holder, TC_TMEM_COLS);
-    __syncthreads();
-    tc_load_A(As, reinterpret_cast<const bf16*>(W1), s_tok, nrows, sh.r);
-    tc_load_W2(Wsm, reinterpret_cast<const bf16*>(W2), sh.V, n0, sh.r);
-    load_X_rows<DT>(Us, su, U, s_offu, nrows, BM, sh.V, n0);
-    load_X_rows<DT>(Ts, su, target, s_offt, nrows, BM, sh.V, n0);
-    cp_async_commit();
-    cp_async_wait_all();
-    fence_async_shared();
-    tc_fence_before();
-    __syncthreads();
-    const uint32_t taddr = *holder;
-    const bool ok = bias_tile_tc(As, Wsm, sh.r, taddr, bar, 0, stage);
-    if (!ok) {
-      if (threadIdx.x == 0) set_status(status, SPEC_DEV_TIMEOUT);
-      mbar_wait(bar, 0, 1u << 22);
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) tc_dealloc(taddr, TC_TMEM_COLS);
-    if (!ok) return;
-    __syncthreads();
-  } else {
+  {
     const TileLayout<DT> lay(BM, sh.r, true);
     DT* As = reinterpret_cast<DT*>(smem_raw + lay.offA);
     DT* Wsm = reinterpret_cast<DT*>(smem_raw + lay.offW);
@@ -295,7 +352,11 @@ __global__ void __launch_bounds__(NT) verify_tile_kernel(Shape sh, const DT* __r
     __syncthreads();
   }
 
+  // epilogue: TPR threads per row, COLS columns each; one partial per
+  // VB-column slice (SPL threads share a slice, or a thread covers CPT slices)
   constexpr int TPR = NT / BM, COLS = BN / TPR;
+  constexpr int SPAN = COLS < VB ? COLS : VB;
+  constexpr int CPT = COLS / SPAN, SPL = VB / SPAN;
   constexpr int SS = TileLayout<DT>::SS;
   const int m = threadIdx.x / TPR, part = threadIdx.x % TPR;
   const bool rowok = m < nrows;
@@ -308,35 +369,234 @@ __global__ void __launch_bounds__(NT) verify_tile_kernel(Shape sh, const DT* __r
     rp = ws.rowp[(size_t)bj.x * (sh.gamma + 1) + bj.y];
   }
   const float invT = rc.x;
-  const int cbeg = part * COLS;
-  const int cend = min(cbeg + COLS, sh.V - n0);
   const DT* urow = Us + (size_t)m * su;
   const DT* trow = Ts + (size_t)m * su;
   const float* brow = stage + m * SS;
-  float cU = -INFINITY, cT = -INFINITY;
-  for (int i = cbeg; i < cend; ++i) {
-    cU = fmaxf(cU, tof(urow[i]));
-    cT = fmaxf(cT, tof(trow[i]));
+#pragma unroll
+  for (int q = 0; q < CPT; ++q) {
+    const int cbeg = part * COLS + q * SPAN;
+    const int cend = min(cbeg + SPAN, sh.V - n0);
+    float cU = -INFINITY, cT = -INFINITY;
+    for (int i = cbeg; i < cend; ++i) {
+      cU = fmaxf(cU, tof(urow[i]));
+      cT = fmaxf(cT, tof(trow[i]));
+    }
+    cU = group_max<SPL>(cU);
+    cT = group_max<SPL>(cT);
+    const float Fq = norm_factor(cU, {rc.x, rc.y}, {rc.z, rc.w});
+    const float Fp = norm_factor(cT, {rc.x, rc.y}, {rp.x, rp.y});
+    float al = 0.f, p2 = 0.f, q2 = 0.f;
+    Kahan kr;
+    const float s2 = __fmul_rn(invT, LOG2E_F);
+    for (int i = cbeg; i < cend; ++i) {
+      const float qv = __fmul_rn(vq(tof(urow[i]), cU, brow[i], s2), Fq);
+      const float pv = __fmul_rn(vp(tof(trow[i]), cT, s2), Fp);
+      al += fminf(pv, qv);
+      kr.add(fmaxf(0.f, __fsub_rn(pv, qv)));
+      p2 = fmaf(pv, pv, p2);
+      q2 = fmaf(qv, qv, q2);
+    }
+    al = group_sum<SPL>(al);
+    const df res = group_sum_df<SPL>(kr.value());
+    p2 = group_sum<SPL>(p2);
+    q2 = group_sum<SPL>(q2);
+    const int vs = (n0 + cbeg) / VB;
+    if (rowok && part % SPL == 0 && vs < sh.NSV)
+      ws.vpart[(size_t)p * sh.NSV + vs] = make_float4(al, df_d(res), p2, q2);
   }
-  cU = group_max<TPR>(cU);
-  cT = group_max<TPR>(cT);
-  const float Fq = norm_factor(cU, {rc.x, rc.y}, {rc.z, rc.w});
-  const float Fp = norm_factor(cT, {rc.x, rc.y}, {rp.x, rp.y});
-  float al = 0.f, p2 = 0.f, q2 = 0.f;
-  Kahan kr;
-  for (int i = cbeg; i < cend; ++i) {
-    const float q = __fmul_rn(__expf(fast_x(tof(urow[i]), cU, brow[i], invT)), Fq);
-    const float pv = __fmul_rn(__expf(fast_tx(tof(trow[i]), cT, invT)), Fp);
-    al += fminf(pv, q);
-    kr.add(fmaxf(0.f, __fsub_rn(pv, q)));
-    p2 = fmaf(pv, pv, p2);
-    q2 = fmaf(q, q, q2);
+}
+
+// ---------------------------------------------------------------- tensor-memory tiles
+// Verification tiles on the warp-specialised engine (spec_tile_tc.cuh), VB =
+// 64 columns per tile: the packed draft rows p = (b, j < L_b) in request
+// tiles of 128, their previous tokens' W1 rows as the A operand, and per row
+// the slice partial (sum min(p, q), sum max(0, p - q), sum p^2, sum q^2).
+struct VerifyEpi {
+  const Shape& sh;
+  const bf16* U;
+  const bf16* T;
+  const Ws& ws;
+  int P;              // packed rows
+
+  __device__ int token(int mt, int m) const {
+    const int p = mt * TC_M + m;
+    return p < P ? min(max(ws.prevtok[p], 0), sh.V - 1) : -1;
   }
-  al = group_sum<TPR>(al);
-  df res = group_sum_df<TPR>(kr.value());
-  p2 = group_sum<TPR>(p2);
-  q2 = group_sum<TPR>(q2);
-  if (rowok && part == 0) ws.vpart[(size_t)p * sh.NS + slice] = make_float4(al, df_d(res), p2, q2);
+  // Row offsets of the producer lane's rows (lane + 32 i) for request tile
+  // `cmt`, refreshed when the request tile changes.
+  mutable int cmt = -1;
+  mutable size_t offu[TC_M / 32], offt[TC_M / 32];
+  __device__ void rows_of(int mt, int lane) const {
+    if (mt == cmt) return;
+    cmt = mt;
+#pragma unroll
+    for (int i = 0; i < TC_M / 32; ++i) {
+      const int p = mt * TC_M + lane + 32 * i;
+      offu[i] = offt[i] = ~(size_t)0;
+      if (p < P) {
+        const int2 bj = ws.prow[p];
+        offu[i] = ((size_t)bj.x * sh.gamma + bj.y) * sh.V;
+        offt[i] = ((size_t)bj.x * (sh.gamma + 1) + bj.y) * sh.V;
+      }
+    }
+  }
+  // U and target rows of the tile's 128 packed rows (lane: rows lane + 32 i),
+  // VT = 64 columns = 8 chunks of 16 bytes each, 128-byte swizzle; U at xb,
+  // the target rows 16 KB further.  Then the next tile's row segments are
+  // prefetched into L2 (one 128-byte line per row and tensor).
+  __device__ void load_x(int mt, int sl, unsigned char* xb, uint64_t* full, int lane, int nmt,
+                         int nsl) const {
+    rows_of(mt, lane);
+    const int n0 = sl * VT;
+#pragma unroll
+    for (int i = 0; i < TC_M / 32; ++i) {
+      const int m = lane + 32 * i;
+      const bool rv = offu[i] != ~(size_t)0;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int n = n0 + 8 * c;
+        const bool valid = rv && n < sh.V;
+        unsigned char* dst = xb + m * 128 + ((c ^ (m & 7)) << 4);
+        cp_async16(dst, valid ? U + offu[i] + n : U, valid);
+        cp_async16(dst + TC_M * 128, valid ? T + offt[i] + n : T, valid);
+      }
+    }
+    cp_async_arrive(full);
+    if (nmt >= 0) {
+      rows_of(nmt, lane);
+      const int m0 = nsl * VT;
+      if (m0 < sh.V) {
+#pragma unroll
+        for (int i = 0; i < TC_M / 32; ++i) {
+          if (offu[i] == ~(size_t)0) continue;
+          asm volatile("prefetch.global.L2 [%0];\n" ::"l"(U + offu[i] + m0));
+          asm volatile("prefetch.global.L2 [%0];\n" ::"l"(T + offt[i] + m0));
+        }
+      }
+    }
+  }
+  // Row m, epilogue group grp: the VB = 32 columns [32 grp, 32 grp + 32) of
+  // the tile, in four groups of 8 (one 16-byte chunk of U and of the target
+  // row, 8 accumulator columns).  Every thread of the warp runs the whole body
+  // (the tensor-memory loads are warp-collective); rows beyond the packed
+  // count compute on zeros and skip the store.
+  __device__ void epilogue(int mt, int sl, int m, const unsigned char* xb, uint32_t trow, int grp) const {
+    const int p = mt * TC_M + m;
+    const bool rowok = p < P;
+    const int c0 = sl * VT + VB * grp;                       // first column of the slice
+    const int nval = rowok ? min(VB, sh.V - c0) : 0;
+    float4 rc = make_float4(1.f, 0.f, 0.f, 0.f);
+    float2 rp = make_float2(0.f, 0.f);
+    if (rowok) {
+      const int2 bj = ws.prow[p];
+      rc = ws.rowc[p];
+      rp = ws.rowp[(size_t)bj.x * (sh.gamma + 1) + bj.y];
+    }
+    const float s2 = __fmul_rn(rc.x, LOG2E_F);
+    const unsigned char* ux = xb + m * 128;
+    const unsigned char* tx = xb + TC_M * 128 + m * 128;
+    auto chunk = [&](const unsigned char* base, int g) { return lds128(base + (((4 * grp + g) ^ (m & 7)) << 4)); };
+    // slice references: the largest U and t of the slice's valid columns
+    float cU = -INFINITY, cT = -INFINITY;
+    if (nval == VB) {
+      __nv_bfloat162 mu = __float2bfloat162_rn(-INFINITY), mtt = mu;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const uint4 a = chunk(ux, g), t = chunk(tx, g);
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wt[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          mu = __hmax2(mu, *reinterpret_cast<const __nv_bfloat162*>(&wa[e]));
+          mtt = __hmax2(mtt, *reinterpret_cast<const __nv_bfloat162*>(&wt[e]));
+        }
+      }
+      cU = fmaxf(__low2float(mu), __high2float(mu));
+      cT = fmaxf(__low2float(mtt), __high2float(mtt));
+    } else {
+      for (int i = 0; i < nval; ++i) {
+        const uint4 a = chunk(ux, i >> 3), t = chunk(tx, i >> 3);
+        const int e = i & 7;
+        const uint32_t wa = (e >> 1) == 0 ? a.x : (e >> 1) == 1 ? a.y : (e >> 1) == 2 ? a.z : a.w;
+        const uint32_t wt = (e >> 1) == 0 ? t.x : (e >> 1) == 1 ? t.y : (e >> 1) == 2 ? t.z : t.w;
+        cU = fmaxf(cU, (e & 1) ? bf_hi(wa) : bf_lo(wa));
+        cT = fmaxf(cT, (e & 1) ? bf_hi(wt) : bf_lo(wt));
+      }
+    }
+    const float Fq = norm_factor(cU, {rc.x, rc.y}, {rc.z, rc.w});
+    const float Fp = norm_factor(cT, {rc.x, rc.y}, {rp.x, rp.y});
+    float al[2] = {0.f, 0.f}, p2[2] = {0.f, 0.f}, q2[2] = {0.f, 0.f};
+    Kahan kr[2];
+#pragma unroll 1
+    for (int g = 0; g < 4; ++g) {
+      float bias[8];
+      tc_ld8_issue(trow + (uint32_t)(VB * grp + 8 * g), bias);
+      const uint4 a = chunk(ux, g), t = chunk(tx, g);
+      tc_wait_ld();
+      const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wt[4] = {t.x, t.y, t.z, t.w};
+      const int nv = nval - 8 * g;                           // valid columns in this group
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (e < nv) {
+          const float uv = (e & 1) ? bf_hi(wa[e >> 1]) : bf_lo(wa[e >> 1]);
+          const float tv = (e & 1) ? bf_hi(wt[e >> 1]) : bf_lo(wt[e >> 1]);
+          const float qv = __fmul_rn(vq(uv, cU, bias[e], s2), Fq);
+          const float pv = __fmul_rn(vp(tv, cT, s2), Fp);
+          al[e & 1] += fminf(pv, qv);
+          kr[e & 1].add(fmaxf(0.f, __fsub_rn(pv, qv)));
+          p2[e & 1] = fmaf(pv, pv, p2[e & 1]);
+          q2[e & 1] = fmaf(qv, qv, q2[e & 1]);
+        }
+      }
+    }
+    if (rowok && nval > 0)
+      ws.vpart[(size_t)p * sh.NSV + c0 / VB] =
+          make_float4(al[0] + al[1], df_d(df_add(kr[0].value(), kr[1].value())), p2[0] + p2[1], q2[0] + q2[1]);
+  }
+};
+
+struct VtParams {
+  TpMaps maps;        // w2 only
+  Shape sh;
+  const bf16* target;
+  const bf16* U;
+  const bf16* W1;
+  Ws ws;
+  uint32_t* status;
+};
+
+// One CTA per SM (384 threads: two epilogue groups); each takes a contiguous
+// run of the (request tile, VT-column slice) tiles of the packed rows (the
+// count is read on the device).
+constexpr int VT_THREADS = 384;
+__global__ void __launch_bounds__(VT_THREADS, 1) verify_tiles_tc_kernel(const __grid_constant__ VtParams P) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ uint64_t s_bar[TB_COUNT];
+  __shared__ uint32_t s_holder;
+  __shared__ int s_tok[TC_M];
+  __shared__ int s_fail;
+  const Shape& sh = P.sh;
+  const int Pk = (int)P.ws.ctrl[CTRL_NPACKED];
+  const int nsl = (sh.V + VT - 1) / VT;
+  const int n_tiles = nsl * ((Pk + TC_M - 1) / TC_M);
+  const int G = (int)gridDim.x, c = (int)blockIdx.x;
+  const int per = n_tiles / G, rem = n_tiles % G;
+  const int t0 = c * per + min(c, rem), n = per + (c < rem ? 1 : 0);
+  if (n <= 0) return;
+  if (threadIdx.x == 0) {
+    tp_init(s_bar, 32, 2);
+    s_fail = 0;
+  }
+  if (threadIdx.x < 32) tc_alloc(&s_holder, 2 * VT);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  TpState st{s_holder, s_bar, &s_fail, 0u, 0u};
+  const VerifyEpi e{sh, P.U, P.target, P.ws, Pk};   // (its row cache is per thread)
+  const bool ok = tp_run<VT, VerifyEpi, 2>(e, sh, P.maps, P.W1, nsl, t0, 1, n, smem_raw, st, s_tok);
+  if (!ok && threadIdx.x == 0) set_status(P.status, SPEC_DEV_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) tc_dealloc(st.tmem, 2 * VT);
 }
 
 // ---------------------------------------------------------------- finalize
@@ -349,11 +609,11 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
     int* accept_len, int* out_tokens, float* alpha, float* p_tok, float* diag, uint32_t* status,
     Ws ws, Eps eps) {
   extern __shared__ __align__(16) unsigned char dsm[];
-  DT* slab = reinterpret_cast<DT*>(dsm);      // [r][BN] W2 slab of the crossing slice
+  DT* slab = reinterpret_cast<DT*>(dsm);      // [r][VB] W2 slab of the crossing slice
   __shared__ float sh_f[72];
   __shared__ float s_a[256];
-  __shared__ float s_part[2][BN];
-  __shared__ float s_w[BN];
+  __shared__ float s_part[NT / VB][VB];
+  __shared__ float s_w[VB];
   __shared__ int s_n, s_slice, s_tok, s_slow;
   __shared__ float s_pref[2], s_lo, s_hi;
   __shared__ df s_tab[DD_EXP_TAB];
@@ -373,7 +633,7 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
   for (int j = 0; j < sh.gamma; ++j) {
     df a = {0.f, 0.f};
     if (j < L)
-      for (int s = threadIdx.x; s < sh.NS; s += NT) a = df_addf(a, ws.vpart[(size_t)(rp + j) * sh.NS + s].x);
+      for (int s = threadIdx.x; s < sh.NSV; s += NT) a = df_addf(a, ws.vpart[(size_t)(rp + j) * sh.NSV + s].x);
     a = block_sum_df(a, sh_f);
     if (threadIdx.x == 0) alpha[(size_t)b * sh.gamma + j] = j < L ? (float)df_d(a) : NAN;
   }
@@ -416,12 +676,12 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
   const int n = s_n;
   const bool resid = n < L;
   const int row = n;                 // draft/target row of the final draw
-  const float4* VP = ws.vpart + (size_t)(rp + row) * sh.NS;
-  const float4* BP = ws.bpart + (size_t)b * sh.NS;
+  const float4* VP = ws.vpart + (size_t)(rp + row) * sh.NSV;
+  const float4* BP = ws.bpart + (size_t)b * sh.NSV;
 
   // ---- slice masses of the final distribution
-  const int per = (sh.NS + NT - 1) / NT;
-  const int s0 = threadIdx.x * per, s1 = min(s0 + per, sh.NS);
+  const int per = (sh.NSV + NT - 1) / NT;
+  const int s0 = threadIdx.x * per, s1 = min(s0 + per, sh.NSV);
   float cM = -INFINITY;
   if (!resid) {
     for (int s = s0; s < s1; ++s) cM = fmaxf(cM, BP[s].x);
@@ -476,7 +736,7 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
   if (s_slice == 0x7fffffff) {
     fallback = true;
     if (threadIdx.x == 0) {
-      int sl = sh.NS - 1;
+      int sl = sh.NSV - 1;
       while (sl > 0 && !((resid ? VP[sl].y : BP[sl].y) > 0.f)) --sl;
       df run = {0.f, 0.f};
       for (int s = 0; s < sl; ++s)
@@ -488,7 +748,7 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
     __syncthreads();
   }
   const int sl = s_slice;
-  const int n0 = sl * BN;
+  const int n0 = sl * VB;
   const df pref = {s_pref[0], s_pref[1]};
   const int prev = row == 0 ? anchor[b] : dtok[(size_t)b * sh.gamma + row - 1];
 
@@ -498,16 +758,18 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
   float w = 0.f, fslice = 1.f;
   if (resid) {
     for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf(W1 + (size_t)prev * sh.r + i);
-    stage_w2_slab<DT>(slab, W2, sh.V, 0, sh.r, n0, BN);
-    const int col = threadIdx.x % BN, half = threadIdx.x / BN;
-    const int kh = sh.r / 2;
+    stage_w2_slab<DT>(slab, W2, sh.V, 0, sh.r, n0, VB);
+    const int col = threadIdx.x % VB, grp = threadIdx.x / VB;
+    const int kg = sh.r / (NT / VB);            // r % 16 == 0
     float acc = 0.f;
-    for (int i = half * kh; i < half * kh + kh; ++i) acc = fmaf(s_a[i], tof(slab[i * BN + col]), acc);
-    s_part[half][col] = acc;
+    for (int i = grp * kg; i < grp * kg + kg; ++i) acc = fmaf(s_a[i], tof(slab[i * VB + col]), acc);
+    s_part[grp][col] = acc;
     __syncthreads();
     float uv = -INFINITY, tv = -INFINITY, bias = 0.f;
-    if (threadIdx.x < BN && n0 + (int)threadIdx.x < sh.V) {
-      bias = __fadd_rn(s_part[0][threadIdx.x], s_part[1][threadIdx.x]);
+    if (threadIdx.x < VB && n0 + (int)threadIdx.x < sh.V) {
+      bias = s_part[0][threadIdx.x];
+#pragma unroll
+      for (int g = 1; g < NT / VB; ++g) bias = __fadd_rn(bias, s_part[g][threadIdx.x]);
       uv = ldf(urow + n0 + threadIdx.x);
       tv = ldf(trow + n0 + threadIdx.x);
     }
@@ -517,28 +779,29 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
     const float2 rpp = ws.rowp[(size_t)b * (sh.gamma + 1) + row];
     const float Fq = norm_factor(cU, {rc.x, rc.y}, {rc.z, rc.w});
     const float Fp = norm_factor(cT, {rc.x, rc.y}, {rpp.x, rpp.y});
-    if (threadIdx.x < BN && n0 + (int)threadIdx.x < sh.V) {
-      const float q = __fmul_rn(__expf(fast_x(uv, cU, bias, invT)), Fq);
-      const float pv = __fmul_rn(__expf(fast_tx(tv, cT, invT)), Fp);
+    if (threadIdx.x < VB && n0 + (int)threadIdx.x < sh.V) {
+      const float s2 = __fmul_rn(rc.x, LOG2E_F);
+      const float q = __fmul_rn(vq(uv, cU, bias, s2), Fq);
+      const float pv = __fmul_rn(vp(tv, cT, s2), Fp);
       w = fmaxf(0.f, __fsub_rn(pv, q));
     }
   } else {
     const float4 v = BP[sl];
     fslice = expf(fast_tx(v.x, cM, invT));
-    if (threadIdx.x < BN && n0 + (int)threadIdx.x < sh.V)
+    if (threadIdx.x < VB && n0 + (int)threadIdx.x < sh.V)
       w = __expf(fast_tx(ldf(trow + n0 + threadIdx.x), v.x, invT));
   }
-  if (threadIdx.x < BN) s_w[threadIdx.x] = w;
+  if (threadIdx.x < VB) s_w[threadIdx.x] = w;
   __syncthreads();
   // in-slice target in slice units
   const df tin = dd_mul(dd_add(tgt, dd_neg(pref)), dd_recip(fslice));
   df wtot;
-  const df wex = block_excl_scan_df(df_make(threadIdx.x < BN ? w : 0.f), &wtot, sh_f);
+  const df wex = block_excl_scan_df(df_make(threadIdx.x < VB ? w : 0.f), &wtot, sh_f);
   if (threadIdx.x == 0) s_tok = 0x7fffffff;
   __syncthreads();
   df my_lo = {0.f, 0.f}, my_hi = {0.f, 0.f};
   bool claim = false;
-  if (!fallback && threadIdx.x < BN && w > 0.f) {
+  if (!fallback && threadIdx.x < VB && w > 0.f) {
     my_lo = wex;
     my_hi = df_addf(wex, w);
     if (dd_le(my_lo, tin) && !dd_le(my_hi, tin)) { claim = true; atomicMin(&s_tok, (int)threadIdx.x); }
@@ -552,7 +815,7 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
   if (s_tok == 0x7fffffff) {
     fallback = true;
     if (threadIdx.x == 0) {
-      int t = BN - 1;
+      int t = VB - 1;
       while (t > 0 && !(s_w[t] > 0.f)) --t;
       s_tok = t;
       s_lo = 0.f;
@@ -617,13 +880,41 @@ cudaError_t launch_target_stats(const Shape& sh, const void* target, const float
 template <typename DT, int BM, int PATH>
 static cudaError_t launch_vtile(const Shape& sh, const DT* target, const DT* U, const DT* W1,
                                 const DT* W2, const Ws& ws, uint32_t* status, cudaStream_t st) {
-  const size_t smem = PATH == 2 ? TcLayout(sh.r, true).total : TileLayout<DT>(BM, sh.r, true).total;
+  const size_t smem = TileLayout<DT>(BM, sh.r, true).total;
   auto kern = verify_tile_kernel<DT, BM, PATH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int pmax = sh.B * sh.gamma;
   dim3 grid(sh.NS, (pmax + BM - 1) / BM);
   kern<<<grid, NT, smem, st>>>(sh, target, U, W1, W2, ws, status);
+  return cudaGetLastError();
+}
+
+// The tensor-memory verification tiles: one CTA per SM (fewer for small
+// problems), W2 through its TMA map.
+static cudaError_t launch_vtiles_tc(const Shape& sh, const bf16* target, const bf16* U,
+                                    const bf16* W1, const bf16* W2, const Ws& ws, uint32_t* status,
+                                    cudaStream_t st) {
+  VtParams P;
+  memset(&P.maps, 0, sizeof(P.maps));
+  cudaError_t e = encode_w2_map(sh, W2, &P.maps.w2);
+  if (e != cudaSuccess) return e;
+  P.sh = sh;
+  P.target = target;
+  P.U = U;
+  P.W1 = W1;
+  P.ws = ws;
+  P.status = status;
+  const size_t smem = TpLayout(sh.r, VT).total;
+  e = cudaFuncSetAttribute(verify_tiles_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, nsm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const int max_tiles = ((sh.V + VT - 1) / VT) * ((sh.B * sh.gamma + TC_M - 1) / TC_M);
+  const int G = nsm < max_tiles ? nsm : max_tiles;
+  verify_tiles_tc_kernel<<<G, VT_THREADS, smem, st>>>(P);
   return cudaGetLastError();
 }
 
@@ -644,7 +935,7 @@ cudaError_t launch_verify_tile(const Shape& sh, const void* target, const void* 
     return SPEC_VT(128, 0);
   }
   if constexpr (sizeof(DT) == 2) {
-    if (path == 2 && sh.r % 64 == 0) return SPEC_VT(128, 2);
+    if (path == 2 && sh.r % 64 == 0) return launch_vtiles_tc(sh, t, u, w1, w2, ws, status, st);
   }
   if (BM == 32) return SPEC_VT(32, 1);
   if (BM == 64) return SPEC_VT(64, 1);
@@ -660,7 +951,7 @@ cudaError_t launch_verify_final(const Shape& sh, const void* target, const void*
                                 int* accept_len, int* out_tokens, float* alpha, float* p_tok,
                                 float* diag, uint32_t* status, const Ws& ws, const Eps& eps,
                                 cudaStream_t st) {
-  const size_t smem = (size_t)sh.r * BN * sizeof(DT);
+  const size_t smem = (size_t)sh.r * VB * sizeof(DT);
   cudaError_t e = cudaFuncSetAttribute(verify_final_kernel<DT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
