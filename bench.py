@@ -62,6 +62,34 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def recorded_traffic(kernel, config):
+    """DRAM bytes per launch of `kernel` from its committed ncu summary
+    (profiles/<kernel>_<config>.md), or None when there is none or when the
+    kernel's sources changed since the counters were taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{config}.md")
+    if not os.path.exists(p):
+        return None
+    fields = {}
+    for line in open(p):
+        line = line.strip()
+        for key in ("traffic_bytes_per_launch:", "sources:", "source_sha256:"):
+            if line.startswith(key):
+                fields[key[:-1]] = line[len(key):].strip()
+    if len(fields) != 3:
+        return None
+    h = hashlib.sha256()
+    for f in fields["sources"].split():
+        fp = os.path.join(ROOT, f)
+        if not os.path.exists(fp):
+            return None
+        with open(fp, "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != fields["source_sha256"]:
+        return None
+    return float(fields["traffic_bytes_per_launch"])
+
+
 def algorithmic_bytes(w):
     """Bytes a cycle must move at least (logits + W2 once per call), after the
     survey's accounting: draft = B*g*V*s + r*V*s; verify = sum(L+1)*V*s (target
@@ -327,7 +355,8 @@ def main():
                     "frac_of_measured": cyc_gbs / hbm_peak},
             "roofline": {"kernel": top, "bound": "hbm", "achieved": ach, "peak": hbm_peak,
                          "peak_source": peak_src, "unit": "GB/s", "frac": ach / hbm_peak,
-                         "traffic": None, "algorithmic_bytes_per_launch": per_stage[top],
+                         "traffic": recorded_traffic(top, args.config),
+                         "algorithmic_bytes_per_launch": per_stage[top],
                          "avg_launch_ms": avg_ms, "share_of_step": t_ms / tot_ms if tot_ms else None},
             "stages_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]},
             "e2e": {"value": pos_all / (e2e_all * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,

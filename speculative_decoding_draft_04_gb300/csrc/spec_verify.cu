@@ -96,11 +96,15 @@ __global__ void __launch_bounds__(NT) verify_prep_kernel(
     if (!temp_ok(temp[b])) bits |= SPEC_DEV_BAD_TEMP;
     const int a = anchor[b];
     if (a < 0 || a >= sh.V) bits |= SPEC_DEV_BAD_TOKEN;
-    if (!(bits & SPEC_DEV_BAD_LEN))
-      for (int j = 0; j < L; ++j) {
-        const int x = dtok[(size_t)b * sh.gamma + j];
-        if (x < 0 || x >= sh.V) bits |= SPEC_DEV_BAD_TOKEN;
-      }
+    if (!(bits & SPEC_DEV_BAD_LEN)) {
+      // all of the row's tokens loaded at once (independent loads)
+      int xs[MAX_GAMMA];
+#pragma unroll
+      for (int j = 0; j < MAX_GAMMA; ++j) xs[j] = j < L ? dtok[(size_t)b * sh.gamma + j] : 0;
+#pragma unroll
+      for (int j = 0; j < MAX_GAMMA; ++j)
+        if (xs[j] < 0 || xs[j] >= sh.V) bits |= SPEC_DEV_BAD_TOKEN;
+    }
     ws.vflags[b] = bits ? 1 : 0;
     ws.accbits[b] = 0;
     if (bits) {
@@ -140,11 +144,22 @@ __global__ void __launch_bounds__(NT) verify_prep_kernel(
     if (ws.vflags[b] & 1) continue;
     const int L = vlen[b];
     const df it = dd_recip(temp[b]);
-    for (int j = 0; j < L; ++j) {
-      ws.prow[run + j] = make_int2(b, j);
-      ws.prevtok[run + j] = j == 0 ? anchor[b] : dtok[(size_t)b * sh.gamma + j - 1];
-      const df nlq = d2df(-lse_q[(size_t)b * sh.gamma + j]);
-      ws.rowc[run + j] = make_float4(it.hi, it.lo, nlq.hi, nlq.lo);
+    const int a = anchor[b];
+    int xs[MAX_GAMMA];
+    double lq[MAX_GAMMA];
+#pragma unroll
+    for (int j = 0; j < MAX_GAMMA; ++j) {
+      xs[j] = j < L ? dtok[(size_t)b * sh.gamma + j] : 0;
+      lq[j] = j < L ? lse_q[(size_t)b * sh.gamma + j] : 0.0;
+    }
+#pragma unroll
+    for (int j = 0; j < MAX_GAMMA; ++j) {
+      if (j < L) {
+        ws.prow[run + j] = make_int2(b, j);
+        ws.prevtok[run + j] = j == 0 ? a : xs[j - 1 < 0 ? 0 : j - 1];
+        const df nlq = d2df(-lq[j]);
+        ws.rowc[run + j] = make_float4(it.hi, it.lo, nlq.hi, nlq.lo);
+      }
     }
     run += L;
   }
@@ -263,7 +278,7 @@ __global__ void __launch_bounds__(NT) target_stats_kernel(Shape sh, const DT* __
   } else {
     // other rows: per-thread online max and compensated sum over 16-byte
     // chunks strided by the block (coalesced), UNR chunks' loads in flight
-    constexpr int UNR = 4;
+    constexpr int UNR = 8;
     const int nch = sh.V / 8;
     for (int c0 = threadIdx.x; c0 < nch; c0 += NT * UNR) {
       float vals[UNR][8];
