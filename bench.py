@@ -90,6 +90,30 @@ def recorded_traffic(kernel, config):
     return float(fields["traffic_bytes_per_launch"])
 
 
+# Target decode step used for the draft cost ratio c: the pages' estimate of a
+# 70B bf16 decode step (about 140 GB of weights read at 3.35 TB/s: ~42 ms).
+TARGET_STEP_MS = 42.0
+
+
+def operating_point(d, bufs, draft_prof, steps):
+    """The analytic speed-up report from this run's measured acceptance (device
+    statistics of the last cycle's outputs) and the draft time per cycle."""
+    import torch
+    from speculative_decoding_draft_04_gb300 import _lib
+    out = torch.zeros(4, dtype=torch.float64, device=bufs.alpha.device)
+    _lib.spec_acceptance_stats(bufs.alpha, d.verify_len, bufs.accept_len, out)
+    s = out.cpu().numpy()
+    alpha = float(s[0] / s[1]) if s[1] else float("nan")
+    tau = float(s[2] / s[3]) if s[3] else float("nan")
+    draft_ms = draft_prof[0] / max(steps, 1)
+    c = draft_ms / (d.gamma * TARGET_STEP_MS) if draft_ms > 0 else float("nan")
+    rep = _lib.spec_operating_point(min(max(alpha, 0.0), 1.0), c, d.gamma, 256) \
+        if alpha == alpha and c == c and c > 0 else {}
+    return {"measured_alpha": alpha, "measured_tau": tau, "draft_ms_per_cycle": draft_ms,
+            "c": c, "c_source": f"draft time / (gamma x {TARGET_STEP_MS} ms 70B decode step, the pages' estimate)",
+            **{k: v for k, v in rep.items()}}
+
+
 def algorithmic_bytes(w):
     """Bytes a cycle must move at least (logits + W2 once per call), after the
     survey's accounting: draft = B*g*V*s + r*V*s; verify = sum(L+1)*V*s (target
@@ -364,6 +388,8 @@ def main():
             "gpu_launches": int(launches * args.steps),
             "clocks": clocks,
         }
+        line["operating_point"] = operating_point(d, bufs, prof.get("draft_persistent", (0.0, 0)),
+                                                  args.steps)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
         print(json.dumps(line), flush=True)

@@ -182,6 +182,51 @@ int32_t spec_verify(const spec_verify_args* args, spec_stream_t stream);
 #define SPEC_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 int32_t spec_markov_draft_static(const spec_draft_args* args, spec_stream_t stream);
 
+/* ---------------------------------------------- operating-point report */
+/* The analytic speed-up model of "Speculative Decoding Part 1: 도입 전에 확인해야
+ * 할 것들" (VESSL AI blog), section "속도 향상을 결정하는 방정식" and the section on
+ * the compute theorem, evaluated on the host (no GPU work).  With i.i.d.
+ * acceptance probability alpha and draft cost ratio c = T_draft/(gamma T_target):
+ * E[tau] = sum_{k<=gamma} alpha^k, S(gamma) = E[tau]/(c gamma + 1),
+ * S <= min(1/c, 1/(1-alpha)), the stationarity condition
+ * alpha^{gamma+1}(c - (c gamma + 1) ln alpha) = c, and the expected compute
+ * ratio (gamma c_hat + gamma + 1)/E[tau].
+ * Returns SPEC_EINVAL (nothing written) unless 0 <= alpha <= 1, c > 0,
+ * c_hat >= 0, 1 <= gamma <= gamma_max <= 100000 and both pointers are set.  */
+typedef struct {
+  double alpha;              /* acceptance probability per position           */
+  double c;                  /* draft cost ratio, > 0                          */
+  double c_hat;              /* draft compute ratio (compute theorem), >= 0    */
+  int32_t gamma;             /* draft length to evaluate                        */
+  int32_t gamma_max;         /* search range 1..gamma_max for the best gamma    */
+} spec_op_args;
+typedef struct {
+  double expected_tau;       /* E[tau] at gamma                                */
+  double speedup;            /* S(gamma)                                       */
+  double speedup_gamma1;     /* S(1) = (1 + alpha)/(c + 1)                     */
+  double bound;              /* min(1/c, 1/(1 - alpha)); +inf terms dropped     */
+  double gamma_continuous;   /* real root of the stationarity condition (0 if S
+                                decreases from gamma = 0)                       */
+  double speedup_star;       /* S(gamma_star)                                  */
+  double compute_ratio;      /* expected compute relative to plain decoding    */
+  int32_t gamma_star;        /* best integer gamma in 1..gamma_max (smallest on
+                                ties)                                           */
+  int32_t gains;             /* 1 if S(gamma) > 1                              */
+} spec_op_result;
+int32_t spec_operating_point(const spec_op_args* args, spec_op_result* out);
+
+/* Measured acceptance statistics of one verification, on the device (no
+ * counterpart formula beyond the report's inputs): out[0] = sum of alpha[b][j]
+ * over j < L_b of valid requests, out[1] = the number of such positions,
+ * out[2] = sum of (accept_len[b] + 1) over valid requests (accept_len >= 0),
+ * out[3] = the number of valid requests.  alpha [B][gamma] and verify_len,
+ * accept_len [B] are the spec_verify inputs/outputs (device pointers); out is
+ * a device double[4], overwritten.  Enqueued on `stream`; SPEC_EINVAL for bad
+ * sizes or NULL pointers.                                                    */
+int32_t spec_acceptance_stats(int32_t B, int32_t gamma, const float* alpha,
+                              const int32_t* verify_len, const int32_t* accept_len, double* out,
+                              spec_stream_t stream);
+
 /* Static text for a spec_status value. */
 const char* spec_status_string(int32_t status);
 

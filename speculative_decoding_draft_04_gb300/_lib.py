@@ -51,6 +51,19 @@ class VerifyArgs(ctypes.Structure):
 _LIB = None
 
 
+class OpArgs(ctypes.Structure):
+    _fields_ = [("alpha", ctypes.c_double), ("c", ctypes.c_double), ("c_hat", ctypes.c_double),
+                ("gamma", ctypes.c_int32), ("gamma_max", ctypes.c_int32)]
+
+
+class OpResult(ctypes.Structure):
+    _fields_ = [("expected_tau", ctypes.c_double), ("speedup", ctypes.c_double),
+                ("speedup_gamma1", ctypes.c_double), ("bound", ctypes.c_double),
+                ("gamma_continuous", ctypes.c_double), ("speedup_star", ctypes.c_double),
+                ("compute_ratio", ctypes.c_double), ("gamma_star", ctypes.c_int32),
+                ("gains", ctypes.c_int32)]
+
+
 def lib(path: str | None = None) -> ctypes.CDLL:
     """Load libspec.so (built in-tree by build.build())."""
     global _LIB
@@ -81,6 +94,10 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.spec_stage_name.argtypes = [_i32]
     L.spec_num_stages.restype = _i32
     L.spec_num_stages.argtypes = []
+    L.spec_operating_point.restype = _i32
+    L.spec_operating_point.argtypes = [ctypes.POINTER(OpArgs), ctypes.POINTER(OpResult)]
+    L.spec_acceptance_stats.restype = _i32
+    L.spec_acceptance_stats.argtypes = [_i32, _i32, _vp, _vp, _vp, _vp, _vp]
     if path is None:
         _LIB = L
     return L
@@ -178,3 +195,19 @@ def spec_profile_read() -> dict[str, tuple[float, int]]:
     cnt = (_i32 * n)()
     _check(L.spec_profile_read(ms, cnt, n), "spec_profile_read")
     return {L.spec_stage_name(i).decode(): (ms[i], cnt[i]) for i in range(n)}
+
+
+def spec_operating_point(alpha: float, c: float, gamma: int, gamma_max: int = 256,
+                         c_hat: float = 0.0) -> dict:
+    """The analytic operating point (host computation, no GPU work)."""
+    out = OpResult()
+    _check(lib().spec_operating_point(ctypes.byref(OpArgs(alpha, c, c_hat, gamma, gamma_max)),
+                                      ctypes.byref(out)), "spec_operating_point")
+    return {f: getattr(out, f) for f, _ in OpResult._fields_}
+
+
+def spec_acceptance_stats(alpha, verify_len, accept_len, out, stream=None) -> None:
+    """Device sums (alpha over j < L_b, positions, tau, requests) into out (float64[4])."""
+    B, gamma = alpha.shape
+    _check(lib().spec_acceptance_stats(B, gamma, _ptr(alpha), _ptr(verify_len), _ptr(accept_len),
+                                       _ptr(out), _stream(stream)), "spec_acceptance_stats")
