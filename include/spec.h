@@ -82,7 +82,9 @@ enum {
   SPEC_DEV_BAD_TEMP = 4,    /* temperature not finite and > 0                */
   SPEC_DEV_TIMEOUT = 8,     /* a bounded device wait gave up                 */
   SPEC_DEV_REFINED = 16,    /* informational: at least one re-decision        */
-  SPEC_DEV_OVERFLOW = 32    /* more near-boundary decisions than list slots   */
+  SPEC_DEV_OVERFLOW = 32,   /* more near-boundary decisions than list slots   */
+  SPEC_DEV_BAD_CONF = 64    /* a confidence logit not finite, or a confidence
+                               outside [0, 1] given to the scheduler           */
 };
 
 /* ---------------------------------------------------------------- draft */
@@ -181,6 +183,70 @@ int32_t spec_verify(const spec_verify_args* args, spec_stream_t stream);
  */
 #define SPEC_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 int32_t spec_markov_draft_static(const spec_draft_args* args, spec_stream_t stream);
+
+/* ------------------------------------- confidence head and prefix scheduler */
+/* DSpark's confidence-scheduled verification ("[논문리뷰] DSpark", section 2.1
+ * "Confidence Head" and section 2.2 "Hardware-Aware Prefix Scheduler").
+ *
+ * spec_confidence: c_{r,k} = sigmoid(w^T [h_k; W1[x_{k-1}]]) for every draft
+ * row k = 1..gamma of every request r, x_0 the anchor.  Row k-1 (0-based) of
+ * `hidden` is h_k, the backbone state that also produced U_k.  The dot
+ * product and the logistic are evaluated in double-float and rounded once to
+ * fp32 (the nearest float of the exact value, except within about 1e-13 of a
+ * rounding midpoint).  One kernel launch.  A token outside [0, V) sets
+ * SPEC_DEV_BAD_TOKEN and a logit that is not finite SPEC_DEV_BAD_CONF; that
+ * row's confidence is NaN.  dev_status bits are OR-ed in and never cleared
+ * by these two calls.
+ * Requires 1 <= R <= 4096, 1 <= gamma <= 16, d >= 8 with d % 8 == 0,
+ * 1 <= V < 2^24, r % 16 == 0 with 16 <= r <= 256, hidden / W1 / w 16-byte
+ * aligned.                                                                  */
+typedef struct {
+  int32_t R, gamma, d, V, r;
+  int32_t dtype;              /* spec_dtype of hidden and W1                    */
+  const void* hidden;         /* [R][gamma][d] backbone hidden states h_1..h_gamma */
+  const void* W1;             /* [V][r] Markov embedding (the draft's W1)       */
+  const float* w;             /* [d + r] head weights: the h part, then the W1 part */
+  const int32_t* anchor;      /* [R] x_0                                        */
+  const int32_t* draft_tokens;/* [R][gamma] x_1..x_gamma (x_gamma is not read)   */
+  float* conf;                /* out [R][gamma] c_1..c_gamma                    */
+  uint32_t* dev_status;       /* uint32_t[4]; bits OR-ed into [0]               */
+} spec_confidence_args;
+int32_t spec_confidence(const spec_confidence_args* args, spec_stream_t stream);
+
+/* spec_prefix_schedule: survival a_{r,j} = c_{r,1} ... c_{r,j} (fp32 products
+ * left to right), then verify lengths l_r maximising Theta = tau * SPS(B),
+ * B = sum_r (1 + l_r), tau = sum_r (1 + sum_{j<=l_r} a_{r,j}): the candidates
+ * (r, j) are admitted in descending order of a (equal a: lower r, then lower
+ * j) while Theta does not decrease; the first admission that would lower
+ * Theta, or that would need SPS beyond the table, ends the search.
+ * tau is accumulated in units of 2^-36 (each a rounded down) and Theta is
+ * (tau units * 2^-36) * sps[B] in float64, so the decisions do not depend on
+ * the order of summation.  A confidence outside [0, 1] or NaN counts as 0 and
+ * sets SPEC_DEV_BAD_CONF.  Two kernel launches (ranking: one CTA per request;
+ * selection: one CTA).
+ * Outputs: survival [R][gamma]; verify_len [R] = l_r in [0, gamma] (the
+ * spec_verify input of the same name); totals int64[4] = {B, tau in units of
+ * 2^-36, admitted candidates, stop reason: 0 all admitted, 1 Theta would
+ * decrease, 2 the cost table ends}; theta double[1] = Theta at the result.
+ * sps: device float64[sps_len], SPS(B') for B' = 0..sps_len-1 (finite,
+ * positive); sps_len must exceed R.  The workspace needs
+ * spec_schedule_workspace_bytes(R, gamma) bytes, 16-byte aligned.
+ * Requires 1 <= R <= 4096, 1 <= gamma <= 16.                                */
+typedef struct {
+  int32_t R, gamma;
+  const float* conf;          /* [R][gamma] c_{r,j}                             */
+  const double* sps;          /* [sps_len] steps per second at batch size B'     */
+  int32_t sps_len;            /* > R                                            */
+  float* survival;            /* out [R][gamma] a_{r,j}                         */
+  int32_t* verify_len;        /* out [R] l_r                                    */
+  int64_t* totals;            /* out [4] B, tau (2^-36 units), admitted, reason  */
+  double* theta;              /* out [1]                                        */
+  uint32_t* dev_status;       /* uint32_t[4]; bits OR-ed into [0]               */
+  void* workspace;
+  size_t workspace_bytes;
+} spec_schedule_args;
+size_t spec_schedule_workspace_bytes(int32_t R, int32_t gamma);
+int32_t spec_prefix_schedule(const spec_schedule_args* args, spec_stream_t stream);
 
 /* ---------------------------------------------- operating-point report */
 /* The analytic speed-up model of "Speculative Decoding Part 1: 도입 전에 확인해야

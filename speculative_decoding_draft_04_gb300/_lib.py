@@ -17,12 +17,13 @@ LIB_PATH = os.path.join(HERE, "libspec.so")
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_OPT_EPS_SCALE, SPEC_OPT_FORCE_SIMT, SPEC_OPT_BIAS_PATH, SPEC_OPT_TRACE = 1, 2, 3, 5
 DEV_BITS = {1: "BAD_TOKEN", 2: "BAD_LEN", 4: "BAD_TEMP", 8: "TIMEOUT", 16: "REFINED",
-            32: "OVERFLOW"}
+            32: "OVERFLOW", 64: "BAD_CONF"}
 
 EXPORTED = ("spec_workspace_bytes", "spec_markov_draft", "spec_markov_draft_static",
             "spec_verify", "spec_status_string",
             "spec_set_option", "spec_profile_enable", "spec_profile_read", "spec_stage_name",
-            "spec_num_stages")
+            "spec_num_stages", "spec_operating_point", "spec_acceptance_stats",
+            "spec_confidence", "spec_schedule_workspace_bytes", "spec_prefix_schedule")
 
 
 class SpecError(RuntimeError):
@@ -64,6 +65,18 @@ class OpResult(ctypes.Structure):
                 ("gains", ctypes.c_int32)]
 
 
+class ConfidenceArgs(ctypes.Structure):
+    _fields_ = [("R", _i32), ("gamma", _i32), ("d", _i32), ("V", _i32), ("r", _i32),
+                ("dtype", _i32), ("hidden", _vp), ("W1", _vp), ("w", _vp), ("anchor", _vp),
+                ("draft_tokens", _vp), ("conf", _vp), ("dev_status", _vp)]
+
+
+class ScheduleArgs(ctypes.Structure):
+    _fields_ = [("R", _i32), ("gamma", _i32), ("conf", _vp), ("sps", _vp), ("sps_len", _i32),
+                ("survival", _vp), ("verify_len", _vp), ("totals", _vp), ("theta", _vp),
+                ("dev_status", _vp), ("workspace", _vp), ("workspace_bytes", _sz)]
+
+
 def lib(path: str | None = None) -> ctypes.CDLL:
     """Load libspec.so (built in-tree by build.build())."""
     global _LIB
@@ -98,6 +111,12 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.spec_operating_point.argtypes = [ctypes.POINTER(OpArgs), ctypes.POINTER(OpResult)]
     L.spec_acceptance_stats.restype = _i32
     L.spec_acceptance_stats.argtypes = [_i32, _i32, _vp, _vp, _vp, _vp, _vp]
+    L.spec_confidence.restype = _i32
+    L.spec_confidence.argtypes = [ctypes.POINTER(ConfidenceArgs), _vp]
+    L.spec_schedule_workspace_bytes.restype = _sz
+    L.spec_schedule_workspace_bytes.argtypes = [_i32, _i32]
+    L.spec_prefix_schedule.restype = _i32
+    L.spec_prefix_schedule.argtypes = [ctypes.POINTER(ScheduleArgs), _vp]
     if path is None:
         _LIB = L
     return L
@@ -211,3 +230,26 @@ def spec_acceptance_stats(alpha, verify_len, accept_len, out, stream=None) -> No
     B, gamma = alpha.shape
     _check(lib().spec_acceptance_stats(B, gamma, _ptr(alpha), _ptr(verify_len), _ptr(accept_len),
                                        _ptr(out), _stream(stream)), "spec_acceptance_stats")
+
+
+def spec_confidence(hidden, W1, w, anchor, draft_tokens, conf, dev_status, stream=None) -> None:
+    """Enqueue the confidence head: conf[r, k] = sigmoid(w . [h; W1[x_k]])."""
+    R, gamma, d = hidden.shape
+    V, r = W1.shape
+    a = ConfidenceArgs(R, gamma, d, V, r, _dtype_code(hidden), _ptr(hidden), _ptr(W1), _ptr(w),
+                       _ptr(anchor), _ptr(draft_tokens), _ptr(conf), _ptr(dev_status))
+    _check(lib().spec_confidence(ctypes.byref(a), _stream(stream)), "spec_confidence")
+
+
+def spec_schedule_workspace_bytes(R: int, gamma: int) -> int:
+    return int(lib().spec_schedule_workspace_bytes(R, gamma))
+
+
+def spec_prefix_schedule(conf, sps, survival, verify_len, totals, theta, dev_status, workspace,
+                         stream=None) -> None:
+    """Enqueue the hardware-aware prefix scheduler (verify lengths from conf)."""
+    R, gamma = conf.shape
+    a = ScheduleArgs(R, gamma, _ptr(conf), _ptr(sps), sps.numel(), _ptr(survival),
+                     _ptr(verify_len), _ptr(totals), _ptr(theta), _ptr(dev_status),
+                     _ptr(workspace), workspace.numel() * workspace.element_size())
+    _check(lib().spec_prefix_schedule(ctypes.byref(a), _stream(stream)), "spec_prefix_schedule")

@@ -8,7 +8,7 @@
 
 namespace spec {
 
-// launchers (spec_draft.cu, spec_verify.cu, spec_refine.cu)
+// launchers (spec_draft.cu, spec_verify.cu, spec_refine.cu, spec_sched.cu)
 template <typename DT>
 cudaError_t launch_draft_persistent(const Shape&, const void*, const void*, const void*, const int*,
                                     const float*, const float*, int*, float*, double*, float*,
@@ -36,6 +36,13 @@ template <typename DT>
 cudaError_t launch_slow_verify(const Shape&, const HpRows&, const Ws&, const int*, const int*,
                                const double*, const int*, const float*, const float*, int*, int*,
                                uint32_t*, int, cudaStream_t);
+template <typename DT>
+cudaError_t launch_confidence(int, int, int, int, int, const void*, const void*, const float*,
+                              const int*, const int*, float*, uint32_t*, cudaStream_t);
+cudaError_t launch_schedule_rank(int, int, const float*, float*, int*, unsigned long long*, uint32_t*,
+                                 cudaStream_t);
+cudaError_t launch_schedule_select(int, int, const double*, int, const int*, const unsigned long long*,
+                                   int*, long long*, double*, cudaStream_t);
 
 // ---------------------------------------------------------------- options
 namespace {
@@ -71,12 +78,12 @@ Eps current_eps() {
 enum Stage {
   ST_DRAFT_PERSISTENT, ST_VERIFY_PREP,
   ST_TARGET_STATS, ST_VERIFY_TILE, ST_VERIFY_FINAL, ST_SLOW_VERIFY, ST_VERIFY_HP_SUMS,
-  ST_VERIFY_HP_RESID, ST_VERIFY_HP_DECIDE, ST_COUNT
+  ST_VERIFY_HP_RESID, ST_VERIFY_HP_DECIDE, ST_CONFIDENCE, ST_SCHED_RANK, ST_SCHED_SELECT, ST_COUNT
 };
 const char* kStageNames[ST_COUNT] = {
     "draft_persistent", "verify_prep",
     "target_stats", "verify_tile", "verify_final", "slow_verify", "verify_hp_sums",
-    "verify_hp_resid", "verify_hp_decide"};
+    "verify_hp_resid", "verify_hp_decide", "confidence", "sched_rank", "sched_select"};
 bool g_prof = false;
 struct EvPair { cudaEvent_t a, b; int stage; };
 std::vector<EvPair> g_pending;
@@ -453,6 +460,69 @@ int32_t spec_markov_draft_static(const spec_draft_args* a, spec_stream_t stream)
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return a->dtype == SPEC_BF16 ? run_draft_static<bf16>(a, scratch, st)
                                : run_draft_static<float>(a, scratch, st);
+}
+
+int32_t spec_confidence(const spec_confidence_args* a, spec_stream_t stream) {
+  if (!a) return SPEC_EINVAL;
+  if (a->R < 1 || a->R > 4096 || a->gamma < 1 || a->d < 8 || a->V < 1 || a->V >= (1 << 24) || a->r < 16)
+    return SPEC_EINVAL;
+  if (a->gamma > MAX_GAMMA || a->d % 8 != 0 || a->r % 16 != 0 || a->r > 256 ||
+      (a->dtype != SPEC_F32 && a->dtype != SPEC_BF16))
+    return SPEC_EUNSUPPORTED;
+  if (!a->hidden || !a->W1 || !a->w || !a->anchor || !a->draft_tokens || !a->conf || !a->dev_status)
+    return SPEC_EINVAL;
+  if (!aligned(a->hidden, 16) || !aligned(a->W1, 16) || !aligned(a->w, 16) || !aligned(a->anchor, 4) ||
+      !aligned(a->draft_tokens, 4) || !aligned(a->conf, 4) || !aligned(a->dev_status, 4))
+    return SPEC_EALIGN;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ProfScope p(st, ST_CONFIDENCE);
+  const cudaError_t e =
+      a->dtype == SPEC_BF16
+          ? launch_confidence<bf16>(a->R, a->gamma, a->d, a->V, a->r, a->hidden, a->W1, a->w, a->anchor,
+                                    a->draft_tokens, a->conf, a->dev_status, st)
+          : launch_confidence<float>(a->R, a->gamma, a->d, a->V, a->r, a->hidden, a->W1, a->w, a->anchor,
+                                     a->draft_tokens, a->conf, a->dev_status, st);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+// Workspace of the scheduler: the candidates' ranks, then their tau
+// increments in sorted order.
+static size_t sched_rank_bytes(int R, int gamma) { return ((size_t)R * gamma * 4 + 255) & ~(size_t)255; }
+
+size_t spec_schedule_workspace_bytes(int32_t R, int32_t gamma) {
+  if (R < 1 || R > 4096 || gamma < 1 || gamma > MAX_GAMMA) return 0;
+  return sched_rank_bytes(R, gamma) + (((size_t)R * gamma * 8 + 255) & ~(size_t)255);
+}
+
+int32_t spec_prefix_schedule(const spec_schedule_args* a, spec_stream_t stream) {
+  if (!a) return SPEC_EINVAL;
+  if (a->R < 1 || a->R > 4096 || a->gamma < 1 || a->sps_len <= a->R) return SPEC_EINVAL;
+  if (a->gamma > MAX_GAMMA) return SPEC_EUNSUPPORTED;
+  if (!a->conf || !a->sps || !a->survival || !a->verify_len || !a->totals || !a->theta || !a->dev_status)
+    return SPEC_EINVAL;
+  if (!aligned(a->conf, 4) || !aligned(a->sps, 8) || !aligned(a->survival, 4) ||
+      !aligned(a->verify_len, 4) || !aligned(a->totals, 8) || !aligned(a->theta, 8) ||
+      !aligned(a->dev_status, 4))
+    return SPEC_EALIGN;
+  const size_t need = spec_schedule_workspace_bytes(a->R, a->gamma);
+  if (!a->workspace || a->workspace_bytes < need) return SPEC_EWORKSPACE;
+  if (!aligned(a->workspace, 16)) return SPEC_EALIGN;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(a->workspace);
+  int* rank = reinterpret_cast<int*>(ws);
+  unsigned long long* su = reinterpret_cast<unsigned long long*>(ws + sched_rank_bytes(a->R, a->gamma));
+  {
+    ProfScope p(st, ST_SCHED_RANK);
+    if (launch_schedule_rank(a->R, a->gamma, a->conf, a->survival, rank, su, a->dev_status, st) != cudaSuccess)
+      return SPEC_ECUDA;
+  }
+  {
+    ProfScope p(st, ST_SCHED_SELECT);
+    if (launch_schedule_select(a->R, a->gamma, a->sps, a->sps_len, rank, su, a->verify_len,
+                               reinterpret_cast<long long*>(a->totals), a->theta, st) != cudaSuccess)
+      return SPEC_ECUDA;
+  }
+  return SPEC_OK;
 }
 
 const char* spec_status_string(int32_t s) {

@@ -138,6 +138,33 @@ struct DdSum {
   SPEC_HD df value() const { return fast_two_sum_df(s, c); }
 };
 
+// Compensated dot product (the "Dot2" scheme of the same paper): each
+// product is split exactly into p + e (TwoProd), p is added with TwoSum and
+// both error terms go to the running correction, so the result is as
+// accurate as a dot product evaluated in twice the working precision.
+struct DdDot {
+  float s = 0.f, c = 0.f;
+  SPEC_HD void add(float a, float b) {
+    const df p = two_prod_df(a, b);
+    const df t = two_sum_df(s, p.hi);
+    s = t.hi;
+    c = rn_add(c, rn_add(t.lo, p.lo));
+  }
+  SPEC_HD df value() const { return fast_two_sum_df(s, c); }
+};
+
+// a / b in double-float: three rounded quotient digits, each from the exact
+// remainder of the previous ones (long division).
+SPEC_HD df dd_div(df a, df b) {
+  const float rb = rn_rcp(b.hi);
+  const float q1 = rn_mul(a.hi, rb);
+  df rem = dd_add(a, dd_neg(dd_mul_f(b, q1)));
+  const float q2 = rn_mul(rem.hi, rb);
+  rem = dd_add(rem, dd_neg(dd_mul_f(b, q2)));
+  const float q3 = rn_mul(rem.hi, rb);
+  return dd_add_f(fast_two_sum_df(q1, q2), q3);
+}
+
 // ---------------------------------------------------------------- exponential
 // Table of 2^(j/64), j = 0..63, as double-floats: entry j is the product of
 // 2^(2^i/64) over the set bits i of j (binary powering from six constants,
@@ -194,6 +221,16 @@ SPEC_HD df dd_exp(df x, const df* tab) {
   const df e = dd_add_f(em1, 1.0f);
   const df v = dd_mul(e, tab[j]);
   return {ldexpf(v.hi, n), ldexpf(v.lo, n)};
+}
+
+// The logistic function 1 / (1 + e^{-z}) in double-float.  The exponential
+// is always taken of -|z| (no overflow): z >= 0 gives 1/(1 + e), z < 0 gives
+// e/(1 + e).  Below z = -103 the result is 0 (true value < 1.5e-45).
+SPEC_HD df dd_sigmoid(df z, const df* tab) {
+  const bool neg = z.hi < 0.f;
+  const df e = dd_exp(neg ? z : dd_neg(z), tab);
+  const df den = dd_add_f(e, 1.0f);
+  return dd_div(neg ? e : df{1.0f, 0.f}, den);
 }
 
 // log(z) for a positive double-float: the fp32 logarithm plus one Newton

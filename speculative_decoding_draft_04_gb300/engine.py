@@ -1,7 +1,9 @@
 """Device-side plumbing around the C ABI: moves a seeded workload to the GPU
 (torch allocations), owns the output buffers and the workspace, and
 enqueues one speculative cycle (spec_markov_draft then spec_verify) on a
-stream.  Nothing here computes any part of the method."""
+stream, or the confidence-scheduled cycle (draft, spec_confidence,
+spec_prefix_schedule, then spec_verify with the scheduled lengths).
+Nothing here computes any part of the method."""
 from __future__ import annotations
 
 import dataclasses
@@ -9,7 +11,7 @@ import dataclasses
 import numpy as np
 
 from . import _lib
-from .workloads import Workload
+from .workloads import ScheduleInputs, Workload
 
 
 def _dev_logits(arr: np.ndarray, dtype: str, device):
@@ -105,11 +107,12 @@ def draft(d: DeviceWorkload, b: Buffers, stream=None) -> None:
 
 
 def verify(d: DeviceWorkload, b: Buffers, stream=None, draft_tokens=None, q_tok=None,
-           lse_q=None) -> None:
+           lse_q=None, verify_len=None) -> None:
     _lib.spec_verify(d.target, d.U, d.W1, d.W2, d.anchor, d.temperature,
                      b.draft_tokens if draft_tokens is None else draft_tokens,
                      b.q_tok if q_tok is None else q_tok,
-                     b.lse_q if lse_q is None else lse_q, d.verify_len, d.u_accept, d.u_final,
+                     b.lse_q if lse_q is None else lse_q,
+                     d.verify_len if verify_len is None else verify_len, d.u_accept, d.u_final,
                      b.accept_len, b.out_tokens, b.alpha, b.vstatus, b.workspace, p_tok=b.p_tok,
                      diag=b.vdiag, stream=stream)
 
@@ -118,6 +121,54 @@ def cycle(d: DeviceWorkload, b: Buffers, stream=None) -> None:
     """One speculative cycle: draft gamma tokens per request, then verify them."""
     draft(d, b, stream)
     verify(d, b, stream)
+
+
+@dataclasses.dataclass
+class DeviceSchedule:
+    """Confidence-head inputs, the cost table and the scheduler's outputs."""
+    hidden: object
+    w: object
+    sps: object
+    conf: object
+    survival: object
+    verify_len: object
+    totals: object
+    theta: object
+    status: object
+    workspace: object
+
+    @classmethod
+    def from_inputs(cls, s: ScheduleInputs, B: int, gamma: int, dtype: str,
+                    device="cuda") -> "DeviceSchedule":
+        import torch
+        o = dict(device=device)
+        nbytes = _lib.spec_schedule_workspace_bytes(B, gamma)
+        if nbytes == 0:
+            raise _lib.SpecError("unsupported shape for the scheduler")
+        return cls(hidden=_dev_logits(s.hidden, dtype, device),
+                   w=torch.from_numpy(np.ascontiguousarray(s.w, dtype=np.float32)).to(device),
+                   sps=torch.from_numpy(np.ascontiguousarray(s.sps, dtype=np.float64)).to(device),
+                   conf=torch.empty((B, gamma), dtype=torch.float32, **o),
+                   survival=torch.empty((B, gamma), dtype=torch.float32, **o),
+                   verify_len=torch.empty(B, dtype=torch.int32, **o),
+                   totals=torch.empty(4, dtype=torch.int64, **o),
+                   theta=torch.empty(1, dtype=torch.float64, **o),
+                   status=torch.zeros(4, dtype=torch.int32, **o),
+                   workspace=torch.empty(nbytes, dtype=torch.uint8, **o))
+
+
+def schedule(d: DeviceWorkload, b: Buffers, s: DeviceSchedule, stream=None) -> None:
+    """Confidence of every drafted row, then the verify lengths."""
+    _lib.spec_confidence(s.hidden, d.W1, s.w, d.anchor, b.draft_tokens, s.conf, s.status, stream)
+    _lib.spec_prefix_schedule(s.conf, s.sps, s.survival, s.verify_len, s.totals, s.theta, s.status,
+                              s.workspace, stream)
+
+
+def scheduled_cycle(d: DeviceWorkload, b: Buffers, s: DeviceSchedule, stream=None) -> None:
+    """Draft, schedule, and verify each request up to its scheduled length."""
+    draft(d, b, stream)
+    schedule(d, b, s, stream)
+    verify(d, b, stream, verify_len=s.verify_len)
 
 
 def status_words(t) -> list[int]:

@@ -37,6 +37,23 @@ scales, temperatures, verify lengths, W1, W2, anchors, then per request
 (target base, permutation if Zipf, noise); uniforms: u_draft, u_accept,
 u_final.
 
+Confidence-head and scheduler inputs (``make_schedule_inputs``, DSpark
+review, sections 2.1 and 2.2), from ``default_rng([seed_index, trial, 2])``:
+
+* ``hidden[b, k, :]`` (the drafter backbone's h_{k+1}, width d): N(0, 1)
+  except coordinate 0, which holds a per-request offset mu_b ~ U[-1, 3] (a
+  stand-in for the domain: low for chat-like, high for code-like requests);
+* ``w [d + r]`` float32: w[0] = 1 (so mu_b shifts the logit), w[1:d] ~
+  N(0, 1/d) (hidden noise of unit variance), w[d:] ~ N(0, (0.5 / (sqrt(r) *
+  w_sd))^2) (the embedding part adds variance 0.25);
+* ``sps[B']`` for B' = 0..B (1 + gamma): the engine's steps per second at
+  batch B', 1000 / t(B') with t(B') = sqrt(t0^2 + (B' t1)^2) ms, t0 = 42 ms
+  (the memory-bound decode step of the VESSL blog's 70B example) and t1 =
+  t0 / (B (1 + gamma / 2)), so the curve bends half-way through the
+  candidates.
+
+Draw order: mu, w, then hidden per request.
+
 bf16 storage is round-to-nearest-even from float64, done directly (no
 intermediate float32 rounding).
 """
@@ -53,19 +70,19 @@ U23 = float(2.0 ** -23)
 # carry the shapes of the pages' drafter (rank 256, vocabulary 32000, k=7 from
 # the H-Spec review, Appx. B.1/B.2) and of larger vocabularies.
 CONFIGS: dict[str, dict[str, Any]] = {
-    "C0": dict(seed_index=0, B=4, gamma=4, V=1000, r=16, dtype="f32",
+    "C0": dict(seed_index=0, d=64, B=4, gamma=4, V=1000, r=16, dtype="f32",
                target=("normal", 3.0), noise=("fixed", 1.0), temps=(1.0,),
                L="full", w_sd=0.1),
-    "C1": dict(seed_index=1, B=32, gamma=7, V=32000, r=256, dtype="bf16",
+    "C1": dict(seed_index=1, d=4096, B=32, gamma=7, V=32000, r=256, dtype="bf16",
                target=("normal", 3.0), noise=("uniform", 0.5, 3.0), temps=(1.0,),
                L="full", w_sd=0.02),
-    "C2": dict(seed_index=2, B=128, gamma=7, V=32000, r=256, dtype="bf16",
+    "C2": dict(seed_index=2, d=4096, B=128, gamma=7, V=32000, r=256, dtype="bf16",
                target=("normal", 3.0), noise=("uniform", 0.5, 3.0), temps=(1.0,),
                L=("uniform", 1, 7), w_sd=0.02),
-    "C3": dict(seed_index=3, B=64, gamma=15, V=151936, r=256, dtype="bf16",
+    "C3": dict(seed_index=3, d=4096, B=64, gamma=15, V=151936, r=256, dtype="bf16",
                target=("zipf", 2.0, 1.1), noise=("uniform", 0.5, 3.0), temps=(0.6, 1.0),
                L="full", w_sd=0.02),
-    "C4": dict(seed_index=4, B=256, gamma=7, V=128256, r=256, dtype="bf16",
+    "C4": dict(seed_index=4, d=4096, B=256, gamma=7, V=128256, r=256, dtype="bf16",
                target=("normal", 3.0), noise=("uniform", 0.3, 4.0), temps=(0.7, 1.0),
                L=("uniform", 0, 7), w_sd=0.02),
 }
@@ -252,6 +269,47 @@ def make_workload(spec: dict[str, Any], trial: int = 0, *, B: int | None = None)
                     u_draft=np.ascontiguousarray(u_draft),
                     u_accept=np.ascontiguousarray(u_acc),
                     u_final=np.ascontiguousarray(u_fin))
+
+
+@dataclasses.dataclass
+class ScheduleInputs:
+    d: int
+    hidden: np.ndarray      # [B, gamma, d] storage dtype
+    w: np.ndarray           # float32 [d + r]
+    sps: np.ndarray         # float64 [B (1 + gamma) + 1]
+
+
+SPS_T0_MS = 42.0
+
+
+def cost_table(B: int, gamma: int, t0: float = SPS_T0_MS) -> np.ndarray:
+    """Synthetic steps-per-second table for batch sizes 0..B (1 + gamma)."""
+    t1 = t0 / (B * (1.0 + gamma / 2.0))
+    Bs = np.arange(B * (1 + gamma) + 1, dtype=np.float64)
+    return 1000.0 / np.sqrt(t0 * t0 + (Bs * t1) ** 2)
+
+
+def make_schedule_inputs(spec: dict[str, Any], trial: int = 0, *,
+                         B: int | None = None) -> ScheduleInputs:
+    """Confidence-head inputs and the cost table of one workload (see the
+    module docstring); ``B`` as in make_workload."""
+    Bn = int(spec["B"] if B is None else B)
+    g, r, d = int(spec["gamma"]), int(spec["r"]), int(spec["d"])
+    dtype = spec["dtype"]
+    rng = np.random.default_rng([int(spec["seed_index"]), int(trial), 2])
+    Bfull = int(spec["B"]) if B is None else max(Bn, int(spec["B"]))
+    mu = rng.uniform(-1.0, 3.0, size=Bfull)
+    w = np.empty(d + r, dtype=np.float64)
+    w[0] = 1.0
+    w[1:d] = rng.normal(0.0, 1.0 / np.sqrt(d), size=d - 1)
+    w[d:] = rng.normal(0.0, 0.5 / (np.sqrt(r) * float(spec["w_sd"])), size=r)
+    sdt = np.uint16 if dtype == "bf16" else np.float32
+    hidden = np.empty((Bn, g, d), dtype=sdt)
+    for b in range(Bn):
+        h = rng.normal(0.0, 1.0, size=(g, d))
+        h[:, 0] = mu[b]
+        hidden[b] = _store(h, dtype)
+    return ScheduleInputs(d=d, hidden=hidden, w=w.astype(np.float32), sps=cost_table(Bn, g))
 
 
 def shard_rows(B: int, rank: int, world: int) -> np.ndarray:

@@ -9,6 +9,9 @@
 //   add <ah> <al> <bh> <bl>    -> hi lo of the double-float sum
 //   rcp <t>                    -> hi lo of 1/t
 //   log <zh> <zl>              -> log(zh + zl) as "<double> 0"
+//   dot2 <n> <a..> <w..>       -> hi lo of the Dot2 dot product (hex floats)
+//   div <ah> <al> <bh> <bl>    -> hi lo of the double-float quotient
+//   sig <zh> <zl>              -> hi lo of 1 / (1 + e^{-(zh + zl)})
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -39,7 +42,7 @@ int main() {
       put(spec::dd_exp(spec::dd_from_double(x), tab));
     } else if (c == "tab") {
       for (int j = 0; j < spec::DD_EXP_TAB; ++j) put(tab[j]);
-    } else if (c == "dot") {
+    } else if (c == "dot" || c == "dot2") {
       int n;
       if (std::scanf("%d", &n) != 1) return 1;
       std::vector<float> a(n), w(n);
@@ -53,9 +56,15 @@ int main() {
         if (std::scanf("%lx", &x) != 1) return 1;
         w[i] = from_bits(x);
       }
-      spec::DdSum k[4];
-      for (int i = 0; i < n; ++i) k[i & 3].add(spec::rn_mul(a[i], w[i]));
-      put(spec::dd_add(spec::dd_add(k[0].value(), k[1].value()), spec::dd_add(k[2].value(), k[3].value())));
+      if (c == "dot2") {
+        spec::DdDot k;
+        for (int i = 0; i < n; ++i) k.add(a[i], w[i]);
+        put(k.value());
+      } else {
+        spec::DdSum k[4];
+        for (int i = 0; i < n; ++i) k[i & 3].add(spec::rn_mul(a[i], w[i]));
+        put(spec::dd_add(spec::dd_add(k[0].value(), k[1].value()), spec::dd_add(k[2].value(), k[3].value())));
+      }
     } else if (c == "rcp") {
       float t;
       if (std::scanf("%f", &t) != 1) return 1;
@@ -64,11 +73,15 @@ int main() {
       float zh, zl;
       if (std::scanf("%f %f", &zh, &zl) != 2) return 1;
       std::printf("%.17g 0\n", spec::dd_log(df{zh, zl}, tab));
-    } else if (c == "mul" || c == "add") {
+    } else if (c == "sig") {
+      float zh, zl;
+      if (std::scanf("%f %f", &zh, &zl) != 2) return 1;
+      put(spec::dd_sigmoid(df{zh, zl}, tab));
+    } else if (c == "mul" || c == "add" || c == "div") {
       float ah, al, bh, bl;
       if (std::scanf("%f %f %f %f", &ah, &al, &bh, &bl) != 4) return 1;
       const df a = {ah, al}, b = {bh, bl};
-      put(c == "mul" ? spec::dd_mul(a, b) : spec::dd_add(a, b));
+      put(c == "mul" ? spec::dd_mul(a, b) : c == "add" ? spec::dd_add(a, b) : spec::dd_div(a, b));
     } else {
       return 2;
     }

@@ -101,9 +101,53 @@ def test_status_strings_and_options(L):
     n = L.spec_num_stages()
     names = [L.spec_stage_name(i).decode() for i in range(n)]
     assert "draft_persistent" in names and "verify_tile" in names and len(set(names)) == n
+    assert {"confidence", "sched_rank", "sched_select"} <= set(names)
     assert L.spec_set_option(4, 1.0) == -1          # unused key
 
 
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(_lib.SpecError):
         _lib.lib(str(tmp_path / "nope.so"))
+
+
+def test_confidence_host_validation(L):
+    def args(**kw):
+        a = _lib.ConfidenceArgs(8, 4, 64, 1000, 16, _lib.SPEC_BF16)
+        for f in ("hidden", "W1", "w", "anchor", "draft_tokens", "conf", "dev_status"):
+            setattr(a, f, 0x100000)
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+    call = lambda a: L.spec_confidence(ctypes.byref(a), None)  # noqa: E731
+    assert L.spec_confidence(None, None) == -1
+    assert call(args(hidden=None)) == -1
+    assert call(args(R=0)) == -1 and call(args(R=4097)) == -1
+    assert call(args(d=4)) == -1
+    assert call(args(gamma=17)) == -2 and call(args(d=12)) == -2 and call(args(r=24)) == -2
+    assert call(args(r=512)) == -2 and call(args(dtype=2)) == -2
+    assert call(args(hidden=0x100008)) == -3 and call(args(w=0x100004)) == -3
+
+
+def test_schedule_host_validation(L):
+    assert _lib.spec_schedule_workspace_bytes(128, 7) == 128 * 7 * 4 + 128 * 7 * 8
+    assert _lib.spec_schedule_workspace_bytes(0, 7) == 0
+    assert _lib.spec_schedule_workspace_bytes(8, 17) == 0
+
+    def args(**kw):
+        a = _lib.ScheduleArgs(8, 4)
+        for f in ("conf", "sps", "survival", "verify_len", "totals", "theta", "dev_status"):
+            setattr(a, f, 0x100000)
+        a.sps_len = 41
+        a.workspace = 0x200000
+        a.workspace_bytes = 1 << 20
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+    call = lambda a: L.spec_prefix_schedule(ctypes.byref(a), None)  # noqa: E731
+    assert L.spec_prefix_schedule(None, None) == -1
+    assert call(args(conf=None)) == -1
+    assert call(args(sps_len=8)) == -1            # the table must cover B = R
+    assert call(args(gamma=17)) == -2
+    assert call(args(totals=0x100004)) == -3
+    assert call(args(workspace=None)) == -4 and call(args(workspace_bytes=64)) == -4
+    assert call(args(workspace=0x200008)) == -3

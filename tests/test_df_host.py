@@ -130,3 +130,59 @@ def test_log_of_double_float(probe):
         exact = (Decimal(float(zh[i])) + Decimal(float(zl[i]))).ln()
         bound = Decimal("3e-14") * (1 + abs(exact))          # the exponential's relative error, carried
         assert abs(Decimal(float(hi[i])) - exact) < bound, (float(z[i]), hi[i], float(exact))
+
+
+@pytest.mark.parametrize("n", [8, 264, 4352])
+def test_dot2_of_bf16_by_fp32_products(probe, n):
+    """Dot2 over products of a bf16 and an fp32 value (the confidence head's
+    w^T [h; e]): the products are not exact in fp32, TwoProd recovers them."""
+    rng = np.random.default_rng(n + 1)
+    lines, exact, mags = [], [], []
+    for _ in range(20):
+        a = _bf16(rng, n, 1.0)
+        w = (rng.standard_normal(n) / np.sqrt(n)).astype(np.float32)
+        lines.append(f"dot2 {n} " + " ".join(f"{x:x}" for x in a.view(np.uint32)) + " " +
+                     " ".join(f"{x:x}" for x in w.view(np.uint32)))
+        prods = [Fraction(float(p)) * Fraction(float(q)) for p, q in zip(a, w)]
+        exact.append(sum(prods, Fraction(0)))
+        mags.append(sum(abs(p) for p in prods))
+    hi, lo = probe(lines)
+    for h, l, e, m in zip(hi, lo, exact, mags):
+        err = abs(Fraction(float(h)) + Fraction(float(l)) - e)
+        assert err <= Fraction(1, 10**13) * m + Fraction(1, 10**40), (float(err), float(m))
+
+
+def test_division(probe):
+    rng = np.random.default_rng(8)
+    a = _split(rng.uniform(-4, 4, 400))
+    b = _split(np.concatenate([rng.uniform(0.5, 3.0, 300), -rng.uniform(1e-3, 1e3, 100)]))
+    ah, bh = a.astype(np.float32), b.astype(np.float32)
+    al, bl = (a - ah).astype(np.float32), (b - bh).astype(np.float32)
+    hi, lo = probe([f"div {x:.9g} {y:.9g} {z:.9g} {t:.9g}" for x, y, z, t in zip(ah, al, bh, bl)])
+    for i in range(len(a)):
+        ex = (Fraction(float(ah[i])) + Fraction(float(al[i]))) / (Fraction(float(bh[i])) + Fraction(float(bl[i])))
+        got = Fraction(float(hi[i])) + Fraction(float(lo[i]))
+        assert abs(got - ex) <= abs(ex) / 2**44, i
+
+
+def test_sigmoid(probe):
+    """1/(1 + e^{-z}) to about 1e-13 relative over the whole fp32 range of c
+    (pinned with 50-digit decimal arithmetic)."""
+    getcontext().prec = 50
+    rng = np.random.default_rng(9)
+    z = _split(np.concatenate([rng.uniform(-8, 8, 2000), rng.uniform(-100, 100, 300),
+                               [0.0, 1e-9, -1e-9, 17.0, -17.0, 30.0, -85.0]]))
+    zh = z.astype(np.float32)
+    zl = (z - zh).astype(np.float32)
+    hi, lo = probe([f"sig {a:.9g} {b:.9g}" for a, b in zip(zh, zl)])
+    for i in range(len(z)):
+        x = Decimal(float(zh[i])) + Decimal(float(zl[i]))
+        exact = 1 / (1 + (-x).exp())
+        got = Decimal(float(hi[i])) + Decimal(float(lo[i]))
+        # relative, down to the double-float's resolution near the fp32 minimum
+        bound = max(Decimal("2e-13") * exact, Decimal("1e-44"))
+        assert abs(got - exact) <= bound, (float(z[i]), float(got), float(exact))
+    # the rounded float is the nearest float of the exact value (no midpoint is near here)
+    c32 = (hi + lo).astype(np.float32)
+    ref = 1 / (1 + np.exp(-z))
+    assert np.mean(c32 == ref.astype(np.float32)) > 0.999
