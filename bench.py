@@ -114,6 +114,60 @@ def operating_point(d, bufs, draft_prof, steps):
             **{k: v for k, v in rep.items()}}
 
 
+def scheduled_pass(args, w, d, bufs, stream, flush, rank, dev):
+    """The confidence-scheduled cycle on the same workload: draft, confidence
+    head, prefix scheduler, then verification at the scheduled lengths.  Timed
+    like the main pass (events around each cycle, L2 flushed outside them),
+    then once more with per-kernel events for the scheduler's stages."""
+    import torch
+    from speculative_decoding_draft_04_gb300 import _lib, engine
+    from speculative_decoding_draft_04_gb300 import workloads as W
+    si = W.make_schedule_inputs(W.config(args.config), trial=rank)
+    s = engine.DeviceSchedule.from_inputs(si, w.B, w.gamma, w.dtype, dev)
+
+    def step():
+        engine.scheduled_cycle(d, bufs, s, stream)
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = float(sum(a.elapsed_time(b) for a, b in evs) / args.steps)
+    _lib.spec_profile_enable(True)
+    _lib.spec_profile_read()
+    for _ in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    prof = _lib.spec_profile_read()
+    _lib.spec_profile_enable(False)
+    tot = s.totals.cpu().numpy()
+    positions = int(s.verify_len.sum().item())
+    esz = 2 if w.dtype == "bf16" else 4
+    conf_bytes = w.B * w.gamma * (si.d + w.r) * esz + (si.d + w.r) * 4 + w.B * w.gamma * 8
+    c_ms, c_n = prof.get("confidence", (0.0, 0))
+    c_avg = c_ms / max(c_n, 1)
+    hbm_peak, _, peak_src = measured_peaks()
+    return {
+        "ms_per_step": ms, "value": positions / (ms * 1e-3), "unit": UNIT,
+        "positions_per_step": positions, "B": int(tot[0]), "tau": float(tot[1]) * 2.0 ** -36,
+        "stop_reason": int(tot[3]), "theta": float(s.theta.item()),
+        "hidden_width": si.d, "cost_table": "1000/sqrt(42^2 + (B t1)^2) steps/s, knee at B(1+gamma/2)",
+        "stages_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]},
+        "confidence_roofline": {"bound": "hbm", "algorithmic_bytes_per_launch": conf_bytes,
+                                "avg_launch_ms": c_avg,
+                                "achieved": conf_bytes / (c_avg * 1e-3) / 1e9 if c_avg else None,
+                                "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s"},
+    }
+
+
 def algorithmic_bytes(w):
     """Bytes a cycle must move at least (logits + W2 once per call), after the
     survey's accounting: draft = B*g*V*s + r*V*s; verify = sum(L+1)*V*s (target
@@ -345,6 +399,10 @@ def main():
     barrier()
     e2e_ms = float(sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps)
 
+    op = operating_point(d, bufs, prof.get("draft_persistent", (0.0, 0)), args.steps) \
+        if rank == 0 else None
+    sched = scheduled_pass(args, w, d, bufs, stream, flush, rank, dev)
+
     positions = int(w.verify_len.sum())
     if world > 1:
         t = torch.tensor([ms, e2e_ms, float(positions)], device=dev)
@@ -388,8 +446,8 @@ def main():
             "gpu_launches": int(launches * args.steps),
             "clocks": clocks,
         }
-        line["operating_point"] = operating_point(d, bufs, prof.get("draft_persistent", (0.0, 0)),
-                                                  args.steps)
+        line["scheduled_cycle"] = sched
+        line["operating_point"] = op
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
         print(json.dumps(line), flush=True)

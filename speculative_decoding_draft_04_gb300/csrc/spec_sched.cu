@@ -3,7 +3,7 @@
 // Generation", sections 2.1 "Confidence Head" and 2.2 "Hardware-Aware Prefix
 // Scheduler").
 //
-//   confidence_kernel     c_{r,k} = sigmoid(w^T [h_k; W1[x_{k-1}]]): one warp
+//   confidence_kernel     c_{r,k} = sigmoid(w^T [h_k; W1[x_{k-1}]]): one CTA
 //                         per draft row; the dot product in Dot2 (double-float)
 //                         and the logistic in double-float, rounded once to
 //                         fp32 -- the nearest float of the exact value except
@@ -31,7 +31,7 @@
 
 namespace spec {
 
-constexpr int CONF_ROWS = 8;         // draft rows per CTA (one warp each)
+constexpr int CONF_THREADS = 128;    // one CTA per draft row
 constexpr int RANK_THREADS = 128;
 constexpr int SEL_THREADS = 1024;
 constexpr float TAU_SCALE_F = 68719476736.0f;   // 2^36
@@ -55,51 +55,55 @@ __device__ __forceinline__ void load8(const float* p, float* o) {
 }
 
 template <class DT>
-__global__ void __launch_bounds__(CONF_ROWS * 32)
+__global__ void __launch_bounds__(CONF_THREADS)
     confidence_kernel(int R, int gamma, int d, int V, int r, const DT* __restrict__ hidden,
                       const DT* __restrict__ W1, const float* __restrict__ w,
                       const int* __restrict__ anchor, const int* __restrict__ tokens,
                       float* __restrict__ conf, uint32_t* status) {
   __shared__ df s_tab[DD_EXP_TAB];
-  if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(s_tab, threadIdx.x);
-  __syncthreads();
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * CONF_ROWS + (threadIdx.x >> 5);
-  if (row >= R * gamma) return;
+  __shared__ df s_part[CONF_THREADS / 32];
+  const int row = blockIdx.x;
   const int b = row / gamma, k = row - b * gamma;
   const int prev = k == 0 ? __ldg(anchor + b) : __ldg(tokens + row - 1);
-  if (prev < 0 || prev >= V) {
-    if (lane == 0) {
+  if (prev < 0 || prev >= V) {             // uniform over the CTA
+    if (threadIdx.x == 0) {
       conf[row] = __int_as_float(0x7fffffff);
       set_status(status, SPEC_DEV_BAD_TOKEN);
     }
     return;
   }
+  if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(s_tab, threadIdx.x);
   DdDot acc;
   float x[8], y[8];
   const DT* h = hidden + (size_t)row * d;
-  for (int i = lane * 8; i < d; i += 256) {
+#pragma unroll 4
+  for (int i = threadIdx.x * 8; i < d; i += CONF_THREADS * 8) {
     load8(h + i, x);
     load8(w + i, y);
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc.add(x[e], y[e]);
   }
   const DT* emb = W1 + (size_t)prev * r;
-  for (int i = lane * 8; i < r; i += 256) {
+  for (int i = threadIdx.x * 8; i < r; i += CONF_THREADS * 8) {
     load8(emb + i, x);
     load8(w + d + i, y);
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc.add(x[e], y[e]);
   }
-  const df z = warp_sum_df(acc.value());
-  if (lane == 0) {
+  const df zw = warp_sum_df(acc.value());
+  if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = zw;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    df z = s_part[0];
+#pragma unroll
+    for (int i = 1; i < CONF_THREADS / 32; ++i) z = dd_add(z, s_part[i]);
     float c;
     if (!isfinite(z.hi)) {
       c = __int_as_float(0x7fffffff);
       set_status(status, SPEC_DEV_BAD_CONF);
     } else {
-      const df s = dd_sigmoid(z, s_tab);
-      c = rn_add(s.hi, s.lo);
+      const df sg = dd_sigmoid(z, s_tab);
+      c = rn_add(sg.hi, sg.lo);
     }
     conf[row] = c;
   }
@@ -257,8 +261,7 @@ template <class DT>
 cudaError_t launch_confidence(int R, int gamma, int d, int V, int r, const void* hidden, const void* W1,
                               const float* w, const int* anchor, const int* tokens, float* conf,
                               uint32_t* status, cudaStream_t st) {
-  const int rows = R * gamma;
-  confidence_kernel<DT><<<(rows + CONF_ROWS - 1) / CONF_ROWS, CONF_ROWS * 32, 0, st>>>(
+  confidence_kernel<DT><<<R * gamma, CONF_THREADS, 0, st>>>(
       R, gamma, d, V, r, static_cast<const DT*>(hidden), static_cast<const DT*>(W1), w, anchor, tokens,
       conf, status);
   return cudaGetLastError();
