@@ -28,10 +28,7 @@ cudaError_t launch_verify_final(const Shape&, const void*, const void*, const vo
                                 const int*, const float*, const float*, int*, int*, float*, float*,
                                 float*, uint32_t*, const Ws&, const Eps&, cudaStream_t);
 template <typename DT>
-cudaError_t launch_hp_sums(const Shape&, const HpRows&, const Ws&, int, int, cudaStream_t);
-template <typename DT>
-cudaError_t launch_hp_decide(const Shape&, const HpRows&, const Ws&, int*, float*, double*, int*,
-                             uint32_t*, int, cudaStream_t);
+cudaError_t launch_hp_sums(const Shape&, const HpRows&, const Ws&, int, int*, uint32_t*, int, cudaStream_t);
 template <typename DT>
 cudaError_t launch_slow_verify(const Shape&, const HpRows&, const Ws&, const int*, const int*,
                                const double*, const int*, const float*, const float*, int*, int*,
@@ -54,13 +51,16 @@ bool g_trace = false;         // SPEC_OPT_TRACE
 
 // Band constants (probability units) of the certified first-pass decisions.
 // Largest first-pass margin error seen against the float64 oracle over C0-C4
-// (about 4.3k draws): 2.6e-8 absolute, at most 1.4e-7 x sqrt(sum q^2) and
-// 1.1e-7 x sqrt(sum slice mass^2).  The constants keep a factor >= 5 on each.
-constexpr float EPS_ELEM = 7.0e-7f;
-constexpr float EPS_SLICE = 7.0e-7f;
+// (about 4.3k draft and 1k final draws): 3.8e-8 absolute, at most
+// 1.4e-7 x sqrt(sum q^2) and 1.1e-7 x sqrt(sum slice mass^2), and never more
+// than 3.5% of the whole band the constants 7e-7 / 7e-7 / 1.5e-7 gave.  The
+// halved constants keep the largest error under 7.1% of the band (a factor
+// above 14); a wider band only sends more draws to the re-decision.
+constexpr float EPS_ELEM = 3.5e-7f;
+constexpr float EPS_SLICE = 3.5e-7f;
 constexpr float EPS_ABS = 1.0e-9f;
 constexpr float EPS_RATIO = 1.0e-6f;
-constexpr float EPS_NORM = 1.5e-7f;
+constexpr float EPS_NORM = 7.5e-8f;
 
 Eps current_eps() {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -78,12 +78,12 @@ Eps current_eps() {
 enum Stage {
   ST_DRAFT_PERSISTENT, ST_VERIFY_PREP,
   ST_TARGET_STATS, ST_VERIFY_TILE, ST_VERIFY_FINAL, ST_SLOW_VERIFY, ST_VERIFY_HP_SUMS,
-  ST_VERIFY_HP_RESID, ST_VERIFY_HP_DECIDE, ST_CONFIDENCE, ST_SCHED_RANK, ST_SCHED_SELECT, ST_COUNT
+  ST_VERIFY_HP_RESID, ST_CONFIDENCE, ST_SCHED_RANK, ST_SCHED_SELECT, ST_COUNT
 };
 const char* kStageNames[ST_COUNT] = {
     "draft_persistent", "verify_prep",
     "target_stats", "verify_tile", "verify_final", "slow_verify", "verify_hp_sums",
-    "verify_hp_resid", "verify_hp_decide", "confidence", "sched_rank", "sched_select"};
+    "verify_hp_resid", "confidence", "sched_rank", "sched_select"};
 bool g_prof = false;
 struct EvPair { cudaEvent_t a, b; int stage; };
 std::vector<EvPair> g_pending;
@@ -139,10 +139,12 @@ int num_sms() {
 }
 
 // ---------------------------------------------------------------- workspace
+// Residual re-decisions whose weights are kept between their two passes.
+constexpr int kHpwItems = 16;
 struct Layout {
-  size_t ctrl, trace, items, hpsum, hpcnt, dpart, rowptr, prow, prevtok, vflags, lse_p, bpart, vpart, slow,
+  size_t ctrl, trace, items, hpsum, hpcnt, hpw, hpnorm, dpart, rowptr, prow, prevtok, vflags, lse_p, bpart, vpart, slow,
       accbits, rowc, rowp, total;
-  int max_items;
+  int max_items, hpw_items;
 };
 
 Layout layout(const Shape& sh) {
@@ -160,6 +162,9 @@ Layout layout(const Shape& sh) {
   L.items = take((size_t)L.max_items * sizeof(HpItem));
   L.hpsum = take((size_t)L.max_items * 3 * sh.NC * sizeof(float2));
   L.hpcnt = take((size_t)L.max_items * sizeof(uint32_t));
+  L.hpw_items = sh.B < kHpwItems ? sh.B : kHpwItems;
+  L.hpw = take((size_t)L.hpw_items * sh.V * sizeof(float4));
+  L.hpnorm = take((size_t)L.max_items * sizeof(float4));
   L.dpart = take(B * sh.NC * sizeof(float4));
   L.rowptr = take((B + 1) * sizeof(int));
   L.prow = take(B * g * sizeof(int2));
@@ -186,6 +191,9 @@ Ws views(const Layout& L, void* base) {
   w.hpsum = reinterpret_cast<float2*>(p + L.hpsum);
   w.hp_cols = 3;
   w.hpcnt = reinterpret_cast<uint32_t*>(p + L.hpcnt);
+  w.hpw = reinterpret_cast<float4*>(p + L.hpw);
+  w.hpw_items = L.hpw_items;
+  w.hpnorm = reinterpret_cast<float4*>(p + L.hpnorm);
   w.dpart = reinterpret_cast<float4*>(p + L.dpart);
   w.rowptr = reinterpret_cast<int*>(p + L.rowptr);
   w.prow = reinterpret_cast<int2*>(p + L.prow);
@@ -307,16 +315,11 @@ int run_verify(const spec_verify_args* a, cudaStream_t st) {
   }
   {
     ProfScope p(st, ST_VERIFY_HP_SUMS);
-    SPEC_TRY(launch_hp_sums<DT>(sh, R, ws, 0, grid, st));
+    SPEC_TRY(launch_hp_sums<DT>(sh, R, ws, 0, a->out_tokens, a->dev_status, grid, st));
   }
   {
     ProfScope p(st, ST_VERIFY_HP_RESID);
-    SPEC_TRY(launch_hp_sums<DT>(sh, R, ws, 1, grid, st));
-  }
-  {
-    ProfScope p(st, ST_VERIFY_HP_DECIDE);
-    SPEC_TRY(launch_hp_decide<DT>(sh, R, ws, nullptr, nullptr, nullptr, a->out_tokens,
-                                  a->dev_status, grid, st));
+    SPEC_TRY(launch_hp_sums<DT>(sh, R, ws, 1, a->out_tokens, a->dev_status, grid, st));
   }
   return SPEC_OK;
 }

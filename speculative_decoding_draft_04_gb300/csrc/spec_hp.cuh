@@ -126,6 +126,68 @@ __device__ __forceinline__ df hp_bias_slab(const float* a, const DT* slab, int r
   if constexpr (sizeof(DT) == 4) s = dd_add_f(s, perr);
   return s;
 }
+// Two adjacent slab entries widened to float (4- or 8-byte aligned).
+__device__ __forceinline__ void slab2(const bf16* p, float& x, float& y) {
+  const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+  x = __uint_as_float(w << 16);
+  y = __uint_as_float(w & 0xffff0000u);
+}
+__device__ __forceinline__ void slab2(const float* p, float& x, float& y) {
+  const float2 w = *reinterpret_cast<const float2*>(p);
+  x = w.x;
+  y = w.y;
+}
+
+// Transition biases of all HPB columns of a block whose W2 columns are staged
+// in `slab` (r x HPB), one per thread (a CTA-wide call).  Thread t of each
+// half of the CTA takes columns 2(t mod NT/2) and 2(t mod NT/2) + 1 (one
+// two-column load per row) over half of the r rows, with four compensated
+// chains per column; the two halves meet in `xch` (HPB double-floats).  `a`
+// is W1[x] widened to float, 16-byte aligned.  Thread t returns column t.
+template <typename DT>
+__device__ __forceinline__ df hp_bias_block(const float* a, const DT* slab, int r, df* xch) {
+  constexpr int H = NT / 2;
+  static_assert(2 * H == HPB, "two columns per thread cover a block");
+  const int c0 = 2 * (threadIdx.x % H), half = threadIdx.x / H;
+  const int rh = r / 2;                         // r % 16 == 0
+  DdSum k0[4], k1[4];
+  float e0 = 0.f, e1 = 0.f;
+  for (int i = half * rh; i < (half + 1) * rh; i += 4) {
+    const float4 av = *reinterpret_cast<const float4*>(a + i);
+    const float aa[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float w0, w1;
+      slab2(slab + (size_t)(i + u) * HPB + c0, w0, w1);
+      const float p0 = __fmul_rn(aa[u], w0), p1 = __fmul_rn(aa[u], w1);
+      if constexpr (sizeof(DT) == 4) {
+        e0 += fmaf(aa[u], w0, -p0);
+        e1 += fmaf(aa[u], w1, -p1);
+      }
+      k0[u].add(p0);
+      k1[u].add(p1);
+    }
+  }
+  df s0 = dd_add(dd_add(k0[0].value(), k0[1].value()), dd_add(k0[2].value(), k0[3].value()));
+  df s1 = dd_add(dd_add(k1[0].value(), k1[1].value()), dd_add(k1[2].value(), k1[3].value()));
+  if constexpr (sizeof(DT) == 4) {
+    s0 = dd_add_f(s0, e0);
+    s1 = dd_add_f(s1, e1);
+  }
+  __syncthreads();                              // xch may still be read by the caller's last use
+  if (half == 1) {
+    xch[c0] = s0;
+    xch[c0 + 1] = s1;
+  }
+  __syncthreads();
+  if (half == 0) {
+    xch[c0] = dd_add(xch[c0], s0);
+    xch[c0 + 1] = dd_add(xch[c0 + 1], s1);
+  }
+  __syncthreads();
+  return xch[threadIdx.x];
+}
+
 // Draft weight exp((U[v] + bias) / T - shift_q) and target weight
 // exp(t[v] / T - shift_p), unnormalised unless the shifts are the row's
 // logsumexp.
@@ -139,6 +201,16 @@ __device__ __forceinline__ df hp_wp(const ItemCtx<DT>& c, int v, const df* tab) 
   const df l = dd_add(dd_mul_f(c.invT, ldf(c.Trow + v)), c.nsp);
   return dd_exp(l, tab);
 }
+// The same weights from preloaded logits (uq = U[v], tp = target[v]).
+template <typename DT>
+__device__ __forceinline__ df hp_wq_val(const ItemCtx<DT>& c, df bias, float uq, const df* tab) {
+  return dd_exp(dd_add(dd_mul(dd_add_f(bias, uq), c.invT), c.nsq), tab);
+}
+template <typename DT>
+__device__ __forceinline__ df hp_wp_val(const ItemCtx<DT>& c, float tp, const df* tab) {
+  return dd_exp(dd_add(dd_mul_f(c.invT, tp), c.nsp), tab);
+}
+
 // Both weights of entry v for an item (zero beyond V; eq is zero for a bonus
 // item, ep for a draft item).
 template <typename DT>
@@ -185,11 +257,31 @@ __device__ __forceinline__ df ld_sum(const float2* p) {
   const float2 v = __ldcg(p);
   return {v.x, v.y};
 }
-// Sum over an item's chunk sums (fixed order).
-__device__ __forceinline__ df item_total(const float2* sums, int NC, float* shf) {
+// Sum of sums[q0, q1) in order; the loads are issued eight at a time so the
+// loop waits on one L2 round trip per eight entries, not per entry.
+__device__ __forceinline__ df range_sum(const float2* sums, int q0, int q1) {
   df s = {0.f, 0.f};
-  for (int q = threadIdx.x; q < NC; q += NT) s = dd_add(s, ld_sum(sums + q));
-  return block_sum_df(s, shf);
+  for (int q = q0; q < q1; q += 8) {
+    float2 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = q + i < q1 ? __ldcg(sums + q + i) : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s = dd_add(s, df{v[i].x, v[i].y});
+  }
+  return s;
+}
+// Contiguous share [q0, q1) of NC entries for this thread.
+__device__ __forceinline__ void thread_range(int NC, int& q0, int& q1) {
+  const int per = (NC + NT - 1) / NT;
+  q0 = min(NC, (int)threadIdx.x * per);
+  q1 = min(NC, q0 + per);
+}
+// Sum over an item's chunk sums (fixed order: per-thread ranges, then the
+// block reduction).
+__device__ __forceinline__ df item_total(const float2* sums, int NC, float* shf) {
+  int q0, q1;
+  thread_range(NC, q0, q1);
+  return block_sum_df(range_sum(sums, q0, q1), shf);
 }
 // Reciprocal of a positive double-float, computed once (thread 0) and shared.
 __device__ __forceinline__ df shared_recip(df z, df* slot) {
@@ -209,7 +301,7 @@ __device__ __forceinline__ df shared_recip(df z, df* slot) {
 struct HpShared {
   df tab[DD_EXP_TAB];
   float shf[72];
-  float a[256];
+  alignas(16) float a[256];
   df part[NT / 32][CW];
   df rc[2];
   df pref;
@@ -229,21 +321,44 @@ struct HpShared {
 template <typename DT>
 __device__ void hp_block(const Shape& sh, const HpRows& R, const Ws& ws, int phase, int item,
                          int blk, const HpItem& it, HpShared& S, DT* slab) {
+  // a residual item among the first hpw_items keeps its weights from phase 0
+  const bool keep = it.kind == HP_RESID && item < ws.hpw_items;
+  const bool stored = keep && phase == 1;
   __syncthreads();
-  if (it.kind != HP_BONUS) {
+  if (it.kind != HP_BONUS && !stored) {
     for (int i = threadIdx.x; i < sh.r; i += NT) S.a[i] = ldf((const DT*)R.W1 + (size_t)it.prev * sh.r + i);
     stage_w2_slab<DT>(slab, (const DT*)R.W2, sh.V, 0, sh.r, blk * HPB, HPB);
   }
   __syncthreads();
   df izp = {0.f, 0.f}, izq = {0.f, 0.f};
   if (phase == 1) {
-    izp = shared_recip(item_total(item_sums(ws, sh, item, 0), sh.NC, S.shf), &S.rc[0]);
-    izq = shared_recip(item_total(item_sums(ws, sh, item, 1), sh.NC, S.shf), &S.rc[1]);
+    const float4 nz = __ldcg(ws.hpnorm + item);
+    izp = {nz.x, nz.y};
+    izq = {nz.z, nz.w};
   }
   const ItemCtx<DT> c = item_ctx_shared<DT>(sh, R, it, S.template ctx<DT>());
   const int v = blk * HPB + threadIdx.x;
-  df eq, ep;
-  hp_weights_slab<DT>(sh, it, c, S.a, slab, S.tab, v, eq, ep);
+  const bool in = v < sh.V;
+  df eq = {0.f, 0.f}, ep = {0.f, 0.f};
+  float4* wslot = keep && in ? ws.hpw + (size_t)item * sh.V + v : nullptr;
+  if (stored) {
+    if (wslot) {
+      const float4 w4 = __ldcg(wslot);
+      eq = {w4.x, w4.y};
+      ep = {w4.z, w4.w};
+    }
+  } else {
+    // logits first, so their loads overlap the bias sums
+    const float uq = (in && it.kind != HP_BONUS) ? ldf(c.Urow + v) : 0.f;
+    const float tp = (in && it.kind != HP_DRAFT) ? ldf(c.Trow + v) : 0.f;
+    const df bias = it.kind != HP_BONUS ? hp_bias_block<DT>(S.a, slab, sh.r, &S.part[0][0])
+                                        : df{0.f, 0.f};
+    if (in) {
+      if (it.kind != HP_BONUS) eq = hp_wq_val<DT>(c, bias, uq, S.tab);
+      if (it.kind != HP_DRAFT) ep = hp_wp_val<DT>(c, tp, S.tab);
+    }
+    if (wslot) *wslot = make_float4(eq.hi, eq.lo, ep.hi, ep.lo);
+  }
   const int chunk = v / CW;                      // = blk * (HPB / CW) + warp
   const bool store = (threadIdx.x & 31) == 0 && chunk < sh.NC;
   if (phase == 0) {
@@ -270,19 +385,17 @@ __device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, i
                                HpShared& S, DT* slab) {
   const HpItem it = ldcg_item(ws.items + item);
   const bool resid = it.kind == HP_RESID;
-  const df Zp = item_total(item_sums(ws, sh, item, 0), sh.NC, S.shf);
-  const df Zq = resid ? item_total(item_sums(ws, sh, item, 1), sh.NC, S.shf) : df{1.f, 0.f};
   const df Zc = resid ? item_total(item_sums(ws, sh, item, 2), sh.NC, S.shf) : df{0.f, 0.f};
   // residual with no mass: draw from p (a probability-zero event)
   const bool use_r = resid && Zc.hi > 0.f;
+  const df Zp = use_r ? df{0.f, 0.f} : item_total(item_sums(ws, sh, item, 0), sh.NC, S.shf);
   const float2* sums = item_sums(ws, sh, item, use_r ? 2 : 0);
   const df Z = use_r ? Zc : Zp;
   const df target = dd_mul_f(Z, it.u);
   // crossing chunk: per-thread contiguous range of chunks, double-float scan
-  const int per = (sh.NC + NT - 1) / NT;
-  const int q0 = threadIdx.x * per, q1 = min(q0 + per, sh.NC);
-  df loc = {0.f, 0.f};
-  for (int q = q0; q < q1; ++q) loc = dd_add(loc, ld_sum(sums + q));
+  int q0, q1;
+  thread_range(sh.NC, q0, q1);
+  const df loc = range_sum(sums, q0, q1);
   df tot;
   const df ex = block_excl_scan_df(loc, &tot, S.shf);
   if (threadIdx.x == 0) S.sel = 0x7fffffff;
@@ -291,16 +404,24 @@ __device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, i
   df mypref = {0.f, 0.f};
   if (q0 < q1 && dd_le(ex, target) && !dd_le(dd_add(ex, loc), target)) {
     df run = ex;
-    for (int q = q0; q < q1; ++q) {
-      const df nx = dd_add(run, ld_sum(sums + q));
-      if (!dd_le(nx, target)) {
-        mine = q;
-        mypref = run;
-        atomicMin(&S.sel, q);
-        break;
+    for (int q = q0; q < q1 && mine < 0; q += 8) {
+      float2 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = q + i < q1 ? __ldcg(sums + q + i) : make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (mine < 0 && q + i < q1) {
+          const df nx = dd_add(run, df{v[i].x, v[i].y});
+          if (!dd_le(nx, target)) {
+            mine = q + i;
+            mypref = run;
+          } else {
+            run = nx;
+          }
+        }
       }
-      run = nx;
     }
+    if (mine >= 0) atomicMin(&S.sel, mine);
   }
   __syncthreads();
   if (mine >= 0 && mine == S.sel) S.pref = mypref;
@@ -318,8 +439,12 @@ __device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, i
     __syncthreads();
   }
   const int n0 = S.sel * CW;
-  const df izp = use_r ? shared_recip(Zp, &S.rc[0]) : df{0.f, 0.f};
-  const df izq = use_r ? shared_recip(Zq, &S.rc[1]) : df{0.f, 0.f};
+  df izp = {0.f, 0.f}, izq = {0.f, 0.f};
+  if (use_r) {
+    const float4 nz = __ldcg(ws.hpnorm + item);
+    izp = {nz.x, nz.y};
+    izq = {nz.z, nz.w};
+  }
   // ---- the chunk's biases: warp w sums rows [w r/8, (w+1) r/8) of column lane
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (it.kind != HP_BONUS) {
@@ -390,14 +515,14 @@ __device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, i
 
 // Block sums of the n queued items (phase 0: weights, phase 1: residuals of
 // residual items), grid-stride over (item, block of HPB columns).  With
-// `fused` (draft items only), the CTA that completes an item's last block
-// re-decides the item at once; the per-item counters start at zero and are
-// left at zero.
+// `fused`, the CTA that completes an item's last block of its final pass
+// (phase 0 for draft and bonus items, phase 1 for residual items) re-decides
+// the item at once; the per-item counters start at zero and are left at zero.
 template <typename DT>
 __device__ void hp_sums_body(const Shape& sh, const HpRows& R, const Ws& ws, int phase, int n,
                              unsigned char* dsm, bool fused = false, int* tokens = nullptr,
                              float* q_tok = nullptr, double* lse_q = nullptr,
-                             uint32_t* status = nullptr) {
+                             uint32_t* status = nullptr, int* out_tokens = nullptr) {
   DT* slab = reinterpret_cast<DT*>(dsm);        // [r][HPB] W2 columns of one block
   __shared__ HpShared S;
   hp_table(S.tab);
@@ -414,24 +539,19 @@ __device__ void hp_sums_body(const Shape& sh, const HpRows& R, const Ws& ws, int
       __syncthreads();
       if (S.last) {
         __threadfence();
-        hp_decide_item<DT>(sh, R, ws, item, tokens, q_tok, lse_q, nullptr, status, S, slab);
+        if (it.kind == HP_RESID && phase == 0) {
+          // both normalisers are complete: their reciprocals serve every block
+          // of the residual pass and the re-decision
+          const df izp = shared_recip(item_total(item_sums(ws, sh, item, 0), sh.NC, S.shf), &S.rc[0]);
+          const df izq = shared_recip(item_total(item_sums(ws, sh, item, 1), sh.NC, S.shf), &S.rc[1]);
+          if (threadIdx.x == 0) ws.hpnorm[item] = make_float4(izp.hi, izp.lo, izq.hi, izq.lo);
+        }
+        if ((it.kind == HP_RESID) == (phase == 1))
+          hp_decide_item<DT>(sh, R, ws, item, tokens, q_tok, lse_q, out_tokens, status, S, slab);
         if (threadIdx.x == 0) ws.hpcnt[item] = 0u;
       }
     }
   }
-}
-
-// Re-decide the n queued items: one CTA per item (grid-stride).
-template <typename DT>
-__device__ void hp_decide_body(const Shape& sh, const HpRows& R, const Ws& ws, int n, int* tokens,
-                               float* q_tok, double* lse_q, int* out_tokens, uint32_t* status,
-                               unsigned char* dsm) {
-  DT* slab = reinterpret_cast<DT*>(dsm);
-  __shared__ HpShared S;
-  hp_table(S.tab);
-  __syncthreads();
-  for (int item = blockIdx.x; item < n; item += gridDim.x)
-    hp_decide_item<DT>(sh, R, ws, item, tokens, q_tok, lse_q, out_tokens, status, S, slab);
 }
 
 }  // namespace spec

@@ -55,6 +55,11 @@ struct Ws {
   float2* hpsum;        // [max_items][hp_cols][NC] chunk sums of the re-decided rows (hi, lo)
   int hp_cols;          // 3 (draft and verify) or 1 (draft only)
   uint32_t* hpcnt;      // [max_items] blocks summed so far (zeroed before the draft)
+  float4* hpw;          // [hpw_items][V] residual items' weights (q hi, q lo, p hi, p lo),
+                        // kept from the first sums pass for the residual pass
+  int hpw_items;        // items with stored weights (0: none)
+  float4* hpnorm;       // [max_items] residual items: 1/Z_p, 1/Z_q (double-floats), written
+                        // once the first sums pass is complete
   // draft
   float4* dpart;        // [B][NC] draft partials per CW-column chunk: (c, m, s, q2)
   // verify

@@ -17,9 +17,11 @@
 //   hp_sums_kernel    grid-stride over (item, block of HPB columns): block sums
 //                     of the item's unnormalised weights (phase 0), or of the
 //                     residual max(0, p - q) once the normalisers are known
-//                     (phase 1, residual items only).
-//   hp_decide_kernel  one CTA per item: crossing block from the block sums,
-//                     recompute that block, scan, write the token.
+//                     (phase 1, residual items only; the weights of the first
+//                     items are kept from phase 0).  The CTA that completes an
+//                     item's last block of its final pass re-decides it:
+//                     crossing chunk from the chunk sums, that chunk
+//                     recomputed and scanned, token written.
 //   slow_verify_kernel one CTA per request whose ratio test itself was near
 //                     its boundary: re-runs that request's verification with
 //                     extended-precision normalisers (rare).
@@ -27,22 +29,15 @@
 
 namespace spec {
 
+// Block sums of the verification's queued items; the CTA that completes an
+// item's last block of its final pass re-decides it (writes out_tokens).
 template <typename DT>
-__global__ void __launch_bounds__(NT) hp_sums_kernel(Shape sh, HpRows R, Ws ws, int phase) {
+__global__ void __launch_bounds__(NT) hp_sums_kernel(Shape sh, HpRows R, Ws ws, int phase,
+                                                     int* out_tokens, uint32_t* status) {
   extern __shared__ __align__(16) unsigned char dsm[];
   const int n = min((int)ws.ctrl[CTRL_ITEMS], ws.max_items);
   if (n == 0) return;
-  hp_sums_body<DT>(sh, R, ws, phase, n, dsm);
-}
-
-template <typename DT>
-__global__ void __launch_bounds__(NT) hp_decide_kernel(Shape sh, HpRows R, Ws ws, int* tokens,
-                                                       float* q_tok, double* lse_q,
-                                                       int* out_tokens, uint32_t* status) {
-  extern __shared__ __align__(16) unsigned char dsm[];
-  const int n = min((int)ws.ctrl[CTRL_ITEMS], ws.max_items);
-  if (n == 0) return;
-  hp_decide_body<DT>(sh, R, ws, n, tokens, q_tok, lse_q, out_tokens, status, dsm);
+  hp_sums_body<DT>(sh, R, ws, phase, n, dsm, true, nullptr, nullptr, nullptr, status, out_tokens);
 }
 
 // ---------------------------------------------------------------- slow path
@@ -184,24 +179,13 @@ __global__ void __launch_bounds__(NT) slow_verify_kernel(
 
 // ---------------------------------------------------------------- launchers
 template <typename DT>
-cudaError_t launch_hp_sums(const Shape& sh, const HpRows& R, const Ws& ws, int phase, int grid,
-                           cudaStream_t st) {
+cudaError_t launch_hp_sums(const Shape& sh, const HpRows& R, const Ws& ws, int phase, int* out_tokens,
+                           uint32_t* status, int grid, cudaStream_t st) {
   const size_t smem = (size_t)sh.r * HPB * sizeof(DT);
   cudaError_t e = cudaFuncSetAttribute(hp_sums_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  hp_sums_kernel<DT><<<grid, NT, smem, st>>>(sh, R, ws, phase);
-  return cudaGetLastError();
-}
-template <typename DT>
-cudaError_t launch_hp_decide(const Shape& sh, const HpRows& R, const Ws& ws, int* tokens,
-                             float* q_tok, double* lse_q, int* out_tokens, uint32_t* status,
-                             int grid, cudaStream_t st) {
-  const size_t smem = (size_t)sh.r * HPB * sizeof(DT);
-  cudaError_t e = cudaFuncSetAttribute(hp_decide_kernel<DT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  hp_decide_kernel<DT><<<grid, NT, smem, st>>>(sh, R, ws, tokens, q_tok, lse_q, out_tokens, status);
+  hp_sums_kernel<DT><<<grid, NT, smem, st>>>(sh, R, ws, phase, out_tokens, status);
   return cudaGetLastError();
 }
 template <typename DT>
@@ -215,10 +199,8 @@ cudaError_t launch_slow_verify(const Shape& sh, const HpRows& R, const Ws& ws, c
 }
 
 #define SPEC_INST(DT)                                                                            \
-  template cudaError_t launch_hp_sums<DT>(const Shape&, const HpRows&, const Ws&, int, int,     \
-                                          cudaStream_t);                                        \
-  template cudaError_t launch_hp_decide<DT>(const Shape&, const HpRows&, const Ws&, int*, float*, \
-                                            double*, int*, uint32_t*, int, cudaStream_t);       \
+  template cudaError_t launch_hp_sums<DT>(const Shape&, const HpRows&, const Ws&, int, int*,    \
+                                          uint32_t*, int, cudaStream_t);                        \
   template cudaError_t launch_slow_verify<DT>(const Shape&, const HpRows&, const Ws&, const int*, \
                                               const int*, const double*, const int*,           \
                                               const float*, const float*, int*, int*, uint32_t*, \

@@ -169,6 +169,8 @@ __global__ void __launch_bounds__(NT) verify_prep_kernel(
     ws.ctrl[CTRL_ITEMS] = 0;
     ws.ctrl[CTRL_SLOW] = 0;
   }
+  // per-item block counters of the re-decision passes start at zero
+  for (int i = threadIdx.x; i < ws.max_items; i += NT) ws.hpcnt[i] = 0u;
 }
 
 // ---------------------------------------------------------------- target statistics
