@@ -153,13 +153,16 @@ class VerifyResult:
 
 
 def verify_request(t_b, U_b, W1, W2, anchor, T, draft_tokens_b, L, u_accept_b, u_final,
-                   return_rows: bool = False) -> VerifyResult:
+                   return_rows: bool = False, a_rows=None) -> VerifyResult:
     """[SpecDec] "알고리즘" + "수락 규칙" for one request with verify length L.
 
     Ratio tests j = 0..L-1 accept iff u_accept[j] < p_j(x_{j+1}) / q_j(x_{j+1});
     n = the first rejected j, else L.  Emit x_1..x_n, then the correction
     token ~ normalize(max(0, p_n - q_n)) if n < L, else the bonus token ~ p_L.
-    alpha_j = sum_v min(p_j(v), q_j(v)) ("수락 규칙", closed form)."""
+    alpha_j = sum_v min(p_j(v), q_j(v)) ("수락 규칙", closed form).
+
+    ``a_rows`` [gamma, r], when given, replaces the Markov head's factor
+    W1[x_j] of draft row j (the RNN head's tanh(W_o z) rows, [DSpark] §1.2)."""
     g = U_b.shape[0]
     V = U_b.shape[1]
     L = int(L)
@@ -167,7 +170,13 @@ def verify_request(t_b, U_b, W1, W2, anchor, T, draft_tokens_b, L, u_accept_b, u
         raise ValueError("verify length out of range")
     prevs = [int(anchor)] + [int(x) for x in draft_tokens_b[: g - 1]]
     p_rows = [target_distribution(t_b[j], T) for j in range(L + 1)]
-    q_rows = [draft_distribution(U_b[j], W1, W2, prevs[j], T) for j in range(L)]
+    if a_rows is None:
+        q_rows = [draft_distribution(U_b[j], W1, W2, prevs[j], T) for j in range(L)]
+    else:
+        W2f = np.asarray(W2, dtype=np.float64)
+        q_rows = [softmax_with_lse((np.asarray(U_b[j], dtype=np.float64)
+                                    + np.asarray(a_rows[j], dtype=np.float64) @ W2f) / float(T))
+                  for j in range(L)]
 
     alpha = np.full(g, np.nan)
     p_tok = np.full(g, np.nan)
