@@ -129,6 +129,9 @@ typedef struct {
   float* alpha;               /* out [B][gamma] sum_v min(p_j, q_j), j < L_b; NaN beyond */
   float* p_tok;               /* optional out [B][gamma] p_j(x_{j+1}), j < L_b; NaN beyond */
   uint32_t* dev_status;       /* out uint32_t[4], zeroed by the call            */
+  const void* a_rows;         /* optional [gamma][B][r] (dtype): the draft head's
+                                 factor rows a_j (spec_rnn_draft); NULL = the
+                                 Markov head's W1[x_j]                          */
   float* diag;                /* optional out [B][4]: final draw's first-pass
                                  margins u - F(c-1), F(c) - u (in the normalised
                                  residual or bonus distribution), the band, and
@@ -153,6 +156,30 @@ int32_t spec_markov_draft(const spec_draft_args* args, spec_stream_t stream);
 /* Verify one drafted block per request.  Writes accept_len, out_tokens,
  * alpha, dev_status (and p_tok, diag when non-NULL).                        */
 int32_t spec_verify(const spec_verify_args* args, spec_stream_t stream);
+
+/* ------------------------------------------------------------- RNN head */
+/* DSpark's RNN head ("[논문리뷰] DSpark", section 1.2, "RNN head"): a state s_k
+ * (s_0 = 0) carries the block's prefix; with z = [s_j; W1[x_j]; h_{j+1}] the
+ * draft row j uses the factor a_j = tanh(W_o z) in place of the Markov head's
+ * W1[x_j] (bias a_j W2) and updates s_{j+1} = sigma(W_g z) s_j +
+ * (1 - sigma(W_g z)) tanh(W_c z).  The h block of z enters the gates linearly
+ * and does not depend on drafted tokens: its three projections arrive as
+ * hproj (formed with U by the parallel stage).  s and a are held in `dtype`
+ * (each the exactly rounded value of the step's float64 result; the kernel
+ * certifies every rounding or recomputes it in double-float).
+ * Work: as spec_markov_draft (3 memsets + 1 cooperative launch), with one
+ * more phase and grid barrier per step.  Writes a_rows, which spec_verify
+ * takes to rebuild q.  Same limits as spec_markov_draft; Wr, hproj and
+ * a_rows 16-byte aligned.                                                   */
+typedef struct {
+  spec_draft_args draft;      /* as for spec_markov_draft                       */
+  const void* Wr;             /* [3r][2r] (dtype): rows g, c, o of the gates; columns
+                                 act on s, then on W1[x]                         */
+  const float* hproj;         /* [B][gamma][3][r]: (W_g^h h, W_c^h h, W_o^h h) of
+                                 draft row j = h_{j+1}                           */
+  void* a_rows;               /* out [gamma][B][r] (dtype)                      */
+} spec_rnn_draft_args;
+int32_t spec_rnn_draft(const spec_rnn_draft_args* args, spec_stream_t stream);
 
 /* ------------------------------------------- draft without caller scratch */
 /* No counterpart on the pages: this is a deployment convenience.

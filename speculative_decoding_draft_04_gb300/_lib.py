@@ -23,7 +23,8 @@ EXPORTED = ("spec_workspace_bytes", "spec_markov_draft", "spec_markov_draft_stat
             "spec_verify", "spec_status_string",
             "spec_set_option", "spec_profile_enable", "spec_profile_read", "spec_stage_name",
             "spec_num_stages", "spec_operating_point", "spec_acceptance_stats",
-            "spec_confidence", "spec_schedule_workspace_bytes", "spec_prefix_schedule")
+            "spec_confidence", "spec_schedule_workspace_bytes", "spec_prefix_schedule",
+            "spec_rnn_draft")
 
 
 class SpecError(RuntimeError):
@@ -46,7 +47,11 @@ class VerifyArgs(ctypes.Structure):
                 ("temperature", _vp), ("draft_tokens", _vp), ("q_tok", _vp), ("lse_q", _vp),
                 ("verify_len", _vp), ("u_accept", _vp), ("u_final", _vp), ("accept_len", _vp),
                 ("out_tokens", _vp), ("alpha", _vp), ("p_tok", _vp), ("dev_status", _vp),
-                ("diag", _vp), ("workspace", _vp), ("workspace_bytes", _sz)]
+                ("a_rows", _vp), ("diag", _vp), ("workspace", _vp), ("workspace_bytes", _sz)]
+
+
+class RnnDraftArgs(ctypes.Structure):
+    _fields_ = [("draft", DraftArgs), ("Wr", _vp), ("hproj", _vp), ("a_rows", _vp)]
 
 
 _LIB = None
@@ -111,6 +116,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.spec_operating_point.argtypes = [ctypes.POINTER(OpArgs), ctypes.POINTER(OpResult)]
     L.spec_acceptance_stats.restype = _i32
     L.spec_acceptance_stats.argtypes = [_i32, _i32, _vp, _vp, _vp, _vp, _vp]
+    L.spec_rnn_draft.restype = _i32
+    L.spec_rnn_draft.argtypes = [ctypes.POINTER(RnnDraftArgs), _vp]
     L.spec_confidence.restype = _i32
     L.spec_confidence.argtypes = [ctypes.POINTER(ConfidenceArgs), _vp]
     L.spec_schedule_workspace_bytes.restype = _sz
@@ -190,14 +197,15 @@ def spec_markov_draft_static(U, W1, W2, anchor, temperature, u_draft, draft_toke
 
 def spec_verify(target, U, W1, W2, anchor, temperature, draft_tokens, q_tok, lse_q, verify_len,
                 u_accept, u_final, accept_len, out_tokens, alpha, dev_status, workspace,
-                p_tok=None, diag=None, stream=None) -> None:
-    """Enqueue the verification (shapes as in include/spec.h)."""
+                p_tok=None, diag=None, stream=None, a_rows=None) -> None:
+    """Enqueue the verification (shapes as in include/spec.h); ``a_rows`` are
+    the RNN head's factor rows (None: the Markov head)."""
     B, gamma, V = U.shape
     a = VerifyArgs(B, gamma, V, W1.shape[1], _dtype_code(U), _ptr(target), _ptr(U), _ptr(W1),
                    _ptr(W2), _ptr(anchor), _ptr(temperature), _ptr(draft_tokens), _ptr(q_tok),
                    _ptr(lse_q), _ptr(verify_len), _ptr(u_accept), _ptr(u_final),
                    _ptr(accept_len), _ptr(out_tokens), _ptr(alpha), _ptr(p_tok),
-                   _ptr(dev_status), _ptr(diag), _ptr(workspace),
+                   _ptr(dev_status), _ptr(a_rows), _ptr(diag), _ptr(workspace),
                    workspace.numel() * workspace.element_size())
     _check(lib().spec_verify(ctypes.byref(a), _stream(stream)), "spec_verify")
 
@@ -253,3 +261,15 @@ def spec_prefix_schedule(conf, sps, survival, verify_len, totals, theta, dev_sta
                      _ptr(verify_len), _ptr(totals), _ptr(theta), _ptr(dev_status),
                      _ptr(workspace), workspace.numel() * workspace.element_size())
     _check(lib().spec_prefix_schedule(ctypes.byref(a), _stream(stream)), "spec_prefix_schedule")
+
+
+def spec_rnn_draft(U, W1, W2, Wr, hproj, anchor, temperature, u_draft, draft_tokens, q_tok,
+                   lse_q, a_rows, dev_status, workspace, diag=None, stream=None) -> None:
+    """Enqueue the RNN head draft (shapes as in include/spec.h)."""
+    B, gamma, V = U.shape
+    d = DraftArgs(B, gamma, V, W1.shape[1], _dtype_code(U), _ptr(U), _ptr(W1), _ptr(W2),
+                  _ptr(anchor), _ptr(temperature), _ptr(u_draft), _ptr(draft_tokens),
+                  _ptr(q_tok), _ptr(lse_q), _ptr(dev_status), _ptr(diag), _ptr(workspace),
+                  workspace.numel() * workspace.element_size())
+    a = RnnDraftArgs(d, _ptr(Wr), _ptr(hproj), _ptr(a_rows))
+    _check(lib().spec_rnn_draft(ctypes.byref(a), _stream(stream)), "spec_rnn_draft")

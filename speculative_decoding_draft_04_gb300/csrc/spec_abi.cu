@@ -12,7 +12,8 @@ namespace spec {
 template <typename DT>
 cudaError_t launch_draft_persistent(const Shape&, const void*, const void*, const void*, const int*,
                                     const float*, const float*, int*, float*, double*, float*,
-                                    uint32_t*, const Ws&, const Eps&, int, int, cudaStream_t);
+                                    uint32_t*, const Ws&, const Eps&, int, int, cudaStream_t,
+                                    const RnnParams*);
 cudaError_t launch_verify_prep(const Shape&, const int*, const float*, const int*, const double*,
                                const int*, const Ws&, uint32_t*, int*, int*, float*, float*,
                                cudaStream_t);
@@ -142,7 +143,7 @@ int num_sms() {
 // Residual re-decisions whose weights are kept between their two passes.
 constexpr int kHpwItems = 16;
 struct Layout {
-  size_t ctrl, trace, items, hpsum, hpcnt, hpw, hpnorm, dpart, rowptr, prow, prevtok, vflags, lse_p, bpart, vpart, slow,
+  size_t ctrl, trace, items, hpsum, hpcnt, hpw, hpnorm, rnnst, dpart, rowptr, prow, prevtok, vflags, lse_p, bpart, vpart, slow,
       accbits, rowc, rowp, total;
   int max_items, hpw_items;
 };
@@ -165,6 +166,7 @@ Layout layout(const Shape& sh) {
   L.hpw_items = sh.B < kHpwItems ? sh.B : kHpwItems;
   L.hpw = take((size_t)L.hpw_items * sh.V * sizeof(float4));
   L.hpnorm = take((size_t)L.max_items * sizeof(float4));
+  L.rnnst = take((size_t)2 * sh.B * sh.r * sizeof(float));    // RNN head state ping-pong
   L.dpart = take(B * sh.NC * sizeof(float4));
   L.rowptr = take((B + 1) * sizeof(int));
   L.prow = take(B * g * sizeof(int2));
@@ -232,6 +234,8 @@ Shape make_shape(int B, int gamma, int V, int r) {
   s.NC = (V + CW - 1) / CW;
   s.NSV = (V + VB - 1) / VB;
   s.HB = (V + HPB - 1) / HPB;
+  s.rnn = 0;
+  s.NA = V;
   return s;
 }
 
@@ -243,7 +247,8 @@ Shape make_shape(int B, int gamma, int V, int r) {
 // The whole draft: one cooperative launch (the control words are zeroed first
 // on the same stream; the grid barrier counts on it).
 template <typename DT>
-int launch_draft(const spec_draft_args* a, const Shape& sh, const Ws& ws, cudaStream_t st) {
+int launch_draft(const spec_draft_args* a, const Shape& sh, const Ws& ws, cudaStream_t st,
+                 const RnnParams* rnn = nullptr) {
   int path;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -255,8 +260,24 @@ int launch_draft(const spec_draft_args* a, const Shape& sh, const Ws& ws, cudaSt
   ProfScope p(st, ST_DRAFT_PERSISTENT);
   SPEC_TRY(launch_draft_persistent<DT>(sh, a->U, a->W1, a->W2, a->anchor, a->temperature, a->u_draft,
                                        a->draft_tokens, a->q_tok, a->lse_q, a->diag, a->dev_status,
-                                       ws, current_eps(), path, num_sms(), st));
+                                       ws, current_eps(), path, num_sms(), st, rnn));
   return SPEC_OK;
+}
+
+template <typename DT>
+int run_rnn_draft(const spec_rnn_draft_args* ra, cudaStream_t st) {
+  const spec_draft_args* a = &ra->draft;
+  Shape sh = make_shape(a->B, a->gamma, a->V, a->r);
+  sh.rnn = 1;
+  sh.NA = a->gamma * a->B;
+  const Layout L = layout(sh);
+  const Ws ws = views(L, a->workspace);
+  RnnParams rp;
+  rp.Wr = ra->Wr;
+  rp.hproj = ra->hproj;
+  rp.arows = ra->a_rows;
+  rp.state = static_cast<unsigned char*>(a->workspace) + L.rnnst;
+  return launch_draft<DT>(a, sh, ws, st, &rp);
 }
 
 template <typename DT>
@@ -274,7 +295,12 @@ int run_draft(const spec_draft_args* a, cudaStream_t st) {
 
 template <typename DT>
 int run_verify(const spec_verify_args* a, cudaStream_t st) {
-  const Shape sh = make_shape(a->B, a->gamma, a->V, a->r);
+  Shape sh = make_shape(a->B, a->gamma, a->V, a->r);
+  if (a->a_rows) {                 // RNN head: factor rows from the draft
+    sh.rnn = 1;
+    sh.NA = a->gamma * a->B;
+  }
+  const void* F = a->a_rows ? a->a_rows : a->W1;
   const Layout L = layout(sh);
   const Ws ws = views(L, a->workspace);
   const Eps eps = current_eps();
@@ -284,7 +310,7 @@ int run_verify(const spec_verify_args* a, cudaStream_t st) {
     path = g_force_simt ? 0 : g_bias_path;
   }
   const int grid = grid_for_refine();
-  HpRows R{a->target, a->U, a->W1, a->W2, a->temperature};
+  HpRows R{a->target, a->U, F, a->W2, a->temperature};
   SPEC_TRY(cudaMemsetAsync(a->dev_status, 0, 4 * sizeof(uint32_t), st));
   {
     ProfScope p(st, ST_VERIFY_PREP);
@@ -298,11 +324,11 @@ int run_verify(const spec_verify_args* a, cudaStream_t st) {
   }
   {
     ProfScope p(st, ST_VERIFY_TILE);
-    SPEC_TRY(launch_verify_tile<DT>(sh, a->target, a->U, a->W1, a->W2, ws, path, a->dev_status, st));
+    SPEC_TRY(launch_verify_tile<DT>(sh, a->target, a->U, F, a->W2, ws, path, a->dev_status, st));
   }
   {
     ProfScope p(st, ST_VERIFY_FINAL);
-    SPEC_TRY(launch_verify_final<DT>(sh, a->target, a->U, a->W1, a->W2, a->anchor, a->temperature,
+    SPEC_TRY(launch_verify_final<DT>(sh, a->target, a->U, F, a->W2, a->anchor, a->temperature,
                                      a->draft_tokens, a->q_tok, a->lse_q, a->verify_len,
                                      a->u_accept, a->u_final, a->accept_len, a->out_tokens,
                                      a->alpha, a->p_tok, a->diag, a->dev_status, ws, eps, st));
@@ -434,13 +460,36 @@ int32_t spec_verify(const spec_verify_args* a, spec_stream_t stream) {
       !aligned(a->q_tok, 4) || !aligned(a->lse_q, 8) || !aligned(a->verify_len, 4) ||
       !aligned(a->u_accept, 4) || !aligned(a->u_final, 4) || !aligned(a->accept_len, 4) ||
       !aligned(a->out_tokens, 4) || !aligned(a->alpha, 4) || !aligned(a->dev_status, 4) ||
-      (a->p_tok && !aligned(a->p_tok, 4)) || (a->diag && !aligned(a->diag, 4)))
+      (a->p_tok && !aligned(a->p_tok, 4)) || (a->diag && !aligned(a->diag, 4)) ||
+      (a->a_rows && !aligned(a->a_rows, 16)))
     return SPEC_EALIGN;
   const size_t need = layout(make_shape(a->B, a->gamma, a->V, a->r)).total;
   if (!a->workspace || a->workspace_bytes < need) return SPEC_EWORKSPACE;
   if (!aligned(a->workspace, 256)) return SPEC_EALIGN;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return a->dtype == SPEC_BF16 ? run_verify<bf16>(a, st) : run_verify<float>(a, st);
+}
+
+int32_t spec_rnn_draft(const spec_rnn_draft_args* ra, spec_stream_t stream) {
+  if (!ra) return SPEC_EINVAL;
+  const spec_draft_args* a = &ra->draft;
+  int rc = check_shape(a->B, a->gamma, a->V, a->r, a->dtype);
+  if (rc != SPEC_OK) return rc;
+  if (!a->U || !a->W1 || !a->W2 || !a->anchor || !a->temperature || !a->u_draft ||
+      !a->draft_tokens || !a->q_tok || !a->lse_q || !a->dev_status || !ra->Wr || !ra->hproj ||
+      !ra->a_rows)
+    return SPEC_EINVAL;
+  if (!aligned(a->U, 16) || !aligned(a->W1, 16) || !aligned(a->W2, 16) || !aligned(a->anchor, 4) ||
+      !aligned(a->temperature, 4) || !aligned(a->u_draft, 4) || !aligned(a->draft_tokens, 4) ||
+      !aligned(a->q_tok, 4) || !aligned(a->lse_q, 8) || !aligned(a->dev_status, 4) ||
+      (a->diag && !aligned(a->diag, 4)) || !aligned(ra->Wr, 16) || !aligned(ra->hproj, 16) ||
+      !aligned(ra->a_rows, 16))
+    return SPEC_EALIGN;
+  const size_t need = layout(make_shape(a->B, a->gamma, a->V, a->r)).total;
+  if (!a->workspace || a->workspace_bytes < need) return SPEC_EWORKSPACE;
+  if (!aligned(a->workspace, 256)) return SPEC_EALIGN;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return a->dtype == SPEC_BF16 ? run_rnn_draft<bf16>(ra, st) : run_rnn_draft<float>(ra, st);
 }
 
 int32_t spec_markov_draft_static(const spec_draft_args* a, spec_stream_t stream) {

@@ -14,6 +14,8 @@
 // polynomial, a table of 2^(j/64)), carried out in double-float.
 #pragma once
 
+#include <string.h>
+
 #include <math.h>
 #include <stdint.h>
 
@@ -231,6 +233,43 @@ SPEC_HD df dd_sigmoid(df z, const df* tab) {
   const df e = dd_exp(neg ? z : dd_neg(z), tab);
   const df den = dd_add_f(e, 1.0f);
   return dd_div(neg ? e : df{1.0f, 0.f}, den);
+}
+
+// tanh(x) in double-float: (1 - e) / (1 + e) with e = e^{-2|x|} (no overflow),
+// the sign restored.  Below |x| = 2^-5, where 1 - e would cancel, the Taylor
+// series x (1 - x^2/3 + 2x^4/15 - 17x^6/315) instead (the next term is below
+// 2e-14 relative; 1/3 is carried as a double-float).
+SPEC_HD df dd_tanh(df x, const df* tab) {
+  if (fabsf(x.hi) < 0.03125f) {
+    const df t = dd_mul(x, x);
+    df p = dd_add_f(dd_mul_f(t, -17.0f / 315.0f), 2.0f / 15.0f);
+    p = dd_add(dd_mul(p, t), df{-0.333333343f, 9.93410776e-09f});
+    return dd_add(x, dd_mul(x, dd_mul(p, t)));
+  }
+  const bool neg = x.hi < 0.f;
+  const df ax = neg ? dd_neg(x) : x;
+  const df e = dd_exp(dd_mul_f(ax, -2.0f), tab);
+  const df t = dd_div(dd_add_f(dd_neg(e), 1.0f), dd_add_f(e, 1.0f));
+  return neg ? dd_neg(t) : t;
+}
+
+// Bit pattern of the bfloat16 nearest (ties to even) to the finite value
+// hi + lo of a normalised double-float.  hi's own rounding is right unless hi
+// is exactly halfway between two bfloat16 values; then lo (|lo| < half an fp32
+// ulp of hi) decides, and only lo == 0 is a true tie.
+SPEC_HD uint16_t dd_to_bf16_bits(df v) {
+  uint32_t u;
+  memcpy(&u, &v.hi, 4);
+  if ((u & 0xffffu) == 0x8000u && v.lo != 0.f) {
+    const bool up = (v.lo > 0.f) == (v.hi > 0.f);          // away from zero
+    return (uint16_t)((up ? u + 0x8000u : u) >> 16);
+  }
+  return (uint16_t)((u + 0x7fffu + ((u >> 16) & 1u)) >> 16);
+}
+SPEC_HD uint16_t f32_to_bf16_bits(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return (uint16_t)((u + 0x7fffu + ((u >> 16) & 1u)) >> 16);
 }
 
 // log(z) for a positive double-float: the fp32 logarithm plus one Newton

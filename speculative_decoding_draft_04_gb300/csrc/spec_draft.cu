@@ -23,6 +23,7 @@
 
 #include "spec_tile_tc.cuh"
 #include "spec_hp.cuh"
+#include "spec_rnn.cuh"
 #include "spec_tmap.cuh"
 
 namespace spec {
@@ -48,7 +49,7 @@ __device__ void draft_tile_body(const Shape& sh, int k, int slice, int mtile, co
     if (m < nrows) {
       int b = m0 + m;
       t = (k == 0) ? anchor[b] : __ldcg(tokens + (size_t)b * sh.gamma + k - 1);
-      t = min(max(t, 0), sh.V - 1);          // bad tokens are reported by the sampler
+      t = factor_row(sh, b, k, min(max(t, 0), sh.V - 1));   // bad tokens: reported by the sampler
       s_off[m] = ((size_t)b * sh.gamma + k) * sh.V;
     } else {
       s_off[m] = 0;
@@ -178,6 +179,7 @@ struct DraftEpi {
   __device__ int token(int mt, int m) const {
     const int b = mt * TC_M + m;
     if (b >= sh.B) return -1;
+    if (sh.rnn) return k * sh.B + b;
     const int t = (k == 0) ? anchor[b] : __ldcg(tokens + (size_t)b * sh.gamma + k - 1);
     return min(max(t, 0), sh.V - 1);          // bad tokens are reported by the sampler
   }
@@ -264,7 +266,8 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
     }
     return;
   }
-  for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf(W1 + (size_t)prev * sh.r + i);
+  const int arow = factor_row(sh, b, k, prev);
+  for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf(W1 + (size_t)arow * sh.r + i);
   const float invT = 1.0f / T;
   const float4* P = ws.dpart + (size_t)b * sh.NC;
 
@@ -438,7 +441,7 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
       uint32_t it = atomicAdd(counter, 1u);
       if ((int)it < ws.max_items) {
         HpItem h;
-        h.b = b; h.j = k; h.kind = HP_DRAFT; h.prev = prev; h.u = u; h.fast_token = tok;
+        h.b = b; h.j = k; h.kind = HP_DRAFT; h.prev = arow; h.u = u; h.fast_token = tok;
         h.shift_q = lse; h.shift_p = 0.0;
         ws.items[it] = h;
       } else {
@@ -466,6 +469,7 @@ struct DraftParams {
   uint32_t* status;
   Ws ws;
   Eps eps;
+  RnnParams rnn;     // RNN head (sh.rnn): gates before each step's tiles
 };
 
 // The whole draft in one cooperative launch: for each step k, the tile phase
@@ -482,7 +486,8 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
   __shared__ int s_fail;
   const Shape& sh = P.sh;
   const DT* U = (const DT*)P.U;
-  const DT* W1 = (const DT*)P.W1;
+  // factor rows of the bias: W1 (Markov head) or the RNN head's a_k rows
+  const DT* W1 = sh.rnn ? (const DT*)P.rnn.arows : (const DT*)P.W1;
   const DT* W2 = (const DT*)P.W2;
   uint32_t* ctrl = P.ws.ctrl;
   TpState st{0u, s_bar, &s_fail, 0u, 0u};
@@ -499,13 +504,17 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
     st.tmem = s_holder;
   }
   uint32_t gen = threadIdx.x == 0 ? ld_acquire_gpu(ctrl + CTRL_BAR_GEN) : 0u;
-  const HpRows R{P.U, P.U, P.W1, P.W2, P.temp};
+  const HpRows R{P.U, P.U, W1, P.W2, P.temp};
   const int n_mt = (sh.B + BM - 1) / BM;
   const int n_tiles = sh.NS * n_mt;
   const uint32_t G = gridDim.x;
   unsigned long long* tr = (P.ws.trace && blockIdx.x == 0 && threadIdx.x == 0) ? P.ws.trace : nullptr;
   for (int k = 0; k < sh.gamma; ++k) {
     bool ok = true;
+    if (sh.rnn) {
+      rnn_gates_body<DT>(sh, k, (const DT*)P.W1, P.anchor, P.tokens, P.rnn, smem_raw);
+      if (!grid_sync(ctrl, G, gen, P.status)) break;
+    }
     if (tr) tr[k * TRACE_SLOTS + 0] = globaltimer_ns();
     if constexpr (PATH == 2) {
       const DraftEpi e{sh, k, P.anchor, P.tokens, P.temp, P.ws.dpart, &P.maps.u};
@@ -557,6 +566,13 @@ static cudaError_t launch_persist(const DraftParams& P, int nsm, cudaStream_t st
   size_t smem = PATH == 2 ? TpLayout(P.sh.r, BN).total : TileLayout<DT>(BM, P.sh.r, false).total;
   const size_t slab = (size_t)P.sh.r * HPB * sizeof(DT);    // re-decision W2 slab (> sampler's)
   smem = smem > slab ? smem : slab;
+  if (P.sh.rnn) {
+    // gate phase: one fallback-list int per (request, state index) of a CTA,
+    // B * ceil(r / G) at most, with G >= min(B, nsm) CTAs
+    const size_t B = P.sh.B, r = P.sh.r, n = (size_t)nsm;
+    const size_t ints = B <= n ? r + B : ((r + n - 1) / n + 1) * B;
+    smem = smem > ints * sizeof(int) ? smem : ints * sizeof(int);
+  }
   auto kern = draft_persistent_kernel<DT, BM, PATH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -588,9 +604,11 @@ cudaError_t launch_draft_persistent(const Shape& sh, const void* U, const void* 
                                     const int* anchor, const float* temp, const float* u_draft,
                                     int* tokens, float* q_tok, double* lse_q, float* diag,
                                     uint32_t* status, const Ws& ws, const Eps& eps, int path,
-                                    int nsm, cudaStream_t st) {
+                                    int nsm, cudaStream_t st, const RnnParams* rnn) {
   DraftParams P;
   memset(&P.maps, 0, sizeof(P.maps));
+  memset(&P.rnn, 0, sizeof(P.rnn));
+  if (rnn) P.rnn = *rnn;
   P.sh = sh;
   P.U = U;
   P.W1 = W1;
@@ -628,11 +646,11 @@ template cudaError_t launch_draft_persistent<float>(const Shape&, const void*, c
                                                     const void*, const int*, const float*,
                                                     const float*, int*, float*, double*, float*,
                                                     uint32_t*, const Ws&, const Eps&, int, int,
-                                                    cudaStream_t);
+                                                    cudaStream_t, const RnnParams*);
 template cudaError_t launch_draft_persistent<bf16>(const Shape&, const void*, const void*,
                                                    const void*, const int*, const float*,
                                                    const float*, int*, float*, double*, float*,
                                                    uint32_t*, const Ws&, const Eps&, int, int,
-                                                   cudaStream_t);
+                                                   cudaStream_t, const RnnParams*);
 
 }  // namespace spec

@@ -25,7 +25,15 @@ constexpr int MAX_GAMMA = 16;
 struct Shape {
   int B, gamma, V, r, NS, NC, NSV, HB;   // NS = ceil(V / BN), NC = ceil(V / CW),
                                           // NSV = ceil(V / VB), HB = ceil(V / HPB)
+  int rnn;     // 0: Markov head, factor rows W1[x_j]; 1: RNN head, factor rows [gamma][B]
+  int NA;      // rows of the factor table: V (Markov) or gamma * B (RNN)
 };
+
+// Row of the transition-factor table for draft row j of request b: the Markov
+// head's W1[x_j] (x_0 = the anchor) or the RNN head's a_j row of request b.
+__device__ __forceinline__ int factor_row(const Shape& sh, int b, int j, int prev_token) {
+  return sh.rnn ? j * sh.B + b : prev_token;
+}
 
 // A decision queued for re-decision in extended precision.
 enum HpKind { HP_DRAFT = 0, HP_BONUS = 1, HP_RESID = 2 };
@@ -74,6 +82,14 @@ struct Ws {
   uint32_t* accbits;    // [B] first-pass ratio-test outcomes
   float4* rowc;         // [B*gamma] packed row: 1/T and -lse_q as double-float pairs
   float2* rowp;         // [B][gamma+1] -lse_p as a double-float pair
+};
+
+// RNN head inputs and outputs of the draft (all null for the Markov head).
+struct RnnParams {
+  const void* Wr;        // [3r][2r] storage type
+  const float* hproj;    // [B][gamma][3][r]
+  void* arows;           // [gamma][B][r] storage type, out: the factor rows a_k
+  void* state;           // [2][B][r] storage type, scratch (s_k ping-pong)
 };
 
 // Inputs the extended-precision kernels read.

@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(NT) slow_verify_kernel(
       if ((flags >> j) & 1u) {
         ++nhp;
         const int x = dtok[(size_t)b * sh.gamma + j];
-        const int prev = j == 0 ? anchor[b] : dtok[(size_t)b * sh.gamma + j - 1];
+        const int prev = factor_row(sh, b, j, j == 0 ? anchor[b] : dtok[(size_t)b * sh.gamma + j - 1]);
         HpItem ip; ip.b = b; ip.j = j; ip.kind = HP_BONUS; ip.prev = prev; ip.u = 0.f;
         ip.fast_token = -1; ip.shift_q = lse_q[(size_t)b * sh.gamma + j];
         ip.shift_p = ws.lse_p[(size_t)b * (sh.gamma + 1) + j];
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(NT) slow_verify_kernel(
     const int row = n;
     const bool resid = n < L;
     HpItem ip; ip.b = b; ip.j = row; ip.kind = HP_BONUS; ip.u = u_fin[b]; ip.fast_token = -1;
-    ip.prev = row == 0 ? anchor[b] : dtok[(size_t)b * sh.gamma + row - 1];
+    ip.prev = factor_row(sh, b, row, row == 0 ? anchor[b] : dtok[(size_t)b * sh.gamma + row - 1]);
     ip.shift_p = ws.lse_p[(size_t)b * (sh.gamma + 1) + row];
     ip.shift_q = resid ? lse_q[(size_t)b * sh.gamma + row] : 0.0;
     HpItem iq = ip; iq.kind = HP_DRAFT;

@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(NT) verify_prep_kernel(
     for (int j = 0; j < MAX_GAMMA; ++j) {
       if (j < L) {
         ws.prow[run + j] = make_int2(b, j);
-        ws.prevtok[run + j] = j == 0 ? a : xs[j - 1 < 0 ? 0 : j - 1];
+        ws.prevtok[run + j] = factor_row(sh, b, j, j == 0 ? a : xs[j - 1 < 0 ? 0 : j - 1]);
         const df nlq = d2df(-lq[j]);
         ws.rowc[run + j] = make_float4(it.hi, it.lo, nlq.hi, nlq.lo);
       }
@@ -437,7 +437,7 @@ struct VerifyEpi {
 
   __device__ int token(int mt, int m) const {
     const int p = mt * TC_M + m;
-    return p < P ? min(max(ws.prevtok[p], 0), sh.V - 1) : -1;
+    return p < P ? min(max(ws.prevtok[p], 0), sh.NA - 1) : -1;
   }
   // Row offsets of the producer lane's rows (lane + 32 i) for request tile
   // `cmt`, refreshed when the request tile changes.
@@ -767,7 +767,7 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
   const int sl = s_slice;
   const int n0 = sl * VB;
   const df pref = {s_pref[0], s_pref[1]};
-  const int prev = row == 0 ? anchor[b] : dtok[(size_t)b * sh.gamma + row - 1];
+  const int prev = factor_row(sh, b, row, row == 0 ? anchor[b] : dtok[(size_t)b * sh.gamma + row - 1]);
 
   // ---- recompute the crossing slice
   const DT* trow = target + ((size_t)b * (sh.gamma + 1) + row) * sh.V;

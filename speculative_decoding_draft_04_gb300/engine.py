@@ -11,7 +11,7 @@ import dataclasses
 import numpy as np
 
 from . import _lib
-from .workloads import ScheduleInputs, Workload
+from .workloads import RnnInputs, ScheduleInputs, Workload
 
 
 def _dev_logits(arr: np.ndarray, dtype: str, device):
@@ -169,6 +169,37 @@ def scheduled_cycle(d: DeviceWorkload, b: Buffers, s: DeviceSchedule, stream=Non
     draft(d, b, stream)
     schedule(d, b, s, stream)
     verify(d, b, stream, verify_len=s.verify_len)
+
+
+@dataclasses.dataclass
+class DeviceRnn:
+    """RNN head inputs on the device and its factor rows (draft output)."""
+    Wr: object
+    hproj: object
+    a_rows: object
+
+    @classmethod
+    def from_inputs(cls, s: RnnInputs, d: DeviceWorkload, device="cuda") -> "DeviceRnn":
+        import torch
+        a = torch.empty((d.gamma, d.B, d.r), dtype=d.W1.dtype, device=device)
+        return cls(Wr=_dev_logits(s.Wr, d.dtype, device),
+                   hproj=torch.from_numpy(np.ascontiguousarray(s.hproj)).to(device), a_rows=a)
+
+
+def rnn_draft(d: DeviceWorkload, b: Buffers, h: DeviceRnn, stream=None) -> None:
+    _lib.spec_rnn_draft(d.U, d.W1, d.W2, h.Wr, h.hproj, d.anchor, d.temperature, d.u_draft,
+                        b.draft_tokens, b.q_tok, b.lse_q, h.a_rows, b.dstatus, b.workspace,
+                        diag=b.ddiag, stream=stream)
+
+
+def rnn_cycle(d: DeviceWorkload, b: Buffers, h: DeviceRnn, stream=None) -> None:
+    """One speculative cycle with the RNN head: draft, then verify with its
+    factor rows."""
+    rnn_draft(d, b, h, stream)
+    _lib.spec_verify(d.target, d.U, d.W1, d.W2, d.anchor, d.temperature, b.draft_tokens, b.q_tok,
+                     b.lse_q, d.verify_len, d.u_accept, d.u_final, b.accept_len, b.out_tokens,
+                     b.alpha, b.vstatus, b.workspace, p_tok=b.p_tok, diag=b.vdiag, stream=stream,
+                     a_rows=h.a_rows)
 
 
 def status_words(t) -> list[int]:

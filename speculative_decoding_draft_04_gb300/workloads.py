@@ -54,6 +54,17 @@ review, sections 2.1 and 2.2), from ``default_rng([seed_index, trial, 2])``:
 
 Draw order: mu, w, then hidden per request.
 
+RNN head inputs (``make_rnn_inputs``, DSpark review, section 1.2 "RNN head"),
+from ``default_rng([seed_index, trial, 3])``:
+
+* ``Wr [3r, 2r]`` (storage dtype): rows g, c, o of the gates' recurrent part;
+  columns [0, r) act on the state, N(0, 1/r); columns [r, 2r) on W1[x],
+  N(0, 1/(r w_sd^2)) (so that part of each pre-activation has unit variance);
+* ``hproj [B, gamma, 3, r]`` float32: the parallel stage's projections of
+  h_k into the three gates, N(0, 1).
+
+Draw order: Wr, then hproj per request.
+
 bf16 storage is round-to-nearest-even from float64, done directly (no
 intermediate float32 rounding).
 """
@@ -310,6 +321,26 @@ def make_schedule_inputs(spec: dict[str, Any], trial: int = 0, *,
         h[:, 0] = mu[b]
         hidden[b] = _store(h, dtype)
     return ScheduleInputs(d=d, hidden=hidden, w=w.astype(np.float32), sps=cost_table(Bn, g))
+
+
+@dataclasses.dataclass
+class RnnInputs:
+    Wr: np.ndarray          # [3r, 2r] storage dtype
+    hproj: np.ndarray       # float32 [B, gamma, 3, r]
+
+
+def make_rnn_inputs(spec: dict[str, Any], trial: int = 0, *, B: int | None = None) -> RnnInputs:
+    """RNN head inputs of one workload (see the module docstring)."""
+    Bn = int(spec["B"] if B is None else B)
+    g, r = int(spec["gamma"]), int(spec["r"])
+    rng = np.random.default_rng([int(spec["seed_index"]), int(trial), 3])
+    Wr = np.empty((3 * r, 2 * r))
+    Wr[:, :r] = rng.normal(0.0, 1.0 / np.sqrt(r), size=(3 * r, r))
+    Wr[:, r:] = rng.normal(0.0, 1.0 / (np.sqrt(r) * float(spec["w_sd"])), size=(3 * r, r))
+    hproj = np.empty((Bn, g, 3, r), dtype=np.float32)
+    for b in range(Bn):
+        hproj[b] = rng.normal(0.0, 1.0, size=(g, 3, r)).astype(np.float32)
+    return RnnInputs(Wr=_store(Wr, spec["dtype"]), hproj=hproj)
 
 
 def shard_rows(B: int, rank: int, world: int) -> np.ndarray:

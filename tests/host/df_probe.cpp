@@ -12,6 +12,8 @@
 //   dot2 <n> <a..> <w..>       -> hi lo of the Dot2 dot product (hex floats)
 //   div <ah> <al> <bh> <bl>    -> hi lo of the double-float quotient
 //   sig <zh> <zl>              -> hi lo of 1 / (1 + e^{-(zh + zl)})
+//   tanh <zh> <zl>             -> hi lo of tanh(zh + zl)
+//   bf16 <hi hex> <lo hex>     -> "<bf16 bits> 0": nearest bfloat16 of hi + lo
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -73,6 +75,14 @@ int main() {
       float zh, zl;
       if (std::scanf("%f %f", &zh, &zl) != 2) return 1;
       std::printf("%.17g 0\n", spec::dd_log(df{zh, zl}, tab));
+    } else if (c == "tanh") {
+      float zh, zl;
+      if (std::scanf("%f %f", &zh, &zl) != 2) return 1;
+      put(spec::dd_tanh(df{zh, zl}, tab));
+    } else if (c == "bf16") {
+      unsigned long h, l;
+      if (std::scanf("%lx %lx", &h, &l) != 2) return 1;
+      std::printf("%u 0\n", (unsigned)spec::dd_to_bf16_bits(df{from_bits(h), from_bits(l)}));
     } else if (c == "sig") {
       float zh, zl;
       if (std::scanf("%f %f", &zh, &zl) != 2) return 1;

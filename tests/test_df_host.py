@@ -186,3 +186,56 @@ def test_sigmoid(probe):
     c32 = (hi + lo).astype(np.float32)
     ref = 1 / (1 + np.exp(-z))
     assert np.mean(c32 == ref.astype(np.float32)) > 0.999
+
+
+def test_tanh(probe):
+    """tanh to about 1e-12 relative from 1e-8 to saturation (50-digit decimal pin)."""
+    getcontext().prec = 50
+    rng = np.random.default_rng(10)
+    mag = np.concatenate([10 ** rng.uniform(-8, 1.7, 3000), [1e-4, 9.9e-5, 1.01e-4, 0.5, 30.0, 60.0]])
+    z = _split(mag * rng.choice([-1.0, 1.0], size=mag.size))
+    zh = z.astype(np.float32)
+    zl = (z - zh).astype(np.float32)
+    hi, lo = probe([f"tanh {a:.9g} {b:.9g}" for a, b in zip(zh, zl)])
+    for i in range(len(z)):
+        x = Decimal(float(zh[i])) + Decimal(float(zl[i]))
+        e = (2 * x).exp()
+        exact = (e - 1) / (e + 1)
+        got = Decimal(float(hi[i])) + Decimal(float(lo[i]))
+        assert abs(got - exact) <= Decimal("1e-12") * abs(exact), (float(x), float(got), float(exact))
+
+
+def _bf16_nearest(v: Fraction) -> int:
+    """Bit pattern of the bfloat16 nearest to v (ties to even), by brute force
+    over the two neighbours of v's float32 truncation."""
+    f = np.float32(float(v))
+    bits = int(f.view(np.uint32)) & 0xFFFF0000
+    cands = [bits, bits + 0x10000, bits - 0x10000]
+    best = None
+    for c in cands:
+        cv = Fraction(float(np.uint32(c & 0xFFFFFFFF).view(np.float32)))
+        d = abs(cv - v)
+        key = (d, (c >> 16) & 1)
+        if best is None or key < best[0]:
+            best = (key, (c >> 16) & 0xFFFF)
+    return best[1]
+
+
+def test_bf16_rounding_of_double_floats(probe):
+    """Nearest bfloat16 of hi + lo, including values whose hi sits exactly on a
+    bfloat16 midpoint (lo then decides) and true ties (lo = 0)."""
+    rng = np.random.default_rng(11)
+    hs, ls = [], []
+    for _ in range(3000):
+        h = np.float32(rng.normal() * 10 ** rng.uniform(-3, 3))
+        if rng.random() < 0.5:                       # force hi onto a midpoint
+            h = np.uint32((int(h.view(np.uint32)) & 0xFFFF0000) | 0x8000).view(np.float32)
+        ulp = float(np.spacing(np.float32(abs(h))))
+        lo = np.float32(rng.choice([0.0, rng.uniform(-0.5, 0.5) * ulp]))
+        hs.append(h)
+        ls.append(lo)
+    out = probe([f"bf16 {int(np.float32(h).view(np.uint32)):x} {int(np.float32(l).view(np.uint32)):x}"
+                 for h, l in zip(hs, ls)])[0]
+    for h, l, got in zip(hs, ls, out):
+        v = Fraction(float(h)) + Fraction(float(l))
+        assert int(got) == _bf16_nearest(v), (float(h), float(l))
