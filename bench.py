@@ -168,6 +168,45 @@ def scheduled_pass(args, w, d, bufs, stream, flush, rank, dev):
     }
 
 
+def rnn_pass(args, w, d, bufs, stream, flush, rank, dev):
+    """The cycle with the RNN head drafting on the same workload (its factor
+    rows feed the verification), timed like the main pass."""
+    import torch
+    from speculative_decoding_draft_04_gb300 import _lib, engine
+    from speculative_decoding_draft_04_gb300 import workloads as W
+    ri = W.make_rnn_inputs(W.config(args.config), trial=rank)
+    h = engine.DeviceRnn.from_inputs(ri, d, dev)
+
+    def step():
+        engine.rnn_cycle(d, bufs, h, stream)
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = float(sum(a.elapsed_time(b) for a, b in evs) / args.steps)
+    _lib.spec_profile_enable(True)
+    _lib.spec_profile_read()
+    for _ in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    prof = _lib.spec_profile_read()
+    _lib.spec_profile_enable(False)
+    positions = int(w.verify_len.sum())
+    return {"ms_per_step": ms, "value": positions / (ms * 1e-3), "unit": UNIT,
+            "positions_per_step": positions,
+            "draft_status": engine.status_words(bufs.dstatus),
+            "stages_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]}}
+
+
 def algorithmic_bytes(w):
     """Bytes a cycle must move at least (logits + W2 once per call), after the
     survey's accounting: draft = B*g*V*s + r*V*s; verify = sum(L+1)*V*s (target
@@ -402,6 +441,7 @@ def main():
     op = operating_point(d, bufs, prof.get("draft_persistent", (0.0, 0)), args.steps) \
         if rank == 0 else None
     sched = scheduled_pass(args, w, d, bufs, stream, flush, rank, dev)
+    rnn = rnn_pass(args, w, d, bufs, stream, flush, rank, dev)
 
     positions = int(w.verify_len.sum())
     if world > 1:
@@ -447,6 +487,7 @@ def main():
             "clocks": clocks,
         }
         line["scheduled_cycle"] = sched
+        line["rnn_cycle"] = rnn
         line["operating_point"] = op
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
