@@ -83,8 +83,10 @@ enum {
   SPEC_DEV_TIMEOUT = 8,     /* a bounded device wait gave up                 */
   SPEC_DEV_REFINED = 16,    /* informational: at least one re-decision        */
   SPEC_DEV_OVERFLOW = 32,   /* more near-boundary decisions than list slots   */
-  SPEC_DEV_BAD_CONF = 64    /* a confidence logit not finite, or a confidence
+  SPEC_DEV_BAD_CONF = 64,   /* a confidence logit not finite, or a confidence
                                outside [0, 1] given to the scheduler           */
+  SPEC_DEV_BAD_TREE = 128   /* a tree slot whose parent does not precede it, or
+                               deeper than gamma                                */
 };
 
 /* ---------------------------------------------------------------- draft */
@@ -274,6 +276,85 @@ typedef struct {
 } spec_schedule_args;
 size_t spec_schedule_workspace_bytes(int32_t R, int32_t gamma);
 int32_t spec_prefix_schedule(const spec_schedule_args* args, spec_stream_t stream);
+
+/* -------------------------------------------------------------- trees */
+/* Tree drafting and verification ("Speculative Decoding Part 1", VESSL AI
+ * blog, section "gamma 재배분: 체인 대신 트리"), the Markov head drafting every
+ * node.  A request's candidate tree has N slots; parent[b][s] is -1 (the
+ * root, the anchor x_0) or a slot < s; depth(s) = depth(parent) + 1 <= gamma.
+ *
+ * spec_tree_select: survival a_s = product of conf[b][.] from the root down
+ * (fp32, left to right), then the top-n slots by a (ties: the shallower slot,
+ * then the lower index) -- closed under prefixes.  mask[b][s] = 1 for the
+ * chosen slots, survival[b][s] = a_s, expected[b] = sum of the chosen a
+ * (optional).  A bad parent sets SPEC_DEV_BAD_TREE and selects nothing for
+ * that request; a factor outside [0, 1] counts as 0 (SPEC_DEV_BAD_CONF).
+ * One launch, one CTA per request.  1 <= N <= 256, 1 <= gamma <= 16.
+ *
+ * spec_tree_draft: every selected slot s at depth d + 1 whose parent node
+ * holds token x (the anchor for the root) gets a token drawn by inverse CDF
+ * with u_draft[b][s] from q = softmax((U[b][d] + W1[x] W2) / T_b); children
+ * of one node are independent draws.  Unselected slots are left untouched.
+ * gamma launches (one per depth), double-float arithmetic throughout.
+ *
+ * spec_tree_verify: walks each request's selected tree from the root.  At a
+ * node with target row p (target[b][0] at the root, target[b][1 + s] at slot
+ * s) and draft q, the selected children are tried in slot order: child c is
+ * accepted iff u_accept[b][c] < r(x_c) / q(x_c), r starting at p and
+ * replaced by normalize(max(0, r - q)) after each rejection (recursive
+ * rejection sampling, for independently drawn children); the accepted child
+ * becomes the next node; when none is accepted the final token is drawn from
+ * r with u_final[b] (at a leaf r = p: the bonus token).  Outputs accept_len
+ * (accepted nodes), out_tokens [B][gamma+1] (accepted tokens, final, -1) and
+ * path [B][gamma] (accepted slots, -1).  One launch, one CTA per request,
+ * double-float arithmetic throughout.
+ *
+ * Both draft and verify take the workspace spec_tree_workspace_bytes(B, N, V)
+ * (16-byte aligned); dev_status bits are OR-ed in and never cleared.        */
+int32_t spec_tree_select(int32_t B, int32_t N, int32_t gamma, const int32_t* parent, const float* conf,
+                         int32_t n, float* survival, uint8_t* mask, float* expected,
+                         uint32_t* dev_status, spec_stream_t stream);
+typedef struct {
+  int32_t B, N, gamma, V, r;
+  int32_t dtype;              /* spec_dtype of U, W1, W2 (and target)            */
+  const void* U;              /* [B][gamma][V]                                   */
+  const void* W1;             /* [V][r]                                          */
+  const void* W2;             /* [r][V]                                          */
+  const int32_t* anchor;      /* [B]                                             */
+  const float* temperature;   /* [B]                                             */
+  const int32_t* parent;      /* [B][N]                                          */
+  const uint8_t* mask;        /* [B][N] from spec_tree_select                    */
+  const float* u_draft;       /* [B][N]                                          */
+  int32_t* tokens;            /* out [B][N] (selected slots)                     */
+  float* q_tok;               /* out [B][N] q(x_s) of each drawn token           */
+  uint32_t* dev_status;
+  void* workspace;
+  size_t workspace_bytes;
+} spec_tree_draft_args;
+int32_t spec_tree_draft(const spec_tree_draft_args* args, spec_stream_t stream);
+typedef struct {
+  int32_t B, N, gamma, V, r;
+  int32_t dtype;
+  const void* target;         /* [B][N+1][V] target logits at the root and slots */
+  const void* U;
+  const void* W1;
+  const void* W2;
+  const int32_t* anchor;
+  const float* temperature;
+  const int32_t* parent;
+  const uint8_t* mask;
+  const int32_t* tokens;      /* [B][N] from spec_tree_draft                     */
+  const float* u_accept;      /* [B][N]                                          */
+  const float* u_final;       /* [B]                                             */
+  int32_t* accept_len;        /* out [B]                                         */
+  int32_t* out_tokens;        /* out [B][gamma+1]                                */
+  int32_t* path;              /* out [B][gamma]                                  */
+  uint32_t* dev_status;
+  void* workspace;
+  size_t workspace_bytes;
+} spec_tree_verify_args;
+int32_t spec_tree_verify(const spec_tree_verify_args* args, spec_stream_t stream);
+size_t spec_tree_workspace_bytes(int32_t B, int32_t N, int32_t V);
 
 /* ---------------------------------------------- operating-point report */
 /* The analytic speed-up model of "Speculative Decoding Part 1: 도입 전에 확인해야

@@ -17,14 +17,15 @@ LIB_PATH = os.path.join(HERE, "libspec.so")
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_OPT_EPS_SCALE, SPEC_OPT_FORCE_SIMT, SPEC_OPT_BIAS_PATH, SPEC_OPT_TRACE = 1, 2, 3, 5
 DEV_BITS = {1: "BAD_TOKEN", 2: "BAD_LEN", 4: "BAD_TEMP", 8: "TIMEOUT", 16: "REFINED",
-            32: "OVERFLOW", 64: "BAD_CONF"}
+            32: "OVERFLOW", 64: "BAD_CONF", 128: "BAD_TREE"}
 
 EXPORTED = ("spec_workspace_bytes", "spec_markov_draft", "spec_markov_draft_static",
             "spec_verify", "spec_status_string",
             "spec_set_option", "spec_profile_enable", "spec_profile_read", "spec_stage_name",
             "spec_num_stages", "spec_operating_point", "spec_acceptance_stats",
             "spec_confidence", "spec_schedule_workspace_bytes", "spec_prefix_schedule",
-            "spec_rnn_draft")
+            "spec_rnn_draft", "spec_tree_select", "spec_tree_draft", "spec_tree_verify",
+            "spec_tree_workspace_bytes")
 
 
 class SpecError(RuntimeError):
@@ -82,6 +83,23 @@ class ScheduleArgs(ctypes.Structure):
                 ("dev_status", _vp), ("workspace", _vp), ("workspace_bytes", _sz)]
 
 
+class TreeDraftArgs(ctypes.Structure):
+    _fields_ = [("B", _i32), ("N", _i32), ("gamma", _i32), ("V", _i32), ("r", _i32),
+                ("dtype", _i32), ("U", _vp), ("W1", _vp), ("W2", _vp), ("anchor", _vp),
+                ("temperature", _vp), ("parent", _vp), ("mask", _vp), ("u_draft", _vp),
+                ("tokens", _vp), ("q_tok", _vp), ("dev_status", _vp), ("workspace", _vp),
+                ("workspace_bytes", _sz)]
+
+
+class TreeVerifyArgs(ctypes.Structure):
+    _fields_ = [("B", _i32), ("N", _i32), ("gamma", _i32), ("V", _i32), ("r", _i32),
+                ("dtype", _i32), ("target", _vp), ("U", _vp), ("W1", _vp), ("W2", _vp),
+                ("anchor", _vp), ("temperature", _vp), ("parent", _vp), ("mask", _vp),
+                ("tokens", _vp), ("u_accept", _vp), ("u_final", _vp), ("accept_len", _vp),
+                ("out_tokens", _vp), ("path", _vp), ("dev_status", _vp), ("workspace", _vp),
+                ("workspace_bytes", _sz)]
+
+
 def lib(path: str | None = None) -> ctypes.CDLL:
     """Load libspec.so (built in-tree by build.build())."""
     global _LIB
@@ -116,6 +134,14 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.spec_operating_point.argtypes = [ctypes.POINTER(OpArgs), ctypes.POINTER(OpResult)]
     L.spec_acceptance_stats.restype = _i32
     L.spec_acceptance_stats.argtypes = [_i32, _i32, _vp, _vp, _vp, _vp, _vp]
+    L.spec_tree_select.restype = _i32
+    L.spec_tree_select.argtypes = [_i32, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]
+    L.spec_tree_draft.restype = _i32
+    L.spec_tree_draft.argtypes = [ctypes.POINTER(TreeDraftArgs), _vp]
+    L.spec_tree_verify.restype = _i32
+    L.spec_tree_verify.argtypes = [ctypes.POINTER(TreeVerifyArgs), _vp]
+    L.spec_tree_workspace_bytes.restype = _sz
+    L.spec_tree_workspace_bytes.argtypes = [_i32, _i32, _i32]
     L.spec_rnn_draft.restype = _i32
     L.spec_rnn_draft.argtypes = [ctypes.POINTER(RnnDraftArgs), _vp]
     L.spec_confidence.restype = _i32
@@ -273,3 +299,38 @@ def spec_rnn_draft(U, W1, W2, Wr, hproj, anchor, temperature, u_draft, draft_tok
                   workspace.numel() * workspace.element_size())
     a = RnnDraftArgs(d, _ptr(Wr), _ptr(hproj), _ptr(a_rows))
     _check(lib().spec_rnn_draft(ctypes.byref(a), _stream(stream)), "spec_rnn_draft")
+
+
+def spec_tree_workspace_bytes(B: int, N: int, V: int) -> int:
+    return int(lib().spec_tree_workspace_bytes(B, N, V))
+
+
+def spec_tree_select(parent, conf, n, survival, mask, dev_status, gamma, expected=None,
+                     stream=None) -> None:
+    """Top-n slots of each request's candidate tree by survival."""
+    B, N = parent.shape
+    _check(lib().spec_tree_select(B, N, gamma, _ptr(parent), _ptr(conf), n, _ptr(survival),
+                                  _ptr(mask), _ptr(expected), _ptr(dev_status), _stream(stream)),
+           "spec_tree_select")
+
+
+def spec_tree_draft(U, W1, W2, anchor, temperature, parent, mask, u_draft, tokens, q_tok,
+                    dev_status, workspace, stream=None) -> None:
+    B, gamma, V = U.shape
+    a = TreeDraftArgs(B, parent.shape[1], gamma, V, W1.shape[1], _dtype_code(U), _ptr(U),
+                      _ptr(W1), _ptr(W2), _ptr(anchor), _ptr(temperature), _ptr(parent),
+                      _ptr(mask), _ptr(u_draft), _ptr(tokens), _ptr(q_tok), _ptr(dev_status),
+                      _ptr(workspace), workspace.numel() * workspace.element_size())
+    _check(lib().spec_tree_draft(ctypes.byref(a), _stream(stream)), "spec_tree_draft")
+
+
+def spec_tree_verify(target, U, W1, W2, anchor, temperature, parent, mask, tokens, u_accept,
+                     u_final, accept_len, out_tokens, path, dev_status, workspace,
+                     stream=None) -> None:
+    B, gamma, V = U.shape
+    a = TreeVerifyArgs(B, parent.shape[1], gamma, V, W1.shape[1], _dtype_code(U), _ptr(target),
+                       _ptr(U), _ptr(W1), _ptr(W2), _ptr(anchor), _ptr(temperature), _ptr(parent),
+                       _ptr(mask), _ptr(tokens), _ptr(u_accept), _ptr(u_final), _ptr(accept_len),
+                       _ptr(out_tokens), _ptr(path), _ptr(dev_status), _ptr(workspace),
+                       workspace.numel() * workspace.element_size())
+    _check(lib().spec_tree_verify(ctypes.byref(a), _stream(stream)), "spec_tree_verify")

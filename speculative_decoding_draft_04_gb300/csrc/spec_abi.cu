@@ -42,6 +42,18 @@ cudaError_t launch_schedule_rank(int, int, const float*, float*, int*, unsigned 
 cudaError_t launch_schedule_select(int, int, const double*, int, const int*, const unsigned long long*,
                                    int*, long long*, double*, cudaStream_t);
 
+cudaError_t launch_tree_select(int, int, int, const int*, const float*, int, float*, uint8_t*, float*,
+                               uint32_t*, cudaStream_t);
+template <typename DT>
+cudaError_t launch_tree_draft(const TreeShape&, const void*, const void*, const void*, const int*,
+                              const float*, const int*, const uint8_t*, const float*, int*, float*, void*,
+                              uint32_t*, cudaStream_t);
+template <typename DT>
+cudaError_t launch_tree_verify(const TreeShape&, const void*, const void*, const void*, const void*,
+                               const int*, const float*, const int*, const uint8_t*, const int*,
+                               const float*, const float*, int*, int*, int*, void*, uint32_t*,
+                               cudaStream_t);
+
 // ---------------------------------------------------------------- options
 namespace {
 std::mutex g_mu;
@@ -79,12 +91,14 @@ Eps current_eps() {
 enum Stage {
   ST_DRAFT_PERSISTENT, ST_VERIFY_PREP,
   ST_TARGET_STATS, ST_VERIFY_TILE, ST_VERIFY_FINAL, ST_SLOW_VERIFY, ST_VERIFY_HP_SUMS,
-  ST_VERIFY_HP_RESID, ST_CONFIDENCE, ST_SCHED_RANK, ST_SCHED_SELECT, ST_COUNT
+  ST_VERIFY_HP_RESID, ST_CONFIDENCE, ST_SCHED_RANK, ST_SCHED_SELECT, ST_TREE_SELECT,
+  ST_TREE_DRAFT, ST_TREE_VERIFY, ST_COUNT
 };
 const char* kStageNames[ST_COUNT] = {
     "draft_persistent", "verify_prep",
     "target_stats", "verify_tile", "verify_final", "slow_verify", "verify_hp_sums",
-    "verify_hp_resid", "confidence", "sched_rank", "sched_select"};
+    "verify_hp_resid", "confidence", "sched_rank", "sched_select", "tree_select",
+    "tree_draft", "tree_verify"};
 bool g_prof = false;
 struct EvPair { cudaEvent_t a, b; int stage; };
 std::vector<EvPair> g_pending;
@@ -575,6 +589,88 @@ int32_t spec_prefix_schedule(const spec_schedule_args* a, spec_stream_t stream) 
       return SPEC_ECUDA;
   }
   return SPEC_OK;
+}
+
+// ---------------------------------------------------------------- trees
+static int tree_check(int B, int N, int gamma, int V, int r, int dtype) {
+  if (B < 1 || B > 4096 || N < 1 || gamma < 1 || V < 16 || V >= (1 << 24) || r < 1) return SPEC_EINVAL;
+  if (N > 256 || gamma > MAX_GAMMA || r % 16 != 0 || r > 256 || V % 8 != 0 ||
+      (dtype != SPEC_F32 && dtype != SPEC_BF16))
+    return SPEC_EUNSUPPORTED;
+  return SPEC_OK;
+}
+
+size_t spec_tree_workspace_bytes(int32_t B, int32_t N, int32_t V) {
+  if (B < 1 || N < 1 || V < 16) return 0;
+  const size_t draft = (size_t)B * (N + 1) * ((V + 31) / 32) * 16;
+  const size_t verify = (size_t)B * 2 * V * 8;
+  return draft > verify ? draft : verify;
+}
+
+int32_t spec_tree_select(int32_t B, int32_t N, int32_t gamma, const int32_t* parent, const float* conf,
+                         int32_t n, float* survival, uint8_t* mask, float* expected, uint32_t* dev_status,
+                         spec_stream_t stream) {
+  if (B < 1 || B > 4096 || N < 1 || gamma < 1 || n < 0 || !parent || !conf || !survival || !mask ||
+      !dev_status)
+    return SPEC_EINVAL;
+  if (N > 256 || gamma > MAX_GAMMA) return SPEC_EUNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ProfScope p(st, ST_TREE_SELECT);
+  return launch_tree_select(B, N, gamma, parent, conf, n, survival, mask, expected, dev_status, st) ==
+                 cudaSuccess
+             ? SPEC_OK
+             : SPEC_ECUDA;
+}
+
+int32_t spec_tree_draft(const spec_tree_draft_args* a, spec_stream_t stream) {
+  if (!a) return SPEC_EINVAL;
+  const int rc = tree_check(a->B, a->N, a->gamma, a->V, a->r, a->dtype);
+  if (rc != SPEC_OK) return rc;
+  if (!a->U || !a->W1 || !a->W2 || !a->anchor || !a->temperature || !a->parent || !a->mask ||
+      !a->u_draft || !a->tokens || !a->q_tok || !a->dev_status)
+    return SPEC_EINVAL;
+  if (!aligned(a->U, 16) || !aligned(a->W1, 16) || !aligned(a->W2, 16)) return SPEC_EALIGN;
+  if (!a->workspace || a->workspace_bytes < spec_tree_workspace_bytes(a->B, a->N, a->V))
+    return SPEC_EWORKSPACE;
+  if (!aligned(a->workspace, 16)) return SPEC_EALIGN;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const TreeShape ts{a->B, a->N, a->gamma, a->V, a->r};
+  ProfScope p(st, ST_TREE_DRAFT);
+  const cudaError_t e =
+      a->dtype == SPEC_BF16
+          ? launch_tree_draft<bf16>(ts, a->U, a->W1, a->W2, a->anchor, a->temperature, a->parent, a->mask,
+                                    a->u_draft, a->tokens, a->q_tok, a->workspace, a->dev_status, st)
+          : launch_tree_draft<float>(ts, a->U, a->W1, a->W2, a->anchor, a->temperature, a->parent, a->mask,
+                                     a->u_draft, a->tokens, a->q_tok, a->workspace, a->dev_status, st);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+int32_t spec_tree_verify(const spec_tree_verify_args* a, spec_stream_t stream) {
+  if (!a) return SPEC_EINVAL;
+  const int rc = tree_check(a->B, a->N, a->gamma, a->V, a->r, a->dtype);
+  if (rc != SPEC_OK) return rc;
+  if (!a->target || !a->U || !a->W1 || !a->W2 || !a->anchor || !a->temperature || !a->parent ||
+      !a->mask || !a->tokens || !a->u_accept || !a->u_final || !a->accept_len || !a->out_tokens ||
+      !a->path || !a->dev_status)
+    return SPEC_EINVAL;
+  if (!aligned(a->target, 16) || !aligned(a->U, 16) || !aligned(a->W1, 16) || !aligned(a->W2, 16))
+    return SPEC_EALIGN;
+  if (!a->workspace || a->workspace_bytes < spec_tree_workspace_bytes(a->B, a->N, a->V))
+    return SPEC_EWORKSPACE;
+  if (!aligned(a->workspace, 16)) return SPEC_EALIGN;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const TreeShape ts{a->B, a->N, a->gamma, a->V, a->r};
+  ProfScope p(st, ST_TREE_VERIFY);
+  const cudaError_t e =
+      a->dtype == SPEC_BF16
+          ? launch_tree_verify<bf16>(ts, a->target, a->U, a->W1, a->W2, a->anchor, a->temperature,
+                                     a->parent, a->mask, a->tokens, a->u_accept, a->u_final, a->accept_len,
+                                     a->out_tokens, a->path, a->workspace, a->dev_status, st)
+          : launch_tree_verify<float>(ts, a->target, a->U, a->W1, a->W2, a->anchor, a->temperature,
+                                      a->parent, a->mask, a->tokens, a->u_accept, a->u_final,
+                                      a->accept_len, a->out_tokens, a->path, a->workspace, a->dev_status,
+                                      st);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
 const char* spec_status_string(int32_t s) {

@@ -84,6 +84,11 @@ struct Ws {
   float2* rowp;         // [B][gamma+1] -lse_p as a double-float pair
 };
 
+// Candidate trees: B requests of N slots, depth <= gamma.
+struct TreeShape {
+  int B, N, gamma, V, r;
+};
+
 // RNN head inputs and outputs of the draft (all null for the Markov head).
 struct RnnParams {
   const void* Wr;        // [3r][2r] storage type

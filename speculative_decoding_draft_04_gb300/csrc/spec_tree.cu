@@ -1,0 +1,481 @@
+// Tree drafting and tree verification ("Speculative Decoding Part 1", VESSL AI
+// blog, section "gamma 재배분: 체인 대신 트리"), with DSpark's Markov head
+// drafting every node.
+//
+//   tree_select_kernel   one CTA per request: survival a_s = fp32 product of the
+//                        slot factors from the root down, then the top-n slots
+//                        (ties: shallower, then lower index) by a comparison
+//                        count -- closed under prefixes because a child's a
+//                        never exceeds its parent's.
+//   tree_draft_kernel    one launch per depth level, one CTA per (request,
+//                        node of that level with selected children): the
+//                        node's draft logits (U row of its depth + W1[x] W2,
+//                        over T) in double-float over the whole vocabulary,
+//                        then each selected child drawn by inverse CDF with its
+//                        own uniform.
+//   tree_verify_kernel   one CTA per request walks the tree from the root: at
+//                        each node, target and draft logits in double-float,
+//                        then recursive rejection over the node's candidates
+//                        (ratio u < r(x)/q(x), r <- normalize(max(0, r - q))
+//                        after a rejection); the first accepted child is the
+//                        next node, otherwise the final token is drawn from r.
+//
+// Every weight, sum and scan is a double-float (transition bias as a
+// compensated sum of exact products), so the decisions agree with a float64
+// computation except within ~1e-12 of a boundary.  This is the direct
+// formulation: it spends ~r double-float multiply-adds per vocabulary entry
+// and node and is not tiled onto the tensor cores.
+#include "spec_hp.cuh"
+
+namespace spec {
+
+constexpr int TREE_MAX_SLOTS = 256;
+
+// ---------------------------------------------------------------- selection
+__global__ void __launch_bounds__(NT) tree_select_kernel(int B, int N, int gamma, const int* parent,
+                                                         const float* conf, int n, float* survival,
+                                                         uint8_t* mask, float* expected,
+                                                         uint32_t* status) {
+  __shared__ float s_a[TREE_MAX_SLOTS];
+  __shared__ int s_d[TREE_MAX_SLOTS];
+  __shared__ int s_bad;
+  const int b = blockIdx.x;
+  const int* par = parent + (size_t)b * N;
+  if (threadIdx.x == 0) {
+    int bad = 0;
+    for (int s = 0; s < N; ++s) {        // parents precede children: one pass
+      const int p = par[s];
+      const float c = conf[(size_t)b * N + s];
+      const float cc = (c >= 0.f && c <= 1.f) ? c : 0.f;
+      if (!(cc == c)) bad |= SPEC_DEV_BAD_CONF;
+      if (p < -1 || p >= s) {
+        bad |= SPEC_DEV_BAD_TREE;
+        s_d[s] = 1;
+        s_a[s] = 0.f;
+      } else {
+        s_d[s] = p < 0 ? 1 : s_d[p] + 1;
+        s_a[s] = p < 0 ? cc : __fmul_rn(s_a[p], cc);
+        if (s_d[s] > gamma) bad |= SPEC_DEV_BAD_TREE;
+      }
+      survival[(size_t)b * N + s] = s_a[s];
+    }
+    s_bad = bad;
+    if (bad) set_status(status, (uint32_t)bad);
+  }
+  __syncthreads();
+  const bool invalid = s_bad & SPEC_DEV_BAD_TREE;
+  float sum = 0.f;
+  for (int s = threadIdx.x; s < N; s += NT) {
+    const float a = s_a[s];
+    const int d = s_d[s];
+    int rank = 0;
+    for (int t = 0; t < N; ++t) {
+      const float at = s_a[t];
+      rank += (at > a) | ((at == a) & ((s_d[t] < d) | ((s_d[t] == d) & (t < s))));
+    }
+    const bool take = !invalid && rank < n;
+    mask[(size_t)b * N + s] = take ? 1 : 0;
+    if (take) sum += a;
+  }
+  sum = block_sum(sum, reinterpret_cast<float*>(s_d));   // s_d no longer needed
+  if (threadIdx.x == 0 && expected) expected[b] = sum;
+}
+
+// ---------------------------------------------------------------- node rows
+// Logits of one node row over the vocabulary into `out` (double-float pairs):
+// draft (U_row + W1[f] W2) / T, or target t_row / T when a == nullptr.
+template <typename DT>
+__device__ void row_logits(const TreeShape& ts, const DT* urow, const DT* W2, const float* a, df invT,
+                           float2* out) {
+  for (int v = threadIdx.x; v < ts.V; v += NT) {
+    df l;
+    if (a) {
+      const df bias = hp_bias<DT>(a, W2, ts.V, ts.r, v);
+      l = dd_mul(dd_add_f(bias, ldf(urow + v)), invT);
+    } else {
+      l = dd_mul_f(invT, ldf(urow + v));
+    }
+    out[v] = make_float2(l.hi, l.lo);
+  }
+}
+
+// Largest logit (its hi part) and the normaliser sum exp(l - m).
+__device__ void row_norm(int V, const float2* l, const df* tab, float* shf, float& m, df& Z) {
+  float mx = -INFINITY;
+  for (int v = threadIdx.x; v < V; v += NT) mx = fmaxf(mx, __ldcg(l + v).x);
+  m = block_max(mx, shf);
+  df s = {0.f, 0.f};
+  for (int v = threadIdx.x; v < V; v += NT) {
+    const float2 x = __ldcg(l + v);
+    s = dd_add(s, dd_exp(dd_add_f(df{x.x, x.y}, -m), tab));
+  }
+  Z = block_sum_df(s, shf);
+}
+
+// Probability of entry v of a row (logits l, shift m, 1/Z).
+__device__ __forceinline__ df row_prob(const float2* l, int v, float m, df iz, const df* tab) {
+  const float2 x = __ldcg(l + v);
+  return dd_mul(dd_exp(dd_add_f(df{x.x, x.y}, -m), tab), iz);
+}
+
+// The running distribution r after i rejections at a node: r_0 = p, r_{k+1} =
+// max(0, r_k - q) / Z_{k+1} (r_k kept when Z_{k+1} = 0).  izr[k] = 1/Z_{k+1},
+// or zero for a kept step.
+__device__ __forceinline__ df resid_prob(const float2* lp, const float2* lq, int v, float mp, df izp,
+                                         float mq, df izq, const df* izr, int i, const df* tab) {
+  df r = row_prob(lp, v, mp, izp, tab);
+  if (i == 0) return r;
+  const df q = row_prob(lq, v, mq, izq, tab);
+  for (int k = 0; k < i; ++k) {
+    if (izr[k].hi == 0.f) continue;
+    const df d = dd_add(r, dd_neg(q));
+    r = d.hi > 0.f ? dd_mul(d, izr[k]) : df{0.f, 0.f};
+  }
+  return r;
+}
+
+// Inverse CDF of an unnormalised row given by `weight(v)`: the smallest v with
+// running sum > target (double-float), else the last v with weight > 0.
+// Per-thread contiguous ranges, block scan, then the crossing thread's walk.
+template <class F>
+__device__ int row_draw(int V, df target, F weight, float* shf, int* s_sel, df* s_w) {
+  const int per = (V + NT - 1) / NT;
+  const int v0 = min(V, (int)threadIdx.x * per), v1 = min(V, v0 + per);
+  df loc = {0.f, 0.f};
+  int lastpos = -1;
+  for (int v = v0; v < v1; ++v) {
+    const df w = weight(v);
+    if (w.hi > 0.f) lastpos = v;
+    loc = dd_add(loc, w);
+  }
+  df tot;
+  const df ex = block_excl_scan_df(loc, &tot, shf);
+  if (threadIdx.x == 0) { s_sel[0] = 0x7fffffff; s_sel[1] = -1; }
+  __syncthreads();
+  if (v0 < v1 && dd_le(ex, target) && !dd_le(dd_add(ex, loc), target)) {
+    df run = ex;
+    for (int v = v0; v < v1; ++v) {
+      const df w = weight(v);
+      const df nx = dd_add(run, w);
+      if (w.hi > 0.f && !dd_le(nx, target)) {
+        atomicMin(&s_sel[0], v);
+        break;
+      }
+      run = nx;
+    }
+  }
+  if (lastpos >= 0) atomicMax(&s_sel[1], lastpos);
+  __syncthreads();
+  const int tok = s_sel[0] != 0x7fffffff ? s_sel[0] : max(s_sel[1], 0);
+  (void)s_w;
+  __syncthreads();
+  return tok;
+}
+
+// ---------------------------------------------------------------- drafting
+// Chunk partials of a draft row: for each 32-column chunk c, (m_c, s_c) with
+// m_c the chunk's largest logit (hi part) and s_c = sum exp(l - m_c), one warp
+// per chunk.  l = (U_row + W1[x] W2) / T in double-float.
+template <typename DT>
+__device__ void draft_row_chunks(const TreeShape& ts, const DT* urow, const DT* W2, const float* a,
+                                 df invT, const df* tab, float4* chunks) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NC = (ts.V + 31) / 32;
+  for (int c = warp; c < NC; c += NT / 32) {
+    const int v = c * 32 + lane;
+    df l = {-INFINITY, 0.f};
+    if (v < ts.V) l = dd_mul(dd_add_f(hp_bias<DT>(a, W2, ts.V, ts.r, v), ldf(urow + v)), invT);
+    const float mc = warp_max(l.hi);
+    const df w = v < ts.V ? dd_exp(dd_add_f(l, -mc), tab) : df{0.f, 0.f};
+    const df sc = warp_sum_df(w);
+    if (lane == 0) chunks[c] = make_float4(mc, sc.hi, sc.lo, 0.f);
+  }
+}
+
+// Mass of chunk c relative to the row's largest logit m: s_c e^{m_c - m}.
+__device__ __forceinline__ df chunk_mass(const float4* chunks, int c, float m, const df* tab) {
+  const float4 p = __ldcg(chunks + c);
+  return dd_mul(df{p.y, p.z}, dd_exp(two_sum_df(p.x, -m), tab));
+}
+
+// Node index of CTA (b, n): n = 0 the root, n = 1 + s slot s.
+template <typename DT>
+__global__ void __launch_bounds__(NT) tree_draft_kernel(TreeShape ts, int level, const DT* U, const DT* W1,
+                                                        const DT* W2, const int* anchor, const float* temp,
+                                                        const int* parent, const uint8_t* mask,
+                                                        const float* u_draft, int* tokens, float* q_tok,
+                                                        float4* scratch, uint32_t* status) {
+  __shared__ df s_tab[DD_EXP_TAB];
+  __shared__ float shf[72];
+  __shared__ float s_a[256];
+  __shared__ int s_sel[2];
+  __shared__ df s_pref;
+  __shared__ int s_go;
+  const int b = blockIdx.x / (ts.N + 1), node = (int)(blockIdx.x % (ts.N + 1)) - 1;
+  const int* par = parent + (size_t)b * ts.N;
+  const uint8_t* msk = mask + (size_t)b * ts.N;
+  if (threadIdx.x == 0) {
+    // depth of the node (root 0; parents checked to precede their children)
+    int d = 0, ok = node < 0 || msk[node];
+    for (int p = node; p >= 0 && ok; p = par[p]) {
+      if (par[p] < -1 || par[p] >= p || ++d > ts.gamma) ok = 0;
+    }
+    int kids = 0;
+    for (int s = node + 1; s < ts.N && ok; ++s) kids += (par[s] == node) & (msk[s] != 0);
+    s_go = (ok && d == level && kids > 0) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_go) return;
+  const float T = temp[b];
+  const int x = node < 0 ? anchor[b] : tokens[(size_t)b * ts.N + node];
+  if (x < 0 || x >= ts.V || !temp_ok(T)) {
+    if (threadIdx.x == 0) {
+      set_status(status, (x < 0 || x >= ts.V) ? SPEC_DEV_BAD_TOKEN : SPEC_DEV_BAD_TEMP);
+      for (int s = node + 1; s < ts.N; ++s)
+        if (par[s] == node && msk[s]) {
+          tokens[(size_t)b * ts.N + s] = -1;
+          q_tok[(size_t)b * ts.N + s] = NAN;
+        }
+    }
+    return;
+  }
+  if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(s_tab, threadIdx.x);
+  for (int i = threadIdx.x; i < ts.r; i += NT) s_a[i] = ldf(W1 + (size_t)x * ts.r + i);
+  __syncthreads();
+  const int NC = (ts.V + 31) / 32;
+  float4* chunks = scratch + (size_t)blockIdx.x * NC;
+  const DT* urow = U + ((size_t)b * ts.gamma + level) * ts.V;
+  const df invT = dd_recip(T);
+  draft_row_chunks<DT>(ts, urow, W2, s_a, invT, s_tab, chunks);
+  __syncthreads();
+  float mx = -INFINITY;
+  for (int c = threadIdx.x; c < NC; c += NT) mx = fmaxf(mx, __ldcg(chunks + c).x);
+  const float m = block_max(mx, shf);
+  // chunk masses: per-thread contiguous ranges
+  const int per = (NC + NT - 1) / NT;
+  const int c0 = min(NC, (int)threadIdx.x * per), c1 = min(NC, c0 + per);
+  df loc = {0.f, 0.f};
+  for (int c = c0; c < c1; ++c) loc = dd_add(loc, chunk_mass(chunks, c, m, s_tab));
+  df Z;
+  const df ex = block_excl_scan_df(loc, &Z, shf);
+  for (int s = node + 1; s < ts.N; ++s) {
+    if (!(par[s] == node && msk[s])) continue;
+    const df target = dd_mul_f(Z, u_draft[(size_t)b * ts.N + s]);
+    if (threadIdx.x == 0) s_sel[0] = 0x7fffffff;
+    __syncthreads();
+    if (c0 < c1 && dd_le(ex, target) && !dd_le(dd_add(ex, loc), target)) {
+      df run = ex;
+      for (int c = c0; c < c1; ++c) {
+        const df nx = dd_add(run, chunk_mass(chunks, c, m, s_tab));
+        if (!dd_le(nx, target)) {
+          s_sel[0] = c;                       // one thread holds the crossing
+          s_pref = run;
+          break;
+        }
+        run = nx;
+      }
+    }
+    __syncthreads();
+    int cs = s_sel[0];
+    df pref = s_pref;
+    if (cs == 0x7fffffff) {                   // rounding: the last chunk with mass
+      cs = NC - 1;
+      while (cs > 0 && !(__ldcg(chunks + cs).y > 0.f)) --cs;
+      pref = dd_add(Z, dd_neg(chunk_mass(chunks, cs, m, s_tab)));
+    }
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x, v = cs * 32 + lane;
+      df w = {0.f, 0.f};
+      if (v < ts.V) {
+        const df l = dd_mul(dd_add_f(hp_bias<DT>(s_a, W2, ts.V, ts.r, v), ldf(urow + v)), invT);
+        w = dd_exp(dd_add_f(l, -m), s_tab);
+      }
+      df inc = w;
+      for (int d = 1; d < 32; d <<= 1) {
+        const df o = shfl_up_df(inc, d);
+        if (lane >= d) inc = dd_add(inc, o);
+      }
+      const df hi = dd_add(pref, inc);
+      const uint32_t cl = __ballot_sync(0xffffffffu, w.hi > 0.f && !dd_le(hi, target));
+      const uint32_t pos = __ballot_sync(0xffffffffu, w.hi > 0.f);
+      const int t = cl ? __ffs(cl) - 1 : (pos ? 31 - __clz(pos) : 0);
+      const float wh = __shfl_sync(0xffffffffu, w.hi, t), wl = __shfl_sync(0xffffffffu, w.lo, t);
+      if (lane == 0) {
+        tokens[(size_t)b * ts.N + s] = cs * 32 + t;
+        q_tok[(size_t)b * ts.N + s] = (float)(dd_to_double(df{wh, wl}) / dd_to_double(Z));
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- verification
+template <typename DT>
+__global__ void __launch_bounds__(NT) tree_verify_kernel(TreeShape ts, const DT* target, const DT* U,
+                                                         const DT* W1, const DT* W2, const int* anchor,
+                                                         const float* temp, const int* parent,
+                                                         const uint8_t* mask, const int* tokens,
+                                                         const float* u_accept, const float* u_final,
+                                                         int* accept_len, int* out_tokens, int* path,
+                                                         float2* scratch, uint32_t* status) {
+  __shared__ df s_tab[DD_EXP_TAB];
+  __shared__ float shf[72];
+  __shared__ float s_a[256];
+  __shared__ int s_sel[2];
+  __shared__ df s_izr[TREE_MAX_SLOTS];
+  __shared__ int s_bad;
+  const int b = blockIdx.x;
+  const int* par = parent + (size_t)b * ts.N;
+  const uint8_t* msk = mask + (size_t)b * ts.N;
+  const int* tok = tokens + (size_t)b * ts.N;
+  int* out = out_tokens + (size_t)b * (ts.gamma + 1);
+  const float T = temp[b];
+  if (threadIdx.x == 0) {
+    int bad = 0;
+    if (!temp_ok(T)) bad |= SPEC_DEV_BAD_TEMP;
+    if (anchor[b] < 0 || anchor[b] >= ts.V) bad |= SPEC_DEV_BAD_TOKEN;
+    for (int s = 0; s < ts.N; ++s) {
+      if (par[s] < -1 || par[s] >= s) {
+        bad |= SPEC_DEV_BAD_TREE;
+        continue;
+      }
+      int d = 1;                                // depth: parents checked to precede
+      for (int p = par[s]; p >= 0 && d <= ts.gamma; p = par[p]) {
+        ++d;
+        if (par[p] < -1 || par[p] >= p) break;  // flagged when slot p was checked
+      }
+      if (d > ts.gamma) bad |= SPEC_DEV_BAD_TREE;
+      if (msk[s] && (tok[s] < 0 || tok[s] >= ts.V)) bad |= SPEC_DEV_BAD_TOKEN;
+    }
+    s_bad = bad;
+    if (bad) {
+      set_status(status, (uint32_t)bad);
+      accept_len[b] = -1;
+      for (int j = 0; j <= ts.gamma; ++j) out[j] = -1;
+      for (int j = 0; j < ts.gamma; ++j) path[(size_t)b * ts.gamma + j] = -1;
+    }
+  }
+  if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(s_tab, threadIdx.x);
+  __syncthreads();
+  if (s_bad) return;
+  float2* lp = scratch + (size_t)b * 2 * ts.V;
+  float2* lq = lp + ts.V;
+  const df invT = dd_recip(T);
+  int node = -1, depth = 0, n_acc = 0;
+  while (true) {
+    const int row = node < 0 ? 0 : 1 + node;
+    row_logits<DT>(ts, target + ((size_t)b * (ts.N + 1) + row) * ts.V, W2, nullptr, invT, lp);
+    // the node's selected children, in slot order
+    int nk = 0;
+    for (int s = node + 1; s < ts.N; ++s) nk += (par[s] == node) & (msk[s] != 0);
+    const int x = node < 0 ? anchor[b] : tok[node];
+    if (nk > 0) {
+      for (int i = threadIdx.x; i < ts.r; i += NT) s_a[i] = ldf(W1 + (size_t)x * ts.r + i);
+      __syncthreads();
+      row_logits<DT>(ts, U + ((size_t)b * ts.gamma + depth) * ts.V, W2, s_a, invT, lq);
+    }
+    __syncthreads();
+    float mp, mq = 0.f;
+    df Zp, Zq = {1.f, 0.f};
+    row_norm(ts.V, lp, s_tab, shf, mp, Zp);
+    if (nk > 0) row_norm(ts.V, lq, s_tab, shf, mq, Zq);
+    const df izp = dd_div(df{1.f, 0.f}, Zp), izq = dd_div(df{1.f, 0.f}, Zq);
+    int nrej = 0, next = -1;
+    for (int s = node + 1; s < ts.N && next < 0; ++s) {
+      if (!(par[s] == node && msk[s])) continue;
+      const int xs = tok[s];
+      const df rx = resid_prob(lp, lq, xs, mp, izp, mq, izq, s_izr, nrej, s_tab);
+      const df qx = row_prob(lq, xs, mq, izq, s_tab);
+      // accept iff u < r(x) / q(x), i.e. u q(x) < r(x)
+      const float u = u_accept[(size_t)b * ts.N + s];
+      if (!dd_le(rx, dd_mul_f(qx, u))) {
+        next = s;
+        break;
+      }
+      // rejected: r <- normalize(max(0, r - q))
+      df zs = {0.f, 0.f};
+      for (int v = threadIdx.x; v < ts.V; v += NT) {
+        const df d = dd_add(resid_prob(lp, lq, v, mp, izp, mq, izq, s_izr, nrej, s_tab),
+                            dd_neg(row_prob(lq, v, mq, izq, s_tab)));
+        if (d.hi > 0.f) zs = dd_add(zs, d);
+      }
+      zs = block_sum_df(zs, shf);
+      if (threadIdx.x == 0) s_izr[nrej] = zs.hi > 0.f ? dd_div(df{1.f, 0.f}, zs) : df{0.f, 0.f};
+      __syncthreads();
+      ++nrej;
+    }
+    if (next >= 0) {
+      if (threadIdx.x == 0) {
+        out[n_acc] = tok[next];
+        path[(size_t)b * ts.gamma + n_acc] = next;
+      }
+      ++n_acc;
+      node = next;
+      ++depth;
+      __syncthreads();
+      continue;
+    }
+    // final token from r (the target row itself at a leaf)
+    const df tgt = df{u_final[b], 0.f};          // r is normalised: target u
+    const int ft = row_draw(
+        ts.V, tgt, [&](int v) { return resid_prob(lp, lq, v, mp, izp, mq, izq, s_izr, nrej, s_tab); }, shf,
+        s_sel, nullptr);
+    if (threadIdx.x == 0) {
+      out[n_acc] = ft;
+      for (int j = n_acc + 1; j <= ts.gamma; ++j) out[j] = -1;
+      for (int j = n_acc; j < ts.gamma; ++j) path[(size_t)b * ts.gamma + j] = -1;
+      accept_len[b] = n_acc;
+    }
+    return;
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_tree_select(int B, int N, int gamma, const int* parent, const float* conf, int n,
+                               float* survival, uint8_t* mask, float* expected, uint32_t* status,
+                               cudaStream_t st) {
+  tree_select_kernel<<<B, NT, 0, st>>>(B, N, gamma, parent, conf, n, survival, mask, expected, status);
+  return cudaGetLastError();
+}
+
+template <typename DT>
+cudaError_t launch_tree_draft(const TreeShape& ts, const void* U, const void* W1, const void* W2,
+                              const int* anchor, const float* temp, const int* parent, const uint8_t* mask,
+                              const float* u_draft, int* tokens, float* q_tok, void* scratch,
+                              uint32_t* status, cudaStream_t st) {
+  for (int level = 0; level < ts.gamma; ++level) {
+    tree_draft_kernel<DT><<<ts.B * (ts.N + 1), NT, 0, st>>>(
+        ts, level, (const DT*)U, (const DT*)W1, (const DT*)W2, anchor, temp, parent, mask, u_draft, tokens,
+        q_tok, (float4*)scratch, status);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <typename DT>
+cudaError_t launch_tree_verify(const TreeShape& ts, const void* target, const void* U, const void* W1,
+                               const void* W2, const int* anchor, const float* temp, const int* parent,
+                               const uint8_t* mask, const int* tokens, const float* u_accept,
+                               const float* u_final, int* accept_len, int* out_tokens, int* path,
+                               void* scratch, uint32_t* status, cudaStream_t st) {
+  tree_verify_kernel<DT><<<ts.B, NT, 0, st>>>(ts, (const DT*)target, (const DT*)U, (const DT*)W1,
+                                              (const DT*)W2, anchor, temp, parent, mask, tokens, u_accept,
+                                              u_final, accept_len, out_tokens, path, (float2*)scratch,
+                                              status);
+  return cudaGetLastError();
+}
+
+#define SPEC_INST(DT)                                                                                   \
+  template cudaError_t launch_tree_draft<DT>(const TreeShape&, const void*, const void*, const void*,   \
+                                             const int*, const float*, const int*, const uint8_t*,      \
+                                             const float*, int*, float*, void*, uint32_t*, cudaStream_t); \
+  template cudaError_t launch_tree_verify<DT>(const TreeShape&, const void*, const void*, const void*,  \
+                                              const void*, const int*, const float*, const int*,        \
+                                              const uint8_t*, const int*, const float*, const float*,   \
+                                              int*, int*, int*, void*, uint32_t*, cudaStream_t);
+SPEC_INST(float)
+SPEC_INST(bf16)
+#undef SPEC_INST
+
+}  // namespace spec

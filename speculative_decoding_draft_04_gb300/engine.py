@@ -11,7 +11,7 @@ import dataclasses
 import numpy as np
 
 from . import _lib
-from .workloads import RnnInputs, ScheduleInputs, Workload
+from .workloads import RnnInputs, ScheduleInputs, TreeInputs, Workload
 
 
 def _dev_logits(arr: np.ndarray, dtype: str, device):
@@ -200,6 +200,61 @@ def rnn_cycle(d: DeviceWorkload, b: Buffers, h: DeviceRnn, stream=None) -> None:
                      b.lse_q, d.verify_len, d.u_accept, d.u_final, b.accept_len, b.out_tokens,
                      b.alpha, b.vstatus, b.workspace, p_tok=b.p_tok, diag=b.vdiag, stream=stream,
                      a_rows=h.a_rows)
+
+
+@dataclasses.dataclass
+class DeviceTree:
+    """A batch of candidate trees on the device and the tree path's outputs."""
+    N: int
+    n: int
+    parent: object
+    conf: object
+    target: object
+    u_draft: object
+    u_accept: object
+    u_final: object
+    survival: object
+    mask: object
+    tokens: object
+    q_tok: object
+    accept_len: object
+    out_tokens: object
+    path: object
+    status: object
+    workspace: object
+
+    @classmethod
+    def from_inputs(cls, t: TreeInputs, d: DeviceWorkload, n: int, device="cuda") -> "DeviceTree":
+        import torch
+        o = dict(device=device)
+        B, N = t.parent.shape
+
+        def dev(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        nbytes = _lib.spec_tree_workspace_bytes(B, N, d.V)
+        return cls(N=N, n=n, parent=dev(t.parent), conf=dev(t.conf),
+                   target=_dev_logits(t.target, d.dtype, device), u_draft=dev(t.u_draft),
+                   u_accept=dev(t.u_accept), u_final=dev(t.u_final),
+                   survival=torch.empty((B, N), dtype=torch.float32, **o),
+                   mask=torch.empty((B, N), dtype=torch.uint8, **o),
+                   tokens=torch.full((B, N), -1, dtype=torch.int32, **o),
+                   q_tok=torch.full((B, N), float("nan"), dtype=torch.float32, **o),
+                   accept_len=torch.empty(B, dtype=torch.int32, **o),
+                   out_tokens=torch.empty((B, d.gamma + 1), dtype=torch.int32, **o),
+                   path=torch.empty((B, d.gamma), dtype=torch.int32, **o),
+                   status=torch.zeros(4, dtype=torch.int32, **o),
+                   workspace=torch.empty(nbytes, dtype=torch.uint8, **o))
+
+
+def tree_cycle(d: DeviceWorkload, t: DeviceTree, stream=None) -> None:
+    """Select each request's tree, draft it, verify it."""
+    _lib.spec_tree_select(t.parent, t.conf, t.n, t.survival, t.mask, t.status, d.gamma,
+                          stream=stream)
+    _lib.spec_tree_draft(d.U, d.W1, d.W2, d.anchor, d.temperature, t.parent, t.mask, t.u_draft,
+                         t.tokens, t.q_tok, t.status, t.workspace, stream)
+    _lib.spec_tree_verify(t.target, d.U, d.W1, d.W2, d.anchor, d.temperature, t.parent, t.mask,
+                          t.tokens, t.u_accept, t.u_final, t.accept_len, t.out_tokens, t.path,
+                          t.status, t.workspace, stream)
 
 
 def status_words(t) -> list[int]:

@@ -54,6 +54,21 @@ review, sections 2.1 and 2.2), from ``default_rng([seed_index, trial, 2])``:
 
 Draw order: mu, w, then hidden per request.
 
+Tree inputs (``make_tree_inputs``, VESSL AI blog, section "gamma 재배분"),
+from ``default_rng([seed_index, trial, 4])`` for a candidate tree of N slots:
+
+* ``parent[b, s]``: slot s hangs under the root or an earlier slot, drawn
+  uniformly among those that keep depth <= gamma (a random bushy tree);
+* ``conf[b, s]`` U[0.3, 0.95]: the slot's conditional survival factor;
+* ``target[b, 0]`` = the workload's target row 0 and ``target[b, 1 + s]`` =
+  its target row depth(s) plus N(0, 0.5^2): every node has its own target
+  row, close to the chain's at that depth, so the shared U row of a depth
+  still agrees with it;
+* uniforms (``uniforms``): u_draft [B, N], u_accept [B, N], u_final [B].
+
+Draw order: per request parent, conf, target noise; then the uniforms from
+``default_rng([trial, 4])``.
+
 RNN head inputs (``make_rnn_inputs``, DSpark review, section 1.2 "RNN head"),
 from ``default_rng([seed_index, trial, 3])``:
 
@@ -321,6 +336,45 @@ def make_schedule_inputs(spec: dict[str, Any], trial: int = 0, *,
         h[:, 0] = mu[b]
         hidden[b] = _store(h, dtype)
     return ScheduleInputs(d=d, hidden=hidden, w=w.astype(np.float32), sps=cost_table(Bn, g))
+
+
+@dataclasses.dataclass
+class TreeInputs:
+    N: int
+    parent: np.ndarray      # int32 [B, N]
+    conf: np.ndarray        # float32 [B, N]
+    target: np.ndarray      # [B, N + 1, V] storage dtype
+    u_draft: np.ndarray     # float32 [B, N]
+    u_accept: np.ndarray    # float32 [B, N]
+    u_final: np.ndarray     # float32 [B]
+
+
+def make_tree_inputs(spec: dict[str, Any], w: "Workload", N: int, trial: int = 0) -> TreeInputs:
+    """Candidate trees and per-node target rows for the requests of ``w``."""
+    B, g, V = w.B, w.gamma, w.V
+    rng = np.random.default_rng([int(spec["seed_index"]), int(trial), 4])
+    parent = np.empty((B, N), np.int32)
+    conf = np.empty((B, N), np.float32)
+    sdt = np.uint16 if w.dtype == "bf16" else np.float32
+    target = np.empty((B, N + 1, V), dtype=sdt)
+    for b in range(B):
+        depth = []
+        for s in range(N):
+            cands = [-1] + [p for p in range(s) if depth[p] < g]
+            p = int(rng.choice(cands))
+            parent[b, s] = p
+            depth.append(1 if p < 0 else depth[p] + 1)
+        conf[b] = rng.uniform(0.3, 0.95, size=N).astype(np.float32)
+        base = to_f64(w.target[b], w.dtype)
+        rows = np.empty((N + 1, V))
+        rows[0] = base[0]
+        for s in range(N):
+            rows[1 + s] = base[depth[s]] + rng.normal(0.0, 0.5, size=V)
+        target[b] = _store(rows, w.dtype)
+    urng = np.random.default_rng([int(trial), 4])
+    return TreeInputs(N=N, parent=parent, conf=conf, target=target,
+                      u_draft=uniforms(urng, (B, N)), u_accept=uniforms(urng, (B, N)),
+                      u_final=uniforms(urng, (B,)))
 
 
 @dataclasses.dataclass
