@@ -207,6 +207,52 @@ def rnn_pass(args, w, d, bufs, stream, flush, rank, dev):
             "stages_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]}}
 
 
+TREE_SLOTS, TREE_BUDGET = 24, 12
+
+
+def tree_pass(args, w, d, flush, rank, dev):
+    """The tree path on the same requests: select the top-12 of 24 candidate
+    slots per request, draft them, verify the tree.  Timed with events around
+    each cycle (L2 flushed outside them), then with per-kernel events."""
+    import torch
+    from speculative_decoding_draft_04_gb300 import _lib, engine
+    from speculative_decoding_draft_04_gb300 import workloads as W
+    ti = W.make_tree_inputs(W.config(args.config), w, TREE_SLOTS, trial=rank)
+    t = engine.DeviceTree.from_inputs(ti, d, TREE_BUDGET, dev)
+    stream = torch.cuda.current_stream(dev)
+    steps = max(1, min(args.steps, 5))
+
+    def step():
+        engine.tree_cycle(d, t, stream)
+    for _ in range(2):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = float(sum(a.elapsed_time(b) for a, b in evs) / steps)
+    _lib.spec_profile_enable(True)
+    _lib.spec_profile_read()
+    flush.zero_()
+    step()
+    torch.cuda.synchronize()
+    prof = _lib.spec_profile_read()
+    _lib.spec_profile_enable(False)
+    acc = t.accept_len.cpu().numpy()
+    return {"ms_per_step": ms, "steps": steps, "slots": TREE_SLOTS, "budget": TREE_BUDGET,
+            "accepted_per_request": float(acc.mean()),
+            "tokens_per_s": float((acc + 1).sum()) / (ms * 1e-3),
+            "status": engine.status_words(t.status),
+            "stages_ms": {k: v[0] for k, v in prof.items() if v[1]},
+            "arithmetic": "double-float throughout (direct formulation, not tiled)"}
+
+
 def algorithmic_bytes(w):
     """Bytes a cycle must move at least (logits + W2 once per call), after the
     survey's accounting: draft = B*g*V*s + r*V*s; verify = sum(L+1)*V*s (target
@@ -442,6 +488,7 @@ def main():
         if rank == 0 else None
     sched = scheduled_pass(args, w, d, bufs, stream, flush, rank, dev)
     rnn = rnn_pass(args, w, d, bufs, stream, flush, rank, dev)
+    tree = tree_pass(args, w, d, flush, rank, dev)
 
     positions = int(w.verify_len.sum())
     if world > 1:
@@ -488,6 +535,7 @@ def main():
         }
         line["scheduled_cycle"] = sched
         line["rnn_cycle"] = rnn
+        line["tree_cycle"] = tree
         line["operating_point"] = op
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)

@@ -75,7 +75,8 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
  *   [0] OR of the bits below
  *   [1] decisions re-decided in extended precision (near a boundary)
  *   [2] decisions whose token or outcome changed after re-deciding
- *   [3] requests verified on the extended-precision slow path            */
+ *   [3] requests verified on the extended-precision slow path (spec_verify);
+ *       RNN head gate outputs recomputed in double-float (spec_rnn_draft)   */
 enum {
   SPEC_DEV_BAD_TOKEN = 1,   /* anchor or draft token outside [0, V)          */
   SPEC_DEV_BAD_LEN = 2,     /* verify_len outside [0, gamma]                 */

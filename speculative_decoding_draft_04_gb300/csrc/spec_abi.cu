@@ -285,7 +285,12 @@ int run_rnn_draft(const spec_rnn_draft_args* ra, cudaStream_t st) {
   sh.rnn = 1;
   sh.NA = a->gamma * a->B;
   const Layout L = layout(sh);
-  const Ws ws = views(L, a->workspace);
+  Ws ws = views(L, a->workspace);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_trace)
+      ws.trace = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(a->workspace) + L.trace);
+  }
   RnnParams rp;
   rp.Wr = ra->Wr;
   rp.hproj = ra->hproj;

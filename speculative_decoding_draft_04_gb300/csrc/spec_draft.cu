@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
   for (int k = 0; k < sh.gamma; ++k) {
     bool ok = true;
     if (sh.rnn) {
-      rnn_gates_body<DT>(sh, k, (const DT*)P.W1, P.anchor, P.tokens, P.rnn, smem_raw);
+      rnn_gates_body<DT>(sh, k, (const DT*)P.W1, P.anchor, P.tokens, P.rnn, smem_raw, P.status);
       if (!grid_sync(ctrl, G, gen, P.status)) break;
     }
     if (tr) tr[k * TRACE_SLOTS + 0] = globaltimer_ns();
@@ -566,12 +566,19 @@ static cudaError_t launch_persist(const DraftParams& P, int nsm, cudaStream_t st
   size_t smem = PATH == 2 ? TpLayout(P.sh.r, BN).total : TileLayout<DT>(BM, P.sh.r, false).total;
   const size_t slab = (size_t)P.sh.r * HPB * sizeof(DT);    // re-decision W2 slab (> sampler's)
   smem = smem > slab ? smem : slab;
+  const int n_tiles = P.sh.NS * ((P.sh.B + BM - 1) / BM);
+  int G = nsm;                             // one CTA per SM (all must be co-resident)
+  G = G < n_tiles ? G : n_tiles;
+  G = G > P.sh.B ? G : (P.sh.B < nsm ? P.sh.B : nsm);
+  G = G < 1 ? 1 : G;
   if (P.sh.rnn) {
-    // gate phase: one fallback-list int per (request, state index) of a CTA,
-    // B * ceil(r / G) at most, with G >= min(B, nsm) CTAs
-    const size_t B = P.sh.B, r = P.sh.r, n = (size_t)nsm;
-    const size_t ints = B <= n ? r + B : ((r + n - 1) / n + 1) * B;
-    smem = smem > ints * sizeof(int) ? smem : ints * sizeof(int);
+    // gate phase of a CTA with nI state indices: its Wr rows and a stage of
+    // RNN_STAGE_ROWS requests' inputs (bf16), then one fallback-list int per
+    // (request, index)
+    const size_t B = P.sh.B, K = 2 * (size_t)P.sh.r, nI = (P.sh.r + G - 1) / G;
+    const size_t stage = sizeof(DT) == 2 ? nI * 3 * K * sizeof(float) + RNN_STAGE_ROWS * K * sizeof(DT) : 0;
+    const size_t need = stage + nI * B * sizeof(int);
+    smem = smem > need ? smem : need;
   }
   auto kern = draft_persistent_kernel<DT, BM, PATH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -580,11 +587,6 @@ static cudaError_t launch_persist(const DraftParams& P, int nsm, cudaStream_t st
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const int n_tiles = P.sh.NS * ((P.sh.B + BM - 1) / BM);
-  int G = nsm;                             // one CTA per SM (all must be co-resident)
-  G = G < n_tiles ? G : n_tiles;
-  G = G > P.sh.B ? G : (P.sh.B < nsm ? P.sh.B : nsm);
-  G = G < 1 ? 1 : G;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(G);
   cfg.blockDim = dim3(NT);
