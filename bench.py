@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the scheduled, RNN-head and tree passes (profiling runs)")
     return ap.parse_args()
 
 
@@ -486,9 +488,11 @@ def main():
 
     op = operating_point(d, bufs, prof.get("draft_persistent", (0.0, 0)), args.steps) \
         if rank == 0 else None
-    sched = scheduled_pass(args, w, d, bufs, stream, flush, rank, dev)
-    rnn = rnn_pass(args, w, d, bufs, stream, flush, rank, dev)
-    tree = tree_pass(args, w, d, flush, rank, dev)
+    sched = rnn = tree = None
+    if not args.no_extras:
+        sched = scheduled_pass(args, w, d, bufs, stream, flush, rank, dev)
+        rnn = rnn_pass(args, w, d, bufs, stream, flush, rank, dev)
+        tree = tree_pass(args, w, d, flush, rank, dev)
 
     positions = int(w.verify_len.sum())
     if world > 1:
@@ -533,9 +537,10 @@ def main():
             "gpu_launches": int(launches * args.steps),
             "clocks": clocks,
         }
-        line["scheduled_cycle"] = sched
-        line["rnn_cycle"] = rnn
-        line["tree_cycle"] = tree
+        if not args.no_extras:
+            line["scheduled_cycle"] = sched
+            line["rnn_cycle"] = rnn
+            line["tree_cycle"] = tree
         line["operating_point"] = op
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)

@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
     tc_fence_after();
     st.tmem = s_holder;
   }
-  uint32_t gen = threadIdx.x == 0 ? ld_acquire_gpu(ctrl + CTRL_BAR_GEN) : 0u;
+  uint32_t gen = 0u;                         // grid barriers passed (thread 0)
   const HpRows R{P.U, P.U, W1, P.W2, P.temp};
   const int n_mt = (sh.B + BM - 1) / BM;
   const int n_tiles = sh.NS * n_mt;

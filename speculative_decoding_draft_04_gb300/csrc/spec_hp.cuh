@@ -188,6 +188,21 @@ __device__ __forceinline__ df hp_bias_block(const float* a, const DT* slab, int 
   return xch[threadIdx.x];
 }
 
+// Issue the cp.async copies of a block's r x HPB W2 columns into `slab`
+// (waited for by hp_block), so they overlap the item's own loads.
+template <typename DT>
+__device__ __forceinline__ void hp_issue_slab(DT* slab, const DT* W2, int V, int r, int c0) {
+  constexpr int E = 16 / sizeof(DT);
+  const int cpr = HPB / E;
+  for (int c = threadIdx.x; c < r * cpr; c += NT) {
+    const int i = c / cpr, q = c - i * cpr;
+    const int n = c0 + q * E;
+    const bool valid = n < V;
+    cp_async16(slab + (size_t)i * HPB + q * E, valid ? W2 + (size_t)i * V + n : W2, valid);
+  }
+  cp_async_commit();
+}
+
 // Draft weight exp((U[v] + bias) / T - shift_q) and target weight
 // exp(t[v] / T - shift_p), unnormalised unless the shifts are the row's
 // logsumexp.
@@ -321,14 +336,15 @@ struct HpShared {
 template <typename DT>
 __device__ void hp_block(const Shape& sh, const HpRows& R, const Ws& ws, int phase, int item,
                          int blk, const HpItem& it, HpShared& S, DT* slab) {
-  // a residual item among the first hpw_items keeps its weights from phase 0
-  const bool keep = it.kind == HP_RESID && item < ws.hpw_items;
+  // the first hpw_items items keep their weights from phase 0 (the residual
+  // pass and the re-decision read them); the slab copies were issued by the
+  // caller in phase 0
+  const bool keep = item < ws.hpw_items;
   const bool stored = keep && phase == 1;
   __syncthreads();
-  if (it.kind != HP_BONUS && !stored) {
+  if (it.kind != HP_BONUS && !stored)
     for (int i = threadIdx.x; i < sh.r; i += NT) S.a[i] = ldf((const DT*)R.W1 + (size_t)it.prev * sh.r + i);
-    stage_w2_slab<DT>(slab, (const DT*)R.W2, sh.V, 0, sh.r, blk * HPB, HPB);
-  }
+  cp_async_wait_all();
   __syncthreads();
   df izp = {0.f, 0.f}, izq = {0.f, 0.f};
   if (phase == 1) {
@@ -385,19 +401,22 @@ __device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, i
                                HpShared& S, DT* slab) {
   const HpItem it = ldcg_item(ws.items + item);
   const bool resid = it.kind == HP_RESID;
-  const df Zc = resid ? item_total(item_sums(ws, sh, item, 2), sh.NC, S.shf) : df{0.f, 0.f};
-  // residual with no mass: draw from p (a probability-zero event)
-  const bool use_r = resid && Zc.hi > 0.f;
-  const df Zp = use_r ? df{0.f, 0.f} : item_total(item_sums(ws, sh, item, 0), sh.NC, S.shf);
-  const float2* sums = item_sums(ws, sh, item, use_r ? 2 : 0);
-  const df Z = use_r ? Zc : Zp;
-  const df target = dd_mul_f(Z, it.u);
-  // crossing chunk: per-thread contiguous range of chunks, double-float scan
+  // one scan of the chunk sums gives both the normaliser (its total) and the
+  // per-thread prefixes; per-thread contiguous ranges of chunks
   int q0, q1;
   thread_range(sh.NC, q0, q1);
-  const df loc = range_sum(sums, q0, q1);
-  df tot;
-  const df ex = block_excl_scan_df(loc, &tot, S.shf);
+  const float2* sums = item_sums(ws, sh, item, resid ? 2 : 0);
+  df loc = range_sum(sums, q0, q1);
+  df Z;
+  df ex = block_excl_scan_df(loc, &Z, S.shf);
+  // residual with no mass: draw from p (a probability-zero event)
+  const bool use_r = resid && Z.hi > 0.f;
+  if (resid && !use_r) {
+    sums = item_sums(ws, sh, item, 0);
+    loc = range_sum(sums, q0, q1);
+    ex = block_excl_scan_df(loc, &Z, S.shf);
+  }
+  const df target = dd_mul_f(Z, it.u);
   if (threadIdx.x == 0) S.sel = 0x7fffffff;
   __syncthreads();
   int mine = -1;
@@ -445,9 +464,11 @@ __device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, i
     izp = {nz.x, nz.y};
     izq = {nz.z, nz.w};
   }
-  // ---- the chunk's biases: warp w sums rows [w r/8, (w+1) r/8) of column lane
+  // ---- the chunk's weights: kept from phase 0 for the first hpw_items items,
+  // else the biases recomputed (warp w sums rows [w r/8, (w+1) r/8) of column lane)
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (it.kind != HP_BONUS) {
+  const bool kept = item < ws.hpw_items;
+  if (it.kind != HP_BONUS && !kept) {
     for (int i = threadIdx.x; i < sh.r; i += NT) S.a[i] = ldf((const DT*)R.W1 + (size_t)it.prev * sh.r + i);
     stage_w2_slab<DT>(slab, (const DT*)R.W2, sh.V, 0, sh.r, n0, CW);
     const int kw = sh.r / (NT / 32);             // r % 16 == 0
@@ -468,7 +489,11 @@ __device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, i
   if (w == 0) {
     const int v = n0 + lane;
     df eq = {0.f, 0.f}, ep = {0.f, 0.f};
-    if (v < sh.V) {
+    if (v < sh.V && kept) {
+      const float4 w4 = __ldcg(ws.hpw + (size_t)item * sh.V + v);
+      eq = {w4.x, w4.y};
+      ep = {w4.z, w4.w};
+    } else if (v < sh.V) {
       if (it.kind != HP_BONUS) {
         df bias = S.part[0][lane];
         for (int g = 1; g < NT / 32; ++g) bias = dd_add(bias, S.part[g][lane]);
@@ -529,8 +554,16 @@ __device__ void hp_sums_body(const Shape& sh, const HpRows& R, const Ws& ws, int
   __syncthreads();
   for (int w = blockIdx.x; w < n * sh.HB; w += gridDim.x) {
     const int item = w / sh.HB, blk = w - item * sh.HB;
+    if (phase == 0) {
+      __syncthreads();                          // the previous unit is done with the slab
+      hp_issue_slab<DT>(slab, (const DT*)R.W2, sh.V, sh.r, blk * HPB);
+    }
     const HpItem it = ldcg_item(ws.items + item);
     if (phase == 1 && it.kind != HP_RESID) continue;
+    if (phase == 1 && item >= ws.hpw_items) {  // no kept weights: recompute the block
+      __syncthreads();
+      hp_issue_slab<DT>(slab, (const DT*)R.W2, sh.V, sh.r, blk * HPB);
+    }
     hp_block<DT>(sh, R, ws, phase, item, blk, it, S, slab);
     if (fused) {
       __threadfence();

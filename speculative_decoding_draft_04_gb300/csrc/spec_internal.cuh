@@ -46,10 +46,10 @@ struct HpItem {
 };
 
 // Control words at the start of the workspace.
-//   CTRL_BAR_COUNT / CTRL_BAR_GEN / CTRL_ABORT: grid barrier of the persistent
-//   draft kernel; CTRL_STEP0 + k: queued re-decisions of draft step k.
+//   CTRL_BAR_COUNT / CTRL_ABORT: grid barrier of the persistent draft kernel
+//   (word 4 is unused); CTRL_STEP0 + k: queued re-decisions of draft step k.
 enum {
-  CTRL_ITEMS = 0, CTRL_SLOW = 1, CTRL_NPACKED = 2, CTRL_BAR_COUNT = 3, CTRL_BAR_GEN = 4,
+  CTRL_ITEMS = 0, CTRL_SLOW = 1, CTRL_NPACKED = 2, CTRL_BAR_COUNT = 3,
   CTRL_ABORT = 5, CTRL_STEP0 = 8, CTRL_WORDS = 32
 };
 
@@ -322,45 +322,44 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
 }
 
 // Barrier across all CTAs of a cooperative launch (all co-resident).  Thread 0
-// of each CTA arrives on a counter; the last arrival resets it and advances
-// the generation word the others wait on.  Every wait is bounded: on timeout,
-// or when another CTA has aborted, it sets SPEC_DEV_TIMEOUT / the abort word
-// and returns false, and the caller leaves the kernel.  `gen` is thread 0's
-// copy of the generation (read once at kernel start).
+// of each CTA adds 1 to a counter that only grows (zeroed before the launch)
+// with a release, and waits with acquire loads until it reaches
+// (barriers passed + 1) x CTAs: one atomic per CTA and no reset.  The CTA's
+// other threads are ordered before the release by the __syncthreads.  Every
+// wait is bounded: on timeout, or when another CTA has aborted, it sets
+// SPEC_DEV_TIMEOUT / the abort word and returns false, and the caller leaves
+// the kernel.  `gen` is thread 0's count of barriers passed (0 at kernel start).
 __device__ __forceinline__ bool grid_sync(uint32_t* ctrl, uint32_t nblocks, uint32_t& gen,
                                           uint32_t* status) {
   __shared__ int s_gs_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    const uint32_t g = gen;
-    __threadfence();
-    const uint32_t arrived = atomicAdd(ctrl + CTRL_BAR_COUNT, 1u);
-    if (arrived == nblocks - 1) {
-      atomicExch(ctrl + CTRL_BAR_COUNT, 0u);
-      __threadfence();
-      atomicAdd(ctrl + CTRL_BAR_GEN, 1u);
-    } else {
-      // bounded by wall-clock time (1 s; a phase takes microseconds)
-      uint32_t it = 0;
-      unsigned long long t0 = 0;
-      while (ld_acquire_gpu(ctrl + CTRL_BAR_GEN) == g) {
-        if (ld_acquire_gpu(ctrl + CTRL_ABORT) != 0u) { ok = 0; break; }
-        ++it;
-        if (it == 32) t0 = globaltimer_ns();
-        if (it > 32) {
-          if ((it & 63) == 0 && globaltimer_ns() - t0 > 1000ull * 1000 * 1000) {
-            ok = 0;
-            atomicExch(ctrl + CTRL_ABORT, 1u);
-            set_status(status, SPEC_DEV_TIMEOUT);
-            break;
-          }
-          __nanosleep(40);
+    const uint32_t target = (gen + 1) * nblocks;
+    uint32_t seen;
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], 1;\n"
+                 : "=r"(seen) : "l"(ctrl + CTRL_BAR_COUNT) : "memory");
+    seen += 1;
+    // bounded by wall-clock time (1 s; a phase takes microseconds)
+    uint32_t it = 0;
+    unsigned long long t0 = 0;
+    while (seen < target) {
+      seen = ld_acquire_gpu(ctrl + CTRL_BAR_COUNT);
+      if (seen >= target) break;
+      ++it;
+      if ((it & 7) == 0 && ld_acquire_gpu(ctrl + CTRL_ABORT) != 0u) { ok = 0; break; }
+      if (it == 64) t0 = globaltimer_ns();
+      if (it > 64) {
+        if ((it & 63) == 0 && globaltimer_ns() - t0 > 1000ull * 1000 * 1000) {
+          ok = 0;
+          atomicExch(ctrl + CTRL_ABORT, 1u);
+          set_status(status, SPEC_DEV_TIMEOUT);
+          break;
         }
+        __nanosleep(32);
       }
     }
-    __threadfence();
-    gen = g + 1;
+    gen += 1;
     s_gs_ok = ok;
   }
   __syncthreads();
