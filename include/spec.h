@@ -413,9 +413,13 @@ const char* spec_status_string(int32_t status);
  *                        2 = tcgen05 with the accumulator in tensor memory
  *                        (default; used when r % 64 == 0)
  *   SPEC_OPT_TRACE       1 = the persistent draft records globaltimer stamps
- *                        of its phase boundaries in the workspace (profiling) */
+ *                        of its phase boundaries in the workspace (profiling)
+ *   SPEC_OPT_PERTURB     1 = test hook: every draft draw queued for
+ *                        re-decision first writes the next token instead of
+ *                        its own, so the re-decision changes it and the
+ *                        draft's later steps are redone (results unchanged)  */
 enum { SPEC_OPT_EPS_SCALE = 1, SPEC_OPT_FORCE_SIMT = 2, SPEC_OPT_BIAS_PATH = 3,
-       SPEC_OPT_TRACE = 5 };   /* 4 is unused */
+       SPEC_OPT_TRACE = 5, SPEC_OPT_PERTURB = 6 };   /* 4 is unused */
 int32_t spec_set_option(int32_t key, double value);
 
 /* Per-stage timing with CUDA events on the calls' streams.  enable(1)

@@ -61,6 +61,7 @@ double g_eps_scale = 1.0;
 bool g_force_simt = false;
 int g_bias_path = 2;          // 1 warp MMA, 2 tcgen05 (see SPEC_OPT_BIAS_PATH)
 bool g_trace = false;         // SPEC_OPT_TRACE
+bool g_perturb = false;       // SPEC_OPT_PERTURB
 
 // Band constants (probability units) of the certified first-pass decisions.
 // Largest first-pass margin error seen against the float64 oracle over C0-C4
@@ -84,6 +85,7 @@ Eps current_eps() {
   e.ratio = EPS_RATIO;
   e.norm = EPS_NORM;
   e.scale = (float)g_eps_scale;
+  e.perturb = g_perturb ? 1.f : 0.f;
   return e;
 }
 
@@ -180,7 +182,7 @@ Layout layout(const Shape& sh) {
   L.hpw_items = sh.B < kHpwItems ? sh.B : kHpwItems;
   L.hpw = take((size_t)L.hpw_items * sh.V * sizeof(float4));
   L.hpnorm = take((size_t)L.max_items * sizeof(float4));
-  L.rnnst = take((size_t)2 * sh.B * sh.r * sizeof(float));    // RNN head state ping-pong
+  L.rnnst = take((size_t)(sh.gamma + 1) * sh.B * sh.r * sizeof(float));   // RNN head states
   L.dpart = take(B * sh.NC * sizeof(float4));
   L.rowptr = take((B + 1) * sizeof(int));
   L.prow = take(B * g * sizeof(int2));
@@ -706,6 +708,9 @@ int32_t spec_set_option(int32_t key, double value) {
       return SPEC_OK;
     case SPEC_OPT_TRACE:
       g_trace = value != 0.0;
+      return SPEC_OK;
+    case SPEC_OPT_PERTURB:
+      g_perturb = value != 0.0;
       return SPEC_OK;
     default:
       return SPEC_EINVAL;

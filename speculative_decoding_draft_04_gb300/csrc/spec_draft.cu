@@ -428,7 +428,20 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
     // lse = cM / T + mM + log Z
     const df ref = dd_add_f(dd_mul_f(dd_recip(T), cM), mM);
     const double lse = dd_to_double(ref) + dd_log(Zdf, s_tab);
-    tokens[ok] = tok;
+    int wtok = tok;                   // the token written until a re-decision
+    if (fallback || dmargin <= band) {
+      uint32_t it = atomicAdd(counter, 1u);
+      if ((int)it < ws.max_items) {
+        if (eps.perturb != 0.f) wtok = tok + 1 < sh.V ? tok + 1 : 0;   // test hook
+        HpItem h;
+        h.b = b; h.j = k; h.kind = HP_DRAFT; h.prev = arow; h.u = u; h.fast_token = wtok;
+        h.shift_q = lse; h.shift_p = 0.0;
+        ws.items[it] = h;
+      } else {
+        set_status(status, SPEC_DEV_OVERFLOW);
+      }
+    }
+    tokens[ok] = wtok;
     q_tok[ok] = s_wtok * scale;
     lse_q[ok] = lse;
     if (diag) {
@@ -436,17 +449,6 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
       diag[ok * 4 + 1] = s_hi * scale;
       diag[ok * 4 + 2] = band;
       diag[ok * 4 + 3] = (float)tok;
-    }
-    if (fallback || dmargin <= band) {
-      uint32_t it = atomicAdd(counter, 1u);
-      if ((int)it < ws.max_items) {
-        HpItem h;
-        h.b = b; h.j = k; h.kind = HP_DRAFT; h.prev = arow; h.u = u; h.fast_token = tok;
-        h.shift_q = lse; h.shift_p = 0.0;
-        ws.items[it] = h;
-      } else {
-        set_status(status, SPEC_DEV_OVERFLOW);
-      }
     }
   }
   __syncthreads();
@@ -472,11 +474,13 @@ struct DraftParams {
   RnnParams rnn;     // RNN head (sh.rnn): gates before each step's tiles
 };
 
-// The whole draft in one cooperative launch: for each step k, the tile phase
-// (tiles strided over the CTAs), a grid barrier, the sampling phase (requests
-// strided over the CTAs), a grid barrier, and -- only when that step queued
-// near-boundary draws -- the two extended-precision phases, each followed by
-// a grid barrier.  Tensor memory is allocated once per CTA.
+// The whole draft in one cooperative launch: for each step k, [the RNN head's
+// gate phase and a grid barrier,] the tile phase (tiles strided over the CTAs,
+// then the previous step's near-boundary draws re-decided by the CTAs as they
+// finish their tiles), a grid barrier, the sampling phase (requests strided
+// over the CTAs) and a grid barrier; then the last step's re-decisions and,
+// if a re-decision changed a token, the steps after it again with their
+// re-decisions in place.  Tensor memory is allocated once per CTA.
 template <typename DT, int BM, int PATH>
 __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_constant__ DraftParams P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -509,11 +513,19 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
   const int n_tiles = sh.NS * n_mt;
   const uint32_t G = gridDim.x;
   unsigned long long* tr = (P.ws.trace && blockIdx.x == 0 && threadIdx.x == 0) ? P.ws.trace : nullptr;
-  for (int k = 0; k < sh.gamma; ++k) {
+  int n_prev = 0;          // draws the previous step queued for re-decision
+  uint32_t hp_base = 0;    // units taken from CTRL_HPNEXT so far (the same in every CTA)
+  // One draft step.  Deferred (the first pass over the steps): the previous
+  // step's queued draws are re-decided in this step's tile phase by CTAs that
+  // have finished their own tiles, taking units from a shared counter; this
+  // step's are left for the next.  A re-decision that changes a token marks
+  // the later steps of that request for a redo.  Not deferred (the redo):
+  // this step's draws are re-decided behind one more grid barrier.
+  auto run_step = [&](int k, bool deferred) -> bool {
     bool ok = true;
     if (sh.rnn) {
       rnn_gates_body<DT>(sh, k, (const DT*)P.W1, P.anchor, P.tokens, P.rnn, smem_raw, P.status);
-      if (!grid_sync(ctrl, G, gen, P.status)) break;
+      if (!grid_sync(ctrl, G, gen, P.status)) return false;
     }
     if (tr) tr[k * TRACE_SLOTS + 0] = globaltimer_ns();
     if constexpr (PATH == 2) {
@@ -529,28 +541,52 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
     }
     if (!ok) {
       if (threadIdx.x == 0) atomicExch(ctrl + CTRL_ABORT, 1u);
-      break;
+      return false;
+    }
+    if (deferred && n_prev > 0) {
+      hp_sums_body<DT>(sh, R, P.ws, 0, n_prev, smem_raw, true, P.tokens, P.q_tok, P.lse_q, P.status,
+                       nullptr, ctrl + CTRL_HPNEXT, hp_base, ctrl + CTRL_REDO);
+      hp_base += (uint32_t)(n_prev * sh.HB) + G;
     }
     if (tr) tr[k * TRACE_SLOTS + 1] = globaltimer_ns();
-    if (!grid_sync(ctrl, G, gen, P.status)) break;
+    if (!grid_sync(ctrl, G, gen, P.status)) return false;
     if (tr) tr[k * TRACE_SLOTS + 2] = globaltimer_ns();
     for (int b = blockIdx.x; b < sh.B; b += G)
       draft_sample_body<DT>(sh, k, b, U, W1, W2, P.anchor, P.temp, P.u_draft, P.tokens, P.q_tok,
                             P.lse_q, P.diag, P.status, P.ws, P.eps, ctrl + CTRL_STEP0 + k,
                             smem_raw);
     if (tr) tr[k * TRACE_SLOTS + 3] = globaltimer_ns();
-    if (!grid_sync(ctrl, G, gen, P.status)) break;
+    if (!grid_sync(ctrl, G, gen, P.status)) return false;
     if (tr) tr[k * TRACE_SLOTS + 4] = globaltimer_ns();
     const int n = min((int)__ldcg(ctrl + CTRL_STEP0 + k), P.ws.max_items);
-    if (n > 0) {
-      // block sums; the CTA that completes an item's last block re-decides it
+    n_prev = deferred ? n : 0;
+    if (!deferred && n > 0) {
       hp_sums_body<DT>(sh, R, P.ws, 0, n, smem_raw, true, P.tokens, P.q_tok, P.lse_q, P.status);
       if (tr) tr[k * TRACE_SLOTS + 5] = globaltimer_ns();
-      if (!grid_sync(ctrl, G, gen, P.status)) break;
+      if (!grid_sync(ctrl, G, gen, P.status)) return false;
     }
     if (tr) {
       tr[k * TRACE_SLOTS + 6] = globaltimer_ns();
       tr[k * TRACE_SLOTS + 7] = (unsigned long long)n;
+    }
+    return true;
+  };
+  bool good = true;
+  for (int k = 0; k < sh.gamma && good; ++k) good = run_step(k, true);
+  if (good && n_prev > 0) {
+    // the last step's draws, then the redo of every step after the earliest
+    // changed token (all requests: the others recompute the same values)
+    hp_sums_body<DT>(sh, R, P.ws, 0, n_prev, smem_raw, true, P.tokens, P.q_tok, P.lse_q, P.status);
+    good = grid_sync(ctrl, G, gen, P.status);
+  }
+  if (good) {
+    const uint32_t redo = __ldcg(ctrl + CTRL_REDO);
+    const int k0 = sh.gamma - (int)redo + 1;            // first step to redo
+    if (redo > 0 && k0 < sh.gamma) {
+      if (blockIdx.x == 0 && threadIdx.x == 0)
+        for (int k = k0; k < sh.gamma; ++k) ctrl[CTRL_STEP0 + k] = 0u;
+      good = grid_sync(ctrl, G, gen, P.status);
+      for (int k = k0; k < sh.gamma && good; ++k) good = run_step(k, false);
     }
   }
   if constexpr (PATH == 2) {

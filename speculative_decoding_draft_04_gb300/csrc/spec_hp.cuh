@@ -398,7 +398,7 @@ __device__ void hp_block(const Shape& sh, const HpRows& R, const Ws& ws, int pha
 template <typename DT>
 __device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, int item, int* tokens,
                                float* q_tok, double* lse_q, int* out_tokens, uint32_t* status,
-                               HpShared& S, DT* slab) {
+                               HpShared& S, DT* slab, uint32_t* redo = nullptr) {
   const HpItem it = ldcg_item(ws.items + item);
   const bool resid = it.kind == HP_RESID;
   // one scan of the chunk sums gives both the normaliser (its total) and the
@@ -530,7 +530,11 @@ __device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, i
       }
       if (status) {
         atomicAdd(status + 1, 1u);
-        if (tok != it.fast_token) atomicAdd(status + 2, 1u);
+        if (tok != it.fast_token) {
+          atomicAdd(status + 2, 1u);
+          // a draft token that changes invalidates that request's later steps
+          if (redo && it.kind == HP_DRAFT) atomicMax(redo, (uint32_t)(sh.gamma - it.j));
+        }
         atomicOr(status, (uint32_t)SPEC_DEV_REFINED);
       }
     }
@@ -539,20 +543,34 @@ __device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, i
 }
 
 // Block sums of the n queued items (phase 0: weights, phase 1: residuals of
-// residual items), grid-stride over (item, block of HPB columns).  With
-// `fused`, the CTA that completes an item's last block of its final pass
-// (phase 0 for draft and bonus items, phase 1 for residual items) re-decides
-// the item at once; the per-item counters start at zero and are left at zero.
+// residual items) over (item, block of HPB columns) units.  With `fused`, the
+// CTA that completes an item's last block of its final pass (phase 0 for draft
+// and bonus items, phase 1 for residual items) re-decides the item at once;
+// the per-item counters start at zero and are left at zero.  Units are strided
+// over the CTAs, or -- when `next` is given -- taken one at a time from the
+// counter *next (unit = *next - base; every CTA makes one last, failing take),
+// so CTAs that arrive early take more.  A changed draft token raises *redo to
+// gamma - step.
 template <typename DT>
 __device__ void hp_sums_body(const Shape& sh, const HpRows& R, const Ws& ws, int phase, int n,
                              unsigned char* dsm, bool fused = false, int* tokens = nullptr,
                              float* q_tok = nullptr, double* lse_q = nullptr,
-                             uint32_t* status = nullptr, int* out_tokens = nullptr) {
+                             uint32_t* status = nullptr, int* out_tokens = nullptr,
+                             uint32_t* next = nullptr, uint32_t base = 0, uint32_t* redo = nullptr) {
   DT* slab = reinterpret_cast<DT*>(dsm);        // [r][HPB] W2 columns of one block
   __shared__ HpShared S;
+  __shared__ uint32_t s_unit;
   hp_table(S.tab);
   __syncthreads();
-  for (int w = blockIdx.x; w < n * sh.HB; w += gridDim.x) {
+  const int total = n * sh.HB;
+  for (int w = blockIdx.x;; w += gridDim.x) {
+    if (next) {
+      __syncthreads();
+      if (threadIdx.x == 0) s_unit = atomicAdd(next, 1u) - base;
+      __syncthreads();
+      w = (int)min(s_unit, (uint32_t)total);
+    }
+    if (w >= total) break;
     const int item = w / sh.HB, blk = w - item * sh.HB;
     if (phase == 0) {
       __syncthreads();                          // the previous unit is done with the slab
@@ -580,7 +598,7 @@ __device__ void hp_sums_body(const Shape& sh, const HpRows& R, const Ws& ws, int
           if (threadIdx.x == 0) ws.hpnorm[item] = make_float4(izp.hi, izp.lo, izq.hi, izq.lo);
         }
         if ((it.kind == HP_RESID) == (phase == 1))
-          hp_decide_item<DT>(sh, R, ws, item, tokens, q_tok, lse_q, out_tokens, status, S, slab);
+          hp_decide_item<DT>(sh, R, ws, item, tokens, q_tok, lse_q, out_tokens, status, S, slab, redo);
         if (threadIdx.x == 0) ws.hpcnt[item] = 0u;
       }
     }

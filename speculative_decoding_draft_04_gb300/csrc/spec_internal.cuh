@@ -47,10 +47,13 @@ struct HpItem {
 
 // Control words at the start of the workspace.
 //   CTRL_BAR_COUNT / CTRL_ABORT: grid barrier of the persistent draft kernel
-//   (word 4 is unused); CTRL_STEP0 + k: queued re-decisions of draft step k.
+//   (word 4 is unused); CTRL_HPNEXT: re-decision units handed out in the
+//   draft's tile phases; CTRL_REDO: gamma - the earliest draft step whose
+//   token a deferred re-decision changed (0: none); CTRL_STEP0 + k: queued
+//   re-decisions of draft step k.
 enum {
   CTRL_ITEMS = 0, CTRL_SLOW = 1, CTRL_NPACKED = 2, CTRL_BAR_COUNT = 3,
-  CTRL_ABORT = 5, CTRL_STEP0 = 8, CTRL_WORDS = 32
+  CTRL_ABORT = 5, CTRL_HPNEXT = 6, CTRL_REDO = 7, CTRL_STEP0 = 8, CTRL_WORDS = 32
 };
 
 // Workspace views (host computes the offsets; see spec_abi.cu).
@@ -94,7 +97,7 @@ struct RnnParams {
   const void* Wr;        // [3r][2r] storage type
   const float* hproj;    // [B][gamma][3][r]
   void* arows;           // [gamma][B][r] storage type, out: the factor rows a_k
-  void* state;           // [2][B][r] storage type, scratch (s_k ping-pong)
+  void* state;           // [gamma+1][B][r] storage type, scratch: s_k of every step
 };
 
 // Inputs the extended-precision kernels read.
@@ -115,6 +118,7 @@ struct Eps {
   float ratio;   // relative band of a ratio test
   float norm;    // residual draws: error of the two row normalisers
   float scale;   // user multiplier (SPEC_OPT_EPS_SCALE)
+  float perturb; // test hook (SPEC_OPT_PERTURB): queued draft draws first write the next token
 };
 
 // ---------------------------------------------------------------- loads

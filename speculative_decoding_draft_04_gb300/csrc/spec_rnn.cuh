@@ -91,8 +91,8 @@ __device__ void rnn_gates_body(const Shape& sh, int k, const DT* __restrict__ W1
   if (nI <= 0) return;
   const DT* Wr = (const DT*)rp.Wr;
   DT* arows = (DT*)rp.arows + (size_t)k * B * r;
-  const DT* s_in = (const DT*)rp.state + (size_t)(k & 1) * B * r;
-  DT* s_out = (DT*)rp.state + (size_t)((k + 1) & 1) * B * r;
+  const DT* s_in = (const DT*)rp.state + (size_t)k * B * r;        // s_k
+  DT* s_out = (DT*)rp.state + (size_t)(k + 1) * B * r;              // s_{k+1}
   const bool last = k == sh.gamma - 1;
   int* list = reinterpret_cast<int*>(dsm);        // fp32: the whole list; bf16: after the stage
   __shared__ int s_n;
