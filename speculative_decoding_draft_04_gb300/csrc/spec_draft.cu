@@ -248,6 +248,7 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   __shared__ float s_a[256];
   __shared__ float s_part[NT / CW][CW];
   __shared__ int s_slice, s_tok;
+  __shared__ float4 s_pm;
   __shared__ float s_pref[2], s_lo, s_hi, s_wtok;
   __shared__ df s_tab[DD_EXP_TAB];
 
@@ -267,7 +268,9 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
     return;
   }
   const int arow = factor_row(sh, b, k, prev);
-  for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf(W1 + (size_t)arow * sh.r + i);
+  // the factor row (r <= NT entries, one per thread): loaded now, stored to
+  // shared memory only when the crossing chunk's dot product needs it
+  const float a_reg = (int)threadIdx.x < sh.r ? ldf(W1 + (size_t)arow * sh.r + threadIdx.x) : 0.f;
   const float invT = 1.0f / T;
   const float4* P = ws.dpart + (size_t)b * sh.NC;
 
@@ -296,8 +299,12 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
       s_slice = c2;
     }
     __syncthreads();
+    // the owner of the reference chunk passes its partial on
+    const int rs = s_slice;
+    if (rs >= s0 && rs < s1) s_pm = (rs - s0 < 8) ? pv[rs - s0] : __ldcg(P + rs);
+    __syncthreads();
   }
-  const float4 PM = __ldcg(P + s_slice);
+  const float4 PM = s_pm;
   const float cM = PM.x, mM = PM.y;
 
   // ---- chunk masses (double-float), normaliser and error-estimate sums
@@ -365,7 +372,11 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   const float fS = chunk_factor(PS, cM, mM, invT);
   const int n0 = sl * CW;
 
-  // ---- recompute the chunk's CW weights: 8 k-groups x CW columns
+  // ---- recompute the chunk's CW weights: 8 k-groups x CW columns (the U
+  // values of the chunk are requested before the W2 columns are staged)
+  const float u_reg =
+      (threadIdx.x < 32 && n0 + (int)threadIdx.x < sh.V) ? ldf(U + ok * sh.V + n0 + threadIdx.x) : 0.f;
+  if ((int)threadIdx.x < sh.r) s_a[threadIdx.x] = a_reg;
   stage_w2_slab<DT>(slab, W2, sh.V, 0, sh.r, n0, CW);
   {
     const int col = threadIdx.x % CW, grp = threadIdx.x / CW;
@@ -383,7 +394,7 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
       float bias = s_part[0][lane];
 #pragma unroll
       for (int g = 1; g < NT / CW; ++g) bias = __fadd_rn(bias, s_part[g][lane]);
-      w = fast_w(fast_x(ldf(U + ok * sh.V + v), PS.x, bias, invT), PS.y);
+      w = fast_w(fast_x(u_reg, PS.x, bias, invT), PS.y);
     }
     // target inside the chunk, in the chunk's units: (u Z - prefix) / fS
     const df tin = dd_mul(dd_add(target, dd_neg(pref)), dd_recip(fS));
