@@ -376,8 +376,10 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   // values of the chunk are requested before the W2 columns are staged)
   const float u_reg =
       (threadIdx.x < 32 && n0 + (int)threadIdx.x < sh.V) ? ldf(U + ok * sh.V + n0 + threadIdx.x) : 0.f;
+  issue_w2_slab<DT>(slab, W2, sh.V, 0, sh.r, n0, CW);
   if ((int)threadIdx.x < sh.r) s_a[threadIdx.x] = a_reg;
-  stage_w2_slab<DT>(slab, W2, sh.V, 0, sh.r, n0, CW);
+  cp_async_wait_all();
+  __syncthreads();
   {
     const int col = threadIdx.x % CW, grp = threadIdx.x / CW;
     const int kg = sh.r / (NT / CW);           // r % 16 == 0, so r / 8 is whole

@@ -36,6 +36,21 @@ __device__ __forceinline__ void stage_w2_slab(DT* dst, const DT* W2, int V, int 
   cp_async_wait_all();
   __syncthreads();
 }
+// The same copies, issued only (the caller waits with cp_async_wait_all and
+// __syncthreads before reading the slab).
+template <typename DT>
+__device__ __forceinline__ void issue_w2_slab(DT* dst, const DT* W2, int V, int i0, int KC, int c0,
+                                              int NC) {
+  constexpr int E = 16 / sizeof(DT);
+  const int cpr = NC / E;
+  for (int c = threadIdx.x; c < KC * cpr; c += NT) {
+    const int i = c / cpr, q = c - i * cpr;
+    const int n = c0 + q * E;
+    const bool valid = n < V;
+    cp_async16(dst + (size_t)i * NC + q * E, valid ? W2 + (size_t)(i0 + i) * V + n : W2, valid);
+  }
+  cp_async_commit();
+}
 
 // ---------------------------------------------------------------- warp MMA
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {

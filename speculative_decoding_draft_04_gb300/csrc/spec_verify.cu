@@ -646,13 +646,30 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
   const df invTdf = dd_recip(T);
   // (fp32 and double-float only below: GB300's fp64 rate is low)
 
-  // ---- alpha_j = sum over slices (double-float, fixed order)
-  for (int j = 0; j < sh.gamma; ++j) {
-    df a = {0.f, 0.f};
-    if (j < L)
-      for (int s = threadIdx.x; s < sh.NSV; s += NT) a = df_addf(a, ws.vpart[(size_t)(rp + j) * sh.NSV + s].x);
-    a = block_sum_df(a, sh_f);
-    if (threadIdx.x == 0) alpha[(size_t)b * sh.gamma + j] = j < L ? (float)df_d(a) : NAN;
+  // ---- alpha_j = sum over slices (double-float, fixed order): every row's
+  // per-thread sums first (all loads independent), then one reduction of all
+  // rows at once (warp shuffles, then one pass over the warps' partials)
+  {
+    df a[MAX_GAMMA];
+#pragma unroll
+    for (int j = 0; j < MAX_GAMMA; ++j) a[j] = {0.f, 0.f};
+    for (int s = threadIdx.x; s < sh.NSV; s += NT)
+#pragma unroll
+      for (int j = 0; j < MAX_GAMMA; ++j)
+        if (j < L) a[j] = df_addf(a[j], ws.vpart[(size_t)(rp + j) * sh.NSV + s].x);
+    __shared__ df s_al[NT / 32][MAX_GAMMA];
+#pragma unroll
+    for (int j = 0; j < MAX_GAMMA; ++j) {
+      const df t = warp_sum_df(a[j]);
+      if ((threadIdx.x & 31) == 0) s_al[threadIdx.x >> 5][j] = t;
+    }
+    __syncthreads();
+    if (threadIdx.x < sh.gamma) {
+      const int j = threadIdx.x;
+      df t = s_al[0][j];
+      for (int w = 1; w < NT / 32; ++w) t = df_add(t, s_al[w][j]);
+      alpha[(size_t)b * sh.gamma + j] = j < L ? (float)df_d(t) : NAN;
+    }
   }
 
   // ---- ratio tests and first reject (warp 0, lane j)
@@ -774,8 +791,16 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
   const DT* urow = U + ((size_t)b * sh.gamma + (resid ? row : 0)) * sh.V;
   float w = 0.f, fslice = 1.f;
   if (resid) {
-    for (int i = threadIdx.x; i < sh.r; i += NT) s_a[i] = ldf(W1 + (size_t)prev * sh.r + i);
-    stage_w2_slab<DT>(slab, W2, sh.V, 0, sh.r, n0, VB);
+    // the slice's U and target values and the factor row are requested before
+    // the W2 columns are staged
+    const bool lane_in = threadIdx.x < VB && n0 + (int)threadIdx.x < sh.V;
+    const float u_pre = lane_in ? ldf(urow + n0 + threadIdx.x) : -INFINITY;
+    const float t_pre = lane_in ? ldf(trow + n0 + threadIdx.x) : -INFINITY;
+    const float a_pre = (int)threadIdx.x < sh.r ? ldf(W1 + (size_t)prev * sh.r + threadIdx.x) : 0.f;
+    issue_w2_slab<DT>(slab, W2, sh.V, 0, sh.r, n0, VB);
+    if ((int)threadIdx.x < sh.r) s_a[threadIdx.x] = a_pre;
+    cp_async_wait_all();
+    __syncthreads();
     const int col = threadIdx.x % VB, grp = threadIdx.x / VB;
     const int kg = sh.r / (NT / VB);            // r % 16 == 0
     float acc = 0.f;
@@ -787,8 +812,8 @@ __global__ void __launch_bounds__(NT) verify_final_kernel(
       bias = s_part[0][threadIdx.x];
 #pragma unroll
       for (int g = 1; g < NT / VB; ++g) bias = __fadd_rn(bias, s_part[g][threadIdx.x]);
-      uv = ldf(urow + n0 + threadIdx.x);
-      tv = ldf(trow + n0 + threadIdx.x);
+      uv = u_pre;
+      tv = t_pre;
     }
     const float cU = block_max(uv, sh_f);
     const float cT = block_max(tv, sh_f);
