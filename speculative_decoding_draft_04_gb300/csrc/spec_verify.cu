@@ -213,7 +213,7 @@ __device__ __forceinline__ void lse_merge(float& m, df& acc, float invT, float* 
 // One CTA per target row j <= L_b of request b: its logsumexp; the bonus row
 // (j = L_b) also writes the per-VB-slice partials (c, s, p2) its draw needs.
 template <typename DT>
-__global__ void __launch_bounds__(NT) target_stats_kernel(Shape sh, const DT* __restrict__ target,
+__global__ void __launch_bounds__(NT, 5) target_stats_kernel(Shape sh, const DT* __restrict__ target,
                                                           const float* __restrict__ temp,
                                                           const int* __restrict__ vlen, Ws ws) {
   __shared__ float s_m[3 * (NT / 32)];
@@ -280,7 +280,8 @@ __global__ void __launch_bounds__(NT) target_stats_kernel(Shape sh, const DT* __
   } else {
     // other rows: per-thread online max and compensated sum over 16-byte
     // chunks strided by the block (coalesced), UNR chunks' loads in flight
-    constexpr int UNR = 8;
+    // (five CTAs per SM keep every row of a cycle resident at once)
+    constexpr int UNR = 4;
     const int nch = sh.V / 8;
     for (int c0 = threadIdx.x; c0 < nch; c0 += NT * UNR) {
       float vals[UNR][8];
