@@ -175,7 +175,7 @@ Layout layout(const Shape& sh) {
   const size_t B = sh.B, g = sh.gamma;
   L.max_items = sh.B;
   L.ctrl = take(CTRL_WORDS * sizeof(uint32_t));
-  L.trace = take(MAX_GAMMA * TRACE_SLOTS * sizeof(unsigned long long));
+  L.trace = take(2 * MAX_GAMMA * TRACE_SLOTS * sizeof(unsigned long long));
   L.items = take((size_t)L.max_items * sizeof(HpItem));
   L.hpsum = take((size_t)L.max_items * 3 * sh.NC * sizeof(float2));
   L.hpcnt = take((size_t)L.max_items * sizeof(uint32_t));

@@ -159,6 +159,7 @@ __device__ __forceinline__ float4 chunk_partial(const uint4 (&u)[4], float (&x)[
 // Draft step k on the warp-specialised engine of spec_tile_tc.cuh: the W1 row
 // of each request's previous token, and the epilogue of one tile row.
 struct DraftEpi {
+  static constexpr bool kHelpGather = true;   // epilogue warps help gather the A rows
   const Shape& sh;
   int k;
   const int* anchor;
@@ -544,8 +545,10 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
     if constexpr (PATH == 2) {
       const DraftEpi e{sh, k, P.anchor, P.tokens, P.temp, P.ws.dpart, &P.maps.u};
       const int n = (int)blockIdx.x < n_tiles ? (n_tiles - (int)blockIdx.x + (int)G - 1) / (int)G : 0;
+      unsigned long long* ttr = (P.ws.trace && blockIdx.x == 0)
+                                    ? P.ws.trace + (MAX_GAMMA + k) * TRACE_SLOTS : nullptr;
       ok = tp_run<BN>(e, sh, P.maps, reinterpret_cast<const bf16*>(W1), sh.NS, (int)blockIdx.x,
-                      (int)G, n, smem_raw, st, s_tok);
+                      (int)G, n, smem_raw, st, s_tok, ttr);
       if (!ok && threadIdx.x == 0) set_status(P.status, SPEC_DEV_TIMEOUT);
     } else {
       for (int t = blockIdx.x; t < n_tiles; t += G)

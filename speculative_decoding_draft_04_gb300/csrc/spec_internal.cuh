@@ -60,7 +60,8 @@ enum {
 constexpr int TRACE_SLOTS = 8;   // timestamps per draft step (persistent kernel trace)
 struct Ws {
   uint32_t* ctrl;       // [CTRL_WORDS]
-  unsigned long long* trace;  // [MAX_GAMMA][TRACE_SLOTS] globaltimer ns, CTA 0
+  unsigned long long* trace;  // [2][MAX_GAMMA][TRACE_SLOTS] globaltimer ns, CTA 0: the
+                              // draft's phases, then events inside its tile phase
   HpItem* items;        // [max_items]
   int max_items;
   float2* hpsum;        // [max_items][hp_cols][NC] chunk sums of the re-decided rows (hi, lo)

@@ -205,10 +205,31 @@ __device__ __forceinline__ const unsigned char* tp_uchunk(const unsigned char* u
 //                                            epilogue group, 0 when EG == 1)
 // `s_tok` is a 128-entry shared array for the gatherers.  Returns false if a
 // wait gave up (after draining what it started).
+// Copy the TC_M rows W1[tok[m]] (r bf16 each, tok < 0: zero row) into the
+// 128-byte-swizzled A tile with cp.async, thread q of `nt` taking 16-byte
+// chunks q, q + nt, ...; waits for its own copies.  r / 8 is a power of two
+// (r % 64 == 0 on this path).
+__device__ __forceinline__ void tp_gather_a(unsigned char* As, const bf16* W1, const int* tok, int r,
+                                            int q, int nt) {
+  const int lg = __ffs(r / 8) - 1;            // log2(chunks per row)
+  const int cmask = (r / 8) - 1;
+  for (int c = q; c < TC_M * (r / 8); c += nt) {
+    const int m = c >> lg, j = c & cmask;
+    const int t = tok[m];
+    const bool valid = t >= 0;
+    const bf16* src = valid ? W1 + (size_t)t * r + j * 8 : W1;
+    unsigned char* dst = As + (size_t)(j >> 3) * 16384 + m * 128 + (((j & 7) ^ (m & 7)) << 4);
+    cp_async16(dst, src, valid);
+  }
+  cp_async_commit();
+  cp_async_wait_all();
+}
+
 template <int N, class E, int EG = 1>
 __device__ __forceinline__ bool tp_run(const E& e, const Shape& sh, const TpMaps& maps,
                                        const bf16* W1, int nsl, int t0, int stride, int n,
-                                       unsigned char* smem_raw, TpState& st, int* s_tok) {
+                                       unsigned char* smem_raw, TpState& st, int* s_tok,
+                                       unsigned long long* ttr = nullptr) {
   static_assert(N == 64 || N == 128, "tile width");
   static_assert(EG == 1 || EG == 2, "epilogue groups");
   if (n <= 0) return true;
@@ -264,6 +285,7 @@ __device__ __forceinline__ bool tp_run(const E& e, const Shape& sh, const TpMaps
         }
         const int s = (int)(g % (uint32_t)lay.nw);
         if (!tp_wait(bar + TB_W2_FULL + s, (g / (uint32_t)lay.nw) & 1u, fail)) break;
+        if (ttr && i == 0) ttr[2] = globaltimer_ns();
         const int b = (int)(g & 1u);
         if (g >= 2 && !tp_wait(bar + TB_T_EMPTY + b, ((g >> 1) - 1) & 1u, fail)) break;
         tc_fence_after();
@@ -276,37 +298,48 @@ __device__ __forceinline__ bool tp_run(const E& e, const Shape& sh, const TpMaps
         }
         tc_commit(bar + TB_T_FULL + b);
         tc_commit(bar + TB_W2_EMPTY + s);
+        if (ttr && i == 0) ttr[3] = globaltimer_ns();
         if (i == n - 1 || mt_of(i + 1) != mt_of(i)) tc_commit(bar + TB_A_EMPTY);
       }
     }
   } else if (warp == 6 || warp == 7) {
-    // 64 gatherers; thread q copies 16-byte chunks q, q + 64, ... of the A tile
+    // 64 gatherers copy the A tile's rows (16-byte chunks); for the first
+    // request tile of the phase the 128 epilogue threads, idle until the first
+    // accumulator is ready, copy with them (E::kHelpGather).  The two 192-thread
+    // barriers of that first tile are always reached, also when a wait fails.
     const int q0 = threadIdx.x - 192;
-    const int cpr = r / 8;
     uint32_t ga = st.ga;
-    for (int i = 0; i < n && !*fail; ++i) {
-      if (i > 0 && mt_of(i) == mt_of(i - 1)) continue;
+    for (int i = 0; i < n; ++i) {
+      const bool helped = E::kHelpGather && i == 0;
+      if (!helped && (*fail || (i > 0 && mt_of(i) == mt_of(i - 1)))) {
+        if (*fail) break;
+        continue;
+      }
       // the last MMA that read the previous request tile's rows
-      if (ga >= 1 && !tp_wait(bar + TB_A_EMPTY, (ga - 1) & 1u, fail)) break;
+      const bool okw = ga < 1 || tp_wait(bar + TB_A_EMPTY, (ga - 1) & 1u, fail);
       ++ga;
       const int mt = mt_of(i);
-      for (int m = q0; m < TC_M; m += 64) s_tok[m] = e.token(mt, m);
-      named_bar(1, 64);
-      for (int c = q0; c < TC_M * cpr; c += 64) {
-        const int m = c / cpr, j = c - m * cpr;
-        const int tok = s_tok[m];
-        const bool valid = tok >= 0;
-        const bf16* src = valid ? W1 + (size_t)tok * r + j * 8 : W1;
-        unsigned char* dst = As + (size_t)(j >> 3) * 16384 + m * 128 + (((j & 7) ^ (m & 7)) << 4);
-        cp_async16(dst, src, valid);
-      }
-      cp_async_commit();
-      cp_async_wait_all();
+      if (okw)
+        for (int m = q0; m < TC_M; m += 64) s_tok[m] = e.token(mt, m);
+      if (helped) named_bar(2, 192); else named_bar(1, 64);
+      if (ttr && q0 == 0 && i == 0) ttr[0] = globaltimer_ns();
+      if (okw) tp_gather_a(As, W1, s_tok, r, helped ? 128 + q0 : q0, helped ? 192 : 64);
+      if (ttr && q0 == 0 && i == 0) ttr[1] = globaltimer_ns();
       fence_async_shared();
+      if (helped) named_bar(2, 192);          // the helpers' copies are in place too
+      if (!okw) break;
       mbar_arrive(bar + TB_A_FULL);
       named_bar(1, 64);          // s_tok is free for the next request tile
     }
   } else {
+    if constexpr (E::kHelpGather) {
+      // help copy the phase's first A tile (the gatherers pass the tokens;
+      // both barriers are reached by the gatherers in every case)
+      named_bar(2, 192);
+      if (!*fail) tp_gather_a(As, W1, s_tok, r, (int)threadIdx.x, 192);
+      fence_async_shared();
+      named_bar(2, 192);
+    }
     // epilogue: thread = row
     const int m = threadIdx.x & (TC_M - 1);
     const int grp = warp >= 8 ? 1 : 0;
@@ -316,14 +349,17 @@ __device__ __forceinline__ bool tp_run(const E& e, const Shape& sh, const TpMaps
       const int b = (int)(g & 1u);
       if (!tp_wait(bar + TB_U_FULL + b, (g >> 1) & 1u, fail)) break;
       if (!tp_wait(bar + TB_T_FULL + b, (g >> 1) & 1u, fail)) break;
+      if (ttr && threadIdx.x == 0 && i == 0) ttr[4] = globaltimer_ns();
       tc_fence_after();
       e.epilogue(mt_of(i), sl_of(i), m, smem + lay.offU + (size_t)b * TP_XBYTES,
                  st.tmem + lane_base + (uint32_t)(b * N), grp);
+      if (ttr && threadIdx.x == 0) ttr[i == 0 ? 5 : 6] = globaltimer_ns();
       tc_fence_before();
       mbar_arrive(bar + TB_T_EMPTY + b);
       mbar_arrive(bar + TB_U_EMPTY + b);
     }
   }
+  if (ttr && threadIdx.x == 0) ttr[7] = globaltimer_ns();
   // advance the running counters identically in every thread
   uint32_t segs = 0;
   for (int i = 0; i < n; ++i) segs += (i == 0 || mt_of(i) != mt_of(i - 1)) ? 1u : 0u;

@@ -430,6 +430,7 @@ __global__ void __launch_bounds__(NT) verify_tile_kernel(Shape sh, const DT* __r
 // tiles of 128, their previous tokens' W1 rows as the A operand, and per row
 // the slice partial (sum min(p, q), sum max(0, p - q), sum p^2, sum q^2).
 struct VerifyEpi {
+  static constexpr bool kHelpGather = false;
   const Shape& sh;
   const bf16* U;
   const bf16* T;
