@@ -160,6 +160,52 @@ int32_t spec_markov_draft(const spec_draft_args* args, spec_stream_t stream);
  * alpha, dev_status (and p_tok, diag when non-NULL).                        */
 int32_t spec_verify(const spec_verify_args* args, spec_stream_t stream);
 
+/* ----------------------------------------- one cycle from host memory */
+/* No counterpart on the pages: the end-to-end form of one speculative cycle
+ * (spec_markov_draft, then spec_verify) for callers whose per-step inputs
+ * arrive in host memory and who want the results there.
+ *
+ * The call enqueues, on `stream`: one cudaMemcpyAsync per input from its
+ * host buffer into the device buffer that `draft` / `verify` name (U,
+ * anchor, temperature, u_draft, verify_len, u_accept, u_final; target too
+ * when copy_stream is NULL), the draft, the verification, and one
+ * cudaMemcpyAsync per result back to host memory (accept_len, out_tokens;
+ * draft_tokens and alpha when their host pointers are non-NULL).  With
+ * copy_stream non-NULL the target logits, which only the verification
+ * reads, are copied on copy_stream while the draft runs: that copy starts
+ * after the other input copies on `stream` (so it neither races with the
+ * previous call's verification nor shares the link with U's copy), and the
+ * verification waits for it (two events, created and released by the call).
+ * The host results are valid once `stream` has been synchronised.  Host
+ * buffers should be page-locked (cudaHostAlloc, cudaHostRegister) for the
+ * copies to be asynchronous.
+ *
+ * `draft` and `verify` must describe one cycle: the same B, gamma, V, r,
+ * dtype, U, W1, W2, anchor, temperature and workspace, and verify's
+ * draft_tokens, q_tok, lse_q equal to draft's outputs.  Every host pointer
+ * except the two optional outputs must be non-NULL.  A violation, or any
+ * error spec_markov_draft / spec_verify would return, is reported before
+ * anything is enqueued; SPEC_ECUDA after a failed copy or launch (work
+ * enqueued before it stays enqueued).                                      */
+typedef struct {
+  spec_draft_args draft;        /* device buffers of the draft (inputs filled by the call) */
+  spec_verify_args verify;      /* device buffers of the verification             */
+  const void* h_U;              /* host [B][gamma][V] (dtype)   -> draft.U          */
+  const void* h_target;         /* host [B][gamma+1][V] (dtype) -> verify.target    */
+  const int32_t* h_anchor;      /* host [B]                     -> draft.anchor     */
+  const float* h_temperature;   /* host [B]                     -> draft.temperature */
+  const float* h_u_draft;       /* host [B][gamma]              -> draft.u_draft    */
+  const int32_t* h_verify_len;  /* host [B]                     -> verify.verify_len */
+  const float* h_u_accept;      /* host [B][gamma]              -> verify.u_accept  */
+  const float* h_u_final;       /* host [B]                     -> verify.u_final   */
+  int32_t* h_accept_len;        /* host out [B]                 <- verify.accept_len */
+  int32_t* h_out_tokens;        /* host out [B][gamma+1]        <- verify.out_tokens */
+  int32_t* h_draft_tokens;      /* optional host out [B][gamma] <- draft.draft_tokens */
+  float* h_alpha;               /* optional host out [B][gamma] <- verify.alpha     */
+  spec_stream_t copy_stream;    /* optional second stream for the target copy (NULL: none) */
+} spec_cycle_host_args;
+int32_t spec_cycle_host(const spec_cycle_host_args* args, spec_stream_t stream);
+
 /* ------------------------------------------------------------- RNN head */
 /* DSpark's RNN head ("[논문리뷰] DSpark", section 1.2, "RNN head"): a state s_k
  * (s_0 = 0) carries the block's prefix; with z = [s_j; W1[x_j]; h_{j+1}] the

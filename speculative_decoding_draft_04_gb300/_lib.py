@@ -26,7 +26,7 @@ EXPORTED = ("spec_workspace_bytes", "spec_markov_draft", "spec_markov_draft_stat
             "spec_num_stages", "spec_operating_point", "spec_acceptance_stats",
             "spec_confidence", "spec_schedule_workspace_bytes", "spec_prefix_schedule",
             "spec_rnn_draft", "spec_tree_select", "spec_tree_draft", "spec_tree_verify",
-            "spec_tree_workspace_bytes")
+            "spec_tree_workspace_bytes", "spec_cycle_host")
 
 
 class SpecError(RuntimeError):
@@ -50,6 +50,14 @@ class VerifyArgs(ctypes.Structure):
                 ("verify_len", _vp), ("u_accept", _vp), ("u_final", _vp), ("accept_len", _vp),
                 ("out_tokens", _vp), ("alpha", _vp), ("p_tok", _vp), ("dev_status", _vp),
                 ("a_rows", _vp), ("diag", _vp), ("workspace", _vp), ("workspace_bytes", _sz)]
+
+
+class CycleHostArgs(ctypes.Structure):
+    _fields_ = [("draft", DraftArgs), ("verify", VerifyArgs), ("h_U", _vp), ("h_target", _vp),
+                ("h_anchor", _vp), ("h_temperature", _vp), ("h_u_draft", _vp),
+                ("h_verify_len", _vp), ("h_u_accept", _vp), ("h_u_final", _vp),
+                ("h_accept_len", _vp), ("h_out_tokens", _vp), ("h_draft_tokens", _vp),
+                ("h_alpha", _vp), ("copy_stream", _vp)]
 
 
 class RnnDraftArgs(ctypes.Structure):
@@ -117,6 +125,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.spec_markov_draft.argtypes = [ctypes.POINTER(DraftArgs), _vp]
     L.spec_markov_draft_static.restype = _i32
     L.spec_markov_draft_static.argtypes = [ctypes.POINTER(DraftArgs), _vp]
+    L.spec_cycle_host.restype = _i32
+    L.spec_cycle_host.argtypes = [ctypes.POINTER(CycleHostArgs), _vp]
     L.spec_verify.restype = _i32
     L.spec_verify.argtypes = [ctypes.POINTER(VerifyArgs), _vp]
     L.spec_status_string.restype = ctypes.c_char_p
@@ -160,6 +170,17 @@ def _check(rc: int, what: str) -> None:
     if rc != 0:
         msg = lib().spec_status_string(rc).decode()
         raise SpecError(f"{what} failed: {rc} ({msg})")
+
+
+def _hptr(t) -> int | None:
+    """Address of a contiguous host (CPU) tensor."""
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise SpecError("host buffers must be CPU tensors")
+    if not t.is_contiguous():
+        raise SpecError("tensors must be contiguous")
+    return t.data_ptr()
 
 
 def _ptr(t) -> int | None:
@@ -235,6 +256,44 @@ def spec_verify(target, U, W1, W2, anchor, temperature, draft_tokens, q_tok, lse
                    _ptr(dev_status), _ptr(a_rows), _ptr(diag), _ptr(workspace),
                    workspace.numel() * workspace.element_size())
     _check(lib().spec_verify(ctypes.byref(a), _stream(stream)), "spec_verify")
+
+
+def spec_cycle_host(draft: DraftArgs, verify: VerifyArgs, h_U, h_target, h_anchor,
+                    h_temperature, h_u_draft, h_verify_len, h_u_accept, h_u_final, h_accept_len,
+                    h_out_tokens, h_draft_tokens=None, h_alpha=None, stream=None,
+                    copy_stream=None) -> None:
+    """Enqueue one cycle whose inputs and results live in host memory (CPU
+    tensors, page-locked for asynchronous copies); ``draft`` / ``verify``
+    name the device buffers (see include/spec.h)."""
+    a = CycleHostArgs(draft, verify, _hptr(h_U), _hptr(h_target), _hptr(h_anchor),
+                      _hptr(h_temperature), _hptr(h_u_draft), _hptr(h_verify_len),
+                      _hptr(h_u_accept), _hptr(h_u_final), _hptr(h_accept_len),
+                      _hptr(h_out_tokens), _hptr(h_draft_tokens), _hptr(h_alpha),
+                      None if copy_stream is None else int(copy_stream.cuda_stream))
+    _check(lib().spec_cycle_host(ctypes.byref(a), _stream(stream)), "spec_cycle_host")
+
+
+def draft_args(U, W1, W2, anchor, temperature, u_draft, draft_tokens, q_tok, lse_q, dev_status,
+               workspace, diag=None) -> DraftArgs:
+    """The spec_draft_args of these device tensors."""
+    B, gamma, V = U.shape
+    return DraftArgs(B, gamma, V, W1.shape[1], _dtype_code(U), _ptr(U), _ptr(W1), _ptr(W2),
+                     _ptr(anchor), _ptr(temperature), _ptr(u_draft), _ptr(draft_tokens),
+                     _ptr(q_tok), _ptr(lse_q), _ptr(dev_status), _ptr(diag), _ptr(workspace),
+                     workspace.numel() * workspace.element_size())
+
+
+def verify_args(target, U, W1, W2, anchor, temperature, draft_tokens, q_tok, lse_q, verify_len,
+                u_accept, u_final, accept_len, out_tokens, alpha, dev_status, workspace,
+                p_tok=None, diag=None, a_rows=None) -> VerifyArgs:
+    """The spec_verify_args of these device tensors."""
+    B, gamma, V = U.shape
+    return VerifyArgs(B, gamma, V, W1.shape[1], _dtype_code(U), _ptr(target), _ptr(U), _ptr(W1),
+                      _ptr(W2), _ptr(anchor), _ptr(temperature), _ptr(draft_tokens),
+                      _ptr(q_tok), _ptr(lse_q), _ptr(verify_len), _ptr(u_accept),
+                      _ptr(u_final), _ptr(accept_len), _ptr(out_tokens), _ptr(alpha),
+                      _ptr(p_tok), _ptr(dev_status), _ptr(a_rows), _ptr(diag), _ptr(workspace),
+                      workspace.numel() * workspace.element_size())
 
 
 def spec_profile_enable(on: bool) -> None:

@@ -437,19 +437,8 @@ int static_scratch_address(void** out) {
   *out = g_static_addr[dev];
   return SPEC_OK;
 }
-}  // namespace
-}  // namespace spec
-
-using namespace spec;
-
-extern "C" {
-
-size_t spec_workspace_bytes(int32_t B, int32_t gamma, int32_t V, int32_t r, int32_t dtype) {
-  if (check_shape(B, gamma, V, r, dtype) != SPEC_OK) return 0;
-  return layout(make_shape(B, gamma, V, r)).total;
-}
-
-int32_t spec_markov_draft(const spec_draft_args* a, spec_stream_t stream) {
+// Argument checks of spec_markov_draft / spec_verify (nothing enqueued).
+int32_t check_draft_args(const spec_draft_args* a) {
   if (!a) return SPEC_EINVAL;
   int rc = check_shape(a->B, a->gamma, a->V, a->r, a->dtype);
   if (rc != SPEC_OK) return rc;
@@ -464,11 +453,10 @@ int32_t spec_markov_draft(const spec_draft_args* a, spec_stream_t stream) {
   const size_t need = layout(make_shape(a->B, a->gamma, a->V, a->r)).total;
   if (!a->workspace || a->workspace_bytes < need) return SPEC_EWORKSPACE;
   if (!aligned(a->workspace, 256)) return SPEC_EALIGN;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  return a->dtype == SPEC_BF16 ? run_draft<bf16>(a, st) : run_draft<float>(a, st);
+  return SPEC_OK;
 }
 
-int32_t spec_verify(const spec_verify_args* a, spec_stream_t stream) {
+int32_t check_verify_args(const spec_verify_args* a) {
   if (!a) return SPEC_EINVAL;
   int rc = check_shape(a->B, a->gamma, a->V, a->r, a->dtype);
   if (rc != SPEC_OK) return rc;
@@ -487,8 +475,96 @@ int32_t spec_verify(const spec_verify_args* a, spec_stream_t stream) {
   const size_t need = layout(make_shape(a->B, a->gamma, a->V, a->r)).total;
   if (!a->workspace || a->workspace_bytes < need) return SPEC_EWORKSPACE;
   if (!aligned(a->workspace, 256)) return SPEC_EALIGN;
+  return SPEC_OK;
+}
+
+}  // namespace
+}  // namespace spec
+
+using namespace spec;
+
+extern "C" {
+
+size_t spec_workspace_bytes(int32_t B, int32_t gamma, int32_t V, int32_t r, int32_t dtype) {
+  if (check_shape(B, gamma, V, r, dtype) != SPEC_OK) return 0;
+  return layout(make_shape(B, gamma, V, r)).total;
+}
+
+int32_t spec_markov_draft(const spec_draft_args* a, spec_stream_t stream) {
+  const int32_t rc = check_draft_args(a);
+  if (rc != SPEC_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return a->dtype == SPEC_BF16 ? run_draft<bf16>(a, st) : run_draft<float>(a, st);
+}
+
+int32_t spec_verify(const spec_verify_args* a, spec_stream_t stream) {
+  const int32_t rc = check_verify_args(a);
+  if (rc != SPEC_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return a->dtype == SPEC_BF16 ? run_verify<bf16>(a, st) : run_verify<float>(a, st);
+}
+
+int32_t spec_cycle_host(const spec_cycle_host_args* c, spec_stream_t stream) {
+  if (!c) return SPEC_EINVAL;
+  const spec_draft_args* d = &c->draft;
+  const spec_verify_args* v = &c->verify;
+  int32_t rc = check_draft_args(d);
+  if (rc != SPEC_OK) return rc;
+  rc = check_verify_args(v);
+  if (rc != SPEC_OK) return rc;
+  if (d->B != v->B || d->gamma != v->gamma || d->V != v->V || d->r != v->r || d->dtype != v->dtype ||
+      d->U != v->U || d->W1 != v->W1 || d->W2 != v->W2 || d->anchor != v->anchor ||
+      d->temperature != v->temperature || d->workspace != v->workspace ||
+      d->draft_tokens != v->draft_tokens || d->q_tok != v->q_tok || d->lse_q != v->lse_q)
+    return SPEC_EINVAL;
+  if (!c->h_U || !c->h_target || !c->h_anchor || !c->h_temperature || !c->h_u_draft ||
+      !c->h_verify_len || !c->h_u_accept || !c->h_u_final || !c->h_accept_len || !c->h_out_tokens)
+    return SPEC_EINVAL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(c->copy_stream);
+  const size_t es = d->dtype == SPEC_BF16 ? 2 : 4;
+  const size_t B = (size_t)d->B, g = (size_t)d->gamma, V = (size_t)d->V;
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  cudaEvent_t ev_in = nullptr, ev_t = nullptr;
+  auto done = [&](int32_t r) {
+    if (ev_in) cudaEventDestroy(ev_in);      // released once the recorded work completes
+    if (ev_t) cudaEventDestroy(ev_t);
+    return r;
+  };
+#define SPEC_CUDA_OR_FAIL(x) \
+  do {                       \
+    if ((x) != cudaSuccess) return done(SPEC_ECUDA); \
+  } while (0)
+  SPEC_CUDA_OR_FAIL(cudaMemcpyAsync((void*)d->U, c->h_U, B * g * V * es, h2d, st));
+  SPEC_CUDA_OR_FAIL(cudaMemcpyAsync((void*)d->anchor, c->h_anchor, B * 4, h2d, st));
+  SPEC_CUDA_OR_FAIL(cudaMemcpyAsync((void*)d->temperature, c->h_temperature, B * 4, h2d, st));
+  SPEC_CUDA_OR_FAIL(cudaMemcpyAsync((void*)d->u_draft, c->h_u_draft, B * g * 4, h2d, st));
+  SPEC_CUDA_OR_FAIL(cudaMemcpyAsync((void*)v->verify_len, c->h_verify_len, B * 4, h2d, st));
+  SPEC_CUDA_OR_FAIL(cudaMemcpyAsync((void*)v->u_accept, c->h_u_accept, B * g * 4, h2d, st));
+  SPEC_CUDA_OR_FAIL(cudaMemcpyAsync((void*)v->u_final, c->h_u_final, B * 4, h2d, st));
+  const size_t tbytes = B * (g + 1) * V * es;
+  if (cs) {
+    SPEC_CUDA_OR_FAIL(cudaEventCreateWithFlags(&ev_in, cudaEventDisableTiming));
+    SPEC_CUDA_OR_FAIL(cudaEventCreateWithFlags(&ev_t, cudaEventDisableTiming));
+    SPEC_CUDA_OR_FAIL(cudaEventRecord(ev_in, st));
+    SPEC_CUDA_OR_FAIL(cudaStreamWaitEvent(cs, ev_in, 0));
+    SPEC_CUDA_OR_FAIL(cudaMemcpyAsync((void*)v->target, c->h_target, tbytes, h2d, cs));
+    SPEC_CUDA_OR_FAIL(cudaEventRecord(ev_t, cs));
+  } else {
+    SPEC_CUDA_OR_FAIL(cudaMemcpyAsync((void*)v->target, c->h_target, tbytes, h2d, st));
+  }
+  rc = d->dtype == SPEC_BF16 ? run_draft<bf16>(d, st) : run_draft<float>(d, st);
+  if (rc != SPEC_OK) return done(rc);
+  if (cs) SPEC_CUDA_OR_FAIL(cudaStreamWaitEvent(st, ev_t, 0));
+  rc = v->dtype == SPEC_BF16 ? run_verify<bf16>(v, st) : run_verify<float>(v, st);
+  if (rc != SPEC_OK) return done(rc);
+  SPEC_CUDA_OR_FAIL(cudaMemcpyAsync(c->h_accept_len, v->accept_len, B * 4, d2h, st));
+  SPEC_CUDA_OR_FAIL(cudaMemcpyAsync(c->h_out_tokens, v->out_tokens, B * (g + 1) * 4, d2h, st));
+  if (c->h_draft_tokens)
+    SPEC_CUDA_OR_FAIL(cudaMemcpyAsync(c->h_draft_tokens, d->draft_tokens, B * g * 4, d2h, st));
+  if (c->h_alpha) SPEC_CUDA_OR_FAIL(cudaMemcpyAsync(c->h_alpha, v->alpha, B * g * 4, d2h, st));
+#undef SPEC_CUDA_OR_FAIL
+  return done(SPEC_OK);
 }
 
 int32_t spec_rnn_draft(const spec_rnn_draft_args* ra, spec_stream_t stream) {

@@ -124,6 +124,66 @@ def cycle(d: DeviceWorkload, b: Buffers, stream=None) -> None:
 
 
 @dataclasses.dataclass
+class HostStep:
+    """One cycle's inputs and results in page-locked host memory."""
+    U: object
+    target: object
+    anchor: object
+    temperature: object
+    u_draft: object
+    verify_len: object
+    u_accept: object
+    u_final: object
+    accept_len: object
+    out_tokens: object
+    draft_tokens: object
+    alpha: object
+
+    @classmethod
+    def like(cls, d: DeviceWorkload) -> "HostStep":
+        """Pinned copies of d's per-cycle inputs, and pinned result buffers."""
+        import torch
+
+        def pin(t):
+            return t.cpu().pin_memory()
+
+        def out(shape, dtype):
+            return torch.empty(shape, dtype=dtype).pin_memory()
+        B, g = d.B, d.gamma
+        return cls(pin(d.U), pin(d.target), pin(d.anchor), pin(d.temperature), pin(d.u_draft),
+                   pin(d.verify_len), pin(d.u_accept), pin(d.u_final),
+                   out((B,), torch.int32), out((B, g + 1), torch.int32),
+                   out((B, g), torch.int32), out((B, g), torch.float32))
+
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in
+                   (self.U, self.target, self.anchor, self.temperature, self.u_draft,
+                    self.verify_len, self.u_accept, self.u_final))
+
+    def d2h_bytes(self, with_extras: bool = False) -> int:
+        ts = [self.accept_len, self.out_tokens] + ([self.draft_tokens, self.alpha]
+                                                   if with_extras else [])
+        return sum(t.numel() * t.element_size() for t in ts)
+
+
+def cycle_host(d: DeviceWorkload, b: Buffers, h: HostStep, stream=None, copy_stream=None,
+               extras: bool = False) -> None:
+    """One cycle through spec_cycle_host: h's inputs are copied into d's device
+    buffers, the cycle runs, and accept_len / out_tokens (with ``extras`` also
+    draft_tokens / alpha) are copied back into h."""
+    da = _lib.draft_args(d.U, d.W1, d.W2, d.anchor, d.temperature, d.u_draft, b.draft_tokens,
+                         b.q_tok, b.lse_q, b.dstatus, b.workspace, diag=b.ddiag)
+    va = _lib.verify_args(d.target, d.U, d.W1, d.W2, d.anchor, d.temperature, b.draft_tokens,
+                          b.q_tok, b.lse_q, d.verify_len, d.u_accept, d.u_final, b.accept_len,
+                          b.out_tokens, b.alpha, b.vstatus, b.workspace, p_tok=b.p_tok,
+                          diag=b.vdiag)
+    _lib.spec_cycle_host(da, va, h.U, h.target, h.anchor, h.temperature, h.u_draft,
+                         h.verify_len, h.u_accept, h.u_final, h.accept_len, h.out_tokens,
+                         h.draft_tokens if extras else None, h.alpha if extras else None,
+                         stream=stream, copy_stream=copy_stream)
+
+
+@dataclasses.dataclass
 class DeviceSchedule:
     """Confidence-head inputs, the cost table and the scheduler's outputs."""
     hidden: object

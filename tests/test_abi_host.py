@@ -91,6 +91,35 @@ def test_verify_host_validation(L):
     assert call() == -4
 
 
+def test_cycle_host_validation(L):
+    """spec_cycle_host checks both argument blocks, their agreement and the
+    host pointers before it enqueues anything."""
+    def cycle(**kw):
+        v = _lib.VerifyArgs(8, 4, 1024, 64, _lib.SPEC_BF16)
+        for f, _ in _lib.VerifyArgs._fields_[5:-2]:
+            setattr(v, f, 0x100000)
+        v.p_tok = v.diag = v.a_rows = None
+        v.workspace, v.workspace_bytes = 0x200000, 1 << 40
+        c = _lib.CycleHostArgs(_draft_args(), v)
+        for f, _ in _lib.CycleHostArgs._fields_[2:-3]:
+            setattr(c, f, 0x300000)
+        for k, val in kw.items():
+            obj, _, f = k.partition("__")
+            if f:
+                setattr(getattr(c, obj), f, val)
+            else:
+                setattr(c, k, val)
+        return L.spec_cycle_host(ctypes.byref(c), None)
+    assert L.spec_cycle_host(None, None) == -1
+    assert cycle(draft__U=None) == -1                   # the draft's own checks
+    assert cycle(verify__target=0x100002) == -3         # the verification's
+    assert cycle(verify__V=2048) == -1                  # the two blocks disagree
+    assert cycle(verify__draft_tokens=0x100100) == -1
+    assert cycle(verify__workspace=0x300000) == -1
+    assert cycle(h_target=None) == -1                   # a host input missing
+    assert cycle(h_out_tokens=None) == -1
+
+
 def test_status_strings_and_options(L):
     for code in (0, -1, -2, -3, -4, -5, 99):
         assert isinstance(_lib.spec_status_string(code), str)
