@@ -258,8 +258,7 @@ def tree_pass(args, w, d, flush, rank, dev):
 
 
 def algorithmic_bytes(w):
-    """Bytes a cycle must move at least (logits + W2 once per call), after the
-    survey's accounting: draft = B*g*V*s + r*V*s; verify = sum(L+1)*V*s (target
+    """Bytes a cycle must move at least (logits + W2 once per call): draft = B*g*V*s + r*V*s; verify = sum(L+1)*V*s (target
     rows) + sum(L)*V*s (U rows re-read to rebuild q) + r*V*s."""
     s = 2 if w.dtype == "bf16" else 4
     L = w.verify_len.astype(np.int64)

@@ -111,7 +111,9 @@ struct HpRows {
 };
 
 // Near-boundary band of a draw from a distribution with first-pass weights
-// (units: probability).  Calibrated constants; see the design doc.
+// (units: probability).  The constants are calibrated: the largest first-pass
+// errors measured against the float64 oracle over the seeded workloads, with
+// a safety factor.
 struct Eps {
   float elem;    // x sqrt(sum q^2): per-weight rounding of the first pass
   float slice;   // x sqrt(sum_slice mass^2): per-slice sums and factors

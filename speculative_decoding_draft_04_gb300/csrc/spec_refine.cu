@@ -24,7 +24,8 @@
 //                     recomputed and scanned, token written.
 //   slow_verify_kernel one CTA per request whose ratio test itself was near
 //                     its boundary: re-runs that request's verification with
-//                     extended-precision normalisers (rare).
+//                     extended-precision normalisers (rare: the uniform must
+//                     lie within a relative 1e-6 of the ratio).
 #include "spec_hp.cuh"
 
 namespace spec {
