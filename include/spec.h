@@ -241,17 +241,28 @@ int32_t spec_rnn_draft(const spec_rnn_draft_args* args, spec_stream_t stream);
  * that owns the allocator.  spec_markov_draft_static does the same work as
  * spec_markov_draft but ignores args->workspace / workspace_bytes and uses a
  * scratch area of SPEC_STATIC_SCRATCH_BYTES compiled into the library as
- * device memory; every GPU that loads the library holds that area until the
- * process exits.  It never calls cudaMalloc, cudaFree or any allocating
+ * device memory.  It never calls cudaMalloc, cudaFree or any allocating
  * library routine.
+ *
+ *   - When the area is committed: the area belongs to the library's device
+ *     code, so it is committed on a device when that code is loaded there.
+ *     With lazy module loading (CUDA_MODULE_LOADING=LAZY, the default since
+ *     CUDA 12) that is the first call of ANY spec_* entry point on that
+ *     device (or this entry point's address look-up); with eager loading it
+ *     is when the CUDA context is created.  Either way the device then holds
+ *     the 32 MiB until the process exits.  Callers under a fixed memory
+ *     budget should count it from their first library call on a device, and
+ *     callers that capture streams should make that first library call
+ *     before any capture begins.
  *
  *   - Size limit: the draft scratch is 128 + B*40 + B*ceil(V/32)*8 + B*4 +
  *     B*ceil(V/32)*16 bytes (each term rounded up to 256); larger problems
  *     are rejected with SPEC_EWORKSPACE before anything is enqueued.  All five
  *     named workloads fit (C4, the largest, needs about 24 MiB).
- *   - The first call on a device looks up the area's device address with
- *     cudaGetSymbolAddress (with that device current) and caches it; make
- *     that first call before any stream capture.
+ *   - The first call of this entry point on a device looks up the area's
+ *     device address with cudaGetSymbolAddress (with that device current)
+ *     and caches it per device; make that first call before any stream
+ *     capture too.
  *   - All calls in the process share the one area, and it keeps the previous
  *     call's contents (the call clears the words that must start at zero).
  *     Calls whose GPU work overlaps -- on different streams, or from

@@ -140,20 +140,28 @@ struct ProfScope {
   }
 };
 
-int g_num_sms = -1;
-int num_sms();
-int grid_for_refine() { return 2 * num_sms(); }
+// SM count of the current device, cached per device ordinal: the cooperative
+// draft sizes its grid from it, so a process that drives devices with
+// different SM counts gets each device's own figure.  0 when the device
+// cannot be queried (the launch then fails with SPEC_ECUDA).
+constexpr int kMaxSmDevices = 64;
+int g_num_sms[kMaxSmDevices] = {};
 int num_sms() {
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (g_num_sms < 0) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 132;
-    g_num_sms = n;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev >= kMaxSmDevices) {
+    int n = 0;
+    return cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess ? n : 0;
   }
-  return g_num_sms;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_num_sms[dev] <= 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
 }
+int grid_for_refine() { return 2 * num_sms(); }
 
 // ---------------------------------------------------------------- workspace
 // Residual re-decisions whose weights are kept between their two passes.
@@ -270,13 +278,15 @@ int launch_draft(const spec_draft_args* a, const Shape& sh, const Ws& ws, cudaSt
     std::lock_guard<std::mutex> lk(g_mu);
     path = g_force_simt ? 0 : g_bias_path;
   }
+  const int nsm = num_sms();
+  if (nsm <= 0) return SPEC_ECUDA;
   SPEC_TRY(cudaMemsetAsync(a->dev_status, 0, 4 * sizeof(uint32_t), st));
   SPEC_TRY(cudaMemsetAsync(ws.ctrl, 0, CTRL_WORDS * sizeof(uint32_t), st));
   SPEC_TRY(cudaMemsetAsync(ws.hpcnt, 0, (size_t)ws.max_items * sizeof(uint32_t), st));
   ProfScope p(st, ST_DRAFT_PERSISTENT);
   SPEC_TRY(launch_draft_persistent<DT>(sh, a->U, a->W1, a->W2, a->anchor, a->temperature, a->u_draft,
                                        a->draft_tokens, a->q_tok, a->lse_q, a->diag, a->dev_status,
-                                       ws, current_eps(), path, num_sms(), st, rnn));
+                                       ws, current_eps(), path, nsm, st, rnn));
   return SPEC_OK;
 }
 
@@ -331,6 +341,7 @@ int run_verify(const spec_verify_args* a, cudaStream_t st) {
     path = g_force_simt ? 0 : g_bias_path;
   }
   const int grid = grid_for_refine();
+  if (grid <= 0) return SPEC_ECUDA;
   HpRows R{a->target, a->U, F, a->W2, a->temperature};
   SPEC_TRY(cudaMemsetAsync(a->dev_status, 0, 4 * sizeof(uint32_t), st));
   {

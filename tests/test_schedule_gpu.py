@@ -251,3 +251,39 @@ def test_scheduled_cycle_parity(torch, name, B):
                   b.out_tokens.cpu().numpy(), b.alpha.cpu().numpy(), b.p_tok.cpu().numpy(),
                   engine.status_words(b.dstatus), engine.status_words(b.vstatus))
     assert_parity(compare(w2, g, oracle_cycle(w2)))
+
+
+@pytest.mark.parametrize("name,B", [("C0", None), ("C1", None), ("C2", None), ("C3", 32), ("C4", 96)])
+def test_schedule_from_the_oracles_own_confidences(torch, name, B):
+    """The whole schedule derived from the ORACLE's confidences (float64 value
+    rounded once to fp32), not from the kernel's: verify lengths, B, tau and
+    Theta must equal the kernel's.  Where a kernel confidence differs from the
+    oracle's by one ulp (within 1e-12 of a rounding midpoint), the two
+    schedules are both computed and any change of l, B or Theta is reported."""
+    from speculative_decoding_draft_04_gb300 import engine
+    spec = W.config(name)
+    w = W.make_workload(spec, 0, B=B)
+    si = W.make_schedule_inputs(spec, 0, B=B)
+    d = engine.DeviceWorkload.from_workload(w)
+    b = engine.Buffers.for_workload(d)
+    s = engine.DeviceSchedule.from_inputs(si, w.B, w.gamma, w.dtype)
+    engine.scheduled_cycle(d, b, s)
+    torch.cuda.synchronize()
+    tokens = b.draft_tokens.cpu().numpy()
+    conf = s.conf.cpu().numpy()
+    ell_k, tot_k = s.verify_len.cpu().numpy(), s.totals.cpu().numpy()
+    theta_k = float(s.theta.item())
+    ref = S.confidences(W.to_f64(si.hidden, w.dtype), w.f64("W1"), si.w.astype(np.float64),
+                        w.anchor, tokens)
+    ref32 = ref.astype(np.float32)
+    ell_o, B_o, tau_o, th_o = S.schedule(S.survival(ref32), si.sps)
+    bad, far = conf_far_mismatches(conf, ref)
+    assert not far
+    same = (np.array_equal(ell_o, ell_k) and tot_k[0] == B_o and tot_k[1] == tau_o and th_o == theta_k)
+    if len(bad) == 0:
+        assert same, (name, np.flatnonzero(ell_o != ell_k)[:10], tot_k, B_o, tau_o, th_o, theta_k)
+    else:
+        print(f"{name}: {len(bad)} confidences one ulp from the oracle's (rounding midpoints); "
+              f"schedule {'unchanged' if same else 'CHANGED'}: l diff at "
+              f"{np.flatnonzero(ell_o != ell_k)[:10].tolist()}, B {tot_k[0]} vs {B_o}, "
+              f"Theta {theta_k} vs {th_o}")
