@@ -266,6 +266,7 @@ def algorithmic_bytes(w):
     verify = int((L + 1).sum()) * w.V * s + int(L.sum()) * w.V * s + w.r * w.V * s
     per_stage = {
         "draft_persistent": draft,                                  # per launch (whole draft)
+        "draft_slice": draft,                                       # the same, slice-resident kernel
         "target_stats": int((L + 1).sum()) * w.V * s,
         "verify_tile": int(L.sum()) * w.V * s + w.r * w.V * s,
     }
@@ -508,7 +509,9 @@ def main():
     barrier()
     e2e_ms = float(sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps)
 
-    op = operating_point(d, bufs, prof.get("draft_persistent", (0.0, 0)), args.steps) \
+    draft_prof = tuple(a + b for a, b in zip(prof.get("draft_persistent", (0.0, 0)),
+                                               prof.get("draft_slice", (0.0, 0))))
+    op = operating_point(d, bufs, draft_prof, args.steps) \
         if rank == 0 else None
     sched = rnn = tree = None
     if not args.no_extras:

@@ -150,10 +150,15 @@ size_t spec_workspace_bytes(int32_t B, int32_t gamma, int32_t V, int32_t r, int3
 /* Draft gamma tokens per request.  Reads U, W1, W2, anchor, temperature,
  * u_draft; writes draft_tokens, q_tok, lse_q, dev_status (and diag).
  * The work is three cudaMemsetAsync (dev_status, the workspace's control
- * words and counters) and ONE cooperative kernel launch on `stream` with one CTA per SM
- * (fewer when there are fewer tiles); it returns SPEC_ECUDA when the device
- * cannot make the CTAs co-resident.  Its grid barriers are bounded waits: a
- * barrier that gives up sets SPEC_DEV_TIMEOUT and every CTA returns.       */
+ * words and counters) and ONE cooperative kernel launch on `stream` with at
+ * most one CTA per SM; it returns SPEC_ECUDA when the device cannot make the
+ * CTAs co-resident.  Two kernels serve it: for bf16 with r % 64 == 0,
+ * B <= 128 and V <= 256 x (SM count) (C1/C2-class shapes) the slice-resident
+ * kernel, in which each CTA keeps the W2 columns of one vocabulary slice in
+ * shared memory for all gamma steps; otherwise the tile-strided kernel.  Both
+ * give the same results (see SPEC_OPT_DRAFT_KERNEL).  Its grid barriers are
+ * bounded waits: a barrier that gives up sets SPEC_DEV_TIMEOUT and every CTA
+ * returns.                                                                 */
 int32_t spec_markov_draft(const spec_draft_args* args, spec_stream_t stream);
 
 /* Verify one drafted block per request.  Writes accept_len, out_tokens,
@@ -471,12 +476,26 @@ const char* spec_status_string(int32_t status);
  *                        (default; used when r % 64 == 0)
  *   SPEC_OPT_TRACE       1 = the persistent draft records globaltimer stamps
  *                        of its phase boundaries in the workspace (profiling)
- *   SPEC_OPT_PERTURB     1 = test hook: every draft draw queued for
- *                        re-decision first writes the next token instead of
- *                        its own, so the re-decision changes it and the
- *                        draft's later steps are redone (results unchanged)  */
+ *   SPEC_OPT_PERTURB     1 = test hook: the draft runs a test build of its
+ *                        kernel in which every draw queued for re-decision
+ *                        first writes the next token instead of its own, so
+ *                        the re-decision changes it and the draft's later
+ *                        steps are redone (results unchanged)
+ *   SPEC_OPT_TEST_STALL  1 = test hook: the draft runs a test build of its
+ *                        kernel whose first grid barrier waits for one CTA
+ *                        more than the grid has; the wait gives up after its
+ *                        one-second limit, dev_status gets SPEC_DEV_TIMEOUT,
+ *                        the outputs are left unspecified, and the kernel
+ *                        returns with its copies drained and its tensor
+ *                        memory freed (the CUDA context stays usable)
+ *   SPEC_OPT_DRAFT_KERNEL  0 = the slice-resident draft kernel wherever the
+ *                        shape fits it (default), 1 = always the tile-strided
+ *                        draft kernel
+ * The two test hooks exist for the library's own tests; the default kernels
+ * carry no trace of them.                                                   */
 enum { SPEC_OPT_EPS_SCALE = 1, SPEC_OPT_FORCE_SIMT = 2, SPEC_OPT_BIAS_PATH = 3,
-       SPEC_OPT_TRACE = 5, SPEC_OPT_PERTURB = 6 };   /* 4 is unused */
+       SPEC_OPT_TRACE = 5, SPEC_OPT_PERTURB = 6, SPEC_OPT_TEST_STALL = 7,
+       SPEC_OPT_DRAFT_KERNEL = 8 };   /* 4 is unused */
 int32_t spec_set_option(int32_t key, double value);
 
 /* Per-stage timing with CUDA events on the calls' streams.  enable(1)

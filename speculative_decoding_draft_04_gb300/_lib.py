@@ -17,6 +17,8 @@ LIB_PATH = os.path.join(HERE, "libspec.so")
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_OPT_EPS_SCALE, SPEC_OPT_FORCE_SIMT, SPEC_OPT_BIAS_PATH, SPEC_OPT_TRACE = 1, 2, 3, 5
 SPEC_OPT_PERTURB = 6
+SPEC_OPT_TEST_STALL = 7
+SPEC_OPT_DRAFT_KERNEL = 8
 DEV_BITS = {1: "BAD_TOKEN", 2: "BAD_LEN", 4: "BAD_TEMP", 8: "TIMEOUT", 16: "REFINED",
             32: "OVERFLOW", 64: "BAD_CONF", 128: "BAD_TREE"}
 

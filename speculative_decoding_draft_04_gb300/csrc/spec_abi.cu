@@ -13,7 +13,10 @@ template <typename DT>
 cudaError_t launch_draft_persistent(const Shape&, const void*, const void*, const void*, const int*,
                                     const float*, const float*, int*, float*, double*, float*,
                                     uint32_t*, const Ws&, const Eps&, int, int, cudaStream_t,
-                                    const RnnParams*);
+                                    const RnnParams*, int);
+cudaError_t launch_draft_slice(const Shape&, const void*, const void*, const void*, const int*,
+                               const float*, const float*, int*, float*, double*, float*, uint32_t*,
+                               const Ws&, const Eps&, int, cudaStream_t, int);
 cudaError_t launch_verify_prep(const Shape&, const int*, const float*, const int*, const double*,
                                const int*, const Ws&, uint32_t*, int*, int*, float*, float*,
                                cudaStream_t);
@@ -61,7 +64,9 @@ double g_eps_scale = 1.0;
 bool g_force_simt = false;
 int g_bias_path = 2;          // 1 warp MMA, 2 tcgen05 (see SPEC_OPT_BIAS_PATH)
 bool g_trace = false;         // SPEC_OPT_TRACE
-bool g_perturb = false;       // SPEC_OPT_PERTURB
+bool g_perturb = false;       // SPEC_OPT_PERTURB (test build of the draft kernels)
+bool g_stall = false;         // SPEC_OPT_TEST_STALL (test build of the draft kernels)
+int g_draft_kernel = 0;       // SPEC_OPT_DRAFT_KERNEL: 0 slice-resident where it fits, 1 tile-strided
 
 // Band constants (probability units) of the certified first-pass decisions.
 // Largest first-pass margin error seen against the float64 oracle over C0-C4
@@ -85,19 +90,18 @@ Eps current_eps() {
   e.ratio = EPS_RATIO;
   e.norm = EPS_NORM;
   e.scale = (float)g_eps_scale;
-  e.perturb = g_perturb ? 1.f : 0.f;
   return e;
 }
 
 // ---------------------------------------------------------------- profiling
 enum Stage {
-  ST_DRAFT_PERSISTENT, ST_VERIFY_PREP,
+  ST_DRAFT_PERSISTENT, ST_DRAFT_SLICE, ST_VERIFY_PREP,
   ST_TARGET_STATS, ST_VERIFY_TILE, ST_VERIFY_FINAL, ST_SLOW_VERIFY, ST_VERIFY_HP_SUMS,
   ST_VERIFY_HP_RESID, ST_CONFIDENCE, ST_SCHED_RANK, ST_SCHED_SELECT, ST_TREE_SELECT,
   ST_TREE_DRAFT, ST_TREE_VERIFY, ST_COUNT
 };
 const char* kStageNames[ST_COUNT] = {
-    "draft_persistent", "verify_prep",
+    "draft_persistent", "draft_slice", "verify_prep",
     "target_stats", "verify_tile", "verify_final", "slow_verify", "verify_hp_sums",
     "verify_hp_resid", "confidence", "sched_rank", "sched_select", "tree_select",
     "tree_draft", "tree_verify"};
@@ -169,7 +173,7 @@ constexpr int kHpwItems = 16;
 struct Layout {
   size_t ctrl, trace, items, hpsum, hpcnt, hpw, hpnorm, rnnst, dpart, rowptr, prow, prevtok, vflags, lse_p, bpart, vpart, slow,
       accbits, rowc, rowp, total;
-  int max_items, hpw_items;
+  int max_items, item_cap, hpw_items;
 };
 
 Layout layout(const Shape& sh) {
@@ -182,9 +186,10 @@ Layout layout(const Shape& sh) {
   };
   const size_t B = sh.B, g = sh.gamma;
   L.max_items = sh.B;
+  L.item_cap = sh.B * sh.gamma;
   L.ctrl = take(CTRL_WORDS * sizeof(uint32_t));
   L.trace = take(2 * MAX_GAMMA * TRACE_SLOTS * sizeof(unsigned long long));
-  L.items = take((size_t)L.max_items * sizeof(HpItem));
+  L.items = take((size_t)L.item_cap * sizeof(HpItem));
   L.hpsum = take((size_t)L.max_items * 3 * sh.NC * sizeof(float2));
   L.hpcnt = take((size_t)L.max_items * sizeof(uint32_t));
   L.hpw_items = sh.B < kHpwItems ? sh.B : kHpwItems;
@@ -214,6 +219,7 @@ Ws views(const Layout& L, void* base) {
   w.trace = nullptr;
   w.items = reinterpret_cast<HpItem*>(p + L.items);
   w.max_items = L.max_items;
+  w.item_cap = L.item_cap;
   w.hpsum = reinterpret_cast<float2*>(p + L.hpsum);
   w.hp_cols = 3;
   w.hpcnt = reinterpret_cast<uint32_t*>(p + L.hpcnt);
@@ -270,23 +276,39 @@ Shape make_shape(int B, int gamma, int V, int r) {
 
 // The whole draft: one cooperative launch (the control words are zeroed first
 // on the same stream; the grid barrier counts on it).
+// The slice-resident kernel (spec_draft_slice.cu) runs the Markov head on the
+// tensor path when the shape fits it (B <= 128, V <= 256 columns per SM);
+// otherwise, and for the RNN head, the tile-strided kernel (spec_draft.cu).
 template <typename DT>
 int launch_draft(const spec_draft_args* a, const Shape& sh, const Ws& ws, cudaStream_t st,
                  const RnnParams* rnn = nullptr) {
-  int path;
+  int path, hook, kernel;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     path = g_force_simt ? 0 : g_bias_path;
+    hook = g_perturb ? HOOK_PERTURB : (g_stall ? HOOK_STALL : HOOK_NONE);
+    kernel = g_draft_kernel;
   }
   const int nsm = num_sms();
   if (nsm <= 0) return SPEC_ECUDA;
   SPEC_TRY(cudaMemsetAsync(a->dev_status, 0, 4 * sizeof(uint32_t), st));
   SPEC_TRY(cudaMemsetAsync(ws.ctrl, 0, CTRL_WORDS * sizeof(uint32_t), st));
   SPEC_TRY(cudaMemsetAsync(ws.hpcnt, 0, (size_t)ws.max_items * sizeof(uint32_t), st));
+  const Eps eps = current_eps();
+  if constexpr (sizeof(DT) == 2) {
+    if (path == 2 && !rnn && kernel == 0) {
+      ProfScope p(st, ST_DRAFT_SLICE);
+      const cudaError_t e = launch_draft_slice(sh, a->U, a->W1, a->W2, a->anchor, a->temperature,
+                                               a->u_draft, a->draft_tokens, a->q_tok, a->lse_q, a->diag,
+                                               a->dev_status, ws, eps, nsm, st, hook);
+      if (e == cudaSuccess) return SPEC_OK;
+      if (e != cudaErrorNotSupported) return SPEC_ECUDA;
+    }
+  }
   ProfScope p(st, ST_DRAFT_PERSISTENT);
   SPEC_TRY(launch_draft_persistent<DT>(sh, a->U, a->W1, a->W2, a->anchor, a->temperature, a->u_draft,
                                        a->draft_tokens, a->q_tok, a->lse_q, a->diag, a->dev_status,
-                                       ws, current_eps(), path, nsm, st, rnn));
+                                       ws, eps, path, nsm, st, rnn, hook));
   return SPEC_OK;
 }
 
@@ -393,8 +415,9 @@ Layout draft_only_layout(const Shape& sh) {
     return o;
   };
   L.max_items = sh.B;
+  L.item_cap = sh.B * sh.gamma;
   L.ctrl = take(CTRL_WORDS * sizeof(uint32_t));
-  L.items = take((size_t)L.max_items * sizeof(HpItem));
+  L.items = take((size_t)L.item_cap * sizeof(HpItem));
   L.hpsum = take((size_t)L.max_items * sh.NC * sizeof(float2));
   L.hpcnt = take((size_t)L.max_items * sizeof(uint32_t));
   L.dpart = take((size_t)sh.B * sh.NC * sizeof(float4));
@@ -408,6 +431,7 @@ Ws draft_only_views(const Layout& L, void* base) {
   w.ctrl = reinterpret_cast<uint32_t*>(p + L.ctrl);
   w.items = reinterpret_cast<HpItem*>(p + L.items);
   w.max_items = L.max_items;
+  w.item_cap = L.item_cap;
   w.hpsum = reinterpret_cast<float2*>(p + L.hpsum);
   w.hp_cols = 1;
   w.hpcnt = reinterpret_cast<uint32_t*>(p + L.hpcnt);
@@ -798,6 +822,13 @@ int32_t spec_set_option(int32_t key, double value) {
       return SPEC_OK;
     case SPEC_OPT_PERTURB:
       g_perturb = value != 0.0;
+      return SPEC_OK;
+    case SPEC_OPT_TEST_STALL:
+      g_stall = value != 0.0;
+      return SPEC_OK;
+    case SPEC_OPT_DRAFT_KERNEL:
+      if (value != 0.0 && value != 1.0) return SPEC_EINVAL;
+      g_draft_kernel = (int)value;
       return SPEC_OK;
     default:
       return SPEC_EINVAL;

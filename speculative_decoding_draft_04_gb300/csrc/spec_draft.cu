@@ -21,8 +21,7 @@
 //             phases of spec_hp.cuh.
 #include <cstring>
 
-#include "spec_tile_tc.cuh"
-#include "spec_hp.cuh"
+#include "spec_sample.cuh"
 #include "spec_rnn.cuh"
 #include "spec_tmap.cuh"
 
@@ -118,44 +117,6 @@ __device__ void draft_tile_body(const Shape& sh, int k, int slice, int mtile, co
   }
 }
 
-// ---------------------------------------------------------------- tensor-memory tiles
-// Partial (c, m, s, q2) of one CW-column chunk of a row from its packed bf16
-// logits `u` (16 words) and its bias row `x` (overwritten with the tempered
-// logits); `nv` valid columns.  Four interleaved max / Kahan / square-sum
-// chains keep the dependent-latency per column low.
-template <bool FULL>
-__device__ __forceinline__ float4 chunk_partial(const uint4 (&u)[4], float (&x)[32], int nv, float invT) {
-  auto uval = [&](int i) {
-    const uint4 q = u[i >> 3];
-    const uint32_t w = ((i >> 1) & 3) == 0 ? q.x : ((i >> 1) & 3) == 1 ? q.y : ((i >> 1) & 3) == 2 ? q.z : q.w;
-    return (i & 1) ? bf_hi(w) : bf_lo(w);
-  };
-  float c4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-  for (int i = 0; i < 32; ++i)
-    if (FULL || i < nv) c4[i & 3] = fmaxf(c4[i & 3], uval(i));
-  const float c = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
-  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    x[i] = fast_x(uval(i), c, x[i], invT);
-    if (FULL || i < nv) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
-  }
-  const float xm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-  Kahan k4[4];
-  float q4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    if (FULL || i < nv) {
-      const float w = fast_w(x[i], xm);
-      k4[i & 3].add(w);
-      q4[i & 3] = fmaf(w, w, q4[i & 3]);
-    }
-  }
-  const df s = df_add(df_add(k4[0].value(), k4[1].value()), df_add(k4[2].value(), k4[3].value()));
-  return make_float4(c, xm, (float)df_d(s), (q4[0] + q4[1]) + (q4[2] + q4[3]));
-}
-
 // Draft step k on the warp-specialised engine of spec_tile_tc.cuh: the W1 row
 // of each request's previous token, and the epilogue of one tile row.
 struct DraftEpi {
@@ -223,271 +184,7 @@ struct DraftEpi {
   }
 };
 
-// Weighted chunk mass relative to the row's largest chunk reference, in units
-// of exp(reference logit):  f = exp((c - cM)/T + (m - mM)).
-__device__ __forceinline__ float chunk_factor(float4 p, float cM, float mM, float invT) {
-  float a = __fadd_rn(__fmul_rn(__fsub_rn(p.x, cM), invT), __fsub_rn(p.y, mM));
-  return expf(a);
-}
-
-// Draw token x_{k+1} of request b from its chunk partials (one CTA): merge
-// the chunk masses (double-float), find the chunk where the running mass
-// crosses u*Z, recompute that chunk's CW weights and scan them.  Queues the
-// draw on `counter` / ws.items when it lies inside the error band.  `dsm`
-// holds an r x CW W2 slab.  Partials and tokens written by other CTAs of the
-// same launch are read through L2.
-
-template <typename DT>
-__device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __restrict__ U,
-                                  const DT* __restrict__ W1, const DT* __restrict__ W2,
-                                  const int* __restrict__ anchor, const float* __restrict__ temp,
-                                  const float* __restrict__ u_draft, int* tokens, float* q_tok,
-                                  double* lse_q, float* diag, uint32_t* status, const Ws& ws,
-                                  const Eps& eps, uint32_t* counter, unsigned char* dsm) {
-  DT* slab = reinterpret_cast<DT*>(dsm);      // [r][CW] W2 columns of the crossing chunk
-  __shared__ float sh_f[72];
-  __shared__ float s_a[256];
-  __shared__ float s_part[NT / CW][CW];
-  __shared__ int s_slice, s_tok;
-  __shared__ float4 s_pm;
-  __shared__ float s_pref[2], s_lo, s_hi, s_wtok;
-  __shared__ df s_tab[DD_EXP_TAB];
-
-  __syncthreads();      // previous use of the shared buffers is finished
-  if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(s_tab, threadIdx.x);
-  const size_t ok = (size_t)b * sh.gamma + k;
-  const int prev = (k == 0) ? anchor[b] : __ldcg(tokens + ok - 1);
-  const float T = temp[b];
-  if (prev < 0 || prev >= sh.V || !temp_ok(T)) {
-    if (threadIdx.x == 0) {
-      tokens[ok] = -1;
-      q_tok[ok] = NAN;
-      lse_q[ok] = NAN;
-      set_status(status, (prev < 0 || prev >= sh.V) ? SPEC_DEV_BAD_TOKEN : SPEC_DEV_BAD_TEMP);
-      if (diag) for (int q = 0; q < 4; ++q) diag[ok * 4 + q] = NAN;
-    }
-    return;
-  }
-  const int arow = factor_row(sh, b, k, prev);
-  // the factor row (r <= NT entries, one per thread): loaded now, stored to
-  // shared memory only when the crossing chunk's dot product needs it
-  const float a_reg = (int)threadIdx.x < sh.r ? ldf(W1 + (size_t)arow * sh.r + threadIdx.x) : 0.f;
-  const float invT = 1.0f / T;
-  const float4* P = ws.dpart + (size_t)b * sh.NC;
-
-  // ---- this thread's contiguous range of chunks (the first 8 kept in registers)
-  const int per = (sh.NC + NT - 1) / NT;
-  const int s0 = threadIdx.x * per, s1 = min(s0 + per, sh.NC);
-  float4 pv[8];
-  float best = -INFINITY;
-  int bidx = 0;
-  for (int s = s0, q = 0; s < s1; ++s, ++q) {
-    const float4 p = __ldcg(P + s);
-    if (q < 8) pv[q] = p;
-    const float key = fmaf(p.x, invT, p.y);
-    if (key > best) { best = key; bidx = s; }
-  }
-  // reference chunk: lowest index attaining the largest c/T + m
-  {
-    const float bmax = block_max(best, sh_f);
-    int cand = (best == bmax) ? bidx : 0x7fffffff;
-    for (int m = 16; m; m >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, m));
-    if ((threadIdx.x & 31) == 0) reinterpret_cast<int*>(sh_f)[32 + (threadIdx.x >> 5)] = cand;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int c2 = 0x7fffffff;
-      for (int w = 0; w < NT / 32; ++w) c2 = min(c2, reinterpret_cast<int*>(sh_f)[32 + w]);
-      s_slice = c2;
-    }
-    __syncthreads();
-    // the owner of the reference chunk passes its partial on
-    const int rs = s_slice;
-    if (rs >= s0 && rs < s1) s_pm = (rs - s0 < 8) ? pv[rs - s0] : __ldcg(P + rs);
-    __syncthreads();
-  }
-  const float4 PM = s_pm;
-  const float cM = PM.x, mM = PM.y;
-
-  // ---- chunk masses (double-float), normaliser and error-estimate sums
-  df loc = {0.f, 0.f};
-  float q2 = 0.f, m2 = 0.f;
-  for (int s = s0, q = 0; s < s1; ++s, ++q) {
-    const float4 p = (q < 8) ? pv[q] : __ldcg(P + s);
-    const float f = chunk_factor(p, cM, mM, invT);
-    const float w = p.z * f;
-    loc = df_addf(loc, w);
-    q2 = fmaf(p.w * f, f, q2);
-    m2 = fmaf(w, w, m2);
-  }
-  df Zdf;
-  const df excl = block_excl_scan_df(loc, &Zdf, sh_f);
-  q2 = block_sum(q2, sh_f);
-  m2 = block_sum(m2, sh_f);
-  // (fp32 and double-float only below: GB300's fp64 rate is low)
-  const float u = u_draft[ok];
-  const df target = dd_mul_f(Zdf, u);
-
-  // ---- crossing chunk: first s with prefix_incl(s) > target
-  if (threadIdx.x == 0) s_slice = 0x7fffffff;
-  __syncthreads();
-  int my_slice = -1;
-  df my_pref = {0.f, 0.f};
-  if (s0 < s1 && dd_le(excl, target) && !dd_le(df_add(excl, loc), target)) {
-    df run = excl;
-    for (int s = s0, q = 0; s < s1; ++s, ++q) {
-      const float4 p = (q < 8) ? pv[q] : __ldcg(P + s);
-      const df nxt = df_addf(run, p.z * chunk_factor(p, cM, mM, invT));
-      if (!dd_le(nxt, target)) {
-        my_slice = s;
-        my_pref = run;
-        atomicMin(&s_slice, s);
-        break;
-      }
-      run = nxt;
-    }
-  }
-  __syncthreads();
-  if (my_slice >= 0 && my_slice == s_slice) { s_pref[0] = my_pref.hi; s_pref[1] = my_pref.lo; }
-  __syncthreads();
-  bool fallback = false;
-  if (s_slice == 0x7fffffff) {
-    // rounding left the total at or below u*Z: last chunk with mass
-    fallback = true;
-    if (threadIdx.x == 0) {
-      int sl = sh.NC - 1;
-      while (sl > 0 && !(__ldcg(P + sl).z > 0.f)) --sl;
-      df run = {0.f, 0.f};
-      for (int s = 0; s < sl; ++s) {
-        const float4 p = __ldcg(P + s);
-        run = df_addf(run, p.z * chunk_factor(p, cM, mM, invT));
-      }
-      s_slice = sl;
-      s_pref[0] = run.hi;
-      s_pref[1] = run.lo;
-    }
-    __syncthreads();
-  }
-  const int sl = s_slice;
-  const df pref = {s_pref[0], s_pref[1]};
-  const float4 PS = __ldcg(P + sl);
-  const float fS = chunk_factor(PS, cM, mM, invT);
-  const int n0 = sl * CW;
-
-  // ---- recompute the chunk's CW weights: 8 k-groups x CW columns (the U
-  // values of the chunk are requested before the W2 columns are staged)
-  const float u_reg =
-      (threadIdx.x < 32 && n0 + (int)threadIdx.x < sh.V) ? ldf(U + ok * sh.V + n0 + threadIdx.x) : 0.f;
-  issue_w2_slab<DT>(slab, W2, sh.V, 0, sh.r, n0, CW);
-  if ((int)threadIdx.x < sh.r) s_a[threadIdx.x] = a_reg;
-  cp_async_wait_all();
-  __syncthreads();
-  {
-    const int col = threadIdx.x % CW, grp = threadIdx.x / CW;
-    const int kg = sh.r / (NT / CW);           // r % 16 == 0, so r / 8 is whole
-    float acc = 0.f;
-    for (int i = grp * kg; i < grp * kg + kg; ++i) acc = fmaf(s_a[i], tof(slab[i * CW + col]), acc);
-    s_part[grp][col] = acc;
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const int v = n0 + lane;
-    float w = 0.f;
-    if (v < sh.V) {
-      float bias = s_part[0][lane];
-#pragma unroll
-      for (int g = 1; g < NT / CW; ++g) bias = __fadd_rn(bias, s_part[g][lane]);
-      w = fast_w(fast_x(u_reg, PS.x, bias, invT), PS.y);
-    }
-    // target inside the chunk, in the chunk's units: (u Z - prefix) / fS
-    const df tin = dd_mul(dd_add(target, dd_neg(pref)), dd_recip(fS));
-    // inclusive double-float scan across the warp
-    df inc = df_make(w);
-    for (int d = 1; d < 32; d <<= 1) {
-      const df o = shfl_up_df(inc, d);
-      if (lane >= d) inc = df_add(inc, o);
-    }
-    df ex = shfl_up_df(inc, 1);
-    if (lane == 0) ex = {0.f, 0.f};
-    const bool claim = w > 0.f && dd_le(ex, tin) && !dd_le(inc, tin);
-    const uint32_t cl = __ballot_sync(0xffffffffu, claim);
-    const uint32_t pos = __ballot_sync(0xffffffffu, w > 0.f);
-    int t;
-    float dlo = 0.f, dhi = 0.f;
-    if (cl) {
-      t = __ffs(cl) - 1;
-      dlo = __shfl_sync(0xffffffffu, dd_add(tin, dd_neg(ex)).hi, t);
-      dhi = __shfl_sync(0xffffffffu, dd_add(inc, dd_neg(tin)).hi, t);
-    } else {
-      fallback = true;
-      t = pos ? 31 - __clz(pos) : 0;           // last entry with mass
-    }
-    const float wt = __shfl_sync(0xffffffffu, w, t);
-    if (lane == 0) {
-      s_tok = t;
-      s_lo = dlo;
-      s_hi = dhi;
-      s_wtok = wt;
-    }
-  }
-  __syncthreads();
-  if (s_lo == 0.f && s_hi == 0.f) fallback = true;
-  if (threadIdx.x == 0) {
-    const int tok = n0 + s_tok;
-    const float Zf = Zdf.hi;
-    const float scale = __fdiv_rn(fS, Zf);                 // chunk units -> probability
-    const float dmargin = fminf(s_lo, s_hi) * scale;
-    const float band = eps.scale * (eps.elem * __fdiv_rn(sqrtf(q2), Zf) +
-                                    eps.slice * __fdiv_rn(sqrtf(m2), Zf) + eps.abs_);
-    // lse = cM / T + mM + log Z
-    const df ref = dd_add_f(dd_mul_f(dd_recip(T), cM), mM);
-    const double lse = dd_to_double(ref) + dd_log(Zdf, s_tab);
-    int wtok = tok;                   // the token written until a re-decision
-    if (fallback || dmargin <= band) {
-      uint32_t it = atomicAdd(counter, 1u);
-      if ((int)it < ws.max_items) {
-        if (eps.perturb != 0.f) wtok = tok + 1 < sh.V ? tok + 1 : 0;   // test hook
-        HpItem h;
-        h.b = b; h.j = k; h.kind = HP_DRAFT; h.prev = arow; h.u = u; h.fast_token = wtok;
-        h.shift_q = lse; h.shift_p = 0.0;
-        ws.items[it] = h;
-      } else {
-        set_status(status, SPEC_DEV_OVERFLOW);
-      }
-    }
-    tokens[ok] = wtok;
-    q_tok[ok] = s_wtok * scale;
-    lse_q[ok] = lse;
-    if (diag) {
-      diag[ok * 4 + 0] = s_lo * scale;
-      diag[ok * 4 + 1] = s_hi * scale;
-      diag[ok * 4 + 2] = band;
-      diag[ok * 4 + 3] = (float)tok;
-    }
-  }
-  __syncthreads();
-}
-
 // ---------------------------------------------------------------- kernel
-struct DraftParams {
-  TpMaps maps;       // tensor-memory path only
-  Shape sh;
-  const void* U;
-  const void* W1;
-  const void* W2;
-  const int* anchor;
-  const float* temp;
-  const float* u_draft;
-  int* tokens;
-  float* q_tok;
-  double* lse_q;
-  float* diag;
-  uint32_t* status;
-  Ws ws;
-  Eps eps;
-  RnnParams rnn;     // RNN head (sh.rnn): gates before each step's tiles
-};
-
 // The whole draft in one cooperative launch: for each step k, [the RNN head's
 // gate phase and a grid barrier,] the tile phase (tiles strided over the CTAs,
 // then the previous step's near-boundary draws re-decided by the CTAs as they
@@ -495,7 +192,7 @@ struct DraftParams {
 // over the CTAs) and a grid barrier; then the last step's re-decisions and,
 // if a re-decision changed a token, the steps after it again with their
 // re-decisions in place.  Tensor memory is allocated once per CTA.
-template <typename DT, int BM, int PATH>
+template <typename DT, int BM, int PATH, int HOOK>
 __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_constant__ DraftParams P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ uint64_t s_bar[TB_COUNT];
@@ -526,6 +223,11 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
   const int n_mt = (sh.B + BM - 1) / BM;
   const int n_tiles = sh.NS * n_mt;
   const uint32_t G = gridDim.x;
+  // HOOK_STALL (a test build): the first barrier expects one arrival more
+  // than the grid has, so it can only end by its time limit
+  auto gsync = [&]() {
+    return grid_sync(ctrl, G, gen, P.status, (HOOK == HOOK_STALL && gen == 0u) ? 1u : 0u);
+  };
   unsigned long long* tr = (P.ws.trace && blockIdx.x == 0 && threadIdx.x == 0) ? P.ws.trace : nullptr;
   int n_prev = 0;          // draws the previous step queued for re-decision
   uint32_t hp_base = 0;    // units taken from CTRL_HPNEXT so far (the same in every CTA)
@@ -539,7 +241,7 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
     bool ok = true;
     if (sh.rnn) {
       rnn_gates_body<DT>(sh, k, (const DT*)P.W1, P.anchor, P.tokens, P.rnn, smem_raw, P.status);
-      if (!grid_sync(ctrl, G, gen, P.status)) return false;
+      if (!gsync()) return false;
     }
     if (tr) tr[k * TRACE_SLOTS + 0] = globaltimer_ns();
     if constexpr (PATH == 2) {
@@ -565,21 +267,21 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
       hp_base += (uint32_t)(n_prev * sh.HB) + G;
     }
     if (tr) tr[k * TRACE_SLOTS + 1] = globaltimer_ns();
-    if (!grid_sync(ctrl, G, gen, P.status)) return false;
+    if (!gsync()) return false;
     if (tr) tr[k * TRACE_SLOTS + 2] = globaltimer_ns();
     for (int b = blockIdx.x; b < sh.B; b += G)
-      draft_sample_body<DT>(sh, k, b, U, W1, W2, P.anchor, P.temp, P.u_draft, P.tokens, P.q_tok,
-                            P.lse_q, P.diag, P.status, P.ws, P.eps, ctrl + CTRL_STEP0 + k,
-                            smem_raw);
+      draft_sample_body<DT, HOOK>(sh, k, b, U, W1, W2, P.anchor, P.temp, P.u_draft, P.tokens,
+                                  P.q_tok, P.lse_q, P.diag, P.status, P.ws, P.eps,
+                                  ctrl + CTRL_STEP0 + k, P.ws.max_items, smem_raw);
     if (tr) tr[k * TRACE_SLOTS + 3] = globaltimer_ns();
-    if (!grid_sync(ctrl, G, gen, P.status)) return false;
+    if (!gsync()) return false;
     if (tr) tr[k * TRACE_SLOTS + 4] = globaltimer_ns();
     const int n = min((int)__ldcg(ctrl + CTRL_STEP0 + k), P.ws.max_items);
     n_prev = deferred ? n : 0;
     if (!deferred && n > 0) {
       hp_sums_body<DT>(sh, R, P.ws, 0, n, smem_raw, true, P.tokens, P.q_tok, P.lse_q, P.status);
       if (tr) tr[k * TRACE_SLOTS + 5] = globaltimer_ns();
-      if (!grid_sync(ctrl, G, gen, P.status)) return false;
+      if (!gsync()) return false;
     }
     if (tr) {
       tr[k * TRACE_SLOTS + 6] = globaltimer_ns();
@@ -593,7 +295,7 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
     // the last step's draws, then the redo of every step after the earliest
     // changed token (all requests: the others recompute the same values)
     hp_sums_body<DT>(sh, R, P.ws, 0, n_prev, smem_raw, true, P.tokens, P.q_tok, P.lse_q, P.status);
-    good = grid_sync(ctrl, G, gen, P.status);
+    good = gsync();
   }
   if (good) {
     const uint32_t redo = __ldcg(ctrl + CTRL_REDO);
@@ -601,7 +303,7 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
     if (redo > 0 && k0 < sh.gamma) {
       if (blockIdx.x == 0 && threadIdx.x == 0)
         for (int k = k0; k < sh.gamma; ++k) ctrl[CTRL_STEP0 + k] = 0u;
-      good = grid_sync(ctrl, G, gen, P.status);
+      good = gsync();
       for (int k = k0; k < sh.gamma && good; ++k) good = run_step(k, false);
     }
   }
@@ -613,7 +315,7 @@ __global__ void __launch_bounds__(NT, 1) draft_persistent_kernel(const __grid_co
 }
 
 // ---------------------------------------------------------------- launcher
-template <typename DT, int BM, int PATH>
+template <typename DT, int BM, int PATH, int HOOK = HOOK_NONE>
 static cudaError_t launch_persist(const DraftParams& P, int nsm, cudaStream_t st) {
   size_t smem = PATH == 2 ? TpLayout(P.sh.r, BN).total : TileLayout<DT>(BM, P.sh.r, false).total;
   const size_t slab = (size_t)P.sh.r * HPB * sizeof(DT);    // re-decision W2 slab (> sampler's)
@@ -632,7 +334,7 @@ static cudaError_t launch_persist(const DraftParams& P, int nsm, cudaStream_t st
     const size_t need = stage + nI * B * sizeof(int);
     smem = smem > need ? smem : need;
   }
-  auto kern = draft_persistent_kernel<DT, BM, PATH>;
+  auto kern = draft_persistent_kernel<DT, BM, PATH, HOOK>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -653,12 +355,15 @@ static cudaError_t launch_persist(const DraftParams& P, int nsm, cudaStream_t st
 }
 
 // Whole draft in one cooperative launch (the control words must be zeroed).
+// `hook` selects a test build (HOOK_PERTURB, HOOK_STALL), available on the
+// fp32 path for batches of up to 32 requests and on the tensor-memory path;
+// elsewhere a hook request fails with cudaErrorNotSupported.
 template <typename DT>
 cudaError_t launch_draft_persistent(const Shape& sh, const void* U, const void* W1, const void* W2,
                                     const int* anchor, const float* temp, const float* u_draft,
                                     int* tokens, float* q_tok, double* lse_q, float* diag,
                                     uint32_t* status, const Ws& ws, const Eps& eps, int path,
-                                    int nsm, cudaStream_t st, const RnnParams* rnn) {
+                                    int nsm, cudaStream_t st, const RnnParams* rnn, int hook) {
   DraftParams P;
   memset(&P.maps, 0, sizeof(P.maps));
   memset(&P.rnn, 0, sizeof(P.rnn));
@@ -678,6 +383,22 @@ cudaError_t launch_draft_persistent(const Shape& sh, const void* U, const void* 
   P.ws = ws;
   P.eps = eps;
   const int BM = sh.B <= 32 ? 32 : (sh.B <= 64 ? 64 : 128);
+  if (hook != HOOK_NONE) {
+    const bool tc = sizeof(DT) == 2 && path == 2 && sh.r % 64 == 0;
+    if (!tc && (path == 0 || sizeof(DT) == 4) && BM == 32)
+      return hook == HOOK_PERTURB ? launch_persist<DT, 32, 0, HOOK_PERTURB>(P, nsm, st)
+                                  : launch_persist<DT, 32, 0, HOOK_STALL>(P, nsm, st);
+    if constexpr (sizeof(DT) == 2) {
+      if (tc) {
+        cudaError_t e = encode_u_map(sh, U, &P.maps.u);
+        if (e == cudaSuccess) e = encode_w2_map(sh, W2, &P.maps.w2);
+        if (e != cudaSuccess) return e;
+        return hook == HOOK_PERTURB ? launch_persist<DT, 128, 2, HOOK_PERTURB>(P, nsm, st)
+                                    : launch_persist<DT, 128, 2, HOOK_STALL>(P, nsm, st);
+      }
+    }
+    return cudaErrorNotSupported;
+  }
   if (path == 0 || sizeof(DT) == 4) {
     if (BM == 32) return launch_persist<DT, 32, 0>(P, nsm, st);
     if (BM == 64) return launch_persist<DT, 64, 0>(P, nsm, st);
@@ -700,11 +421,11 @@ template cudaError_t launch_draft_persistent<float>(const Shape&, const void*, c
                                                     const void*, const int*, const float*,
                                                     const float*, int*, float*, double*, float*,
                                                     uint32_t*, const Ws&, const Eps&, int, int,
-                                                    cudaStream_t, const RnnParams*);
+                                                    cudaStream_t, const RnnParams*, int);
 template cudaError_t launch_draft_persistent<bf16>(const Shape&, const void*, const void*,
                                                    const void*, const int*, const float*,
                                                    const float*, int*, float*, double*, float*,
                                                    uint32_t*, const Ws&, const Eps&, int, int,
-                                                   cudaStream_t, const RnnParams*);
+                                                   cudaStream_t, const RnnParams*, int);
 
 }  // namespace spec

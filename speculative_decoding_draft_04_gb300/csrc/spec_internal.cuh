@@ -46,15 +46,22 @@ struct HpItem {
 };
 
 // Control words at the start of the workspace.
-//   CTRL_BAR_COUNT / CTRL_ABORT: grid barrier of the persistent draft kernel
-//   (word 4 is unused); CTRL_HPNEXT: re-decision units handed out in the
+//   CTRL_BAR_COUNT / CTRL_ABORT: grid barrier of the persistent draft kernels;
+//   CTRL_DITEMS: draws queued by the slice-resident draft over all its steps
+//   (ws.items, up to ws.item_cap); CTRL_HPNEXT: re-decision units handed out in the
 //   draft's tile phases; CTRL_REDO: gamma - the earliest draft step whose
 //   token a deferred re-decision changed (0: none); CTRL_STEP0 + k: queued
 //   re-decisions of draft step k.
 enum {
-  CTRL_ITEMS = 0, CTRL_SLOW = 1, CTRL_NPACKED = 2, CTRL_BAR_COUNT = 3,
+  CTRL_ITEMS = 0, CTRL_SLOW = 1, CTRL_NPACKED = 2, CTRL_BAR_COUNT = 3, CTRL_DITEMS = 4,
   CTRL_ABORT = 5, CTRL_HPNEXT = 6, CTRL_REDO = 7, CTRL_STEP0 = 8, CTRL_WORDS = 32
 };
+
+// Test builds of the draft kernels (never the default): HOOK_PERTURB makes
+// queued draws write a wrong token first (the re-decision must correct it and
+// trigger the redo); HOOK_STALL makes the first grid barrier wait for one
+// arrival more than the grid has, so it can only end by its time limit.
+enum { HOOK_NONE = 0, HOOK_PERTURB = 1, HOOK_STALL = 2 };
 
 // Workspace views (host computes the offsets; see spec_abi.cu).
 constexpr int TRACE_SLOTS = 8;   // timestamps per draft step (persistent kernel trace)
@@ -62,8 +69,9 @@ struct Ws {
   uint32_t* ctrl;       // [CTRL_WORDS]
   unsigned long long* trace;  // [2][MAX_GAMMA][TRACE_SLOTS] globaltimer ns, CTA 0: the
                               // draft's phases, then events inside its tile phase
-  HpItem* items;        // [max_items]
-  int max_items;
+  HpItem* items;        // [item_cap] queued decisions
+  int max_items;        // decisions re-decided together (hpsum / hpcnt / hpnorm slots)
+  int item_cap;         // entries of `items` (B * gamma: every draft draw of a cycle)
   float2* hpsum;        // [max_items][hp_cols][NC] chunk sums of the re-decided rows (hi, lo)
   int hp_cols;          // 3 (draft and verify) or 1 (draft only)
   uint32_t* hpcnt;      // [max_items] blocks summed so far (zeroed before the draft)
@@ -121,7 +129,6 @@ struct Eps {
   float ratio;   // relative band of a ratio test
   float norm;    // residual draws: error of the two row normalisers
   float scale;   // user multiplier (SPEC_OPT_EPS_SCALE)
-  float perturb; // test hook (SPEC_OPT_PERTURB): queued draft draws first write the next token
 };
 
 // ---------------------------------------------------------------- loads
@@ -336,13 +343,14 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
 // wait is bounded: on timeout, or when another CTA has aborted, it sets
 // SPEC_DEV_TIMEOUT / the abort word and returns false, and the caller leaves
 // the kernel.  `gen` is thread 0's count of barriers passed (0 at kernel start).
+// `extra` (test builds only) raises the count the barrier waits for.
 __device__ __forceinline__ bool grid_sync(uint32_t* ctrl, uint32_t nblocks, uint32_t& gen,
-                                          uint32_t* status) {
+                                          uint32_t* status, uint32_t extra = 0u) {
   __shared__ int s_gs_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    const uint32_t target = (gen + 1) * nblocks;
+    const uint32_t target = (gen + 1) * nblocks + extra;
     uint32_t seen;
     asm volatile("atom.add.release.gpu.global.u32 %0, [%1], 1;\n"
                  : "=r"(seen) : "l"(ctrl + CTRL_BAR_COUNT) : "memory");

@@ -1,0 +1,320 @@
+// Draft-side device code shared by the two persistent draft kernels
+// (spec_draft.cu, spec_draft_slice.cu): the per-chunk softmax partial of the
+// first pass and the sampler that turns a request's chunk partials into its
+// next token (DSpark review, section 1.2: p_k = softmax(U_k + B_k) sampled
+// left to right, B = W1[x_{k-1}] W2; tempered by T_b).
+#pragma once
+
+#include "spec_tile_tc.cuh"
+#include "spec_hp.cuh"
+
+namespace spec {
+
+// ---------------------------------------------------------------- tensor-memory tiles
+// Partial (c, m, s, q2) of one CW-column chunk of a row from its packed bf16
+// logits `u` (16 words) and its bias row `x` (overwritten with the tempered
+// logits); `nv` valid columns.  Four interleaved max / Kahan / square-sum
+// chains keep the dependent-latency per column low.
+template <bool FULL>
+__device__ __forceinline__ float4 chunk_partial(const uint4 (&u)[4], float (&x)[32], int nv, float invT) {
+  auto uval = [&](int i) {
+    const uint4 q = u[i >> 3];
+    const uint32_t w = ((i >> 1) & 3) == 0 ? q.x : ((i >> 1) & 3) == 1 ? q.y : ((i >> 1) & 3) == 2 ? q.z : q.w;
+    return (i & 1) ? bf_hi(w) : bf_lo(w);
+  };
+  float c4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (FULL || i < nv) c4[i & 3] = fmaxf(c4[i & 3], uval(i));
+  const float c = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    x[i] = fast_x(uval(i), c, x[i], invT);
+    if (FULL || i < nv) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+  }
+  const float xm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+  Kahan k4[4];
+  float q4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    if (FULL || i < nv) {
+      const float w = fast_w(x[i], xm);
+      k4[i & 3].add(w);
+      q4[i & 3] = fmaf(w, w, q4[i & 3]);
+    }
+  }
+  const df s = df_add(df_add(k4[0].value(), k4[1].value()), df_add(k4[2].value(), k4[3].value()));
+  return make_float4(c, xm, (float)df_d(s), (q4[0] + q4[1]) + (q4[2] + q4[3]));
+}
+
+// Weighted chunk mass relative to the row's largest chunk reference, in units
+// of exp(reference logit):  f = exp((c - cM)/T + (m - mM)).
+__device__ __forceinline__ float chunk_factor(float4 p, float cM, float mM, float invT) {
+  float a = __fadd_rn(__fmul_rn(__fsub_rn(p.x, cM), invT), __fsub_rn(p.y, mM));
+  return expf(a);
+}
+
+// Draw token x_{k+1} of request b from its chunk partials (one CTA): merge
+// the chunk masses (double-float), find the chunk where the running mass
+// crosses u*Z, recompute that chunk's CW weights and scan them.  Queues the
+// draw at ws.items[atomicAdd(counter, 1)] (at most `cap` entries; beyond
+// that SPEC_DEV_OVERFLOW) when it lies inside the error band.  `dsm` holds an
+// r x CW W2 slab.  Partials and tokens written by other CTAs of the same
+// launch are read through L2.  HOOK_PERTURB (a test build of the kernel)
+// makes every queued draw first write the next token, so that the
+// re-decision has a token to correct.
+
+template <typename DT, int HOOK>
+__device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __restrict__ U,
+                                  const DT* __restrict__ W1, const DT* __restrict__ W2,
+                                  const int* __restrict__ anchor, const float* __restrict__ temp,
+                                  const float* __restrict__ u_draft, int* tokens, float* q_tok,
+                                  double* lse_q, float* diag, uint32_t* status, const Ws& ws,
+                                  const Eps& eps, uint32_t* counter, int cap, unsigned char* dsm) {
+  DT* slab = reinterpret_cast<DT*>(dsm);      // [r][CW] W2 columns of the crossing chunk
+  __shared__ float sh_f[72];
+  __shared__ float s_a[256];
+  __shared__ float s_part[NT / CW][CW];
+  __shared__ int s_slice, s_tok;
+  __shared__ float4 s_pm;
+  __shared__ float s_pref[2], s_lo, s_hi, s_wtok;
+  __shared__ df s_tab[DD_EXP_TAB];
+
+  __syncthreads();      // previous use of the shared buffers is finished
+  if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(s_tab, threadIdx.x);
+  const size_t ok = (size_t)b * sh.gamma + k;
+  const int prev = (k == 0) ? anchor[b] : __ldcg(tokens + ok - 1);
+  const float T = temp[b];
+  if (prev < 0 || prev >= sh.V || !temp_ok(T)) {
+    if (threadIdx.x == 0) {
+      tokens[ok] = -1;
+      q_tok[ok] = NAN;
+      lse_q[ok] = NAN;
+      set_status(status, (prev < 0 || prev >= sh.V) ? SPEC_DEV_BAD_TOKEN : SPEC_DEV_BAD_TEMP);
+      if (diag) for (int q = 0; q < 4; ++q) diag[ok * 4 + q] = NAN;
+    }
+    return;
+  }
+  const int arow = factor_row(sh, b, k, prev);
+  // the factor row (r <= NT entries, one per thread): loaded now, stored to
+  // shared memory only when the crossing chunk's dot product needs it
+  const float a_reg = (int)threadIdx.x < sh.r ? ldf(W1 + (size_t)arow * sh.r + threadIdx.x) : 0.f;
+  const float invT = 1.0f / T;
+  const float4* P = ws.dpart + (size_t)b * sh.NC;
+
+  // ---- this thread's contiguous range of chunks (the first 8 kept in registers)
+  const int per = (sh.NC + NT - 1) / NT;
+  const int s0 = threadIdx.x * per, s1 = min(s0 + per, sh.NC);
+  float4 pv[8];
+  float best = -INFINITY;
+  int bidx = 0;
+  for (int s = s0, q = 0; s < s1; ++s, ++q) {
+    const float4 p = __ldcg(P + s);
+    if (q < 8) pv[q] = p;
+    const float key = fmaf(p.x, invT, p.y);
+    if (key > best) { best = key; bidx = s; }
+  }
+  // reference chunk: lowest index attaining the largest c/T + m
+  {
+    const float bmax = block_max(best, sh_f);
+    int cand = (best == bmax) ? bidx : 0x7fffffff;
+    for (int m = 16; m; m >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, m));
+    if ((threadIdx.x & 31) == 0) reinterpret_cast<int*>(sh_f)[32 + (threadIdx.x >> 5)] = cand;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int c2 = 0x7fffffff;
+      for (int w = 0; w < NT / 32; ++w) c2 = min(c2, reinterpret_cast<int*>(sh_f)[32 + w]);
+      s_slice = c2;
+    }
+    __syncthreads();
+    // the owner of the reference chunk passes its partial on
+    const int rs = s_slice;
+    if (rs >= s0 && rs < s1) s_pm = (rs - s0 < 8) ? pv[rs - s0] : __ldcg(P + rs);
+    __syncthreads();
+  }
+  const float4 PM = s_pm;
+  const float cM = PM.x, mM = PM.y;
+
+  // ---- chunk masses (double-float), normaliser and error-estimate sums
+  df loc = {0.f, 0.f};
+  float q2 = 0.f, m2 = 0.f;
+  for (int s = s0, q = 0; s < s1; ++s, ++q) {
+    const float4 p = (q < 8) ? pv[q] : __ldcg(P + s);
+    const float f = chunk_factor(p, cM, mM, invT);
+    const float w = p.z * f;
+    loc = df_addf(loc, w);
+    q2 = fmaf(p.w * f, f, q2);
+    m2 = fmaf(w, w, m2);
+  }
+  df Zdf;
+  const df excl = block_excl_scan_df(loc, &Zdf, sh_f);
+  q2 = block_sum(q2, sh_f);
+  m2 = block_sum(m2, sh_f);
+  // (fp32 and double-float only below: GB300's fp64 rate is low)
+  const float u = u_draft[ok];
+  const df target = dd_mul_f(Zdf, u);
+
+  // ---- crossing chunk: first s with prefix_incl(s) > target
+  if (threadIdx.x == 0) s_slice = 0x7fffffff;
+  __syncthreads();
+  int my_slice = -1;
+  df my_pref = {0.f, 0.f};
+  if (s0 < s1 && dd_le(excl, target) && !dd_le(df_add(excl, loc), target)) {
+    df run = excl;
+    for (int s = s0, q = 0; s < s1; ++s, ++q) {
+      const float4 p = (q < 8) ? pv[q] : __ldcg(P + s);
+      const df nxt = df_addf(run, p.z * chunk_factor(p, cM, mM, invT));
+      if (!dd_le(nxt, target)) {
+        my_slice = s;
+        my_pref = run;
+        atomicMin(&s_slice, s);
+        break;
+      }
+      run = nxt;
+    }
+  }
+  __syncthreads();
+  if (my_slice >= 0 && my_slice == s_slice) { s_pref[0] = my_pref.hi; s_pref[1] = my_pref.lo; }
+  __syncthreads();
+  bool fallback = false;
+  if (s_slice == 0x7fffffff) {
+    // rounding left the total at or below u*Z: last chunk with mass
+    fallback = true;
+    if (threadIdx.x == 0) {
+      int sl = sh.NC - 1;
+      while (sl > 0 && !(__ldcg(P + sl).z > 0.f)) --sl;
+      df run = {0.f, 0.f};
+      for (int s = 0; s < sl; ++s) {
+        const float4 p = __ldcg(P + s);
+        run = df_addf(run, p.z * chunk_factor(p, cM, mM, invT));
+      }
+      s_slice = sl;
+      s_pref[0] = run.hi;
+      s_pref[1] = run.lo;
+    }
+    __syncthreads();
+  }
+  const int sl = s_slice;
+  const df pref = {s_pref[0], s_pref[1]};
+  const float4 PS = __ldcg(P + sl);
+  const float fS = chunk_factor(PS, cM, mM, invT);
+  const int n0 = sl * CW;
+
+  // ---- recompute the chunk's CW weights: 8 k-groups x CW columns (the U
+  // values of the chunk are requested before the W2 columns are staged)
+  const float u_reg =
+      (threadIdx.x < 32 && n0 + (int)threadIdx.x < sh.V) ? ldf(U + ok * sh.V + n0 + threadIdx.x) : 0.f;
+  issue_w2_slab<DT>(slab, W2, sh.V, 0, sh.r, n0, CW);
+  if ((int)threadIdx.x < sh.r) s_a[threadIdx.x] = a_reg;
+  cp_async_wait_all();
+  __syncthreads();
+  {
+    const int col = threadIdx.x % CW, grp = threadIdx.x / CW;
+    const int kg = sh.r / (NT / CW);           // r % 16 == 0, so r / 8 is whole
+    float acc = 0.f;
+    for (int i = grp * kg; i < grp * kg + kg; ++i) acc = fmaf(s_a[i], tof(slab[i * CW + col]), acc);
+    s_part[grp][col] = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int v = n0 + lane;
+    float w = 0.f;
+    if (v < sh.V) {
+      float bias = s_part[0][lane];
+#pragma unroll
+      for (int g = 1; g < NT / CW; ++g) bias = __fadd_rn(bias, s_part[g][lane]);
+      w = fast_w(fast_x(u_reg, PS.x, bias, invT), PS.y);
+    }
+    // target inside the chunk, in the chunk's units: (u Z - prefix) / fS
+    const df tin = dd_mul(dd_add(target, dd_neg(pref)), dd_recip(fS));
+    // inclusive double-float scan across the warp
+    df inc = df_make(w);
+    for (int d = 1; d < 32; d <<= 1) {
+      const df o = shfl_up_df(inc, d);
+      if (lane >= d) inc = df_add(inc, o);
+    }
+    df ex = shfl_up_df(inc, 1);
+    if (lane == 0) ex = {0.f, 0.f};
+    const bool claim = w > 0.f && dd_le(ex, tin) && !dd_le(inc, tin);
+    const uint32_t cl = __ballot_sync(0xffffffffu, claim);
+    const uint32_t pos = __ballot_sync(0xffffffffu, w > 0.f);
+    int t;
+    float dlo = 0.f, dhi = 0.f;
+    if (cl) {
+      t = __ffs(cl) - 1;
+      dlo = __shfl_sync(0xffffffffu, dd_add(tin, dd_neg(ex)).hi, t);
+      dhi = __shfl_sync(0xffffffffu, dd_add(inc, dd_neg(tin)).hi, t);
+    } else {
+      fallback = true;
+      t = pos ? 31 - __clz(pos) : 0;           // last entry with mass
+    }
+    const float wt = __shfl_sync(0xffffffffu, w, t);
+    if (lane == 0) {
+      s_tok = t;
+      s_lo = dlo;
+      s_hi = dhi;
+      s_wtok = wt;
+    }
+  }
+  __syncthreads();
+  if (s_lo == 0.f && s_hi == 0.f) fallback = true;
+  if (threadIdx.x == 0) {
+    const int tok = n0 + s_tok;
+    const float Zf = Zdf.hi;
+    const float scale = __fdiv_rn(fS, Zf);                 // chunk units -> probability
+    const float dmargin = fminf(s_lo, s_hi) * scale;
+    const float band = eps.scale * (eps.elem * __fdiv_rn(sqrtf(q2), Zf) +
+                                    eps.slice * __fdiv_rn(sqrtf(m2), Zf) + eps.abs_);
+    // lse = cM / T + mM + log Z
+    const df ref = dd_add_f(dd_mul_f(dd_recip(T), cM), mM);
+    const double lse = dd_to_double(ref) + dd_log(Zdf, s_tab);
+    int wtok = tok;                   // the token written until a re-decision
+    if (fallback || dmargin <= band) {
+      uint32_t it = atomicAdd(counter, 1u);
+      if ((int)it < cap) {
+        if constexpr (HOOK == HOOK_PERTURB) wtok = tok + 1 < sh.V ? tok + 1 : 0;
+        HpItem h;
+        h.b = b; h.j = k; h.kind = HP_DRAFT; h.prev = arow; h.u = u; h.fast_token = wtok;
+        h.shift_q = lse; h.shift_p = 0.0;
+        ws.items[it] = h;
+      } else {
+        set_status(status, SPEC_DEV_OVERFLOW);
+      }
+    }
+    tokens[ok] = wtok;
+    q_tok[ok] = s_wtok * scale;
+    lse_q[ok] = lse;
+    if (diag) {
+      diag[ok * 4 + 0] = s_lo * scale;
+      diag[ok * 4 + 1] = s_hi * scale;
+      diag[ok * 4 + 2] = band;
+      diag[ok * 4 + 3] = (float)tok;
+    }
+  }
+  __syncthreads();
+}
+
+struct DraftParams {
+  TpMaps maps;       // tensor-memory path only
+  Shape sh;
+  const void* U;
+  const void* W1;
+  const void* W2;
+  const int* anchor;
+  const float* temp;
+  const float* u_draft;
+  int* tokens;
+  float* q_tok;
+  double* lse_q;
+  float* diag;
+  uint32_t* status;
+  Ws ws;
+  Eps eps;
+  RnnParams rnn;     // RNN head (sh.rnn): gates before each step's tiles
+  int slK;           // slice-resident kernel: chunks of CW columns per CTA
+};
+
+
+}  // namespace spec

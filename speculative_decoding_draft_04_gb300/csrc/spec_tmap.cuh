@@ -45,6 +45,24 @@ inline cudaError_t encode_u_map(const Shape& sh, const void* U, CUtensorMap* map
   return cudaSuccess;
 }
 
+// U as [B][gamma][V] bf16 in chunks of 32 columns: boxes of 32 columns x 1
+// step x 128 requests, 64-byte swizzle (one 8 KB chunk of a 128-request
+// tile); reads outside the tensor return zeros.
+inline cudaError_t encode_u_chunk_map(const Shape& sh, const void* U, CUtensorMap* map) {
+  const EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t V = (cuuint64_t)sh.V;
+  const cuuint64_t dims[3] = {V, (cuuint64_t)sh.gamma, (cuuint64_t)sh.B};
+  const cuuint64_t strides[2] = {V * 2, V * 2 * (cuuint64_t)sh.gamma};
+  const cuuint32_t box[3] = {32, 1, 128};
+  const cuuint32_t es[3] = {1, 1, 1};
+  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(U), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
 // W2 as [r][V] bf16, boxes of 64 columns x r rows (one MN-major operand
 // atom), 128-byte swizzle; reads outside the tensor return zeros.
 inline cudaError_t encode_w2_map(const Shape& sh, const void* W2, CUtensorMap* map) {

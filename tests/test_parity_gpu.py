@@ -218,7 +218,8 @@ def test_profile_api_counts_launches():
         prof = _lib.spec_profile_read()
     finally:
         _lib.spec_profile_enable(False)
-    assert prof["draft_persistent"][1] == 1           # the whole draft: one cooperative launch
+    # the whole draft is one cooperative launch (of one of the two draft kernels)
+    assert prof["draft_persistent"][1] + prof["draft_slice"][1] == 1
     assert prof["verify_tile"][1] == 1
     assert all(ms >= 0 for ms, _ in prof.values())
 

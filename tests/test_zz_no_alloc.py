@@ -61,6 +61,45 @@ def test_static_draft_matches_workspace_draft_twice(name, overrides):
         _check(ref, out)
 
 
+MODES = {
+    # each kernel family the static entry point can run
+    "simt": {_lib.SPEC_OPT_FORCE_SIMT: 1},
+    "warp-mma": {_lib.SPEC_OPT_BIAS_PATH: 1},
+    "tile-strided": {_lib.SPEC_OPT_DRAFT_KERNEL: 1},
+    # most draws queued: the queue, block sums and counters in the shared
+    # area carry state from one call's re-decisions to the next call's
+    "re-decided": {_lib.SPEC_OPT_EPS_SCALE: 3000.0},
+    # every queued draw first writes a wrong token, so re-decisions change
+    # tokens and the later steps are redone
+    "redo": {_lib.SPEC_OPT_EPS_SCALE: 3000.0, _lib.SPEC_OPT_PERTURB: 1},
+}
+DEFAULTS = {_lib.SPEC_OPT_FORCE_SIMT: 0, _lib.SPEC_OPT_BIAS_PATH: 2, _lib.SPEC_OPT_DRAFT_KERNEL: 0,
+            _lib.SPEC_OPT_EPS_SCALE: 1.0, _lib.SPEC_OPT_PERTURB: 0}
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+def test_static_draft_in_every_mode(mode):
+    """Two calls in a row per mode, each equal to the workspace draft run in the
+    same mode; in the re-decision modes the re-decisions (and the redo) must
+    actually have run through the shared area."""
+    spec = W.config("C2", B=48, V=8200, r=256, name="noalloc-mode")
+    try:
+        for k, v in MODES[mode].items():
+            _lib.spec_set_option(k, v)
+        for trial in (2, 3):
+            w = W.make_workload(spec, trial=trial)
+            ref, out = _draft_both(w)
+            _check(ref, out)
+            st = engine.status_words(out["st"])
+            if mode in ("re-decided", "redo"):
+                assert st[1] > 0, st              # re-decisions ran
+            if mode == "redo":
+                assert st[2] > 0, st              # ... changed tokens, and the steps were redone
+    finally:
+        for k, v in DEFAULTS.items():
+            _lib.spec_set_option(k, v)
+
+
 def test_static_draft_rejects_problems_beyond_its_scratch():
     L = _lib.lib()
     a = _lib.DraftArgs(4096, 16, 8 << 20, 256, _lib.SPEC_BF16)
