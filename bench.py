@@ -47,6 +47,8 @@ def parse():
                     help="launch the timed cycles one call at a time instead of replaying a CUDA graph")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the scheduled, RNN-head and tree passes (profiling runs)")
+    ap.add_argument("--other-configs", default="C1,C3,C4",
+                    help="other named workloads timed at full size beside the headline ('' = none)")
     return ap.parse_args()
 
 
@@ -211,6 +213,65 @@ def rnn_pass(args, w, d, bufs, stream, flush, rank, dev):
             "stages_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]}}
 
 
+def config_pass(name, args, flush, dev, warmup=3, steps=10):
+    """One other named workload at its full size: cycles with L2 flushed
+    between them (cold, events around each cycle) and back to back (warm),
+    then once more with per-kernel events for the draft / verification split.
+    Returns the times and the cycle's algorithmic HBM rate."""
+    import torch
+    from speculative_decoding_draft_04_gb300 import _lib, engine
+    from speculative_decoding_draft_04_gb300 import workloads as W
+    w = W.make_workload(W.config(name), trial=0)
+    d = engine.DeviceWorkload.from_workload(w, dev)
+    b = engine.Buffers.for_workload(d, dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        flush.zero_()
+        engine.cycle(d, b, stream)
+    torch.cuda.synchronize()
+
+    def timed(cold):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i in range(steps):
+            if cold:
+                flush.zero_()
+            evs[i][0].record(stream)
+            engine.cycle(d, b, stream)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return float(sum(a.elapsed_time(e) for a, e in evs) / steps)
+    cold, warm = timed(True), timed(False)
+    _lib.spec_profile_enable(True)
+    _lib.spec_profile_read()
+    for _ in range(steps):
+        flush.zero_()
+        engine.cycle(d, b, stream)
+    torch.cuda.synchronize()
+    prof = _lib.spec_profile_read()
+    _lib.spec_profile_enable(False)
+    stages = {k: v[0] / steps for k, v in prof.items() if v[1]}
+    draft_ms = stages.get("draft_persistent", 0.0) + stages.get("draft_slice", 0.0)
+    verify_ms = sum(v for k, v in stages.items() if not k.startswith("draft"))
+    hbm_peak, _, _ = measured_peaks()
+    db, vb, _ = algorithmic_bytes(w)
+    gbs = (db + vb) / (cold * 1e-3) / 1e9
+    positions = int(w.verify_len.sum())
+    out = {"workload": name + ": " + W.CONFIG_DESCRIPTIONS[name],
+           "draft_kernel": "slice-resident" if "draft_slice" in stages else "tile-strided",
+           "ms_per_cycle_cold": cold, "ms_per_cycle_warm": warm,
+           "draft_ms": draft_ms, "verify_ms": verify_ms,
+           "value": positions / (cold * 1e-3), "unit": UNIT, "positions_per_cycle": positions,
+           "cycle_algorithmic_bytes": db + vb, "cycle_gbs_cold": gbs,
+           "frac_of_8TBs": gbs / NOMINAL_HBM_GBS, "frac_of_measured": gbs / hbm_peak,
+           "draft_gbs": db / (draft_ms * 1e-3) / 1e9 if draft_ms else None,
+           "stages_ms_per_cycle": stages,
+           "status": [engine.status_words(b.dstatus), engine.status_words(b.vstatus)]}
+    del d, b
+    torch.cuda.empty_cache()
+    return out
+
+
 TREE_SLOTS, TREE_BUDGET = 24, 12
 
 
@@ -367,11 +428,62 @@ print(json.dumps([sample({seconds}) for _ in range({steps})]))
     return json.loads(out.stdout.strip().splitlines()[-1])
 
 
+def oracle_timing_all_cores(name, seconds, procs=None):
+    """The same oracle on every host core: `procs` single-threaded processes
+    (spawned), each drawing the workload, waiting at a common start, then
+    running whole requests (request b, b + procs, ...) for about `seconds`;
+    returns (requests, positions, wall seconds of the slowest, procs)."""
+    procs = procs or (os.cpu_count() or 1)
+    code = f"""
+import os, sys, time, json
+import multiprocessing as mp
+sys.path.insert(0, {ROOT!r})
+def work(i, n, bar, q):
+    import numpy as np
+    from speculative_decoding_draft_04_gb300 import workloads as W
+    from oracle import spec_oracle as O
+    w = W.make_workload(W.config({name!r}), trial=0)
+    W1, W2 = w.f64("W1"), w.f64("W2")
+    bar.wait()
+    t0 = time.perf_counter(); done = 0; pos = 0; b = i % w.B
+    while True:
+        tb = W.to_f64(w.target[b], w.dtype); ub = W.to_f64(w.U[b], w.dtype)
+        O.cycle_request(tb, ub, W1, W2, w.anchor[b], float(w.temperature[b]),
+                        w.u_draft[b].astype(np.float64), int(w.verify_len[b]),
+                        w.u_accept[b].astype(np.float64), float(w.u_final[b]))
+        done += 1; pos += int(w.verify_len[b]); b = (b + n) % w.B
+        el = time.perf_counter() - t0
+        if el > {seconds}: break
+    q.put((done, pos, el))
+if __name__ == "__main__":
+    ctx = mp.get_context("spawn")
+    n = {procs}
+    bar = ctx.Barrier(n); q = ctx.Queue()
+    ps = [ctx.Process(target=work, args=(i, n, bar, q)) for i in range(n)]
+    for p in ps: p.start()
+    res = [q.get() for _ in ps]
+    for p in ps: p.join()
+    print(json.dumps(res))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                         timeout=seconds * 4 + 900)
+    if out.returncode != 0:
+        raise RuntimeError("all-core oracle timing failed: " + out.stderr[-500:])
+    res = json.loads(out.stdout.strip().splitlines()[-1])
+    return (sum(r[0] for r in res), sum(r[1] for r in res), max(r[2] for r in res), procs)
+
+
 def cpu_baseline(name, seconds):
-    (req, pos, el), = oracle_timing(name, 0, 0, 1, seconds)
-    return {"value": pos / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{req} whole requests of {name} (draft + verify, float64 numpy, 1 thread) "
-                      f"in {el:.1f} s; host cpus={os.cpu_count()}"}
+    """The float64 oracle on all host cores (one process per core, whole
+    requests), with the single-core figure beside it."""
+    (req1, pos1, el1), = oracle_timing(name, 0, 0, 1, seconds / 2)
+    req, pos, el, n = oracle_timing_all_cores(name, seconds / 2)
+    return {"value": pos / el, "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": f"{req} whole requests of {name} (draft + verify, float64 numpy) on {n} "
+                      f"single-threaded processes in {el:.1f} s; host cpus={os.cpu_count()}",
+            "one_core": {"value": pos1 / el1, "unit": UNIT, "cores": 1,
+                         "sample": f"{req1} whole requests in {el1:.1f} s, 1 thread"}}
 
 
 def run_reference(args):
@@ -380,10 +492,14 @@ def run_reference(args):
         return
     from speculative_decoding_draft_04_gb300 import workloads as W
     per_step = min(20.0, max(1.0, 150.0 / max(1, args.steps + args.warmup)))
-    samples = oracle_timing(args.config, 0, args.warmup, args.steps, per_step)
-    req = sum(s[0] for s in samples)
-    pos = sum(s[1] for s in samples)
-    el = sum(s[2] for s in samples)
+    # warm-up steps: one short single-process sample (imports, first touch)
+    oracle_timing(args.config, 0, 0, 1, 1.0)
+    req = pos = 0
+    el = 0.0
+    ncores = 1
+    for _ in range(args.steps):
+        r, p, e, ncores = oracle_timing_all_cores(args.config, per_step)
+        req, pos, el = req + r, pos + p, el + e
     v = pos / el
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
@@ -391,9 +507,9 @@ def run_reference(args):
             "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.config + ": " + W.CONFIG_DESCRIPTIONS[args.config],
                        "step": f"a bounded sample of about {per_step:.1f} s of whole requests"},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"{req} whole requests over {args.steps} steps in {el:.1f} s; "
-                                       f"host cpus={os.cpu_count()}"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": ncores, "kind": "oracle",
+                             "sample": f"{req} whole requests over {args.steps} steps in {el:.1f} s "
+                                       f"on {ncores} single-threaded processes; host cpus={os.cpu_count()}"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -476,6 +592,15 @@ def main():
     times = [a.elapsed_time(b) for a, b in evs]
     ms = float(sum(times) / len(times))
     clocks = clk.summary()
+    # the same cycles back to back without the flush (warm L2), for context
+    wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        wev[i][0].record(stream)
+        step()
+        wev[i][1].record(stream)
+    torch.cuda.synchronize()
+    warm_ms = float(sum(a.elapsed_time(b) for a, b in wev) / args.steps)
 
     # ---- second timed pass with per-kernel events (roofline of the top kernel)
     _lib.spec_profile_enable(True)
@@ -514,6 +639,10 @@ def main():
     op = operating_point(d, bufs, draft_prof, args.steps) \
         if rank == 0 else None
     sched = rnn = tree = None
+    others = {}
+    if rank == 0 and world == 1:
+        for name in [c for c in args.other_configs.split(",") if c and c != args.config]:
+            others[name] = config_pass(name, args, flush, dev)
     if not args.no_extras:
         sched = scheduled_pass(args, w, d, bufs, stream, flush, rank, dev)
         rnn = rnn_pass(args, w, d, bufs, stream, flush, rank, dev)
@@ -549,6 +678,8 @@ def main():
                        "l2": f"flushed between steps ({flush.numel() >> 20} MiB write, outside the events)",
                        "launch": launch_mode,
                        "positions_per_step": positions},
+            "warm_l2": {"ms_per_step": warm_ms, "value": float(positions) / (warm_ms * 1e-3),
+                        "note": "the same cycles back to back, no L2 flush (context only)"},
             "hbm": {"cycle_algorithmic_bytes": draft_b + verify_b, "cycle_gbs": cyc_gbs,
                     "frac_of_8TBs": cyc_gbs / NOMINAL_HBM_GBS,
                     "frac_of_measured": cyc_gbs / hbm_peak},
@@ -565,6 +696,8 @@ def main():
             "gpu_launches": int(launches * args.steps),
             "clocks": clocks,
         }
+        if others:
+            line["other_configs"] = others
         if not args.no_extras:
             line["scheduled_cycle"] = sched
             line["rnn_cycle"] = rnn

@@ -17,6 +17,7 @@ cudaError_t launch_draft_persistent(const Shape&, const void*, const void*, cons
 cudaError_t launch_draft_slice(const Shape&, const void*, const void*, const void*, const int*,
                                const float*, const float*, int*, float*, double*, float*, uint32_t*,
                                const Ws&, const Eps&, int, cudaStream_t, int);
+int slice_chunks(const Shape&, int);
 cudaError_t launch_verify_prep(const Shape&, const int*, const float*, const int*, const double*,
                                const int*, const Ws&, uint32_t*, int*, int*, float*, float*,
                                cudaStream_t);
@@ -171,8 +172,8 @@ int grid_for_refine() { return 2 * num_sms(); }
 // Residual re-decisions whose weights are kept between their two passes.
 constexpr int kHpwItems = 16;
 struct Layout {
-  size_t ctrl, trace, items, hpsum, hpcnt, hpw, hpnorm, rnnst, dpart, rowptr, prow, prevtok, vflags, lse_p, bpart, vpart, slow,
-      accbits, rowc, rowp, total;
+  size_t ctrl, trace, items, hpsum, hpcnt, hpw, hpnorm, rnnst, dpart, abuf, rowptr, prow, prevtok, vflags, lse_p,
+      bpart, vpart, slow, accbits, rowc, rowp, total;
   int max_items, item_cap, hpw_items;
 };
 
@@ -197,6 +198,7 @@ Layout layout(const Shape& sh) {
   L.hpnorm = take((size_t)L.max_items * sizeof(float4));
   L.rnnst = take((size_t)(sh.gamma + 1) * sh.B * sh.r * sizeof(float));   // RNN head states
   L.dpart = take(B * sh.NC * sizeof(float4));
+  L.abuf = take((size_t)(sh.B < 128 ? sh.B : 128) * sh.r * 4);
   L.rowptr = take((B + 1) * sizeof(int));
   L.prow = take(B * g * sizeof(int2));
   L.prevtok = take(B * g * sizeof(int));
@@ -227,6 +229,7 @@ Ws views(const Layout& L, void* base) {
   w.hpw_items = L.hpw_items;
   w.hpnorm = reinterpret_cast<float4*>(p + L.hpnorm);
   w.dpart = reinterpret_cast<float4*>(p + L.dpart);
+  w.abuf = p + L.abuf;
   w.rowptr = reinterpret_cast<int*>(p + L.rowptr);
   w.prow = reinterpret_cast<int2*>(p + L.prow);
   w.prevtok = reinterpret_cast<int*>(p + L.prevtok);
@@ -296,7 +299,7 @@ int launch_draft(const spec_draft_args* a, const Shape& sh, const Ws& ws, cudaSt
   SPEC_TRY(cudaMemsetAsync(ws.hpcnt, 0, (size_t)ws.max_items * sizeof(uint32_t), st));
   const Eps eps = current_eps();
   if constexpr (sizeof(DT) == 2) {
-    if (path == 2 && !rnn && kernel == 0) {
+    if (path == 2 && !rnn && kernel == 0 && slice_chunks(sh, nsm) > 0) {
       ProfScope p(st, ST_DRAFT_SLICE);
       const cudaError_t e = launch_draft_slice(sh, a->U, a->W1, a->W2, a->anchor, a->temperature,
                                                a->u_draft, a->draft_tokens, a->q_tok, a->lse_q, a->diag,
@@ -421,6 +424,7 @@ Layout draft_only_layout(const Shape& sh) {
   L.hpsum = take((size_t)L.max_items * sh.NC * sizeof(float2));
   L.hpcnt = take((size_t)L.max_items * sizeof(uint32_t));
   L.dpart = take((size_t)sh.B * sh.NC * sizeof(float4));
+  L.abuf = take((size_t)(sh.B < 128 ? sh.B : 128) * sh.r * 4);
   L.total = off;
   return L;
 }
@@ -436,6 +440,7 @@ Ws draft_only_views(const Layout& L, void* base) {
   w.hp_cols = 1;
   w.hpcnt = reinterpret_cast<uint32_t*>(p + L.hpcnt);
   w.dpart = reinterpret_cast<float4*>(p + L.dpart);
+  w.abuf = p + L.abuf;
   return w;
 }
 

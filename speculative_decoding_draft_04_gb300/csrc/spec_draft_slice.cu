@@ -27,10 +27,12 @@
 //     sampler of spec_sample.cuh), grid barrier.
 //
 // Draws within the first pass's error band are queued over all steps and
-// re-decided in extended precision after the last step (spec_hp.cuh), in
-// batches of ws.max_items; a re-decision that changes a token sends every
-// step after the earliest change through a redo with its re-decisions in
-// place.  Every wait is bounded; a CTA that gives up raises the abort word,
+// re-decided in extended precision after the last step (spec_hp.cuh's
+// method), in batches of ws.max_items: every CTA computes the items'
+// double-float weights of its own columns from its resident W2 columns, then
+// one CTA per item finds the crossing chunk and scans it.  A re-decision that
+// changes a token sends every step after the earliest change through a redo
+// with its re-decisions in place.  Every wait is bounded; a CTA that gives up raises the abort word,
 // waits for its own copies and MMAs in flight, frees its tensor memory and
 // returns.
 #include <cstring>
@@ -75,9 +77,10 @@ struct SlLayout {
 
 // Barrier slots: the W2 load, the gathered A tile, the two MMA groups, the U
 // chunks.  Each completes once per tile phase (W2 once per load).
-enum : int { SB_W2 = 0, SB_AFULL = 1, SB_ACC0 = 2, SB_ACC1 = 3, SB_U0 = 4, SB_COUNT = SB_U0 + SL_MAX_K };
+enum : int { SB_W2 = 0, SB_AFULL = 1, SB_ACC0 = 2, SB_ACC1 = 3, SB_ATMA = 4, SB_U0 = 5,
+             SB_COUNT = SB_U0 + SL_MAX_K };
 // Bits of the "armed" word: async operations issued and not yet waited for.
-enum : uint32_t { ARM_W2 = 1u << 8, ARM_MMA = 1u << 9 };
+enum : uint32_t { ARM_W2 = 1u << 8, ARM_MMA = 1u << 9, ARM_A = 1u << 10 };
 
 // 16-byte piece j (0..3) of row m of a 64-byte-swizzled [128][32] bf16 chunk.
 __device__ __forceinline__ const unsigned char* sl_upiece(const unsigned char* ub, int m, int j) {
@@ -122,11 +125,13 @@ __global__ void __launch_bounds__(NT, 1) draft_slice_kernel(const __grid_constan
     mbar_init(s_bar + SB_AFULL, NT);
     mbar_init(s_bar + SB_ACC0, 1);
     mbar_init(s_bar + SB_ACC1, 1);
+    mbar_init(s_bar + SB_ATMA, 1);
     for (int c = 0; c < SL_MAX_K; ++c) mbar_init(s_bar + SB_U0 + c, 1);
     s_fail = 0;
     s_armed = 0u;
     tma_prefetch_map(&P.maps.u);
     tma_prefetch_map(&P.maps.w2);
+    tma_prefetch_map(&P.maps.a);
   }
   if (warp == 0) tc_alloc(&s_holder, SL_TMEM_COLS);
   tc_fence_before();
@@ -137,6 +142,9 @@ __global__ void __launch_bounds__(NT, 1) draft_slice_kernel(const __grid_constan
   uint32_t gen = 0u;        // grid barriers passed (thread 0)
   uint32_t gi = 0u;         // tile phases run: the parity of the per-phase barriers
   uint32_t nw2 = 0u;        // W2 loads issued
+  uint32_t ngath = 0u;      // A tiles gathered by cp.async (phases of SB_AFULL)
+  uint32_t natma = 0u;      // A tiles loaded by TMA from the A-row buffer (phases of SB_ATMA)
+  bool redo_mode = false;   // steps after a changed re-decision: A rows gathered from the tokens
   bool w2_ok = false;       // the W2 columns are resident
   int ring_step = -1;       // step whose first chunks are loaded or in flight (not yet consumed)
   unsigned long long* tr = (P.ws.trace && blockIdx.x == 0 && threadIdx.x == 0) ? P.ws.trace : nullptr;
@@ -185,14 +193,35 @@ __global__ void __launch_bounds__(NT, 1) draft_slice_kernel(const __grid_constan
         w2_ok = true;
       }
       if (ring_step != k) issue_ring(k);
-      for (int m = threadIdx.x; m < TC_M; m += NT) s_tok[m] = token(k, m);
-      __syncthreads();
-      tp_gather_a(smem + lay.offA, W1, s_tok, sh.r, (int)threadIdx.x, NT);
-      fence_async_shared();
-      mbar_arrive(s_bar + SB_AFULL);
+      // A operand: rows W1[x_{k-1}].  After the first step the samplers have
+      // copied them into the A-row buffer, loaded here by TMA (4 boxes of 64
+      // columns); the first step and the redo gather them by cp.async.
+      const bool by_tma = k > 0 && !redo_mode;
+      uint64_t* abar = by_tma ? s_bar + SB_ATMA : s_bar + SB_AFULL;
+      const uint32_t apar = by_tma ? (natma & 1u) : (ngath & 1u);
+      if (by_tma) {
+        if (threadIdx.x == 0) {
+          // the rows were written by other CTAs (generic proxy) before the grid barrier
+          asm volatile("fence.proxy.async.global;\n" ::: "memory");
+          mbar_expect_tx(abar, (uint32_t)(sh.r / 64) * 16384u);
+          for (int a = 0; a < sh.r / 64; ++a)
+            tma_load_2d(smem + lay.offA + (size_t)a * 16384, &P.maps.a, 64 * a, 0, abar);
+          atomicOr(&s_armed, ARM_A);
+        }
+        ++natma;
+      } else {
+        for (int m = threadIdx.x; m < TC_M; m += NT) s_tok[m] = token(k, m);
+        __syncthreads();
+        if (tr) tr[k * TRACE_SLOTS + 6] = globaltimer_ns();
+        tp_gather_a(smem + lay.offA, W1, s_tok, sh.r, (int)threadIdx.x, NT);
+        if (tr) tr[k * TRACE_SLOTS + 7] = globaltimer_ns();
+        fence_async_shared();
+        mbar_arrive(abar);
+        ++ngath;
+      }
       const uint32_t par = gi & 1u;
       if (threadIdx.x == 0) {
-        if (tp_wait(s_bar + SB_AFULL, par, fail) && tp_wait(s_bar + SB_W2, (nw2 - 1u) & 1u, fail)) {
+        if (tp_wait(abar, apar, fail) && tp_wait(s_bar + SB_W2, (nw2 - 1u) & 1u, fail)) {
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + lay.offA), w0 = smem_u32(smem + lay.offW);
           const uint32_t ab = (uint32_t)(sh.r * 128);      // bytes of one 64-column W2 atom
@@ -273,23 +302,101 @@ __global__ void __launch_bounds__(NT, 1) draft_slice_kernel(const __grid_constan
     for (int b = blockIdx.x; b < sh.B; b += G)
       draft_sample_body<bf16, HOOK>(sh, k, b, U, W1, W2, P.anchor, P.temp, P.u_draft, P.tokens,
                                     P.q_tok, P.lse_q, P.diag, P.status, P.ws, P.eps,
-                                    ctrl + CTRL_DITEMS, P.ws.item_cap, smem + lay.offA);
+                                    ctrl + CTRL_DITEMS, P.ws.item_cap, smem + lay.offA,
+                                    (P.ws.trace && blockIdx.x == 0 && b == 0)
+                                        ? P.ws.trace + (MAX_GAMMA + k) * TRACE_SLOTS : nullptr,
+                                    redo_mode ? nullptr : reinterpret_cast<bf16*>(P.ws.abuf));
   };
 
-  // ---- re-decision of the queued draws, ws.max_items at a time; the W2
-  // space is used as the pass's slab, so the columns are reloaded afterwards
+  // ---- re-decision of the queued draws, ws.max_items at a time, on the
+  // slice layout: each CTA computes the items' extended-precision weights of
+  // its own columns from the W2 columns already in its shared memory (the
+  // compensated dot products of spec_hp.cuh's method) and writes their
+  // 32-column chunk sums; after a grid barrier one CTA per item finds the
+  // crossing chunk, recomputes its 32 weights and scans them
+  // (hp_decide_item).  W2 stays resident.
+  __shared__ HpShared S_hp;
   auto redecide = [&](uint32_t* redo) -> bool {
     const int n = min((int)__ldcg(ctrl + CTRL_DITEMS), P.ws.item_cap);
     if (n == 0) return true;
+    constexpr int SUB = 8;                                  // items whose rows are staged together
+    // scratch in the A tile's space (free after a tile phase; at least r x 256
+    // bytes): item records (<= 128 x 40 bytes), SUB factor rows, SUB contexts
+    unsigned char* scratch = smem + lay.offA;
+    HpItem* s_items = reinterpret_cast<HpItem*>(scratch);
+    float* arows = reinterpret_cast<float*>(scratch + 8192);
+    ItemCtx<bf16>* ictx = reinterpret_cast<ItemCtx<bf16>*>(scratch + 8192 + (size_t)SUB * sh.r * 4);
+    hp_table(S_hp.tab);
     for (int base = 0; base < n; base += P.ws.max_items) {
       Ws wb = P.ws;
       wb.items = P.ws.items + base;
       const int nb = min(P.ws.max_items, n - base);
-      hp_sums_body<bf16>(sh, R, wb, 0, nb, smem_raw, true, P.tokens, P.q_tok, P.lse_q, P.status,
-                         nullptr, nullptr, 0u, redo);
+      if (kc > 0) {
+        const int col = (int)threadIdx.x;        // this thread's column of the range
+        const int v = n0 + col;
+        const bool mine = col < kc * CW && v < sh.V;
+        const int a = col >> 6, cc = col & 63;
+        const unsigned char* wcol = smem + lay.offW + (size_t)a * sh.r * 128 + (cc & 7) * 2;
+        __syncthreads();                         // the scratch space is free
+        for (int i = threadIdx.x; i < nb; i += NT) s_items[i] = ldcg_item(wb.items + i);
+        __syncthreads();
+        for (int i0 = 0; i0 < nb; i0 += SUB) {
+          const int cnt = min(SUB, nb - i0);
+          // every item's factor row, context and this thread's logit, all loads at once
+          for (int q = threadIdx.x; q < cnt * sh.r; q += NT) {
+            const int i = q / sh.r, e = q - i * sh.r;
+            arows[i * sh.r + e] = ldf(W1 + (size_t)s_items[i0 + i].prev * sh.r + e);
+          }
+          if ((int)threadIdx.x < cnt) ictx[threadIdx.x] = item_ctx<bf16>(sh, R, s_items[i0 + threadIdx.x]);
+          float uq[SUB];
+#pragma unroll
+          for (int i = 0; i < SUB; ++i) {
+            uq[i] = 0.f;
+            if (i < cnt && mine) {
+              const HpItem& it = s_items[i0 + i];
+              uq[i] = ldf(U + ((size_t)it.b * sh.gamma + it.j) * sh.V + v);
+            }
+          }
+          __syncthreads();
+#pragma unroll 1
+          for (int i = 0; i < cnt; ++i) {
+            df wq = {0.f, 0.f};
+            if (mine) {
+              const float* ar = arows + i * sh.r;
+              DdSum k0, k1;
+              for (int q0 = 0; q0 < sh.r; q0 += 8) {
+                const unsigned char* rb = wcol + (size_t)q0 * 128;
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {
+                  // row q0 + j of the swizzled atom: 16-byte chunk (cc / 8) ^ j
+                  const float w0 = __bfloat162float(
+                      *reinterpret_cast<const bf16*>(rb + j * 128 + (((cc >> 3) ^ j) << 4)));
+                  const float w1 = __bfloat162float(
+                      *reinterpret_cast<const bf16*>(rb + (j + 1) * 128 + (((cc >> 3) ^ (j + 1)) << 4)));
+                  k0.add(__fmul_rn(ar[q0 + j], w0));   // bf16 x bf16 products are exact in fp32
+                  k1.add(__fmul_rn(ar[q0 + j + 1], w1));
+                }
+              }
+              wq = hp_wq_val<bf16>(ictx[i], dd_add(k0.value(), k1.value()), uq[i], S_hp.tab);
+              // the first items keep their weights for the decision
+              if (i0 + i < wb.hpw_items) wb.hpw[(size_t)(i0 + i) * sh.V + v] = make_float4(wq.hi, wq.lo, 0.f, 0.f);
+            }
+            const df csum = warp_sum_df(wq);
+            if (lane == 0 && warp < kc)
+              item_sums(wb, sh, i0 + i, 0)[c0 + warp] = make_float2(csum.hi, csum.lo);
+          }
+          __syncthreads();                       // the staged rows are consumed
+        }
+      }
+      if (tr) tr[(2 * MAX_GAMMA - 1) * TRACE_SLOTS + 1] = globaltimer_ns();
+      if (!gsync()) return false;
+      if (tr) tr[(2 * MAX_GAMMA - 1) * TRACE_SLOTS + 2] = globaltimer_ns();
+      for (int i = (int)blockIdx.x; i < nb; i += (int)G)
+        hp_decide_item<bf16>(sh, R, wb, i, P.tokens, P.q_tok, P.lse_q, nullptr, P.status, S_hp,
+                             reinterpret_cast<bf16*>(smem + lay.offA), redo);
+      if (tr) tr[(2 * MAX_GAMMA - 1) * TRACE_SLOTS + 3] = globaltimer_ns();
       if (!gsync()) return false;
     }
-    w2_ok = false;
     return true;
   };
 
@@ -309,12 +416,14 @@ __global__ void __launch_bounds__(NT, 1) draft_slice_kernel(const __grid_constan
   if (kc > 0) issue_ring(0);
   bool good = true;
   for (int k = 0; k < sh.gamma && good; ++k) good = run_step(k);
+  if (tr) tr[(2 * MAX_GAMMA - 1) * TRACE_SLOTS] = globaltimer_ns();
   if (good) good = redecide(ctrl + CTRL_REDO);
-  if (tr) tr[MAX_GAMMA * TRACE_SLOTS] = globaltimer_ns();
+  if (tr) tr[(2 * MAX_GAMMA - 1) * TRACE_SLOTS + 4] = globaltimer_ns();
   if (good) {
     const uint32_t redo = __ldcg(ctrl + CTRL_REDO);
     const int k0 = sh.gamma - (int)redo + 1;            // first step to redo
     if (redo > 0 && k0 < sh.gamma) {
+      redo_mode = true;
       for (int k = k0; k < sh.gamma && good; ++k) {
         if (blockIdx.x == 0 && threadIdx.x == 0) ctrl[CTRL_DITEMS] = 0u;
         good = run_step(k) && redecide(nullptr);
@@ -330,6 +439,7 @@ __global__ void __launch_bounds__(NT, 1) draft_slice_kernel(const __grid_constan
       for (int c = 0; c < SL_MAX_K; ++c)
         if (a & (1u << c)) mbar_wait(s_bar + SB_U0 + c, gi & 1u, 1u << 20);
       if (a & ARM_W2) mbar_wait(s_bar + SB_W2, (nw2 - 1u) & 1u, 1u << 20);
+      if (a & ARM_A) mbar_wait(s_bar + SB_ATMA, (natma - 1u) & 1u, 1u << 20);
       if (a & ARM_MMA) mbar_wait(s_bar + SB_ACC1, gi & 1u, 1u << 20);
     }
   }
@@ -405,6 +515,7 @@ cudaError_t launch_draft_slice(const Shape& sh, const void* U, const void* W1, c
   P.slK = K;
   cudaError_t e = encode_u_chunk_map(sh, U, &P.maps.u);
   if (e == cudaSuccess) e = encode_w2_map(sh, W2, &P.maps.w2);
+  if (e == cudaSuccess) e = encode_abuf_map(sh.B, sh.r, ws.abuf, &P.maps.a);
   if (e != cudaSuccess) return e;
   const int tiles = (sh.NC + K - 1) / K;       // CTAs with columns
   int G = tiles > sh.B ? tiles : (sh.B < nsm ? sh.B : nsm);

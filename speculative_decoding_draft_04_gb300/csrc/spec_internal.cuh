@@ -82,6 +82,8 @@ struct Ws {
                         // once the first sums pass is complete
   // draft
   float4* dpart;        // [B][NC] draft partials per CW-column chunk: (c, m, s, q2)
+  void* abuf;           // [min(B, 128)][r] storage type: the next draft step's A rows
+                        // W1[x_k] (slice-resident draft kernel)
   // verify
   int* rowptr;          // [B+1]
   int2* prow;           // [B*gamma] packed (b, j), j < L_b

@@ -71,21 +71,34 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
                                   const int* __restrict__ anchor, const float* __restrict__ temp,
                                   const float* __restrict__ u_draft, int* tokens, float* q_tok,
                                   double* lse_q, float* diag, uint32_t* status, const Ws& ws,
-                                  const Eps& eps, uint32_t* counter, int cap, unsigned char* dsm) {
+                                  const Eps& eps, uint32_t* counter, int cap, unsigned char* dsm,
+                                  unsigned long long* str = nullptr, DT* abuf = nullptr) {
   DT* slab = reinterpret_cast<DT*>(dsm);      // [r][CW] W2 columns of the crossing chunk
   __shared__ float sh_f[72];
   __shared__ float s_a[256];
   __shared__ float s_part[NT / CW][CW];
   __shared__ int s_slice, s_tok;
-  __shared__ float4 s_pm;
+  __shared__ float4 s_pm, s_ps;
   __shared__ float s_pref[2], s_lo, s_hi, s_wtok;
   __shared__ df s_tab[DD_EXP_TAB];
 
   __syncthreads();      // previous use of the shared buffers is finished
-  if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(s_tab, threadIdx.x);
+  unsigned long long* tstamp = (str && threadIdx.x == 0) ? str : nullptr;
+  if (tstamp) tstamp[0] = globaltimer_ns();
   const size_t ok = (size_t)b * sh.gamma + k;
+  const float4* P = ws.dpart + (size_t)b * sh.NC;
+  // ---- this thread's contiguous range of chunks (the first 8 kept in
+  // registers): their loads are issued first, so they overlap the token's
+  // and the exponential table's set-up
+  const int per = (sh.NC + NT - 1) / NT;
+  const int s0 = threadIdx.x * per, s1 = min(s0 + per, sh.NC);
+  float4 pv[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    if (s0 + q < s1) pv[q] = __ldcg(P + s0 + q);
   const int prev = (k == 0) ? anchor[b] : __ldcg(tokens + ok - 1);
   const float T = temp[b];
+  if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(s_tab, threadIdx.x);
   if (prev < 0 || prev >= sh.V || !temp_ok(T)) {
     if (threadIdx.x == 0) {
       tokens[ok] = -1;
@@ -94,6 +107,9 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
       set_status(status, (prev < 0 || prev >= sh.V) ? SPEC_DEV_BAD_TOKEN : SPEC_DEV_BAD_TEMP);
       if (diag) for (int q = 0; q < 4; ++q) diag[ok * 4 + q] = NAN;
     }
+    // the next step's A row of this request: zeros (its outputs are invalid)
+    if (abuf && (int)threadIdx.x * 8 < sh.r)
+      *reinterpret_cast<uint4*>(abuf + (size_t)b * sh.r + threadIdx.x * 8) = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
   const int arow = factor_row(sh, b, k, prev);
@@ -101,17 +117,11 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   // shared memory only when the crossing chunk's dot product needs it
   const float a_reg = (int)threadIdx.x < sh.r ? ldf(W1 + (size_t)arow * sh.r + threadIdx.x) : 0.f;
   const float invT = 1.0f / T;
-  const float4* P = ws.dpart + (size_t)b * sh.NC;
 
-  // ---- this thread's contiguous range of chunks (the first 8 kept in registers)
-  const int per = (sh.NC + NT - 1) / NT;
-  const int s0 = threadIdx.x * per, s1 = min(s0 + per, sh.NC);
-  float4 pv[8];
   float best = -INFINITY;
   int bidx = 0;
   for (int s = s0, q = 0; s < s1; ++s, ++q) {
-    const float4 p = __ldcg(P + s);
-    if (q < 8) pv[q] = p;
+    const float4 p = (q < 8) ? pv[q] : __ldcg(P + s);
     const float key = fmaf(p.x, invT, p.y);
     if (key > best) { best = key; bidx = s; }
   }
@@ -135,6 +145,7 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   }
   const float4 PM = s_pm;
   const float cM = PM.x, mM = PM.y;
+  if (tstamp) tstamp[1] = globaltimer_ns();
 
   // ---- chunk masses (double-float), normaliser and error-estimate sums
   df loc = {0.f, 0.f};
@@ -160,6 +171,7 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   __syncthreads();
   int my_slice = -1;
   df my_pref = {0.f, 0.f};
+  float4 my_ps = make_float4(0.f, 0.f, 0.f, 0.f);
   if (s0 < s1 && dd_le(excl, target) && !dd_le(df_add(excl, loc), target)) {
     df run = excl;
     for (int s = s0, q = 0; s < s1; ++s, ++q) {
@@ -168,6 +180,7 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
       if (!dd_le(nxt, target)) {
         my_slice = s;
         my_pref = run;
+        my_ps = p;
         atomicMin(&s_slice, s);
         break;
       }
@@ -175,7 +188,11 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
     }
   }
   __syncthreads();
-  if (my_slice >= 0 && my_slice == s_slice) { s_pref[0] = my_pref.hi; s_pref[1] = my_pref.lo; }
+  if (my_slice >= 0 && my_slice == s_slice) {
+    s_pref[0] = my_pref.hi;
+    s_pref[1] = my_pref.lo;
+    s_ps = my_ps;                     // the crossing chunk's partial, passed on chip
+  }
   __syncthreads();
   bool fallback = false;
   if (s_slice == 0x7fffffff) {
@@ -192,12 +209,14 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
       s_slice = sl;
       s_pref[0] = run.hi;
       s_pref[1] = run.lo;
+      s_ps = __ldcg(P + sl);
     }
     __syncthreads();
   }
   const int sl = s_slice;
   const df pref = {s_pref[0], s_pref[1]};
-  const float4 PS = __ldcg(P + sl);
+  const float4 PS = s_ps;
+  if (tstamp) tstamp[2] = globaltimer_ns();
   const float fS = chunk_factor(PS, cM, mM, invT);
   const int n0 = sl * CW;
 
@@ -209,6 +228,7 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   if ((int)threadIdx.x < sh.r) s_a[threadIdx.x] = a_reg;
   cp_async_wait_all();
   __syncthreads();
+  if (tstamp) tstamp[3] = globaltimer_ns();
   {
     const int col = threadIdx.x % CW, grp = threadIdx.x / CW;
     const int kg = sh.r / (NT / CW);           // r % 16 == 0, so r / 8 is whole
@@ -259,6 +279,7 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
     }
   }
   __syncthreads();
+  if (tstamp) tstamp[4] = globaltimer_ns();
   if (s_lo == 0.f && s_hi == 0.f) fallback = true;
   if (threadIdx.x == 0) {
     const int tok = n0 + s_tok;
@@ -286,6 +307,7 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
     tokens[ok] = wtok;
     q_tok[ok] = s_wtok * scale;
     lse_q[ok] = lse;
+    s_tok = wtok;                     // the token written (for the prefetch below)
     if (diag) {
       diag[ok * 4 + 0] = s_lo * scale;
       diag[ok * 4 + 1] = s_hi * scale;
@@ -294,6 +316,21 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
     }
   }
   __syncthreads();
+  if (tstamp) tstamp[5] = globaltimer_ns();
+  // the next step's A operand row of this request: W1[x_{k+1}] copied into
+  // `abuf` (row b), which the next tile phase loads by TMA; without `abuf`
+  // the row is only brought into L2 for the next step's gather
+  if (!sh.rnn && k + 1 < sh.gamma) {
+    const int t = s_tok;
+    if (abuf) {
+      if ((int)threadIdx.x * 8 < sh.r && t >= 0 && t < sh.V)
+        *reinterpret_cast<uint4*>(abuf + (size_t)b * sh.r + threadIdx.x * 8) =
+            __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)t * sh.r + threadIdx.x * 8));
+    } else if ((int)threadIdx.x * 128 < sh.r * (int)sizeof(DT) && t >= 0 && t < sh.V) {
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char*>(W1 + (size_t)t * sh.r) +
+                                                      threadIdx.x * 128));
+    }
+  }
 }
 
 struct DraftParams {

@@ -79,6 +79,7 @@ struct TpLayout {
 struct TpMaps {
   CUtensorMap u;     // U viewed as [B][gamma][V], box 64 x 1 x 128, 128-byte swizzle
   CUtensorMap w2;    // W2 viewed as [r][V],       box 64 x r,       128-byte swizzle
+  CUtensorMap a;     // slice-resident draft: its A-row buffer [rows][r], box 64 x 128
 };
 
 // Pipeline state of a CTA, identical in every thread.

@@ -63,6 +63,23 @@ inline cudaError_t encode_u_chunk_map(const Shape& sh, const void* U, CUtensorMa
   return cudaSuccess;
 }
 
+// The draft's A-row buffer as [rows][r] bf16, boxes of 64 columns x 128 rows
+// (one K atom of the A operand), 128-byte swizzle; rows beyond `rows` read as
+// zeros.
+inline cudaError_t encode_abuf_map(int rows, int r, const void* abuf, CUtensorMap* map) {
+  const EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)r, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)r * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t es[2] = {1, 1};
+  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(abuf), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
 // W2 as [r][V] bf16, boxes of 64 columns x r rows (one MN-major operand
 // atom), 128-byte swizzle; reads outside the tensor return zeros.
 inline cudaError_t encode_w2_map(const Shape& sh, const void* W2, CUtensorMap* map) {
