@@ -330,6 +330,7 @@ def algorithmic_bytes(w):
         "draft_slice": draft,                                       # the same, slice-resident kernel
         "target_stats": int((L + 1).sum()) * w.V * s,
         "verify_tile": int(L.sum()) * w.V * s + w.r * w.V * s,
+        "verify_slice": int(L.sum()) * w.V * s + w.r * w.V * s,   # the same, slice-resident tiles
     }
     return draft, verify, per_stage
 

@@ -491,11 +491,14 @@ const char* spec_status_string(int32_t status);
  *   SPEC_OPT_DRAFT_KERNEL  0 = the slice-resident draft kernel wherever the
  *                        shape fits it (default), 1 = always the tile-strided
  *                        draft kernel
+ *   SPEC_OPT_VERIFY_KERNEL 0 = the slice-resident verification tiles wherever
+ *                        the shape fits them (bf16, r % 64 == 0, V <= 256 x
+ *                        SM count; default), 1 = always the tile-strided ones
  * The two test hooks exist for the library's own tests; the default kernels
  * carry no trace of them.                                                   */
 enum { SPEC_OPT_EPS_SCALE = 1, SPEC_OPT_FORCE_SIMT = 2, SPEC_OPT_BIAS_PATH = 3,
        SPEC_OPT_TRACE = 5, SPEC_OPT_PERTURB = 6, SPEC_OPT_TEST_STALL = 7,
-       SPEC_OPT_DRAFT_KERNEL = 8 };   /* 4 is unused */
+       SPEC_OPT_DRAFT_KERNEL = 8, SPEC_OPT_VERIFY_KERNEL = 9 };   /* 4 is unused */
 int32_t spec_set_option(int32_t key, double value);
 
 /* Per-stage timing with CUDA events on the calls' streams.  enable(1)

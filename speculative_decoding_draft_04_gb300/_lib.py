@@ -19,6 +19,7 @@ SPEC_OPT_EPS_SCALE, SPEC_OPT_FORCE_SIMT, SPEC_OPT_BIAS_PATH, SPEC_OPT_TRACE = 1,
 SPEC_OPT_PERTURB = 6
 SPEC_OPT_TEST_STALL = 7
 SPEC_OPT_DRAFT_KERNEL = 8
+SPEC_OPT_VERIFY_KERNEL = 9
 DEV_BITS = {1: "BAD_TOKEN", 2: "BAD_LEN", 4: "BAD_TEMP", 8: "TIMEOUT", 16: "REFINED",
             32: "OVERFLOW", 64: "BAD_CONF", 128: "BAD_TREE"}
 

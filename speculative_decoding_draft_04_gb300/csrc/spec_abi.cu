@@ -18,6 +18,9 @@ cudaError_t launch_draft_slice(const Shape&, const void*, const void*, const voi
                                const float*, const float*, int*, float*, double*, float*, uint32_t*,
                                const Ws&, const Eps&, int, cudaStream_t, int);
 int slice_chunks(const Shape&, int);
+cudaError_t launch_verify_slice(const Shape&, const bf16*, const bf16*, const bf16*, const bf16*, const Ws&,
+                                uint32_t*, int, cudaStream_t);
+int vslice_chunks(const Shape&, int);
 cudaError_t launch_verify_prep(const Shape&, const int*, const float*, const int*, const double*,
                                const int*, const Ws&, uint32_t*, int*, int*, float*, float*,
                                cudaStream_t);
@@ -68,6 +71,7 @@ bool g_trace = false;         // SPEC_OPT_TRACE
 bool g_perturb = false;       // SPEC_OPT_PERTURB (test build of the draft kernels)
 bool g_stall = false;         // SPEC_OPT_TEST_STALL (test build of the draft kernels)
 int g_draft_kernel = 0;       // SPEC_OPT_DRAFT_KERNEL: 0 slice-resident where it fits, 1 tile-strided
+int g_verify_kernel = 0;      // SPEC_OPT_VERIFY_KERNEL: 0 slice-resident tiles where they fit, 1 tile-strided
 
 // Band constants (probability units) of the certified first-pass decisions.
 // Largest first-pass margin error seen against the float64 oracle over C0-C4
@@ -97,13 +101,13 @@ Eps current_eps() {
 // ---------------------------------------------------------------- profiling
 enum Stage {
   ST_DRAFT_PERSISTENT, ST_DRAFT_SLICE, ST_VERIFY_PREP,
-  ST_TARGET_STATS, ST_VERIFY_TILE, ST_VERIFY_FINAL, ST_SLOW_VERIFY, ST_VERIFY_HP_SUMS,
+  ST_TARGET_STATS, ST_VERIFY_TILE, ST_VERIFY_SLICE, ST_VERIFY_FINAL, ST_SLOW_VERIFY, ST_VERIFY_HP_SUMS,
   ST_VERIFY_HP_RESID, ST_CONFIDENCE, ST_SCHED_RANK, ST_SCHED_SELECT, ST_TREE_SELECT,
   ST_TREE_DRAFT, ST_TREE_VERIFY, ST_COUNT
 };
 const char* kStageNames[ST_COUNT] = {
     "draft_persistent", "draft_slice", "verify_prep",
-    "target_stats", "verify_tile", "verify_final", "slow_verify", "verify_hp_sums",
+    "target_stats", "verify_tile", "verify_slice", "verify_final", "slow_verify", "verify_hp_sums",
     "verify_hp_resid", "confidence", "sched_rank", "sched_select", "tree_select",
     "tree_draft", "tree_verify"};
 bool g_prof = false;
@@ -358,13 +362,20 @@ int run_verify(const spec_verify_args* a, cudaStream_t st) {
   }
   const void* F = a->a_rows ? a->a_rows : a->W1;
   const Layout L = layout(sh);
-  const Ws ws = views(L, a->workspace);
+  Ws ws = views(L, a->workspace);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_trace)
+      ws.trace = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(a->workspace) + L.trace);
+  }
   const Eps eps = current_eps();
-  int path;
+  int path, vkernel;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     path = g_force_simt ? 0 : g_bias_path;
+    vkernel = g_verify_kernel;
   }
+  const int nsm = num_sms();
   const int grid = grid_for_refine();
   if (grid <= 0) return SPEC_ECUDA;
   HpRows R{a->target, a->U, F, a->W2, a->temperature};
@@ -379,7 +390,17 @@ int run_verify(const spec_verify_args* a, cudaStream_t st) {
     ProfScope p(st, ST_TARGET_STATS);
     SPEC_TRY(launch_target_stats<DT>(sh, a->target, a->temperature, a->verify_len, ws, st));
   }
-  {
+  bool sliced = false;
+  if constexpr (sizeof(DT) == 2) {
+    if (path == 2 && vkernel == 0 && vslice_chunks(sh, nsm) > 0) {
+      ProfScope p(st, ST_VERIFY_SLICE);
+      const cudaError_t e = launch_verify_slice(sh, (const bf16*)a->target, (const bf16*)a->U, (const bf16*)F,
+                                                (const bf16*)a->W2, ws, a->dev_status, nsm, st);
+      if (e != cudaSuccess && e != cudaErrorNotSupported) return SPEC_ECUDA;
+      sliced = e == cudaSuccess;
+    }
+  }
+  if (!sliced) {
     ProfScope p(st, ST_VERIFY_TILE);
     SPEC_TRY(launch_verify_tile<DT>(sh, a->target, a->U, F, a->W2, ws, path, a->dev_status, st));
   }
@@ -834,6 +855,10 @@ int32_t spec_set_option(int32_t key, double value) {
     case SPEC_OPT_DRAFT_KERNEL:
       if (value != 0.0 && value != 1.0) return SPEC_EINVAL;
       g_draft_kernel = (int)value;
+      return SPEC_OK;
+    case SPEC_OPT_VERIFY_KERNEL:
+      if (value != 0.0 && value != 1.0) return SPEC_EINVAL;
+      g_verify_kernel = (int)value;
       return SPEC_OK;
     default:
       return SPEC_EINVAL;

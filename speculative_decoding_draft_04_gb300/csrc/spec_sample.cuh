@@ -120,8 +120,16 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
 
   float best = -INFINITY;
   int bidx = 0;
-  for (int s = s0, q = 0; s < s1; ++s, ++q) {
-    const float4 p = (q < 8) ? pv[q] : __ldcg(P + s);
+  // (the first 8 chunks from registers with compile-time indices, the rest,
+  // for vocabularies beyond 8 x 32 x 256 columns, from L2)
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    if (s0 + q < s1) {
+      const float key = fmaf(pv[q].x, invT, pv[q].y);
+      if (key > best) { best = key; bidx = s0 + q; }
+    }
+  for (int s = s0 + 8; s < s1; ++s) {
+    const float4 p = __ldcg(P + s);
     const float key = fmaf(p.x, invT, p.y);
     if (key > best) { best = key; bidx = s; }
   }
@@ -140,7 +148,10 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
     __syncthreads();
     // the owner of the reference chunk passes its partial on
     const int rs = s_slice;
-    if (rs >= s0 && rs < s1) s_pm = (rs - s0 < 8) ? pv[rs - s0] : __ldcg(P + rs);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (rs == s0 + q && rs < s1) s_pm = pv[q];
+    if (rs >= s0 + 8 && rs < s1) s_pm = __ldcg(P + rs);
     __syncthreads();
   }
   const float4 PM = s_pm;
@@ -150,8 +161,20 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   // ---- chunk masses (double-float), normaliser and error-estimate sums
   df loc = {0.f, 0.f};
   float q2 = 0.f, m2 = 0.f;
-  for (int s = s0, q = 0; s < s1; ++s, ++q) {
-    const float4 p = (q < 8) ? pv[q] : __ldcg(P + s);
+  float wv[8];                       // the chunk masses kept for the crossing search
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    wv[q] = 0.f;
+    if (s0 + q < s1) {
+      const float f = chunk_factor(pv[q], cM, mM, invT);
+      wv[q] = pv[q].z * f;
+      loc = df_addf(loc, wv[q]);
+      q2 = fmaf(pv[q].w * f, f, q2);
+      m2 = fmaf(wv[q], wv[q], m2);
+    }
+  }
+  for (int s = s0 + 8; s < s1; ++s) {
+    const float4 p = __ldcg(P + s);
     const float f = chunk_factor(p, cM, mM, invT);
     const float w = p.z * f;
     loc = df_addf(loc, w);
@@ -174,18 +197,31 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   float4 my_ps = make_float4(0.f, 0.f, 0.f, 0.f);
   if (s0 < s1 && dd_le(excl, target) && !dd_le(df_add(excl, loc), target)) {
     df run = excl;
-    for (int s = s0, q = 0; s < s1; ++s, ++q) {
-      const float4 p = (q < 8) ? pv[q] : __ldcg(P + s);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (my_slice < 0 && s0 + q < s1) {
+        const df nxt = df_addf(run, wv[q]);
+        if (!dd_le(nxt, target)) {
+          my_slice = s0 + q;
+          my_pref = run;
+          my_ps = pv[q];
+        } else {
+          run = nxt;
+        }
+      }
+    }
+    for (int s = s0 + 8; s < s1 && my_slice < 0; ++s) {
+      const float4 p = __ldcg(P + s);
       const df nxt = df_addf(run, p.z * chunk_factor(p, cM, mM, invT));
       if (!dd_le(nxt, target)) {
         my_slice = s;
         my_pref = run;
         my_ps = p;
-        atomicMin(&s_slice, s);
-        break;
+      } else {
+        run = nxt;
       }
-      run = nxt;
     }
+    if (my_slice >= 0) atomicMin(&s_slice, my_slice);
   }
   __syncthreads();
   if (my_slice >= 0 && my_slice == s_slice) {

@@ -148,3 +148,32 @@ def test_stalled_barrier_times_out_and_the_context_survives(spec_fn):
     assert g.dstatus[0] & 8 == 0 and g.vstatus[0] & 8 == 0
     rows = None if w.B <= 8 else list(range(0, w.B, 8))
     assert_parity(compare(w, g, oracle_cycle(w, rows=rows), rows=rows))
+
+
+# ----------------------------------------------------------------- verification tiles
+
+def _with_verify_kernel(kernel, w):
+    _lib.spec_set_option(_lib.SPEC_OPT_VERIFY_KERNEL, kernel)
+    try:
+        return gpu_cycle(w)
+    finally:
+        _lib.spec_set_option(_lib.SPEC_OPT_VERIFY_KERNEL, 0)
+
+
+@pytest.mark.parametrize("B_,V,r,gamma", SHAPES + [(200, 9000, 256, 7)])
+def test_slice_verification_tiles_match_oracle_and_tile_strided(B_, V, r, gamma):
+    """The slice-resident verification tiles (W2 columns resident per CTA,
+    packed rows in tiles of 128 with two TMEM accumulators; 200 requests give
+    up to 1400 packed rows, i.e. 11 row tiles) against the oracle and against
+    the tile-strided verification tiles on the same draft."""
+    w = W.make_workload(_spec(B_, V, r, gamma), trial=4)
+    rows = None if B_ * gamma * V <= 40_000_000 else list(range(0, B_, 5))
+    g = _with_verify_kernel(0, w)
+    assert g.dstatus[0] & 8 == 0 and g.vstatus[0] & 8 == 0
+    assert_parity(compare(w, g, oracle_cycle(w, rows=rows), rows=rows))
+    g1 = _with_verify_kernel(1, w)
+    np.testing.assert_array_equal(g.draft_tokens, g1.draft_tokens)
+    np.testing.assert_array_equal(g.accept_len, g1.accept_len)
+    np.testing.assert_array_equal(g.out_tokens, g1.out_tokens)
+    np.testing.assert_allclose(g.alpha, g1.alpha, atol=1e-5, rtol=0, equal_nan=True)
+    np.testing.assert_allclose(g.p_tok, g1.p_tok, atol=1e-5, rtol=0, equal_nan=True)
