@@ -429,11 +429,13 @@ print(json.dumps([sample({seconds}) for _ in range({steps})]))
     return json.loads(out.stdout.strip().splitlines()[-1])
 
 
-def oracle_timing_all_cores(name, seconds, procs=None):
+def oracle_timing_all_cores(name, seconds, procs=None, steps=1):
     """The same oracle on every host core: `procs` single-threaded processes
-    (spawned), each drawing the workload, waiting at a common start, then
-    running whole requests (request b, b + procs, ...) for about `seconds`;
-    returns (requests, positions, wall seconds of the slowest, procs)."""
+    (spawned once), each drawing the workload; then `steps` timed samples,
+    each started by all processes together and ended when every process has
+    run whole requests (request b, b + procs, ...) for about `seconds`.
+    Returns per step (requests, positions, wall seconds of the slowest), and
+    the process count."""
     procs = procs or (os.cpu_count() or 1)
     code = f"""
 import os, sys, time, json
@@ -445,41 +447,54 @@ def work(i, n, bar, q):
     from oracle import spec_oracle as O
     w = W.make_workload(W.config({name!r}), trial=0)
     W1, W2 = w.f64("W1"), w.f64("W2")
-    bar.wait()
-    t0 = time.perf_counter(); done = 0; pos = 0; b = i % w.B
-    while True:
-        tb = W.to_f64(w.target[b], w.dtype); ub = W.to_f64(w.U[b], w.dtype)
-        O.cycle_request(tb, ub, W1, W2, w.anchor[b], float(w.temperature[b]),
-                        w.u_draft[b].astype(np.float64), int(w.verify_len[b]),
-                        w.u_accept[b].astype(np.float64), float(w.u_final[b]))
-        done += 1; pos += int(w.verify_len[b]); b = (b + n) % w.B
-        el = time.perf_counter() - t0
-        if el > {seconds}: break
-    q.put((done, pos, el))
+    b = i % w.B
+    for step in range({steps}):
+        bar.wait()
+        t0 = time.perf_counter(); done = 0; pos = 0
+        while True:
+            tb = W.to_f64(w.target[b], w.dtype); ub = W.to_f64(w.U[b], w.dtype)
+            O.cycle_request(tb, ub, W1, W2, w.anchor[b], float(w.temperature[b]),
+                            w.u_draft[b].astype(np.float64), int(w.verify_len[b]),
+                            w.u_accept[b].astype(np.float64), float(w.u_final[b]))
+            done += 1; pos += int(w.verify_len[b]); b = (b + n) % w.B
+            el = time.perf_counter() - t0
+            if el > {seconds}: break
+        q.put((step, done, pos, el))
 if __name__ == "__main__":
     ctx = mp.get_context("spawn")
     n = {procs}
-    bar = ctx.Barrier(n); q = ctx.Queue()
+    bar = ctx.Barrier(n, timeout=300); q = ctx.Queue()
     ps = [ctx.Process(target=work, args=(i, n, bar, q)) for i in range(n)]
     for p in ps: p.start()
-    res = [q.get() for _ in ps]
+    res = [q.get(timeout={seconds} * 4 + 300) for _ in range(n * {steps})]
     for p in ps: p.join()
     print(json.dumps(res))
 """
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
-                         timeout=seconds * 4 + 900)
+    # spawned children import the script's functions by file, so it runs from a file
+    with tempfile.NamedTemporaryFile("w", suffix=".py", delete=False) as f:
+        f.write(code)
+        script = f.name
+    try:
+        out = subprocess.run([sys.executable, script], capture_output=True, text=True, env=env,
+                             timeout=(seconds + 60) * steps + 700)
+    finally:
+        os.unlink(script)
     if out.returncode != 0:
         raise RuntimeError("all-core oracle timing failed: " + out.stderr[-500:])
     res = json.loads(out.stdout.strip().splitlines()[-1])
-    return (sum(r[0] for r in res), sum(r[1] for r in res), max(r[2] for r in res), procs)
+    per = []
+    for st in range(steps):
+        rs = [r for r in res if r[0] == st]
+        per.append((sum(r[1] for r in rs), sum(r[2] for r in rs), max(r[3] for r in rs)))
+    return per, procs
 
 
 def cpu_baseline(name, seconds):
     """The float64 oracle on all host cores (one process per core, whole
     requests), with the single-core figure beside it."""
     (req1, pos1, el1), = oracle_timing(name, 0, 0, 1, seconds / 2)
-    req, pos, el, n = oracle_timing_all_cores(name, seconds / 2)
+    ((req, pos, el),), n = oracle_timing_all_cores(name, seconds / 2)
     return {"value": pos / el, "unit": UNIT, "cores": n, "kind": "oracle",
             "sample": f"{req} whole requests of {name} (draft + verify, float64 numpy) on {n} "
                       f"single-threaded processes in {el:.1f} s; host cpus={os.cpu_count()}",
@@ -492,15 +507,13 @@ def run_reference(args):
     if rank != 0:
         return
     from speculative_decoding_draft_04_gb300 import workloads as W
-    per_step = min(20.0, max(1.0, 150.0 / max(1, args.steps + args.warmup)))
-    # warm-up steps: one short single-process sample (imports, first touch)
-    oracle_timing(args.config, 0, 0, 1, 1.0)
-    req = pos = 0
-    el = 0.0
-    ncores = 1
-    for _ in range(args.steps):
-        r, p, e, ncores = oracle_timing_all_cores(args.config, per_step)
-        req, pos, el = req + r, pos + p, el + e
+    per_step = min(20.0, max(0.5, 120.0 / max(1, args.steps + args.warmup)))
+    # warm-up steps (untimed) then the timed steps, in one set of processes
+    samples, ncores = oracle_timing_all_cores(args.config, per_step, steps=args.warmup + args.steps)
+    samples = samples[args.warmup:]
+    req = sum(x[0] for x in samples)
+    pos = sum(x[1] for x in samples)
+    el = sum(x[2] for x in samples)
     v = pos / el
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,

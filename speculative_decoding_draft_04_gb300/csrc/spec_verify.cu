@@ -212,8 +212,18 @@ __device__ __forceinline__ void lse_merge(float& m, df& acc, float invT, float* 
 
 // One CTA per target row j <= L_b of request b: its logsumexp; the bonus row
 // (j = L_b) also writes the per-VB-slice partials (c, s, p2) its draw needs.
+// 8 consecutive values from a raw 16-byte word of bf16 data.
+__device__ __forceinline__ void unpack8(const uint4& q, float* v) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    v[2 * e] = bf_lo(w[e]);
+    v[2 * e + 1] = bf_hi(w[e]);
+  }
+}
+
 template <typename DT>
-__global__ void __launch_bounds__(NT, 5) target_stats_kernel(Shape sh, const DT* __restrict__ target,
+__global__ void __launch_bounds__(NT, 3) target_stats_kernel(Shape sh, const DT* __restrict__ target,
                                                           const float* __restrict__ temp,
                                                           const int* __restrict__ vlen, Ws ws) {
   __shared__ float s_m[3 * (NT / 32)];
@@ -232,32 +242,47 @@ __global__ void __launch_bounds__(NT, 5) target_stats_kernel(Shape sh, const DT*
     // bonus row: GS threads (8 columns each) per VB-column slice; every lane
     // runs the same trip count (full-warp shuffles); UNR slices' loads issued
     // before any is reduced
-    constexpr int GS = VB / 8, NG = NT / GS, UNR = 4;
+    // (bf16 rows keep the raw 16-byte words of 8 slices in flight; fp32 rows
+    // load 4 slices at a time)
+    constexpr int GS = VB / 8, NG = NT / GS, UNR = sizeof(DT) == 2 ? 8 : 4;
     const int hw = threadIdx.x / GS, hl = threadIdx.x % GS;
     for (int base = 0; base < sh.NSV; base += NG * UNR) {
-      float vals[UNR][8];
+      uint4 raw[sizeof(DT) == 2 ? UNR : 1];
+      float fv[sizeof(DT) == 2 ? 1 : UNR][8];
       bool ok[UNR];
 #pragma unroll
       for (int u = 0; u < UNR; ++u) {
         const int s = base + hw + NG * u;
         const int n = s * VB + hl * 8;
         ok[u] = s < sh.NSV && n < sh.V;
-        if (ok[u]) load8(row + n, vals[u]);
+        if constexpr (sizeof(DT) == 2) {
+          if (ok[u]) raw[u] = __ldcs(reinterpret_cast<const uint4*>(row + n));
+        } else {
+          if (ok[u]) load8(row + n, fv[u]);
+        }
       }
 #pragma unroll
       for (int u = 0; u < UNR; ++u) {
         const int s = base + hw + NG * u;
+        float vv[8];
+        if constexpr (sizeof(DT) == 2) {
+          if (ok[u]) unpack8(raw[u], vv);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) vv[e] = fv[u][e];
+        }
+        float (&vals_u)[8] = vv;
         float c = -INFINITY;
         if (ok[u])
 #pragma unroll
-          for (int e = 0; e < 8; ++e) c = fmaxf(c, vals[u][e]);
+          for (int e = 0; e < 8; ++e) c = fmaxf(c, vals_u[e]);
 #pragma unroll
         for (int m = GS / 2; m; m >>= 1) c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, m));
         float ssum = 0.f, p2 = 0.f;
         if (ok[u])
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float wv = __expf(fast_tx(vals[u][e], c, invT));
+            const float wv = __expf(fast_tx(vals_u[e], c, invT));
             ssum = __fadd_rn(ssum, wv);
             p2 = fmaf(wv, wv, p2);
           }
@@ -281,30 +306,42 @@ __global__ void __launch_bounds__(NT, 5) target_stats_kernel(Shape sh, const DT*
     // other rows: per-thread online max and compensated sum over 16-byte
     // chunks strided by the block (coalesced), UNR chunks' loads in flight
     // (five CTAs per SM keep every row of a cycle resident at once)
-    constexpr int UNR = 4;
+    constexpr int UNR = sizeof(DT) == 2 ? 8 : 4;
     const int nch = sh.V / 8;
     for (int c0 = threadIdx.x; c0 < nch; c0 += NT * UNR) {
-      float vals[UNR][8];
+      uint4 raw[sizeof(DT) == 2 ? UNR : 1];
+      float fv[sizeof(DT) == 2 ? 1 : UNR][8];
       bool ok[UNR];
 #pragma unroll
       for (int u = 0; u < UNR; ++u) {
         const int c = c0 + NT * u;
         ok[u] = c < nch;
-        if (ok[u]) load8(row + (size_t)c * 8, vals[u]);
+        if constexpr (sizeof(DT) == 2) {
+          if (ok[u]) raw[u] = __ldcs(reinterpret_cast<const uint4*>(row + (size_t)c * 8));
+        } else {
+          if (ok[u]) load8(row + (size_t)c * 8, fv[u]);
+        }
       }
 #pragma unroll
       for (int u = 0; u < UNR; ++u) {
         if (!ok[u]) continue;
-        float c = vals[u][0];
+        float vals_u[8];
+        if constexpr (sizeof(DT) == 2) {
+          unpack8(raw[u], vals_u);
+        } else {
 #pragma unroll
-        for (int e = 1; e < 8; ++e) c = fmaxf(c, vals[u][e]);
+          for (int e = 0; e < 8; ++e) vals_u[e] = fv[u][e];
+        }
+        float c = vals_u[0];
+#pragma unroll
+        for (int e = 1; e < 8; ++e) c = fmaxf(c, vals_u[e]);
         if (c > mref) {
           if (mref != -INFINITY) acc = df_mulf(acc, expf(fast_tx(mref, c, invT)));
           mref = c;
         }
         float ssum = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ssum = __fadd_rn(ssum, __expf(fast_tx(vals[u][e], mref, invT)));
+        for (int e = 0; e < 8; ++e) ssum = __fadd_rn(ssum, __expf(fast_tx(vals_u[e], mref, invT)));
         acc = df_addf(acc, ssum);
       }
     }

@@ -203,8 +203,12 @@ __global__ void __launch_bounds__(VS_THREADS, 1) verify_slice_kernel(const __gri
       // mt's MMAs are complete (its accumulator is ready), overlapping tile
       // mt's epilogue; the copies are waited for after the first chunk.
       const int tid = (int)threadIdx.x;                 // 0..255
+      // Tile-local row i sits in TMEM lane (i % 4) * 32 + i / 4, so the rows of a
+      // partial tile are spread evenly over the four lane quadrants (the warps
+      // of the four sub-partitions).
+      auto row_of_lane = [&](int mt, int m) -> int { return mt * TC_M + (m & 31) * 4 + (m >> 5); };
       auto token = [&](int mt, int m) -> int {
-        const int p = mt * TC_M + m;
+        const int p = row_of_lane(mt, m);
         return p < Pk ? min(max(__ldcg(ws.prevtok + p), 0), sh.NA - 1) : -1;
       };
       auto gather = [&](const int* tok) {
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(VS_THREADS, 1) verify_slice_kernel(const __gri
         const bool more = mt + 1 < ntiles;
         int* tok_next = s_tok + ((mt + 1) & 1) * TC_M;
         if (more && tid < TC_M) tok_next[tid] = token(mt + 1, tid);
-        const int p = mt * TC_M + m;
+        const int p = row_of_lane(mt, m);
         const bool rowok = p < Pk;
         float4 rc = make_float4(1.f, 0.f, 0.f, 0.f);
         float2 rp = make_float2(0.f, 0.f);
@@ -264,6 +268,7 @@ __global__ void __launch_bounds__(VS_THREADS, 1) verify_slice_kernel(const __gri
         tc_fence_after();
         if (more) gather(tok_next);
         bool pending = more;
+        if (!__any_sync(0xffffffffu, rowok)) c = kc;   // a warp without rows skips the chunks
         for (; c < kc; c += 2) {
           const int v0 = n0 + c * CW;
           uint4 un[4], tn[4];
