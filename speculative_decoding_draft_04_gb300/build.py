@@ -18,7 +18,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspec.so")
 SOURCES = ["spec_abi.cu", "spec_draft.cu", "spec_draft_slice.cu", "spec_verify.cu",
-           "spec_verify_slice.cu", "spec_refine.cu", "spec_report.cu",
+           "spec_verify_slice.cu", "spec_verify_redecide.cu", "spec_refine.cu", "spec_report.cu",
            "spec_sched.cu", "spec_tree.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 NVCC_FLAGS = [ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -21,6 +21,8 @@ int slice_chunks(const Shape&, int);
 cudaError_t launch_verify_slice(const Shape&, const bf16*, const bf16*, const bf16*, const bf16*, const Ws&,
                                 uint32_t*, int, cudaStream_t);
 int vslice_chunks(const Shape&, int);
+template <typename DT>
+cudaError_t launch_verify_redecide(const Shape&, const HpRows&, const Ws&, int*, uint32_t*, int, cudaStream_t);
 cudaError_t launch_verify_prep(const Shape&, const int*, const float*, const int*, const double*,
                                const int*, const Ws&, uint32_t*, int*, int*, float*, float*,
                                cudaStream_t);
@@ -102,13 +104,13 @@ Eps current_eps() {
 enum Stage {
   ST_DRAFT_PERSISTENT, ST_DRAFT_SLICE, ST_VERIFY_PREP,
   ST_TARGET_STATS, ST_VERIFY_TILE, ST_VERIFY_SLICE, ST_VERIFY_FINAL, ST_SLOW_VERIFY, ST_VERIFY_HP_SUMS,
-  ST_VERIFY_HP_RESID, ST_CONFIDENCE, ST_SCHED_RANK, ST_SCHED_SELECT, ST_TREE_SELECT,
+  ST_VERIFY_HP_RESID, ST_VERIFY_REDECIDE, ST_CONFIDENCE, ST_SCHED_RANK, ST_SCHED_SELECT, ST_TREE_SELECT,
   ST_TREE_DRAFT, ST_TREE_VERIFY, ST_COUNT
 };
 const char* kStageNames[ST_COUNT] = {
     "draft_persistent", "draft_slice", "verify_prep",
     "target_stats", "verify_tile", "verify_slice", "verify_final", "slow_verify", "verify_hp_sums",
-    "verify_hp_resid", "confidence", "sched_rank", "sched_select", "tree_select",
+    "verify_hp_resid", "verify_redecide", "confidence", "sched_rank", "sched_select", "tree_select",
     "tree_draft", "tree_verify"};
 bool g_prof = false;
 struct EvPair { cudaEvent_t a, b; int stage; };
@@ -417,13 +419,20 @@ int run_verify(const spec_verify_args* a, cudaStream_t st) {
                                     a->u_accept, a->u_final, a->accept_len, a->out_tokens,
                                     a->dev_status, grid, st));
   }
-  {
-    ProfScope p(st, ST_VERIFY_HP_SUMS);
-    SPEC_TRY(launch_hp_sums<DT>(sh, R, ws, 0, a->out_tokens, a->dev_status, grid, st));
-  }
-  {
-    ProfScope p(st, ST_VERIFY_HP_RESID);
-    SPEC_TRY(launch_hp_sums<DT>(sh, R, ws, 1, a->out_tokens, a->dev_status, grid, st));
+  if (vkernel == 0) {
+    // one cooperative launch: the vocabulary split over the CTAs
+    ProfScope p(st, ST_VERIFY_REDECIDE);
+    SPEC_TRY(launch_verify_redecide<DT>(sh, R, ws, a->out_tokens, a->dev_status, nsm, st));
+  } else {
+    // (the work-unit passes of the tile-strided verification)
+    {
+      ProfScope p(st, ST_VERIFY_HP_SUMS);
+      SPEC_TRY(launch_hp_sums<DT>(sh, R, ws, 0, a->out_tokens, a->dev_status, grid, st));
+    }
+    {
+      ProfScope p(st, ST_VERIFY_HP_RESID);
+      SPEC_TRY(launch_hp_sums<DT>(sh, R, ws, 1, a->out_tokens, a->dev_status, grid, st));
+    }
   }
   return SPEC_OK;
 }

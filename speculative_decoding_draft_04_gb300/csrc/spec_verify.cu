@@ -167,6 +167,8 @@ __global__ void __launch_bounds__(NT) verify_prep_kernel(
     ws.rowptr[sh.B] = s_w[NT / 32];
     ws.ctrl[CTRL_NPACKED] = s_w[NT / 32];
     ws.ctrl[CTRL_ITEMS] = 0;
+    ws.ctrl[CTRL_BAR_COUNT] = 0;       // the re-decision launch's grid barrier
+    ws.ctrl[CTRL_ABORT] = 0;
     ws.ctrl[CTRL_SLOW] = 0;
   }
   // per-item block counters of the re-decision passes start at zero

@@ -177,3 +177,21 @@ def test_slice_verification_tiles_match_oracle_and_tile_strided(B_, V, r, gamma)
     np.testing.assert_array_equal(g.out_tokens, g1.out_tokens)
     np.testing.assert_allclose(g.alpha, g1.alpha, atol=1e-5, rtol=0, equal_nan=True)
     np.testing.assert_allclose(g.p_tok, g1.p_tok, atol=1e-5, rtol=0, equal_nan=True)
+
+
+@pytest.mark.parametrize("kernel", [0, 1], ids=["cooperative-redecide", "work-unit-passes"])
+def test_many_final_draws_redecided(kernel):
+    """Every request's final draw (correction or bonus) placed on one of the
+    oracle's own CDF breakpoints: 64 queued verification items, beyond the 16
+    whose weights are kept, so the re-decision also recomputes weights column
+    by column; both re-decision implementations must give the oracle's tokens."""
+    w = W.make_workload(_spec(64, 9000, 256, 5), trial=6)
+    res = oracle_cycle(w)
+    for b in range(w.B):
+        v = res.verify[b]
+        F = v.final.F_hi if b % 2 else v.final.F_lo
+        w.u_final[b] = np.float32(min(max(F, 1e-7), 1.0 - 6e-8))
+    g = _with_verify_kernel(kernel, w)
+    assert g.vstatus[1] >= 17, g.vstatus                 # more items than the kept ones
+    assert g.vstatus[0] & 8 == 0
+    assert_parity(compare(w, g, oracle_cycle(w)))
