@@ -177,6 +177,12 @@ __global__ void __launch_bounds__(NT, 1) draft_slice_kernel(const __grid_constan
 
   // ---- tile phase of step k: partials of this CTA's chunks for every request
   auto tile_phase = [&](int k) -> bool {
+    // trace (CTA 0): A requested, A and W2 landed, first chunk of each epilogue
+    // group done, each group done (rows 2 MAX_GAMMA - 8 + k, if free)
+    unsigned long long* tx = (P.ws.trace && blockIdx.x == 0 && (threadIdx.x & 127u) == 0u &&
+                              MAX_GAMMA + sh.gamma <= 2 * MAX_GAMMA - 8 && k < 7)
+                                 ? P.ws.trace + (2 * MAX_GAMMA - 8 + k) * TRACE_SLOTS
+                                 : nullptr;
     fence_async_shared();        // earlier generic use of the buffers precedes the async proxy's
     __syncthreads();
     if (kc > 0) {
@@ -221,28 +227,26 @@ __global__ void __launch_bounds__(NT, 1) draft_slice_kernel(const __grid_constan
       }
       const uint32_t par = gi & 1u;
       if (threadIdx.x == 0) {
+        if (tx) tx[0] = globaltimer_ns();
         if (tp_wait(abar, apar, fail) && tp_wait(s_bar + SB_W2, (nw2 - 1u) & 1u, fail)) {
+          if (tx) tx[1] = globaltimer_ns();
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + lay.offA), w0 = smem_u32(smem + lay.offW);
           const uint32_t ab = (uint32_t)(sh.r * 128);      // bytes of one 64-column W2 atom
+          // one MMA of N = K x 32 columns per 16-row step of r (the A tile
+          // is read once per step; the W2 atoms are LBO apart); both
+          // accumulator barriers complete with it
           for (int kk = 0; kk < sh.r; kk += 16) {
             const uint64_t ad = tc_sdesc(a0 + (uint32_t)((kk >> 6) * 16384 + (kk & 63) * 2), 16, 1024);
             const uint64_t bd = tc_sdesc(w0 + (uint32_t)(kk * 128), ab, 1024);
-            tc_mma(tmem, ad, bd, tc_idesc_n(N0), kk > 0 ? 1u : 0u);
+            tc_mma(tmem, ad, bd, tc_idesc_n(N0 + N1), kk > 0 ? 1u : 0u);
           }
           tc_commit(s_bar + SB_ACC0);
-          if (N1 > 0) {
-            for (int kk = 0; kk < sh.r; kk += 16) {
-              const uint64_t ad = tc_sdesc(a0 + (uint32_t)((kk >> 6) * 16384 + (kk & 63) * 2), 16, 1024);
-              const uint64_t bd = tc_sdesc(w0 + 2u * ab + (uint32_t)(kk * 128), ab, 1024);
-              tc_mma(tmem + 128u, ad, bd, tc_idesc_n(N1), kk > 0 ? 1u : 0u);
-            }
-          }
           tc_commit(s_bar + SB_ACC1);
           atomicOr(&s_armed, ARM_MMA);
         }
       }
-      if (tr && k >= 0) tr[k * TRACE_SLOTS + 1] = globaltimer_ns();
+      if (tr) tr[k * TRACE_SLOTS + 1] = globaltimer_ns();
       // epilogue: group grp takes chunks grp, grp + 2, ...; thread = request row
       const int grp = warp >> 2, q = warp & 3;
       const int m = 32 * q + lane;
@@ -279,7 +283,9 @@ __global__ void __launch_bounds__(NT, 1) draft_slice_kernel(const __grid_constan
         const int nv = min(CW, sh.V - (n0 + c * CW));
         const float4 pv = nv >= CW ? chunk_partial<true>(u, x, CW, invT) : chunk_partial<false>(u, x, nv, invT);
         if (rowok) P.ws.dpart[(size_t)m * sh.NC + c0 + c] = pv;
+        if (tx && threadIdx.x == 128u * grp && c == grp) tx[2 + grp] = globaltimer_ns();
       }
+      if (tx && threadIdx.x == 128u * grp) tx[4 + grp] = globaltimer_ns();
     }
     tc_fence_before();
     __syncthreads();

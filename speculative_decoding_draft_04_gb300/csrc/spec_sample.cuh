@@ -98,6 +98,7 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
     if (s0 + q < s1) pv[q] = __ldcg(P + s0 + q);
   const int prev = (k == 0) ? anchor[b] : __ldcg(tokens + ok - 1);
   const float T = temp[b];
+  const float u = u_draft[ok];               // (requested early: its latency overlaps the merge)
   if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(s_tab, threadIdx.x);
   if (prev < 0 || prev >= sh.V || !temp_ok(T)) {
     if (threadIdx.x == 0) {
@@ -186,7 +187,6 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   q2 = block_sum(q2, sh_f);
   m2 = block_sum(m2, sh_f);
   // (fp32 and double-float only below: GB300's fp64 rate is low)
-  const float u = u_draft[ok];
   const df target = dd_mul_f(Zdf, u);
 
   // ---- crossing chunk: first s with prefix_incl(s) > target

@@ -180,6 +180,11 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, i
                "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// Contiguous bytes [p, p + bytes) into L2 by the bulk-copy engine (p 16-byte
+// aligned, bytes a multiple of 16); no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -127,8 +127,7 @@ __global__ void __launch_bounds__(VS_THREADS, 1) verify_slice_kernel(const __gri
   const int c0 = (int)blockIdx.x * K;
   const int kc = max(0, min(K, sh.NC - c0));
   const int n0 = c0 * CW;
-  const int N = K * CW;
-  const int N0 = N < 128 ? N : 128, N1 = N - N0;
+  const int N = K * CW;                           // accumulator columns (<= 256)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* fail = &s_fail;
   const int Pk = (int)__ldcg(ws.ctrl + CTRL_NPACKED);
@@ -176,16 +175,12 @@ __global__ void __launch_bounds__(VS_THREADS, 1) verify_slice_kernel(const __gri
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + lay.offA), w0 = smem_u32(smem + lay.offW);
           const uint32_t d = tmem + (uint32_t)(buf * 256);
+          // one MMA of N = K x 32 columns per 16-row step of r (the A tile is
+          // read once per step; the W2 atoms are LBO apart)
           for (int kk = 0; kk < sh.r; kk += 16) {
             const uint64_t ad = tc_sdesc(a0 + (uint32_t)((kk >> 6) * 16384 + (kk & 63) * 2), 16, 1024);
-            tc_mma(d, ad, tc_sdesc(w0 + (uint32_t)(kk * 128), ab, 1024), tc_idesc_n(N0), kk > 0 ? 1u : 0u);
+            tc_mma(d, ad, tc_sdesc(w0 + (uint32_t)(kk * 128), ab, 1024), tc_idesc_n(N), kk > 0 ? 1u : 0u);
           }
-          if (N1 > 0)
-            for (int kk = 0; kk < sh.r; kk += 16) {
-              const uint64_t ad = tc_sdesc(a0 + (uint32_t)((kk >> 6) * 16384 + (kk & 63) * 2), 16, 1024);
-              tc_mma(d + 128u, ad, tc_sdesc(w0 + 2u * ab + (uint32_t)(kk * 128), ab, 1024), tc_idesc_n(N1),
-                     kk > 0 ? 1u : 0u);
-            }
           tc_commit(s_bar + VB_FULL0 + buf);
           issued = mt + 1;
           if (vtr && mt < 8) vtr[mt * TRACE_SLOTS + 2] = globaltimer_ns();
@@ -228,6 +223,22 @@ __global__ void __launch_bounds__(VS_THREADS, 1) verify_slice_kernel(const __gri
         fence_async_shared();            // the rows are visible to the MMA's async proxy
         mbar_arrive(s_bar + VB_AFULL);
       };
+      // L2 prefetch of a tile's row slices [n0, n0 + kc CW) of U (threads
+      // 0..127) and of the target (128..255): one bulk prefetch per row and
+      // tensor, a tile ahead of the epilogue's register loads
+      const uint32_t pf_bytes = (uint32_t)(min(kc * CW, sh.V - n0) * (int)sizeof(bf16));
+      auto pf_row = [&](int mt2) -> int2 {
+        const int p = mt2 * TC_M + (tid & (TC_M - 1));
+        return (mt2 < ntiles && p < Pk) ? __ldcg(ws.prow + p) : make_int2(-1, -1);
+      };
+      auto pf_issue = [&](int2 bj) {
+        if (bj.x < 0) return;
+        const bf16* row = tid < TC_M ? P.U + ((size_t)bj.x * sh.gamma + bj.y) * sh.V
+                                     : P.target + ((size_t)bj.x * (sh.gamma + 1) + bj.y) * sh.V;
+        bulk_prefetch_l2(row + n0, pf_bytes);
+      };
+      pf_issue(pf_row(0));
+      int2 pf_next = pf_row(1);
       if (tid < TC_M) s_tok[tid] = token(0, tid);
       named_bar(1, 256);
       gather(s_tok);
@@ -267,6 +278,8 @@ __global__ void __launch_bounds__(VS_THREADS, 1) verify_slice_kernel(const __gri
         if (vtr && threadIdx.x == 0 && mt < 8) vtr[mt * TRACE_SLOTS + 3] = globaltimer_ns();
         tc_fence_after();
         if (more) gather(tok_next);
+        pf_issue(pf_next);
+        pf_next = pf_row(mt + 2);
         bool pending = more;
         if (!__any_sync(0xffffffffu, rowok)) c = kc;   // a warp without rows skips the chunks
         for (; c < kc; c += 2) {
