@@ -74,10 +74,13 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
                                   const Eps& eps, uint32_t* counter, int cap, unsigned char* dsm,
                                   unsigned long long* str = nullptr, DT* abuf = nullptr) {
   DT* slab = reinterpret_cast<DT*>(dsm);      // [r][CW] W2 columns of the crossing chunk
-  __shared__ float sh_f[72];
+  __shared__ float s_rkey[NT / 32];
+  __shared__ int s_ridx[NT / 32];
+  __shared__ float4 s_wsum[NT / 32];
+  __shared__ int s_cross;
   __shared__ float s_a[256];
   __shared__ float s_part[NT / CW][CW];
-  __shared__ int s_slice, s_tok;
+  __shared__ int s_tok;
   __shared__ float4 s_pm, s_ps;
   __shared__ float s_pref[2], s_lo, s_hi, s_wtok;
   __shared__ df s_tab[DD_EXP_TAB];
@@ -134,21 +137,33 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
     const float key = fmaf(p.x, invT, p.y);
     if (key > best) { best = key; bidx = s; }
   }
-  // reference chunk: lowest index attaining the largest c/T + m
+  // reference chunk: lowest index attaining the largest c/T + m (a selection,
+  // so every thread reaches the same one): warp butterflies, then every
+  // thread combines the eight warp winners in warp order; its owner passes
+  // the partial on
   {
-    const float bmax = block_max(best, sh_f);
-    int cand = (best == bmax) ? bidx : 0x7fffffff;
-    for (int m = 16; m; m >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, m));
-    if ((threadIdx.x & 31) == 0) reinterpret_cast<int*>(sh_f)[32 + (threadIdx.x >> 5)] = cand;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int c2 = 0x7fffffff;
-      for (int w = 0; w < NT / 32; ++w) c2 = min(c2, reinterpret_cast<int*>(sh_f)[32 + w]);
-      s_slice = c2;
+    float key = best;
+    int idx = s0 < s1 ? bidx : 0x7fffffff;
+#pragma unroll
+    for (int m = 16; m; m >>= 1) {
+      const float k2 = __shfl_xor_sync(0xffffffffu, key, m);
+      const int i2 = __shfl_xor_sync(0xffffffffu, idx, m);
+      if (k2 > key || (k2 == key && i2 < idx)) { key = k2; idx = i2; }
     }
+    if ((threadIdx.x & 31) == 0) {
+      s_rkey[threadIdx.x >> 5] = key;
+      s_ridx[threadIdx.x >> 5] = idx;
+    }
+    if (threadIdx.x == 0) s_cross = 0x7fffffff;
     __syncthreads();
-    // the owner of the reference chunk passes its partial on
-    const int rs = s_slice;
+    float kb = s_rkey[0];
+    int rs = s_ridx[0];
+#pragma unroll
+    for (int w = 1; w < NT / 32; ++w) {
+      const float k2 = s_rkey[w];
+      const int i2 = s_ridx[w];
+      if (k2 > kb || (k2 == kb && i2 < rs)) { kb = k2; rs = i2; }
+    }
 #pragma unroll
     for (int q = 0; q < 8; ++q)
       if (rs == s0 + q && rs < s1) s_pm = pv[q];
@@ -182,16 +197,46 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
     q2 = fmaf(p.w * f, f, q2);
     m2 = fmaf(w, w, m2);
   }
-  df Zdf;
-  const df excl = block_excl_scan_df(loc, &Zdf, sh_f);
-  q2 = block_sum(q2, sh_f);
-  m2 = block_sum(m2, sh_f);
+  // exclusive scan of the masses with their total, and the two error sums,
+  // with one barrier: warp scans by shuffles, then every thread adds the
+  // eight warp totals in warp order (so all hold the same total)
+  df Zdf = {0.f, 0.f}, excl;
+  {
+    const int lane = threadIdx.x & 31, wq = threadIdx.x >> 5;
+    df inc = loc;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const df o = shfl_up_df(inc, d);
+      if (lane >= d) inc = df_add(inc, o);
+    }
+#pragma unroll
+    for (int m = 16; m; m >>= 1) {
+      q2 += __shfl_xor_sync(0xffffffffu, q2, m);
+      m2 += __shfl_xor_sync(0xffffffffu, m2, m);
+    }
+    if (lane == 31) s_wsum[wq] = make_float4(inc.hi, inc.lo, q2, m2);
+    df within = shfl_up_df(inc, 1);
+    if (lane == 0) within = {0.f, 0.f};
+    __syncthreads();
+    df off = {0.f, 0.f};
+    float tq = 0.f, tm = 0.f;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+      const float4 t = s_wsum[w];
+      if (w == wq) off = Zdf;
+      Zdf = df_add(Zdf, df{t.x, t.y});
+      tq += t.z;
+      tm += t.w;
+    }
+    q2 = tq;
+    m2 = tm;
+    excl = df_add(off, within);
+  }
   // (fp32 and double-float only below: GB300's fp64 rate is low)
   const df target = dd_mul_f(Zdf, u);
 
-  // ---- crossing chunk: first s with prefix_incl(s) > target
-  if (threadIdx.x == 0) s_slice = 0x7fffffff;
-  __syncthreads();
+  // ---- crossing chunk: first s with prefix_incl(s) > target (s_cross was
+  // reset before the barrier of the reference step)
   int my_slice = -1;
   df my_pref = {0.f, 0.f};
   float4 my_ps = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -221,17 +266,17 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
         run = nxt;
       }
     }
-    if (my_slice >= 0) atomicMin(&s_slice, my_slice);
+    if (my_slice >= 0) atomicMin(&s_cross, my_slice);
   }
   __syncthreads();
-  if (my_slice >= 0 && my_slice == s_slice) {
+  if (my_slice >= 0 && my_slice == s_cross) {
     s_pref[0] = my_pref.hi;
     s_pref[1] = my_pref.lo;
     s_ps = my_ps;                     // the crossing chunk's partial, passed on chip
   }
   __syncthreads();
   bool fallback = false;
-  if (s_slice == 0x7fffffff) {
+  if (s_cross == 0x7fffffff) {
     // rounding left the total at or below u*Z: last chunk with mass
     fallback = true;
     if (threadIdx.x == 0) {
@@ -242,20 +287,23 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
         const float4 p = __ldcg(P + s);
         run = df_addf(run, p.z * chunk_factor(p, cM, mM, invT));
       }
-      s_slice = sl;
+      s_cross = sl;
       s_pref[0] = run.hi;
       s_pref[1] = run.lo;
       s_ps = __ldcg(P + sl);
     }
     __syncthreads();
   }
-  const int sl = s_slice;
+  const int sl = s_cross;
   const df pref = {s_pref[0], s_pref[1]};
   const float4 PS = s_ps;
   if (tstamp) tstamp[2] = globaltimer_ns();
   const float fS = chunk_factor(PS, cM, mM, invT);
   const int n0 = sl * CW;
 
+  // (the next step's A row is fetched by warp 0 as soon as the token is known)
+  const bool early_row = abuf != nullptr && !sh.rnn && k + 1 < sh.gamma;
+  uint4 arow_v = make_uint4(0u, 0u, 0u, 0u);
   // ---- recompute the chunk's CW weights: 8 k-groups x CW columns (the U
   // values of the chunk are requested before the W2 columns are staged)
   const float u_reg =
@@ -313,6 +361,12 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
       s_hi = dhi;
       s_wtok = wt;
     }
+    // the next step's A row W1[token]: requested now, stored to `abuf` below
+    // (its latency overlaps the band and logsumexp of thread 0)
+    if constexpr (sizeof(DT) == 2 && HOOK != HOOK_PERTURB) {
+      if (early_row && lane * 8 < sh.r)
+        arow_v = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)(n0 + t) * sh.r + lane * 8));
+    }
   }
   __syncthreads();
   if (tstamp) tstamp[4] = globaltimer_ns();
@@ -358,7 +412,10 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   // the row is only brought into L2 for the next step's gather
   if (!sh.rnn && k + 1 < sh.gamma) {
     const int t = s_tok;
-    if (abuf) {
+    if (sizeof(DT) == 2 && HOOK != HOOK_PERTURB && early_row) {
+      if (threadIdx.x < 32 && (int)threadIdx.x * 8 < sh.r)
+        *reinterpret_cast<uint4*>(abuf + (size_t)b * sh.r + threadIdx.x * 8) = arow_v;
+    } else if (abuf) {
       if ((int)threadIdx.x * 8 < sh.r && t >= 0 && t < sh.V)
         *reinterpret_cast<uint4*>(abuf + (size_t)b * sh.r + threadIdx.x * 8) =
             __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)t * sh.r + threadIdx.x * 8));
