@@ -364,6 +364,7 @@ __global__ void __launch_bounds__(NT, 1) draft_slice_kernel(const __grid_constan
             }
           }
           __syncthreads();
+          if (tr && i0 == 0) tr[(2 * MAX_GAMMA - 1) * TRACE_SLOTS + 5] = globaltimer_ns();
 #pragma unroll 1
           for (int i = 0; i < cnt; ++i) {
             df wq = {0.f, 0.f};
@@ -391,6 +392,7 @@ __global__ void __launch_bounds__(NT, 1) draft_slice_kernel(const __grid_constan
             if (lane == 0 && warp < kc)
               item_sums(wb, sh, i0 + i, 0)[c0 + warp] = make_float2(csum.hi, csum.lo);
           }
+          if (tr && i0 == 0) tr[(2 * MAX_GAMMA - 1) * TRACE_SLOTS + 6] = globaltimer_ns();
           __syncthreads();                       // the staged rows are consumed
         }
       }
@@ -399,7 +401,10 @@ __global__ void __launch_bounds__(NT, 1) draft_slice_kernel(const __grid_constan
       if (tr) tr[(2 * MAX_GAMMA - 1) * TRACE_SLOTS + 2] = globaltimer_ns();
       for (int i = (int)blockIdx.x; i < nb; i += (int)G)
         hp_decide_item<bf16>(sh, R, wb, i, P.tokens, P.q_tok, P.lse_q, nullptr, P.status, S_hp,
-                             reinterpret_cast<bf16*>(smem + lay.offA), redo);
+                             reinterpret_cast<bf16*>(smem + lay.offA), redo,
+                             (P.ws.trace && i == 0 && MAX_GAMMA + sh.gamma <= 2 * MAX_GAMMA - 9)
+                                 ? P.ws.trace + (2 * MAX_GAMMA - 9) * TRACE_SLOTS
+                                 : nullptr);
       if (tr) tr[(2 * MAX_GAMMA - 1) * TRACE_SLOTS + 3] = globaltimer_ns();
       if (!gsync()) return false;
     }

@@ -398,32 +398,71 @@ __device__ void hp_block(const Shape& sh, const HpRows& R, const Ws& ws, int pha
 template <typename DT>
 __device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, int item, int* tokens,
                                float* q_tok, double* lse_q, int* out_tokens, uint32_t* status,
-                               HpShared& S, DT* slab, uint32_t* redo = nullptr) {
+                               HpShared& S, DT* slab, uint32_t* redo = nullptr,
+                               unsigned long long* st = nullptr) {
+  // (st: optional globaltimer stamps of thread 0 at the steps below)
+  unsigned long long* ts = (st && threadIdx.x == 0) ? st : nullptr;
+  if (ts) ts[0] = globaltimer_ns();
   const HpItem it = ldcg_item(ws.items + item);
   const bool resid = it.kind == HP_RESID;
+  // the item's constants (thread 0) and normalisers, requested now: the
+  // scan's barrier publishes the former, the latter are used after the scan
+  if (threadIdx.x == 0) *S.template ctx<DT>() = item_ctx<DT>(sh, R, it);
+  const float4 nz = resid ? __ldcg(ws.hpnorm + item) : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (threadIdx.x == 0) S.sel = 0x7fffffff;
   // one scan of the chunk sums gives both the normaliser (its total) and the
-  // per-thread prefixes; per-thread contiguous ranges of chunks
+  // per-thread prefixes; per-thread contiguous ranges of chunks, the first
+  // eight sums of each kept in registers for the crossing search
   int q0, q1;
   thread_range(sh.NC, q0, q1);
   const float2* sums = item_sums(ws, sh, item, resid ? 2 : 0);
-  df loc = range_sum(sums, q0, q1);
+  float2 sv[8];
+  auto load_range = [&]() -> df {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sv[i] = q0 + i < q1 ? __ldcg(sums + q0 + i) : make_float2(0.f, 0.f);
+    df acc = {0.f, 0.f};                         // (in index order, as the search adds)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc = dd_add(acc, df{sv[i].x, sv[i].y});
+    for (int q = q0 + 8; q < q1; q += 8) {
+      float2 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = q + i < q1 ? __ldcg(sums + q + i) : make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc = dd_add(acc, df{v[i].x, v[i].y});
+    }
+    return acc;
+  };
+  df loc = load_range();
+  if (ts) ts[1] = globaltimer_ns();
   df Z;
-  df ex = block_excl_scan_df(loc, &Z, S.shf);
+  df ex = block_scan1_df(loc, &Z, reinterpret_cast<float2*>(S.shf));
+  if (ts) ts[2] = globaltimer_ns();
   // residual with no mass: draw from p (a probability-zero event)
   const bool use_r = resid && Z.hi > 0.f;
   if (resid && !use_r) {
     sums = item_sums(ws, sh, item, 0);
-    loc = range_sum(sums, q0, q1);
-    ex = block_excl_scan_df(loc, &Z, S.shf);
+    loc = load_range();
+    __syncthreads();                            // S.shf is read by every thread
+    ex = block_scan1_df(loc, &Z, reinterpret_cast<float2*>(S.shf));
   }
   const df target = dd_mul_f(Z, it.u);
-  if (threadIdx.x == 0) S.sel = 0x7fffffff;
-  __syncthreads();
   int mine = -1;
   df mypref = {0.f, 0.f};
   if (q0 < q1 && dd_le(ex, target) && !dd_le(dd_add(ex, loc), target)) {
     df run = ex;
-    for (int q = q0; q < q1 && mine < 0; q += 8) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (mine < 0 && q0 + i < q1) {
+        const df nx = dd_add(run, df{sv[i].x, sv[i].y});
+        if (!dd_le(nx, target)) {
+          mine = q0 + i;
+          mypref = run;
+        } else {
+          run = nx;
+        }
+      }
+    }
+    for (int q = q0 + 8; q < q1 && mine < 0; q += 8) {
       float2 v[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = q + i < q1 ? __ldcg(sums + q + i) : make_float2(0.f, 0.f);
@@ -457,10 +496,10 @@ __device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, i
     }
     __syncthreads();
   }
+  if (ts) ts[3] = globaltimer_ns();
   const int n0 = S.sel * CW;
   df izp = {0.f, 0.f}, izq = {0.f, 0.f};
   if (use_r) {
-    const float4 nz = __ldcg(ws.hpnorm + item);
     izp = {nz.x, nz.y};
     izq = {nz.z, nz.w};
   }
@@ -485,7 +524,8 @@ __device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, i
     S.part[w][lane] = part;
   }
   __syncthreads();
-  const ItemCtx<DT> c = item_ctx_shared<DT>(sh, R, it, S.template ctx<DT>());
+  if (ts) ts[4] = globaltimer_ns();
+  const ItemCtx<DT> c = *S.template ctx<DT>();     // (written before the scan's barrier)
   if (w == 0) {
     const int v = n0 + lane;
     df eq = {0.f, 0.f}, ep = {0.f, 0.f};
@@ -539,7 +579,9 @@ __device__ void hp_decide_item(const Shape& sh, const HpRows& R, const Ws& ws, i
       }
     }
   }
+  if (ts) ts[5] = globaltimer_ns();
   __syncthreads();
+  if (ts) ts[6] = globaltimer_ns();
 }
 
 // Block sums of the n queued items (phase 0: weights, phase 1: residuals of

@@ -262,6 +262,66 @@ __device__ __forceinline__ df block_sum_df(df v, float* sh) {
 }
 // Exclusive prefix (double-float) of one value per thread in thread order;
 // *total receives the block total.  `sh` holds >= 66 floats.
+// Exclusive block scan of v with the block total, one barrier: warp scans by
+// shuffles, then every thread adds the warp totals in warp order (so all hold
+// the same total, and each warp's offset is a prefix of that same sum).  `sw`
+// (NT / 32 entries) may be written again only after a later barrier.
+__device__ __forceinline__ df block_scan1_df(df v, df* total, float2* sw) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  df inc = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const df o = shfl_up_df(inc, d);
+    if (lane >= d) inc = df_add(inc, o);
+  }
+  if (lane == 31) sw[w] = make_float2(inc.hi, inc.lo);
+  df within = shfl_up_df(inc, 1);
+  if (lane == 0) within = {0.f, 0.f};
+  __syncthreads();
+  df off = {0.f, 0.f}, tot = {0.f, 0.f};
+#pragma unroll
+  for (int q = 0; q < NT / 32; ++q) {
+    if (q == w) off = tot;
+    const float2 t = sw[q];
+    tot = df_add(tot, df{t.x, t.y});
+  }
+  *total = tot;
+  return df_add(off, within);
+}
+// block_scan1_df with two fp32 block sums riding on the same barrier (every
+// thread adds the warp sums in warp order, so all hold the same values).
+__device__ __forceinline__ df block_scan1_df2(df v, df* total, float& a, float& c, float4* sw) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  df inc = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const df o = shfl_up_df(inc, d);
+    if (lane >= d) inc = df_add(inc, o);
+  }
+#pragma unroll
+  for (int m = 16; m; m >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, m);
+    c += __shfl_xor_sync(0xffffffffu, c, m);
+  }
+  if (lane == 31) sw[w] = make_float4(inc.hi, inc.lo, a, c);
+  df within = shfl_up_df(inc, 1);
+  if (lane == 0) within = {0.f, 0.f};
+  __syncthreads();
+  df off = {0.f, 0.f}, tot = {0.f, 0.f};
+  float ta = 0.f, tc = 0.f;
+#pragma unroll
+  for (int q = 0; q < NT / 32; ++q) {
+    if (q == w) off = tot;
+    const float4 t = sw[q];
+    tot = df_add(tot, df{t.x, t.y});
+    ta += t.z;
+    tc += t.w;
+  }
+  a = ta;
+  c = tc;
+  *total = tot;
+  return df_add(off, within);
+}
 __device__ __forceinline__ df block_excl_scan_df(df v, df* total, float* sh) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   df inc = v;

@@ -200,38 +200,8 @@ __device__ void draft_sample_body(const Shape& sh, int k, int b, const DT* __res
   // exclusive scan of the masses with their total, and the two error sums,
   // with one barrier: warp scans by shuffles, then every thread adds the
   // eight warp totals in warp order (so all hold the same total)
-  df Zdf = {0.f, 0.f}, excl;
-  {
-    const int lane = threadIdx.x & 31, wq = threadIdx.x >> 5;
-    df inc = loc;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const df o = shfl_up_df(inc, d);
-      if (lane >= d) inc = df_add(inc, o);
-    }
-#pragma unroll
-    for (int m = 16; m; m >>= 1) {
-      q2 += __shfl_xor_sync(0xffffffffu, q2, m);
-      m2 += __shfl_xor_sync(0xffffffffu, m2, m);
-    }
-    if (lane == 31) s_wsum[wq] = make_float4(inc.hi, inc.lo, q2, m2);
-    df within = shfl_up_df(inc, 1);
-    if (lane == 0) within = {0.f, 0.f};
-    __syncthreads();
-    df off = {0.f, 0.f};
-    float tq = 0.f, tm = 0.f;
-#pragma unroll
-    for (int w = 0; w < NT / 32; ++w) {
-      const float4 t = s_wsum[w];
-      if (w == wq) off = Zdf;
-      Zdf = df_add(Zdf, df{t.x, t.y});
-      tq += t.z;
-      tm += t.w;
-    }
-    q2 = tq;
-    m2 = tm;
-    excl = df_add(off, within);
-  }
+  df Zdf;
+  const df excl = block_scan1_df2(loc, &Zdf, q2, m2, s_wsum);
   // (fp32 and double-float only below: GB300's fp64 rate is low)
   const df target = dd_mul_f(Zdf, u);
 
