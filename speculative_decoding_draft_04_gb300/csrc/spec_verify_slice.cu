@@ -15,7 +15,7 @@
 //   warp 8       control: gathers the tile's rows W1[x_j] (or the RNN head's
 //                factor rows) into the A operand (cp.async, K-major, 128-byte
 //                swizzle) once the previous tile's MMAs have read it, then one
-//                lane issues the MMAs (M = 128 rows, N = 32K in two groups,
+//                lane issues the MMAs (M = 128 rows, N = 32K in one group,
 //                K = r) into one of two 256-column TMEM accumulators;
 //   warps 0-7    epilogue, two column groups of four warps, thread = packed
 //                row = TMEM lane: each 32-column chunk's bias from TMEM
