@@ -16,10 +16,12 @@
 //     during step k's sampling phase (U does not depend on the drawn tokens),
 //     the rest prefetched into L2 then and loaded into the A operand's space
 //     once the step's MMAs have read it;
-//   * per step: every thread gathers the rows W1[x_{k-1}] (the A operand,
-//     K-major, 128-byte swizzle, cp.async), one thread issues the tcgen05
-//     MMAs (M = 128 requests, N = 32K columns in two groups, K = r) into a TMEM
-//     accumulator, and all eight warps read it back (tcgen05.ld) as two column
+//   * per step: the rows W1[x_{k-1}] (the A operand, K-major, 128-byte
+//     swizzle) arrive by TMA from the A-row buffer the samplers filled (the
+//     first step and a redo gather them by cp.async), one thread issues the
+//     tcgen05 MMAs (M = 128 requests, one MMA of N = 32K columns per 16-row
+//     step of K = r) into a TMEM accumulator, and all eight warps read it back
+//     (tcgen05.ld) as two column
 //     groups, thread = request row, reducing each 32-column chunk to its
 //     partial (c, m, s, q2) with the same arithmetic as the tile-strided draft
 //     kernel.  The transition bias never leaves the SM;
@@ -75,7 +77,9 @@ struct SlLayout {
   }
 };
 
-// Barrier slots: the W2 load, the gathered A tile, the two MMA groups, the U
+// Barrier slots: the W2 load, the gathered A tile, the accumulator (two slots,
+// both committed after the step's MMAs: the first chunks' epilogue waits on
+// one, the A tile's reuse for U chunks on the other), the A tile by TMA, the U
 // chunks.  Each completes once per tile phase (W2 once per load).
 enum : int { SB_W2 = 0, SB_AFULL = 1, SB_ACC0 = 2, SB_ACC1 = 3, SB_ATMA = 4, SB_U0 = 5,
              SB_COUNT = SB_U0 + SL_MAX_K };
@@ -112,8 +116,7 @@ __global__ void __launch_bounds__(NT, 1) draft_slice_kernel(const __grid_constan
   const int c0 = (int)blockIdx.x * K;               // first chunk of this CTA's columns
   const int kc = max(0, min(K, sh.NC - c0));        // chunks it owns
   const int n0 = c0 * CW;
-  const int N = K * CW;                             // accumulator columns
-  const int N0 = N < 128 ? N : 128, N1 = N - N0;
+  const int N = K * CW;                             // accumulator columns (<= 256)
   const int nring = min(lay.nring, kc);
   const uint32_t G = gridDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -239,7 +242,7 @@ __global__ void __launch_bounds__(NT, 1) draft_slice_kernel(const __grid_constan
           for (int kk = 0; kk < sh.r; kk += 16) {
             const uint64_t ad = tc_sdesc(a0 + (uint32_t)((kk >> 6) * 16384 + (kk & 63) * 2), 16, 1024);
             const uint64_t bd = tc_sdesc(w0 + (uint32_t)(kk * 128), ab, 1024);
-            tc_mma(tmem, ad, bd, tc_idesc_n(N0 + N1), kk > 0 ? 1u : 0u);
+            tc_mma(tmem, ad, bd, tc_idesc_n(N), kk > 0 ? 1u : 0u);
           }
           tc_commit(s_bar + SB_ACC0);
           tc_commit(s_bar + SB_ACC1);

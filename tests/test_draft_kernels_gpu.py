@@ -4,8 +4,8 @@ float64 oracle and against each other, and the bounded-wait error path.
 * The slice-resident kernel (each CTA keeps the W2 columns of one vocabulary
   slice in shared memory for every step; B <= 128, V <= 256 x SMs) runs by
   default where it fits; SPEC_OPT_DRAFT_KERNEL = 1 forces the tile-strided
-  kernel.  Shapes below span 1 to 8 chunks of 32 columns per CTA (one or two
-  MMA groups, U chunks in the ring only or also in the A tile's space),
+  kernel.  Shapes below span 1 to 8 chunks of 32 columns per CTA (MMAs of
+  N = 32 to 256, U chunks in the ring only or also in the A tile's space),
   ragged vocabulary tails, r = 64 / 128 / 256, and rows beyond B.
 * Both kernels must reproduce the oracle (tokens and accept lengths
   bit-exact up to the near-boundary rule, probabilities within 1e-5) and,
@@ -69,8 +69,8 @@ SHAPES = [
     (1, 16, 64, 1),            # one chunk, one request
     (40, 4104, 64, 5),         # 1 chunk per CTA, 8-column tail chunk
     (128, 9000, 128, 4),       # 2 chunks, ragged
-    (96, 19456, 256, 3),       # 4 chunks: one MMA group, U chunk 3 in the A tile's space
-    (128, 32000, 256, 7),      # 7 chunks (C2's shape), two MMA groups
+    (96, 19456, 256, 3),       # 4 chunks (N = 128), U chunk 3 in the A tile's space
+    (128, 32000, 256, 7),      # 7 chunks (C2's shape), N = 224
 ]
 
 
