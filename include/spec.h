@@ -358,7 +358,9 @@ int32_t spec_prefix_schedule(const spec_schedule_args* args, spec_stream_t strea
  * holds token x (the anchor for the root) gets a token drawn by inverse CDF
  * with u_draft[b][s] from q = softmax((U[b][d] + W1[x] W2) / T_b); children
  * of one node are independent draws.  Unselected slots are left untouched.
- * gamma launches (one per depth), double-float arithmetic throughout.
+ * One planning launch, then two launches per depth (each drafted node's
+ * vocabulary split over 8 CTAs, then one CTA per node for its children's
+ * draws), double-float arithmetic throughout.
  *
  * spec_tree_verify: walks each request's selected tree from the root.  At a
  * node with target row p (target[b][0] at the root, target[b][1 + s] at slot
@@ -369,8 +371,10 @@ int32_t spec_prefix_schedule(const spec_schedule_args* args, spec_stream_t strea
  * becomes the next node; when none is accepted the final token is drawn from
  * r with u_final[b] (at a leaf r = p: the bonus token).  Outputs accept_len
  * (accepted nodes), out_tokens [B][gamma+1] (accepted tokens, final, -1) and
- * path [B][gamma] (accepted slots, -1).  One launch, one CTA per request,
- * double-float arithmetic throughout.
+ * path [B][gamma] (accepted slots, -1).  gamma + 1 steps of two launches
+ * (the current node's draft row over several CTAs per request, then one CTA
+ * per request for the node's tests and draws), double-float arithmetic
+ * throughout.
  *
  * Both draft and verify take the workspace spec_tree_workspace_bytes(B, N, V)
  * (16-byte aligned); dev_status bits are OR-ed in and never cleared.        */

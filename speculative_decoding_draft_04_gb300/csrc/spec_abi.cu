@@ -53,6 +53,7 @@ cudaError_t launch_schedule_select(int, int, const double*, int, const int*, con
 
 cudaError_t launch_tree_select(int, int, int, const int*, const float*, int, float*, uint8_t*, float*,
                                uint32_t*, cudaStream_t);
+size_t tree_workspace_bytes(const TreeShape&);
 template <typename DT>
 cudaError_t launch_tree_draft(const TreeShape&, const void*, const void*, const void*, const int*,
                               const float*, const int*, const uint8_t*, const float*, int*, float*, void*,
@@ -755,9 +756,7 @@ static int tree_check(int B, int N, int gamma, int V, int r, int dtype) {
 
 size_t spec_tree_workspace_bytes(int32_t B, int32_t N, int32_t V) {
   if (B < 1 || N < 1 || V < 16) return 0;
-  const size_t draft = (size_t)B * (N + 1) * ((V + 31) / 32) * 16;
-  const size_t verify = (size_t)B * 2 * V * 8;
-  return draft > verify ? draft : verify;
+  return tree_workspace_bytes(TreeShape{B, N, 0, V, 0});
 }
 
 int32_t spec_tree_select(int32_t B, int32_t N, int32_t gamma, const int32_t* parent, const float* conf,

@@ -7,24 +7,33 @@
 //                        (ties: shallower, then lower index) by a comparison
 //                        count -- closed under prefixes because a child's a
 //                        never exceeds its parent's.
-//   tree_draft_kernel    one launch per depth level, one CTA per (request,
-//                        node of that level with selected children): the
-//                        node's draft logits (U row of its depth + W1[x] W2,
-//                        over T) in double-float over the whole vocabulary,
-//                        then each selected child drawn by inverse CDF with its
-//                        own uniform.
-//   tree_verify_kernel   one CTA per request walks the tree from the root: at
-//                        each node, target and draft logits in double-float,
-//                        then recursive rejection over the node's candidates
-//                        (ratio u < r(x)/q(x), r <- normalize(max(0, r - q))
-//                        after a rejection); the first accepted child is the
-//                        next node, otherwise the final token is drawn from r.
+//   tree_plan_kernel     one CTA per request: the depth level at which each
+//                        node (the root and every selected slot) is drafted --
+//                        its depth when it has selected children, else none.
+//   tree_chunks_kernel   per depth level, S CTAs per node of that level, each a
+//                        share of the vocabulary: the node's draft logits (U row
+//                        of its depth + W1[x] W2, over T) in double-float, as
+//                        32-column chunk partials.
+//   tree_draft_kernel    per depth level, one CTA per node of that level: the
+//                        chunk partials merged, then each selected child drawn
+//                        by inverse CDF with its own uniform (crossing chunk,
+//                        its 32 weights recomputed and scanned).
+//   tree_vrow_kernel,    verification, one pair of launches per depth level: S
+//   tree_vstep_kernel    CTAs per request compute the draft logits row of the
+//                        request's current node (when it has selected children);
+//                        then one CTA per request takes one step of its walk from
+//                        the root: target logits of the node, recursive rejection
+//                        over the node's candidates (ratio u < r(x)/q(x),
+//                        r <- normalize(max(0, r - q)) after a rejection); the
+//                        first accepted child is the next level's node, otherwise
+//                        the final token is drawn from r and the walk ends.
 //
 // Every weight, sum and scan is a double-float (transition bias as a
 // compensated sum of exact products), so the decisions agree with a float64
 // computation except within ~1e-12 of a boundary.  This is the direct
 // formulation: it spends ~r double-float multiply-adds per vocabulary entry
-// and node and is not tiled onto the tensor cores.
+// and node (spread over many CTAs per node) and is not tiled onto the tensor
+// cores.
 #include "spec_hp.cuh"
 
 namespace spec {
@@ -173,15 +182,14 @@ __device__ int row_draw(int V, df target, F weight, float* shf, int* s_sel, df* 
 }
 
 // ---------------------------------------------------------------- drafting
-// Chunk partials of a draft row: for each 32-column chunk c, (m_c, s_c) with
+// Chunk partials of a draft row: for each 32-column chunk c in [c_lo, c_hi), (m_c, s_c) with
 // m_c the chunk's largest logit (hi part) and s_c = sum exp(l - m_c), one warp
 // per chunk.  l = (U_row + W1[x] W2) / T in double-float.
 template <typename DT>
 __device__ void draft_row_chunks(const TreeShape& ts, const DT* urow, const DT* W2, const float* a,
-                                 df invT, const df* tab, float4* chunks) {
+                                 df invT, const df* tab, float4* chunks, int c_lo, int c_hi) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NC = (ts.V + 31) / 32;
-  for (int c = warp; c < NC; c += NT / 32) {
+  for (int c = c_lo + warp; c < c_hi; c += NT / 32) {
     const int v = c * 32 + lane;
     df l = {-INFINITY, 0.f};
     if (v < ts.V) l = dd_mul(dd_add_f(hp_bias<DT>(a, W2, ts.V, ts.r, v), ldf(urow + v)), invT);
@@ -198,23 +206,15 @@ __device__ __forceinline__ df chunk_mass(const float4* chunks, int c, float m, c
   return dd_mul(df{p.y, p.z}, dd_exp(two_sum_df(p.x, -m), tab));
 }
 
-// Node index of CTA (b, n): n = 0 the root, n = 1 + s slot s.
-template <typename DT>
-__global__ void __launch_bounds__(NT) tree_draft_kernel(TreeShape ts, int level, const DT* U, const DT* W1,
-                                                        const DT* W2, const int* anchor, const float* temp,
-                                                        const int* parent, const uint8_t* mask,
-                                                        const float* u_draft, int* tokens, float* q_tok,
-                                                        float4* scratch, uint32_t* status) {
-  __shared__ df s_tab[DD_EXP_TAB];
-  __shared__ float shf[72];
-  __shared__ float s_a[256];
-  __shared__ int s_sel[2];
-  __shared__ df s_pref;
-  __shared__ int s_go;
-  const int b = blockIdx.x / (ts.N + 1), node = (int)(blockIdx.x % (ts.N + 1)) - 1;
+// Node index (b, n): n = 0 the root, n = 1 + s slot s; plan[b][n] = the level
+// at which the node is drafted, -1 for none.
+__global__ void __launch_bounds__(NT) tree_plan_kernel(TreeShape ts, const int* parent, const uint8_t* mask,
+                                                       int8_t* plan) {
+  const int b = blockIdx.x;
   const int* par = parent + (size_t)b * ts.N;
   const uint8_t* msk = mask + (size_t)b * ts.N;
-  if (threadIdx.x == 0) {
+  for (int n = threadIdx.x; n <= ts.N; n += NT) {
+    const int node = n - 1;
     // depth of the node (root 0; parents checked to precede their children)
     int d = 0, ok = node < 0 || msk[node];
     for (int p = node; p >= 0 && ok; p = par[p]) {
@@ -222,10 +222,54 @@ __global__ void __launch_bounds__(NT) tree_draft_kernel(TreeShape ts, int level,
     }
     int kids = 0;
     for (int s = node + 1; s < ts.N && ok; ++s) kids += (par[s] == node) & (msk[s] != 0);
-    s_go = (ok && d == level && kids > 0) ? 1 : 0;
+    plan[(size_t)b * (ts.N + 1) + n] = (int8_t)((ok && kids > 0) ? d : -1);
   }
+}
+
+// S CTAs per node slot: CTA part of the nodes drafted at `level` computes the
+// chunk partials of its share of the vocabulary.  (Nodes with a bad token or
+// temperature are left to tree_draft_kernel, which reports them.)
+template <typename DT>
+__global__ void __launch_bounds__(NT) tree_chunks_kernel(TreeShape ts, int level, int S, const DT* U,
+                                                         const DT* W1, const DT* W2, const int* anchor,
+                                                         const float* temp, const int* tokens,
+                                                         const int8_t* plan, float4* scratch) {
+  __shared__ df s_tab[DD_EXP_TAB];
+  __shared__ float s_a[256];
+  const int nidx = blockIdx.x / S, part = blockIdx.x % S;
+  if (plan[nidx] != level) return;
+  const int b = nidx / (ts.N + 1), node = nidx % (ts.N + 1) - 1;
+  const float T = temp[b];
+  const int x = node < 0 ? anchor[b] : tokens[(size_t)b * ts.N + node];
+  if (x < 0 || x >= ts.V || !temp_ok(T)) return;
+  if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(s_tab, threadIdx.x);
+  for (int i = threadIdx.x; i < ts.r; i += NT) s_a[i] = ldf(W1 + (size_t)x * ts.r + i);
   __syncthreads();
-  if (!s_go) return;
+  const int NC = (ts.V + 31) / 32;
+  const int per = (NC + S - 1) / S;
+  const int c_lo = min(NC, part * per), c_hi = min(NC, c_lo + per);
+  const DT* urow = U + ((size_t)b * ts.gamma + level) * ts.V;
+  draft_row_chunks<DT>(ts, urow, W2, s_a, dd_recip(T), s_tab, scratch + (size_t)nidx * NC, c_lo, c_hi);
+}
+
+// One CTA per node slot; the nodes drafted at `level` draw their children from
+// the chunk partials of tree_chunks_kernel.
+template <typename DT>
+__global__ void __launch_bounds__(NT) tree_draft_kernel(TreeShape ts, int level, const DT* U, const DT* W1,
+                                                        const DT* W2, const int* anchor, const float* temp,
+                                                        const int* parent, const uint8_t* mask,
+                                                        const float* u_draft, int* tokens, float* q_tok,
+                                                        const int8_t* plan, float4* scratch,
+                                                        uint32_t* status) {
+  __shared__ df s_tab[DD_EXP_TAB];
+  __shared__ float shf[72];
+  __shared__ float s_a[256];
+  __shared__ int s_sel[2];
+  __shared__ df s_pref;
+  const int b = blockIdx.x / (ts.N + 1), node = (int)(blockIdx.x % (ts.N + 1)) - 1;
+  const int* par = parent + (size_t)b * ts.N;
+  const uint8_t* msk = mask + (size_t)b * ts.N;
+  if (plan[blockIdx.x] != level) return;
   const float T = temp[b];
   const int x = node < 0 ? anchor[b] : tokens[(size_t)b * ts.N + node];
   if (x < 0 || x >= ts.V || !temp_ok(T)) {
@@ -246,8 +290,6 @@ __global__ void __launch_bounds__(NT) tree_draft_kernel(TreeShape ts, int level,
   float4* chunks = scratch + (size_t)blockIdx.x * NC;
   const DT* urow = U + ((size_t)b * ts.gamma + level) * ts.V;
   const df invT = dd_recip(T);
-  draft_row_chunks<DT>(ts, urow, W2, s_a, invT, s_tab, chunks);
-  __syncthreads();
   float mx = -INFINITY;
   for (int c = threadIdx.x; c < NC; c += NT) mx = fmaxf(mx, __ldcg(chunks + c).x);
   const float m = block_max(mx, shf);
@@ -310,17 +352,64 @@ __global__ void __launch_bounds__(NT) tree_draft_kernel(TreeShape ts, int level,
 }
 
 // ---------------------------------------------------------------- verification
+// Walk state of a request between levels: (node, depth, accepted, done).
+// Level 0 starts at the root without reading it.
+
+// Selected children of `node` (-1: the root).
+__device__ __forceinline__ int tree_kids(const TreeShape& ts, const int* par, const uint8_t* msk, int node) {
+  int nk = 0;
+  for (int s = node + 1; s < ts.N; ++s) nk += (par[s] == node) & (msk[s] != 0);
+  return nk;
+}
+
+// S CTAs per request: the draft logits row of the request's current node
+// (U row of its depth + W1[x] W2, over T, in double-float), when the node has
+// selected children; CTA part takes a contiguous share of the columns.
 template <typename DT>
-__global__ void __launch_bounds__(NT) tree_verify_kernel(TreeShape ts, const DT* target, const DT* U,
-                                                         const DT* W1, const DT* W2, const int* anchor,
-                                                         const float* temp, const int* parent,
-                                                         const uint8_t* mask, const int* tokens,
-                                                         const float* u_accept, const float* u_final,
-                                                         int* accept_len, int* out_tokens, int* path,
-                                                         float2* scratch, uint32_t* status) {
+__global__ void __launch_bounds__(NT) tree_vrow_kernel(TreeShape ts, int level, int S, const DT* U,
+                                                       const DT* W1, const DT* W2, const int* anchor,
+                                                       const float* temp, const int* parent,
+                                                       const uint8_t* mask, const int* tokens,
+                                                       const int4* state, float2* scratch) {
+  __shared__ float s_a[256];
+  const int b = blockIdx.x / S, part = blockIdx.x % S;
+  int node = -1, depth = 0;
+  if (level > 0) {
+    const int4 w = __ldcg(state + b);
+    if (w.w) return;                         // the walk has ended
+    node = w.x;
+    depth = w.y;
+  }
+  const int* par = parent + (size_t)b * ts.N;
+  const uint8_t* msk = mask + (size_t)b * ts.N;
+  // (a root with a bad anchor or temperature, or bad slots, are reported by
+  // the step kernel; the tokens of selected slots were checked at level 0)
+  const float T = temp[b];
+  const int x = node < 0 ? anchor[b] : tokens[(size_t)b * ts.N + node];
+  if (x < 0 || x >= ts.V || !temp_ok(T) || tree_kids(ts, par, msk, node) == 0) return;
+  for (int i = threadIdx.x; i < ts.r; i += NT) s_a[i] = ldf(W1 + (size_t)x * ts.r + i);
+  __syncthreads();
+  const df invT = dd_recip(T);
+  const DT* urow = U + ((size_t)b * ts.gamma + depth) * ts.V;
+  float2* lq = scratch + (size_t)b * 2 * ts.V + ts.V;
+  const int per = (ts.V + S - 1) / S;
+  const int v1 = min(ts.V, (part + 1) * per);
+  for (int v = part * per + (int)threadIdx.x; v < v1; v += NT) {
+    const df l = dd_mul(dd_add_f(hp_bias<DT>(s_a, W2, ts.V, ts.r, v), ldf(urow + v)), invT);
+    lq[v] = make_float2(l.hi, l.lo);
+  }
+}
+
+// One CTA per request: one step of the walk at its current node.
+template <typename DT>
+__global__ void __launch_bounds__(NT) tree_vstep_kernel(TreeShape ts, int level, const DT* target,
+                                                        const int* anchor, const float* temp, const int* parent,
+                                                        const uint8_t* mask, const int* tokens,
+                                                        const float* u_accept, const float* u_final,
+                                                        int* accept_len, int* out_tokens, int* path,
+                                                        float2* scratch, int4* state, uint32_t* status) {
   __shared__ df s_tab[DD_EXP_TAB];
   __shared__ float shf[72];
-  __shared__ float s_a[256];
   __shared__ int s_sel[2];
   __shared__ df s_izr[TREE_MAX_SLOTS];
   __shared__ int s_bad;
@@ -330,103 +419,100 @@ __global__ void __launch_bounds__(NT) tree_verify_kernel(TreeShape ts, const DT*
   const int* tok = tokens + (size_t)b * ts.N;
   int* out = out_tokens + (size_t)b * (ts.gamma + 1);
   const float T = temp[b];
-  if (threadIdx.x == 0) {
-    int bad = 0;
-    if (!temp_ok(T)) bad |= SPEC_DEV_BAD_TEMP;
-    if (anchor[b] < 0 || anchor[b] >= ts.V) bad |= SPEC_DEV_BAD_TOKEN;
-    for (int s = 0; s < ts.N; ++s) {
-      if (par[s] < -1 || par[s] >= s) {
-        bad |= SPEC_DEV_BAD_TREE;
-        continue;
+  int node = -1, depth = 0, n_acc = 0;
+  if (level == 0) {
+    if (threadIdx.x == 0) {
+      int bad = 0;
+      if (!temp_ok(T)) bad |= SPEC_DEV_BAD_TEMP;
+      if (anchor[b] < 0 || anchor[b] >= ts.V) bad |= SPEC_DEV_BAD_TOKEN;
+      for (int s = 0; s < ts.N; ++s) {
+        if (par[s] < -1 || par[s] >= s) {
+          bad |= SPEC_DEV_BAD_TREE;
+          continue;
+        }
+        int d = 1;                              // depth: parents checked to precede
+        for (int p = par[s]; p >= 0 && d <= ts.gamma; p = par[p]) {
+          ++d;
+          if (par[p] < -1 || par[p] >= p) break;  // flagged when slot p was checked
+        }
+        if (d > ts.gamma) bad |= SPEC_DEV_BAD_TREE;
+        if (msk[s] && (tok[s] < 0 || tok[s] >= ts.V)) bad |= SPEC_DEV_BAD_TOKEN;
       }
-      int d = 1;                                // depth: parents checked to precede
-      for (int p = par[s]; p >= 0 && d <= ts.gamma; p = par[p]) {
-        ++d;
-        if (par[p] < -1 || par[p] >= p) break;  // flagged when slot p was checked
+      s_bad = bad;
+      if (bad) {
+        set_status(status, (uint32_t)bad);
+        accept_len[b] = -1;
+        for (int j = 0; j <= ts.gamma; ++j) out[j] = -1;
+        for (int j = 0; j < ts.gamma; ++j) path[(size_t)b * ts.gamma + j] = -1;
+        state[b] = make_int4(-1, 0, 0, 1);
       }
-      if (d > ts.gamma) bad |= SPEC_DEV_BAD_TREE;
-      if (msk[s] && (tok[s] < 0 || tok[s] >= ts.V)) bad |= SPEC_DEV_BAD_TOKEN;
     }
-    s_bad = bad;
-    if (bad) {
-      set_status(status, (uint32_t)bad);
-      accept_len[b] = -1;
-      for (int j = 0; j <= ts.gamma; ++j) out[j] = -1;
-      for (int j = 0; j < ts.gamma; ++j) path[(size_t)b * ts.gamma + j] = -1;
-    }
+    __syncthreads();
+    if (s_bad) return;
+  } else {
+    const int4 w = __ldcg(state + b);
+    if (w.w) return;
+    node = w.x;
+    depth = w.y;
+    n_acc = w.z;
   }
   if (threadIdx.x < DD_EXP_TAB) dd_exp_table_entry(s_tab, threadIdx.x);
   __syncthreads();
-  if (s_bad) return;
   float2* lp = scratch + (size_t)b * 2 * ts.V;
-  float2* lq = lp + ts.V;
+  const float2* lq = lp + ts.V;                // this level's draft row (tree_vrow_kernel)
   const df invT = dd_recip(T);
-  int node = -1, depth = 0, n_acc = 0;
-  while (true) {
-    const int row = node < 0 ? 0 : 1 + node;
-    row_logits<DT>(ts, target + ((size_t)b * (ts.N + 1) + row) * ts.V, W2, nullptr, invT, lp);
-    // the node's selected children, in slot order
-    int nk = 0;
-    for (int s = node + 1; s < ts.N; ++s) nk += (par[s] == node) & (msk[s] != 0);
-    const int x = node < 0 ? anchor[b] : tok[node];
-    if (nk > 0) {
-      for (int i = threadIdx.x; i < ts.r; i += NT) s_a[i] = ldf(W1 + (size_t)x * ts.r + i);
-      __syncthreads();
-      row_logits<DT>(ts, U + ((size_t)b * ts.gamma + depth) * ts.V, W2, s_a, invT, lq);
+  const int row = node < 0 ? 0 : 1 + node;
+  row_logits<DT>(ts, target + ((size_t)b * (ts.N + 1) + row) * ts.V, nullptr, nullptr, invT, lp);
+  const int nk = tree_kids(ts, par, msk, node);
+  __syncthreads();
+  float mp, mq = 0.f;
+  df Zp, Zq = {1.f, 0.f};
+  row_norm(ts.V, lp, s_tab, shf, mp, Zp);
+  if (nk > 0) row_norm(ts.V, lq, s_tab, shf, mq, Zq);
+  const df izp = dd_div(df{1.f, 0.f}, Zp), izq = dd_div(df{1.f, 0.f}, Zq);
+  int nrej = 0, next = -1;
+  for (int s = node + 1; s < ts.N && next < 0; ++s) {
+    if (!(par[s] == node && msk[s])) continue;
+    const int xs = tok[s];
+    const df rx = resid_prob(lp, lq, xs, mp, izp, mq, izq, s_izr, nrej, s_tab);
+    const df qx = row_prob(lq, xs, mq, izq, s_tab);
+    // accept iff u < r(x) / q(x), i.e. u q(x) < r(x)
+    const float u = u_accept[(size_t)b * ts.N + s];
+    if (!dd_le(rx, dd_mul_f(qx, u))) {
+      next = s;
+      break;
     }
+    // rejected: r <- normalize(max(0, r - q))
+    df zs = {0.f, 0.f};
+    for (int v = threadIdx.x; v < ts.V; v += NT) {
+      const df d = dd_add(resid_prob(lp, lq, v, mp, izp, mq, izq, s_izr, nrej, s_tab),
+                          dd_neg(row_prob(lq, v, mq, izq, s_tab)));
+      if (d.hi > 0.f) zs = dd_add(zs, d);
+    }
+    zs = block_sum_df(zs, shf);
+    if (threadIdx.x == 0) s_izr[nrej] = zs.hi > 0.f ? dd_div(df{1.f, 0.f}, zs) : df{0.f, 0.f};
     __syncthreads();
-    float mp, mq = 0.f;
-    df Zp, Zq = {1.f, 0.f};
-    row_norm(ts.V, lp, s_tab, shf, mp, Zp);
-    if (nk > 0) row_norm(ts.V, lq, s_tab, shf, mq, Zq);
-    const df izp = dd_div(df{1.f, 0.f}, Zp), izq = dd_div(df{1.f, 0.f}, Zq);
-    int nrej = 0, next = -1;
-    for (int s = node + 1; s < ts.N && next < 0; ++s) {
-      if (!(par[s] == node && msk[s])) continue;
-      const int xs = tok[s];
-      const df rx = resid_prob(lp, lq, xs, mp, izp, mq, izq, s_izr, nrej, s_tab);
-      const df qx = row_prob(lq, xs, mq, izq, s_tab);
-      // accept iff u < r(x) / q(x), i.e. u q(x) < r(x)
-      const float u = u_accept[(size_t)b * ts.N + s];
-      if (!dd_le(rx, dd_mul_f(qx, u))) {
-        next = s;
-        break;
-      }
-      // rejected: r <- normalize(max(0, r - q))
-      df zs = {0.f, 0.f};
-      for (int v = threadIdx.x; v < ts.V; v += NT) {
-        const df d = dd_add(resid_prob(lp, lq, v, mp, izp, mq, izq, s_izr, nrej, s_tab),
-                            dd_neg(row_prob(lq, v, mq, izq, s_tab)));
-        if (d.hi > 0.f) zs = dd_add(zs, d);
-      }
-      zs = block_sum_df(zs, shf);
-      if (threadIdx.x == 0) s_izr[nrej] = zs.hi > 0.f ? dd_div(df{1.f, 0.f}, zs) : df{0.f, 0.f};
-      __syncthreads();
-      ++nrej;
-    }
-    if (next >= 0) {
-      if (threadIdx.x == 0) {
-        out[n_acc] = tok[next];
-        path[(size_t)b * ts.gamma + n_acc] = next;
-      }
-      ++n_acc;
-      node = next;
-      ++depth;
-      __syncthreads();
-      continue;
-    }
-    // final token from r (the target row itself at a leaf)
-    const df tgt = df{u_final[b], 0.f};          // r is normalised: target u
-    const int ft = row_draw(
-        ts.V, tgt, [&](int v) { return resid_prob(lp, lq, v, mp, izp, mq, izq, s_izr, nrej, s_tab); }, shf,
-        s_sel, nullptr);
+    ++nrej;
+  }
+  if (next >= 0) {
     if (threadIdx.x == 0) {
-      out[n_acc] = ft;
-      for (int j = n_acc + 1; j <= ts.gamma; ++j) out[j] = -1;
-      for (int j = n_acc; j < ts.gamma; ++j) path[(size_t)b * ts.gamma + j] = -1;
-      accept_len[b] = n_acc;
+      out[n_acc] = tok[next];
+      path[(size_t)b * ts.gamma + n_acc] = next;
+      state[b] = make_int4(next, depth + 1, n_acc + 1, 0);
     }
     return;
+  }
+  // final token from r (the target row itself at a leaf)
+  const df tgt = df{u_final[b], 0.f};            // r is normalised: target u
+  const int ft = row_draw(
+      ts.V, tgt, [&](int v) { return resid_prob(lp, lq, v, mp, izp, mq, izq, s_izr, nrej, s_tab); }, shf,
+      s_sel, nullptr);
+  if (threadIdx.x == 0) {
+    out[n_acc] = ft;
+    for (int j = n_acc + 1; j <= ts.gamma; ++j) out[j] = -1;
+    for (int j = n_acc; j < ts.gamma; ++j) path[(size_t)b * ts.gamma + j] = -1;
+    accept_len[b] = n_acc;
+    state[b] = make_int4(node, depth, n_acc, 1);
   }
 }
 
@@ -438,16 +524,41 @@ cudaError_t launch_tree_select(int B, int N, int gamma, const int* parent, const
   return cudaGetLastError();
 }
 
+// Workspace of the tree calls: the draft's chunk partials [B][N+1][NC] and
+// plan [B][N+1]; the verification's two rows per request [B][2][V] and walk
+// states [B] (the draft's area is dead by then).
+static size_t tree_plan_offset(const TreeShape& ts) {
+  return ((size_t)ts.B * (ts.N + 1) * ((ts.V + 31) / 32) * 16 + 255) / 256 * 256;
+}
+static size_t tree_state_offset(const TreeShape& ts) {
+  return ((size_t)ts.B * 2 * ts.V * 8 + 255) / 256 * 256;
+}
+size_t tree_workspace_bytes(const TreeShape& ts) {
+  const size_t draft = tree_plan_offset(ts) + (size_t)ts.B * (ts.N + 1);
+  const size_t verify = tree_state_offset(ts) + (size_t)ts.B * 16;
+  return draft > verify ? draft : verify;
+}
+
 template <typename DT>
 cudaError_t launch_tree_draft(const TreeShape& ts, const void* U, const void* W1, const void* W2,
                               const int* anchor, const float* temp, const int* parent, const uint8_t* mask,
                               const float* u_draft, int* tokens, float* q_tok, void* scratch,
                               uint32_t* status, cudaStream_t st) {
+  int8_t* plan = reinterpret_cast<int8_t*>(static_cast<unsigned char*>(scratch) + tree_plan_offset(ts));
+  tree_plan_kernel<<<ts.B, NT, 0, st>>>(ts, parent, mask, plan);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  constexpr int S = 8;                          // CTAs per drafted node
   for (int level = 0; level < ts.gamma; ++level) {
+    tree_chunks_kernel<DT><<<ts.B * (ts.N + 1) * S, NT, 0, st>>>(ts, level, S, (const DT*)U, (const DT*)W1,
+                                                                (const DT*)W2, anchor, temp, tokens, plan,
+                                                                (float4*)scratch);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     tree_draft_kernel<DT><<<ts.B * (ts.N + 1), NT, 0, st>>>(
         ts, level, (const DT*)U, (const DT*)W1, (const DT*)W2, anchor, temp, parent, mask, u_draft, tokens,
-        q_tok, (float4*)scratch, status);
-    const cudaError_t e = cudaGetLastError();
+        q_tok, plan, (float4*)scratch, status);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -459,11 +570,21 @@ cudaError_t launch_tree_verify(const TreeShape& ts, const void* target, const vo
                                const uint8_t* mask, const int* tokens, const float* u_accept,
                                const float* u_final, int* accept_len, int* out_tokens, int* path,
                                void* scratch, uint32_t* status, cudaStream_t st) {
-  tree_verify_kernel<DT><<<ts.B, NT, 0, st>>>(ts, (const DT*)target, (const DT*)U, (const DT*)W1,
-                                              (const DT*)W2, anchor, temp, parent, mask, tokens, u_accept,
-                                              u_final, accept_len, out_tokens, path, (float2*)scratch,
-                                              status);
-  return cudaGetLastError();
+  int4* state = reinterpret_cast<int4*>(static_cast<unsigned char*>(scratch) + tree_state_offset(ts));
+  const int S = ts.B >= 600 ? 1 : (600 + ts.B - 1) / ts.B;   // about 600 CTAs per row pass
+  // a walk accepts at most gamma nodes, so gamma + 1 steps end every request
+  for (int level = 0; level <= ts.gamma; ++level) {
+    tree_vrow_kernel<DT><<<ts.B * S, NT, 0, st>>>(ts, level, S, (const DT*)U, (const DT*)W1, (const DT*)W2,
+                                                  anchor, temp, parent, mask, tokens, state, (float2*)scratch);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    tree_vstep_kernel<DT><<<ts.B, NT, 0, st>>>(ts, level, (const DT*)target, anchor, temp, parent, mask,
+                                               tokens, u_accept, u_final, accept_len, out_tokens, path,
+                                               (float2*)scratch, state, status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 #define SPEC_INST(DT)                                                                                   \
