@@ -90,13 +90,69 @@ __global__ void __launch_bounds__(NT) tree_select_kernel(int B, int N, int gamma
   if (threadIdx.x == 0 && expected) expected[b] = sum;
 }
 
+// ---------------------------------------------------------------- block helpers
+// Block reductions for a CTA of T threads (T / 32 warps; `sh` holds 2 T / 32
+// floats and is free again when they return).  Every thread combines the warp
+// results in warp order, so all hold the same value.
+template <int T>
+__device__ __forceinline__ float tblock_max(float v, float* sh) {
+  v = warp_max(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float m = sh[0];
+  for (int q = 1; q < T / 32; ++q) m = fmaxf(m, sh[q]);
+  __syncthreads();
+  return m;
+}
+template <int T>
+__device__ __forceinline__ df tblock_sum_df(df v, float* sh) {
+  v = warp_sum_df(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    sh[2 * (threadIdx.x >> 5)] = v.hi;
+    sh[2 * (threadIdx.x >> 5) + 1] = v.lo;
+  }
+  __syncthreads();
+  df t = {0.f, 0.f};
+  for (int q = 0; q < T / 32; ++q) t = dd_add(t, df{sh[2 * q], sh[2 * q + 1]});
+  __syncthreads();
+  return t;
+}
+// Exclusive scan with the block total.
+template <int T>
+__device__ __forceinline__ df tblock_excl_scan_df(df v, df* total, float* sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  df inc = v;
+  for (int d = 1; d < 32; d <<= 1) {
+    const df o = shfl_up_df(inc, d);
+    if (lane >= d) inc = df_add(inc, o);
+  }
+  __syncthreads();
+  if (lane == 31) {
+    sh[2 * w] = inc.hi;
+    sh[2 * w + 1] = inc.lo;
+  }
+  df within = shfl_up_df(inc, 1);
+  if (lane == 0) within = {0.f, 0.f};
+  __syncthreads();
+  df off = {0.f, 0.f}, tot = {0.f, 0.f};
+  for (int q = 0; q < T / 32; ++q) {
+    if (q == w) off = tot;
+    tot = df_add(tot, df{sh[2 * q], sh[2 * q + 1]});
+  }
+  __syncthreads();
+  *total = tot;
+  return df_add(off, within);
+}
+
 // ---------------------------------------------------------------- node rows
 // Logits of one node row over the vocabulary into `out` (double-float pairs):
 // draft (U_row + W1[f] W2) / T, or target t_row / T when a == nullptr.
-template <typename DT>
+template <typename DT, int T = NT>
 __device__ void row_logits(const TreeShape& ts, const DT* urow, const DT* W2, const float* a, df invT,
                            float2* out) {
-  for (int v = threadIdx.x; v < ts.V; v += NT) {
+  for (int v = threadIdx.x; v < ts.V; v += T) {
     df l;
     if (a) {
       const df bias = hp_bias<DT>(a, W2, ts.V, ts.r, v);
@@ -109,16 +165,17 @@ __device__ void row_logits(const TreeShape& ts, const DT* urow, const DT* W2, co
 }
 
 // Largest logit (its hi part) and the normaliser sum exp(l - m).
+template <int T = NT>
 __device__ void row_norm(int V, const float2* l, const df* tab, float* shf, float& m, df& Z) {
   float mx = -INFINITY;
-  for (int v = threadIdx.x; v < V; v += NT) mx = fmaxf(mx, __ldcg(l + v).x);
-  m = block_max(mx, shf);
+  for (int v = threadIdx.x; v < V; v += T) mx = fmaxf(mx, __ldcg(l + v).x);
+  m = tblock_max<T>(mx, shf);
   df s = {0.f, 0.f};
-  for (int v = threadIdx.x; v < V; v += NT) {
+  for (int v = threadIdx.x; v < V; v += T) {
     const float2 x = __ldcg(l + v);
     s = dd_add(s, dd_exp(dd_add_f(df{x.x, x.y}, -m), tab));
   }
-  Z = block_sum_df(s, shf);
+  Z = tblock_sum_df<T>(s, shf);
 }
 
 // Probability of entry v of a row (logits l, shift m, 1/Z).
@@ -146,9 +203,9 @@ __device__ __forceinline__ df resid_prob(const float2* lp, const float2* lq, int
 // Inverse CDF of an unnormalised row given by `weight(v)`: the smallest v with
 // running sum > target (double-float), else the last v with weight > 0.
 // Per-thread contiguous ranges, block scan, then the crossing thread's walk.
-template <class F>
+template <int T, class F>
 __device__ int row_draw(int V, df target, F weight, float* shf, int* s_sel, df* s_w) {
-  const int per = (V + NT - 1) / NT;
+  const int per = (V + T - 1) / T;
   const int v0 = min(V, (int)threadIdx.x * per), v1 = min(V, v0 + per);
   df loc = {0.f, 0.f};
   int lastpos = -1;
@@ -158,7 +215,7 @@ __device__ int row_draw(int V, df target, F weight, float* shf, int* s_sel, df* 
     loc = dd_add(loc, w);
   }
   df tot;
-  const df ex = block_excl_scan_df(loc, &tot, shf);
+  const df ex = tblock_excl_scan_df<T>(loc, &tot, shf);
   if (threadIdx.x == 0) { s_sel[0] = 0x7fffffff; s_sel[1] = -1; }
   __syncthreads();
   if (v0 < v1 && dd_le(ex, target) && !dd_le(dd_add(ex, loc), target)) {
@@ -400,9 +457,12 @@ __global__ void __launch_bounds__(NT) tree_vrow_kernel(TreeShape ts, int level, 
   }
 }
 
-// One CTA per request: one step of the walk at its current node.
+// One CTA of TV_THREADS per request: one step of the walk at its current
+// node (its double-float passes over the vocabulary are the tree
+// verification's bulk, so the CTA is four times the usual width).
+constexpr int TV_THREADS = 1024;
 template <typename DT>
-__global__ void __launch_bounds__(NT) tree_vstep_kernel(TreeShape ts, int level, const DT* target,
+__global__ void __launch_bounds__(TV_THREADS) tree_vstep_kernel(TreeShape ts, int level, const DT* target,
                                                         const int* anchor, const float* temp, const int* parent,
                                                         const uint8_t* mask, const int* tokens,
                                                         const float* u_accept, const float* u_final,
@@ -462,13 +522,13 @@ __global__ void __launch_bounds__(NT) tree_vstep_kernel(TreeShape ts, int level,
   const float2* lq = lp + ts.V;                // this level's draft row (tree_vrow_kernel)
   const df invT = dd_recip(T);
   const int row = node < 0 ? 0 : 1 + node;
-  row_logits<DT>(ts, target + ((size_t)b * (ts.N + 1) + row) * ts.V, nullptr, nullptr, invT, lp);
+  row_logits<DT, TV_THREADS>(ts, target + ((size_t)b * (ts.N + 1) + row) * ts.V, nullptr, nullptr, invT, lp);
   const int nk = tree_kids(ts, par, msk, node);
   __syncthreads();
   float mp, mq = 0.f;
   df Zp, Zq = {1.f, 0.f};
-  row_norm(ts.V, lp, s_tab, shf, mp, Zp);
-  if (nk > 0) row_norm(ts.V, lq, s_tab, shf, mq, Zq);
+  row_norm<TV_THREADS>(ts.V, lp, s_tab, shf, mp, Zp);
+  if (nk > 0) row_norm<TV_THREADS>(ts.V, lq, s_tab, shf, mq, Zq);
   const df izp = dd_div(df{1.f, 0.f}, Zp), izq = dd_div(df{1.f, 0.f}, Zq);
   int nrej = 0, next = -1;
   for (int s = node + 1; s < ts.N && next < 0; ++s) {
@@ -484,12 +544,12 @@ __global__ void __launch_bounds__(NT) tree_vstep_kernel(TreeShape ts, int level,
     }
     // rejected: r <- normalize(max(0, r - q))
     df zs = {0.f, 0.f};
-    for (int v = threadIdx.x; v < ts.V; v += NT) {
+    for (int v = threadIdx.x; v < ts.V; v += TV_THREADS) {
       const df d = dd_add(resid_prob(lp, lq, v, mp, izp, mq, izq, s_izr, nrej, s_tab),
                           dd_neg(row_prob(lq, v, mq, izq, s_tab)));
       if (d.hi > 0.f) zs = dd_add(zs, d);
     }
-    zs = block_sum_df(zs, shf);
+    zs = tblock_sum_df<TV_THREADS>(zs, shf);
     if (threadIdx.x == 0) s_izr[nrej] = zs.hi > 0.f ? dd_div(df{1.f, 0.f}, zs) : df{0.f, 0.f};
     __syncthreads();
     ++nrej;
@@ -504,7 +564,7 @@ __global__ void __launch_bounds__(NT) tree_vstep_kernel(TreeShape ts, int level,
   }
   // final token from r (the target row itself at a leaf)
   const df tgt = df{u_final[b], 0.f};            // r is normalised: target u
-  const int ft = row_draw(
+  const int ft = row_draw<TV_THREADS>(
       ts.V, tgt, [&](int v) { return resid_prob(lp, lq, v, mp, izp, mq, izq, s_izr, nrej, s_tab); }, shf,
       s_sel, nullptr);
   if (threadIdx.x == 0) {
@@ -578,7 +638,7 @@ cudaError_t launch_tree_verify(const TreeShape& ts, const void* target, const vo
                                                   anchor, temp, parent, mask, tokens, state, (float2*)scratch);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    tree_vstep_kernel<DT><<<ts.B, NT, 0, st>>>(ts, level, (const DT*)target, anchor, temp, parent, mask,
+    tree_vstep_kernel<DT><<<ts.B, TV_THREADS, 0, st>>>(ts, level, (const DT*)target, anchor, temp, parent, mask,
                                                tokens, u_accept, u_final, accept_len, out_tokens, path,
                                                (float2*)scratch, state, status);
     e = cudaGetLastError();
