@@ -359,7 +359,7 @@ int32_t spec_prefix_schedule(const spec_schedule_args* args, spec_stream_t strea
  * with u_draft[b][s] from q = softmax((U[b][d] + W1[x] W2) / T_b); children
  * of one node are independent draws.  Unselected slots are left untouched.
  * One planning launch, then two launches per depth (each drafted node's
- * vocabulary split over 8 CTAs, then one CTA per node for its children's
+ * vocabulary split over 16 CTAs, then one CTA per node for its children's
  * draws), double-float arithmetic throughout.
  *
  * spec_tree_verify: walks each request's selected tree from the root.  At a

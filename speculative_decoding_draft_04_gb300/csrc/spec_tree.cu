@@ -10,7 +10,7 @@
 //   tree_plan_kernel     one CTA per request: the depth level at which each
 //                        node (the root and every selected slot) is drafted --
 //                        its depth when it has selected children, else none.
-//   tree_chunks_kernel   per depth level, S CTAs per node of that level, each a
+//   tree_chunks_kernel   per depth level, 16 CTAs per node of that level, each a
 //                        share of the vocabulary: the node's draft logits (U row
 //                        of its depth + W1[x] W2, over T) in double-float, as
 //                        32-column chunk partials.
@@ -608,7 +608,7 @@ cudaError_t launch_tree_draft(const TreeShape& ts, const void* U, const void* W1
   tree_plan_kernel<<<ts.B, NT, 0, st>>>(ts, parent, mask, plan);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  constexpr int S = 8;                          // CTAs per drafted node
+  constexpr int S = 16;                         // CTAs per drafted node
   for (int level = 0; level < ts.gamma; ++level) {
     tree_chunks_kernel<DT><<<ts.B * (ts.N + 1) * S, NT, 0, st>>>(ts, level, S, (const DT*)U, (const DT*)W1,
                                                                 (const DT*)W2, anchor, temp, tokens, plan,
