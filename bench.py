@@ -647,6 +647,23 @@ def main():
     torch.cuda.synchronize()
     barrier()
     e2e_ms = float(sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps)
+    # the same host-to-device copies alone (U, then the target logits, one
+    # stream): the link rate, and how much of the copy the overlap hides
+    link_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    big = (hs.U.numel() * hs.U.element_size() + hs.target.numel() * hs.target.element_size())
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            d.U.copy_(hs.U, non_blocking=True)
+            d.target.copy_(hs.target, non_blocking=True)
+        torch.cuda.synchronize()
+        flush.zero_()
+        link_ev[0].record(stream)
+        for _ in range(args.steps):
+            d.U.copy_(hs.U, non_blocking=True)
+            d.target.copy_(hs.target, non_blocking=True)
+        link_ev[1].record(stream)
+    torch.cuda.synchronize()
+    link_ms = float(link_ev[0].elapsed_time(link_ev[1]) / args.steps)
 
     draft_prof = tuple(a + b for a, b in zip(prof.get("draft_persistent", (0.0, 0)),
                                                prof.get("draft_slice", (0.0, 0))))
@@ -706,7 +723,12 @@ def main():
             "e2e": {"value": pos_all / (e2e_all * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_all,
                     "call": "spec_cycle_host (pinned host inputs and results; the target "
-                            "logits copied on a second stream during the draft)"},
+                            "logits copied on a second stream during the draft)",
+                    "link": {"h2d_ms_alone": link_ms, "h2d_gbs": big / (link_ms * 1e6),
+                             "bytes": big,
+                             "hidden_ms": link_ms + ms - e2e_ms,
+                             "note": "U and target logits copied alone, back to back on one "
+                                     "stream; hidden_ms = copy alone + device cycle - e2e"}},
             "gpu_launches": int(launches * args.steps),
             "clocks": clocks,
         }
