@@ -1,4 +1,4 @@
-"""Parity sweep of the spec token gate at scale.
+"""Parity sweep of the token parity gate at scale.
 
 The gate: on every workload, every request whose GPU tokens or accept length
 differ from the float64 oracle must have a consumed uniform within 1e-6 of a

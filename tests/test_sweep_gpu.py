@@ -3,7 +3,7 @@ request of a few seeded full-size trials of C0, C1 and C2 — trials outside
 the range of the committed sweep record — through the C ABI on the GPU, then
 compared with the float64 oracle request by request under input checksums.
 
-The north-star gate (VESSL blog, "수락 규칙": the emitted sequence must follow
+The token parity gate (VESSL blog, "수락 규칙": the emitted sequence must follow
 the target, so the GPU's tokens must be the oracle's): mismatched requests
 below 0.01 % and none away from a decision boundary.  At these sample sizes
 (a few hundred requests per workload) that allows no mismatch at all; the

@@ -1,6 +1,6 @@
 """The committed record of the full parity sweep (tests/parity_sweep.py:
 every request of many seeded full-size trials, GPU outputs compared with the
-float64 oracle under input checksums) meets the spec gate at its own
+float64 oracle under input checksums) meets the token parity gate at its own
 scale: at least 1000 trials of C0-C2 and 100 of C3/C4, at least 10^4
 requests each, mismatched requests below 0.01 % with none away from a
 decision boundary, identical inputs on both sides, and every probability
