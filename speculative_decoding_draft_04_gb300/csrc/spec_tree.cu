@@ -631,7 +631,7 @@ cudaError_t launch_tree_verify(const TreeShape& ts, const void* target, const vo
                                const float* u_final, int* accept_len, int* out_tokens, int* path,
                                void* scratch, uint32_t* status, cudaStream_t st) {
   int4* state = reinterpret_cast<int4*>(static_cast<unsigned char*>(scratch) + tree_state_offset(ts));
-  const int S = ts.B >= 600 ? 1 : (600 + ts.B - 1) / ts.B;   // about 600 CTAs per row pass
+  const int S = ts.B >= 2400 ? 1 : (2400 + ts.B - 1) / ts.B;  // about 2400 CTAs per row pass
   // a walk accepts at most gamma nodes, so gamma + 1 steps end every request
   for (int level = 0; level <= ts.gamma; ++level) {
     tree_vrow_kernel<DT><<<ts.B * S, NT, 0, st>>>(ts, level, S, (const DT*)U, (const DT*)W1, (const DT*)W2,
