@@ -497,7 +497,10 @@ const char* spec_status_string(int32_t status);
  *                        draft kernel
  *   SPEC_OPT_VERIFY_KERNEL 0 = the slice-resident verification tiles wherever
  *                        the shape fits them (bf16, r % 64 == 0, V <= 256 x
- *                        SM count; default), 1 = always the tile-strided ones
+ *                        SM count) and the re-decision of queued draws in one
+ *                        cooperative launch (default); 1 = always the
+ *                        tile-strided tiles and the two work-unit re-decision
+ *                        passes
  * The two test hooks exist for the library's own tests; the default kernels
  * carry no trace of them.                                                   */
 enum { SPEC_OPT_EPS_SCALE = 1, SPEC_OPT_FORCE_SIMT = 2, SPEC_OPT_BIAS_PATH = 3,
